@@ -1,0 +1,70 @@
+"""Plain-Python model of the partition planner (test oracle).
+
+"feat: add paged-attention monolithic decode-only AR foundation" (lucebox
+pull 555), Summary, says only that context partitioning is occupancy-aware
+and that the partials are merged by a stable split-softmax merge; Benchmark
+results notes that short sequences in a ragged batch carry dead partitions
+sized by the longest sequence.  The exact rule is this build's reading,
+frozen here so that the C++ planner can be compared with it exactly:
+
+- partitions are whole multiples of TILE = 32 tokens (so they start on a
+  block boundary for block sizes 16 and 32);
+- forced: part_tokens = roundup(ceil(max_len / force_parts), 32);
+- otherwise the total live work is spread over the resident CTA slots:
+  part_tokens = roundup(ceil(total_len / (sm_count * ctas_per_sm)), 32),
+  at least MIN_PART = 128 tokens and at most roundup(max_len, 32);
+- n_parts = ceil(max_len / part_tokens) (partition slots per sequence, the
+  partial buffers' second dimension); a sequence of length L has
+  ceil(L / part_tokens) live partitions;
+- n_parts == 1 selects direct mode: no partials, the decode kernel writes
+  the output itself;
+- the decode grid has n_ctas = S in direct mode, otherwise
+  min(S * n_parts, ceil(total_len / part_tokens) + S) CTAs, an upper bound
+  on the live (sequence, partition) pairs;
+- an empty batch (max_len == 0) is direct with part_tokens = 32.
+"""
+
+TILE = 32
+MIN_PART = 128
+
+OK, INVALID = 0, -1
+
+
+def _cdiv(a: int, b: int) -> int:
+    return -(-a // b)
+
+
+def _roundup(a: int, b: int) -> int:
+    return _cdiv(a, b) * b
+
+
+def plan(*, n_seqs, max_len, total_len, block_size, hq, hkv, d, k_type, v_type,
+         sm_count, ctas_per_sm, force_parts=0):
+    """Returns (rc, dict).  dict keys: part_tokens, n_parts, direct, n_ctas,
+    part_o_bytes, part_ml_bytes."""
+    if (n_seqs < 1 or block_size not in (16, 32) or hkv < 1 or hq < hkv or hq % hkv
+            or hq // hkv > 8 or d not in (128, 256) or k_type not in (0, 1, 2)
+            or v_type not in (0, 1, 2) or sm_count < 1 or ctas_per_sm < 1
+            or force_parts < 0 or max_len < 0 or total_len < max_len
+            or total_len > n_seqs * max_len):
+        return INVALID, None
+    if max_len == 0:
+        part, n_parts = TILE, 1
+    elif force_parts > 0:
+        part = _roundup(_cdiv(max_len, force_parts), TILE)
+        n_parts = _cdiv(max_len, part)
+    else:
+        slots = sm_count * ctas_per_sm
+        part = max(MIN_PART, _roundup(_cdiv(total_len, slots), TILE))
+        part = min(part, _roundup(max_len, TILE))
+        n_parts = _cdiv(max_len, part)
+    direct = 1 if n_parts == 1 else 0
+    if direct:
+        n_ctas = n_seqs
+        po = pm = 0
+    else:
+        n_ctas = min(n_seqs * n_parts, _cdiv(total_len, part) + n_seqs)
+        po = n_seqs * hq * n_parts * d * 2
+        pm = n_seqs * hq * n_parts * 8
+    return OK, dict(part_tokens=part, n_parts=n_parts, direct=direct, n_ctas=n_ctas,
+                    part_o_bytes=po, part_ml_bytes=pm)

@@ -1,0 +1,138 @@
+"""Pins for the plain-Python allocator and planner models: the properties
+the pages state (all-or-nothing allocation, stale-handle detection,
+immediate release; partitions cover every token, direct mode has one) and
+the build's frozen reading of the order."""
+import math
+import random
+
+from oracle import plan_model, pool_model
+
+
+def test_pool_fresh_order_and_handles():
+    p = pool_model.PoolModel(5)
+    rc, hs = p.alloc(3)
+    assert rc == pool_model.OK
+    assert [pool_model.PoolModel.block_of(h) for h in hs] == [0, 1, 2]
+    assert all(h >> 32 == 1 for h in hs) and 0 not in hs
+    assert p.free_count() == 2
+
+
+def test_pool_all_or_nothing():
+    p = pool_model.PoolModel(4)
+    p.alloc(3)
+    before = (list(p.stack), list(p.gen), list(p.live))
+    rc, hs = p.alloc(2)
+    assert rc == pool_model.NOMEM and hs == []
+    assert (list(p.stack), list(p.gen), list(p.live)) == before
+
+
+def test_pool_stale_double_and_duplicate_free_release_nothing():
+    p = pool_model.PoolModel(4)
+    _, hs = p.alloc(3)
+    assert p.free([hs[1]]) == pool_model.OK
+    snap = (list(p.stack), list(p.gen), list(p.live))
+    assert p.free([hs[0], hs[1]]) == pool_model.STALE      # hs[1] already freed
+    assert p.free([hs[0], hs[0]]) == pool_model.STALE      # listed twice
+    assert p.free([(7 << 32) | 2]) == pool_model.STALE     # wrong generation
+    assert p.free([(1 << 32) | 9]) == pool_model.STALE     # id out of range
+    assert (list(p.stack), list(p.gen), list(p.live)) == snap
+    # the stale handle stays stale after its block is reused
+    _, again = p.alloc(1)
+    assert pool_model.PoolModel.block_of(again[0]) == 1 and again[0] != hs[1]
+    assert p.free([hs[1]]) == pool_model.STALE
+
+
+def test_pool_release_is_immediate_and_lifo():
+    p = pool_model.PoolModel(6)
+    _, hs = p.alloc(6)
+    assert p.free_count() == 0
+    assert p.free([hs[4], hs[2]]) == pool_model.OK
+    assert p.free_count() == 2
+    _, hs2 = p.alloc(2)
+    assert [pool_model.PoolModel.block_of(h) for h in hs2] == [2, 4]
+
+
+def test_pool_generation_skips_zero_on_wrap():
+    p = pool_model.PoolModel(1)
+    p.gen[0] = 0xFFFFFFFF
+    _, hs = p.alloc(1)
+    assert hs[0] >> 32 == 0xFFFFFFFF
+    p.free(hs)
+    _, hs = p.alloc(1)
+    assert hs[0] >> 32 == 1
+
+
+def test_pool_random_trace_invariants():
+    rng = random.Random(0)
+    p = pool_model.PoolModel(50)
+    live = set()
+    for _ in range(2000):
+        if rng.random() < 0.55:
+            rc, hs = p.alloc(rng.randint(0, 12))
+            if rc == pool_model.OK:
+                assert not (set(hs) & live)
+                live |= set(hs)
+        elif live:
+            k = rng.randint(1, min(5, len(live)))
+            hs = rng.sample(sorted(live), k)
+            assert p.free(hs) == pool_model.OK
+            live -= set(hs)
+        assert p.free_count() + len(live) == 50
+        ids = [pool_model.PoolModel.block_of(h) for h in live]
+        assert len(set(ids)) == len(ids)
+
+
+def _plan(**kw):
+    base = dict(n_seqs=1, max_len=0, total_len=0, block_size=16, hq=24, hkv=4, d=256,
+                k_type=2, v_type=2, sm_count=152, ctas_per_sm=1, force_parts=0)
+    base.update(kw)
+    return plan_model.plan(**base)
+
+
+def test_plan_covers_every_token_and_bounds_the_grid():
+    rng = random.Random(1)
+    for _ in range(3000):
+        S = rng.randint(1, 40)
+        lens = [rng.choice([0, 1, 15, 16, 17, 200, rng.randint(0, 300000)]) for _ in range(S)]
+        mx, tot = max(lens), sum(lens)
+        force = rng.choice([0, 0, 1, 2, 7, 1000])
+        rc, p = _plan(n_seqs=S, max_len=mx, total_len=tot, force_parts=force,
+                      block_size=rng.choice([16, 32]), sm_count=rng.choice([1, 152, 160]),
+                      ctas_per_sm=rng.choice([1, 2, 3]))
+        assert rc == plan_model.OK
+        P, n = p["part_tokens"], p["n_parts"]
+        assert P % 32 == 0 and P > 0
+        assert n * P >= mx and (n - 1) * P < max(mx, 1)
+        assert p["direct"] == (n == 1)
+        live = sum(math.ceil(L / P) for L in lens)
+        assert p["n_ctas"] >= (S if p["direct"] else live)
+        assert p["n_ctas"] <= S * n
+        if force:
+            assert n <= force
+        if not p["direct"]:
+            assert p["part_o_bytes"] == S * 24 * n * 256 * 2
+            assert p["part_ml_bytes"] == S * 24 * n * 8
+
+
+def test_plan_worked_examples():
+    # uniform 8 x 128K on 152 SMs: the live work spread over one wave
+    rc, p = _plan(n_seqs=8, max_len=131072, total_len=8 * 131072)
+    assert (p["part_tokens"], p["n_parts"], p["n_ctas"]) == (6912, 19, 152)
+    # ragged 128K + 7 x 8K: partitions sized by total work, not by the longest sequence
+    rc, p = _plan(n_seqs=8, max_len=131072, total_len=131072 + 7 * 8192)
+    assert p["part_tokens"] == 1248 and p["n_parts"] == 106
+    assert sum(math.ceil(L / 1248) for L in [131072] + [8192] * 7) <= p["n_ctas"] == 159
+    # a batch at least as wide as the machine runs direct
+    rc, p = _plan(n_seqs=512, max_len=4096, total_len=512 * 4096)
+    assert p["direct"] == 1 and p["n_ctas"] == 512
+    # forcing one partition is direct; empty batch is direct
+    assert _plan(n_seqs=4, max_len=32768, total_len=4 * 32768, force_parts=1)[1]["direct"] == 1
+    assert _plan(n_seqs=3, max_len=0, total_len=0)[1]["direct"] == 1
+
+
+def test_plan_rejects_bad_input():
+    assert _plan(hq=25)[0] == plan_model.INVALID
+    assert _plan(block_size=8)[0] == plan_model.INVALID
+    assert _plan(d=96)[0] == plan_model.INVALID
+    assert _plan(n_seqs=2, max_len=10, total_len=30)[0] == plan_model.INVALID
+    assert _plan(hq=48, hkv=4)[0] == plan_model.INVALID  # group of 12 > 8
