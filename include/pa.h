@@ -1,0 +1,247 @@
+/*
+ * pa.h -- C ABI of the paged decode-attention library (libpa.so) for GB300.
+ *
+ * One decode step of attention over a paged K/V cache: for every sequence,
+ * one query token per query head attends to that sequence's K/V rows, which
+ * are gathered through a per-sequence block table of fixed-size blocks kept
+ * in one pool.  Sources (page title + section):
+ *
+ *  [P1] "feat: add paged-attention monolithic decode-only AR foundation"
+ *       (lucebox pull 555): Summary (allocator; the decode op for GQA with
+ *       F16/Q4_0/Q8_0 K/V; Q quantised once per step; f16 partials; an
+ *       occupancy-aware partition count with a stable split-softmax merge),
+ *       Scope (unsupported combinations fail explicitly), Benchmark results
+ *       (dead partitions of short sequences), Validation (empty sequences,
+ *       page boundaries, shuffled blocks, corrupt block-table bounds guards).
+ *  [P4] "fix(paged-attention): use 64-bit pool offsets in the fused decode
+ *       kernels" (mlxcel issue 2153): Proposed Solution (the pool offset is
+ *       widened to 64 bits before the multiply; tables stay int32; an
+ *       oversize launch is refused by name instead of wrapping).
+ *
+ * Conventions for every call:
+ *  - All device memory (pools, Q, q8_1, tables, lengths, partials, output,
+ *    status word) is allocated and owned by the caller.  The library never
+ *    allocates or frees device memory and never synchronises, except
+ *    pa_status_read, which synchronises its stream by design.
+ *  - Device pointers are plain pointers into the current device's memory;
+ *    every kernel is launched asynchronously on the given stream.
+ *  - Return value: PA_OK or a negative PA_ERR_* code.  On failure nothing is
+ *    launched and no caller buffer is touched; pa_last_error() then names the
+ *    entry point and the reason (thread-local text).  No C++ exception ever
+ *    crosses this interface.
+ *
+ * Data layouts (block = 32 values along the head dimension d):
+ *  - F16 row:  d IEEE binary16 values (2*d bytes).
+ *  - Q8_0 row: d/32 blocks of 34 bytes: f16 scale, 32 int8; value = q*scale.
+ *  - Q4_0 row: d/32 blocks of 18 bytes: f16 scale, 16 bytes of nibbles;
+ *    value j < 16 is the low nibble of byte j, value j+16 its high nibble;
+ *    value = (nibble - 8) * scale.
+ *  - q8_1 row: d/32 blocks of 36 bytes: f16 d, f16 s, 32 int8 q;
+ *    value = q * d, s = d * sum(q).
+ *  - A pool is token-major bytes [n_blocks][block_size][hkv][row_bytes]; the
+ *    row of (block b, slot j, K/V head g) starts at byte
+ *    (((uint64_t)b * block_size + j) * hkv + g) * row_bytes.
+ *  - Block table: int32 [n_seqs][table_stride]; token t of sequence s lives
+ *    in block table[s][t / block_size], slot t % block_size.
+ *  - Query head h reads K/V head h / (hq / hkv).
+ */
+#ifndef PA_H
+#define PA_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* The CUDA runtime's stream handle (identical to cudaStream_t); NULL is the
+ * legacy default stream. */
+typedef struct CUstream_st *pa_stream_t;
+
+/* ------------------------------------------------------------- codes */
+#define PA_OK 0
+#define PA_ERR_INVALID (-1)       /* bad or unsupported argument */
+#define PA_ERR_NOMEM (-2)         /* allocator: request exceeds the free count */
+#define PA_ERR_STALE (-3)         /* allocator: bad, stale or duplicate handle */
+#define PA_ERR_CUDA (-4)          /* a CUDA runtime call or launch failed */
+#define PA_ERR_CORRUPT_TABLE (-5) /* device guard saw a block id outside the pool */
+#define PA_ERR_RANGE (-6)         /* a size beyond a documented limit */
+
+/* Device status word bits (written by the kernels with atomicOr). */
+#define PA_STATUS_CORRUPT_TABLE 1 /* a block id outside [0, n_pool_blocks) */
+
+typedef enum { PA_F16 = 0, PA_Q8_0 = 1, PA_Q4_0 = 2 } pa_type;
+
+/* Name of a return code ("PA_OK", "PA_ERR_INVALID", ...); never NULL. */
+const char *pa_strerror(int code);
+/* Text of the last failure on this thread: "<entry point>: <reason>". */
+const char *pa_last_error(void);
+/* Bytes of one K or V row of d values of the given type; 0 if unsupported. */
+uint64_t pa_row_bytes(pa_type type, uint32_t d);
+
+/* ------------------------------------------------------- allocator
+ * [P1] Summary: an exact pool of fixed-size blocks; allocation is
+ * transactional, stale handles are detected, release is immediate.
+ * Host-only; the object is owned by the library (create/destroy) and is not
+ * thread-safe (one owner thread, or external locking).
+ * Policy: ids 0..n-1 on a LIFO free stack (a fresh pool hands out 0, 1, 2,
+ * ...).  A handle is (generation << 32) | block id; generations start at 1,
+ * advance by one on release and skip 0 on wrap, so 0 is never a valid
+ * handle. */
+typedef uint64_t pa_handle;
+typedef struct pa_pool pa_pool;
+
+/* n_blocks in [1, 2^31 - 1].  *out receives the pool.  PA_ERR_INVALID on a
+ * bad count or NULL out; PA_ERR_NOMEM if host memory runs out. */
+int pa_pool_create(uint32_t n_blocks, pa_pool **out);
+void pa_pool_destroy(pa_pool *pool);
+/* All or nothing: n handles into out[0..n), or PA_ERR_NOMEM with the pool
+ * and out untouched when n exceeds the free count.  n == 0 is a no-op. */
+int pa_pool_alloc(pa_pool *pool, uint32_t n, pa_handle *out);
+/* Validates every handle first (id in range, block live, generation current,
+ * no handle listed twice); any failure returns PA_ERR_STALE and releases
+ * nothing.  Otherwise releases them in order; each block is reusable at
+ * once and the last one released is the next one handed out. */
+int pa_pool_free(pa_pool *pool, uint32_t n, const pa_handle *handles);
+/* The int32 block id to write into a block table. */
+int32_t pa_handle_block(pa_handle h);
+uint32_t pa_pool_free_count(const pa_pool *pool);
+uint32_t pa_pool_capacity(const pa_pool *pool);
+
+/* ------------------------------------------------------- Q pre-pass
+ * [P1] Summary: Q is quantised once per step by a pre-pass, and the
+ * quantised-K dot products use it.  q: float32 [n_rows][d] (device);
+ * q8_1: n_rows * d/32 blocks of 36 bytes (device).  Per block of 32, in
+ * float32: amax = max|x|, d = amax / 127, q = clamp(roundf(x / d), -127,
+ * 127) (IEEE division, ties away from zero), d = q = 0 for an all-zero
+ * block; stores f16_rn(d) and f16_rn(d * sum(q)).  Inputs must be finite.
+ * d must be a multiple of 32; n_rows == 0 is a no-op.
+ * PA_ERR_INVALID / PA_ERR_CUDA. */
+int pa_quantize_q(const float *q, void *q8_1, uint32_t n_rows, uint32_t d, pa_stream_t stream);
+
+/* ------------------------------------------------------- planner
+ * [P1] Summary and Benchmark results: occupancy-aware context partitioning;
+ * dead partitions of short sequences are sized by the longest one, so this
+ * rule sizes partitions by the total live work instead.  The rule (pure
+ * integer function, host only):
+ *  - partitions are multiples of 32 tokens;
+ *  - force_parts > 0: part_tokens = roundup(ceil(max_len / force_parts), 32);
+ *  - else part_tokens = roundup(ceil(total_len / (sm_count * ctas_per_sm)),
+ *    32), clamped to [128, roundup(max_len, 32)];
+ *  - n_parts = ceil(max_len / part_tokens); direct = (n_parts == 1): no
+ *    partials, the decode kernel writes the output;
+ *  - n_ctas = n_seqs when direct, else min(n_seqs * n_parts,
+ *    ceil(total_len / part_tokens) + n_seqs) (>= the live partitions);
+ *  - partial buffers: part_o f16 [n_seqs][hq][n_parts][d] and part_ml
+ *    float32 [n_seqs][hq][n_parts][2] (0 bytes when direct).
+ * Limits: block_size 16 or 32, d 128 or 256, hq a multiple of hkv with
+ * hq / hkv <= 8, total_len <= n_seqs * max_len.  PA_ERR_INVALID otherwise. */
+typedef struct {
+    uint32_t n_seqs, max_len;
+    uint64_t total_len;          /* sum of the sequence lengths */
+    uint32_t block_size, hq, hkv, d;
+    pa_type k_type, v_type;
+    int32_t sm_count, ctas_per_sm;
+    int32_t force_parts;         /* 0 = automatic */
+} pa_plan_in;
+
+typedef struct {
+    uint32_t part_tokens, n_parts, direct, n_ctas;
+    uint64_t part_o_bytes, part_ml_bytes;
+} pa_plan_t;
+
+int pa_plan(const pa_plan_in *in, pa_plan_t *out);
+/* Fills sm_count and ctas_per_sm of the current device for the decode
+ * kernel that pa_decode_partial would choose for these shapes.
+ * PA_ERR_INVALID / PA_ERR_CUDA. */
+int pa_query_occupancy(const pa_plan_in *in, int32_t *sm_count, int32_t *ctas_per_sm);
+
+/* ------------------------------------------------------- decode
+ * [P1] Summary / [P4] Proposed Solution.  For sequence s of length L_s and
+ * query head h (g = h / (hq/hkv)): scores s_t = scale * <Qhat_h, Khat_t,g>
+ * over t < L_s, p = softmax(s), O[s][h] = sum_t p_t * Vhat_t,g.  Qhat is
+ * the float32 query for F16 K and the q8_1 row otherwise; Khat / Vhat are
+ * the dequantised rows.  L_s == 0 gives O = 0.  Only the first
+ * ceil(L_s / block_size) table entries of a sequence and only slots < L_s
+ * are read.
+ * Partitioned plans write, for each live partition p of each (s, h),
+ * part_o[s][h][p][:] = (sum over the partition of 2^(s2_t - m) V_t) / l in
+ * f16 and part_ml[s][h][p] = (m, l), where s2_t = s_t * log2(e), m is the
+ * partition maximum of s2_t and l = sum 2^(s2_t - m); pa_merge then forms
+ * O.  Direct plans write out directly and touch no partial.
+ * A block id outside [0, n_pool_blocks) is never dereferenced: the kernel
+ * sets PA_STATUS_CORRUPT_TABLE in *status and treats that block's tokens as
+ * absent (pa_status_read reports it).  Pool offsets are 64-bit throughout:
+ * pools past 2^32 elements are supported. */
+typedef struct {
+    const void *k_pool, *v_pool;     /* device, token-major pools, 16-byte aligned */
+    uint64_t n_pool_blocks;          /* 1 .. 2^31 */
+    const int32_t *block_table;      /* device int32 [n_seqs][table_stride] */
+    uint32_t table_stride;
+    const int32_t *seq_lens;         /* device int32 [n_seqs], 0 <= L <= table_stride*block_size */
+    const void *q;                   /* device: float32 [n_seqs][hq][d] for F16 K,
+                                        q8_1 [n_seqs][hq][d/32] otherwise */
+    float scale;                     /* softmax scale; callers pass 1/sqrt(d) */
+    void *part_o;                    /* device f16 [n_seqs][hq][n_parts][d] (unused if direct) */
+    float *part_ml;                  /* device float32 [n_seqs][hq][n_parts][2] */
+    float *out;                      /* device float32 [n_seqs][hq][d] (written if direct) */
+    int32_t *status;                 /* device int32 status word (required) */
+    uint32_t n_seqs, hq, hkv, d, block_size;
+    pa_type k_type, v_type;
+    uint32_t flags;                  /* PA_FLAG_* */
+} pa_decode_args;
+
+/* flags: choose the kernel.  0 = the fast sm_103a kernel where it supports
+ * the shapes, else the plain kernel; PA_FLAG_PLAIN forces the plain kernel
+ * (one warp per query head, CUDA cores), kept as a second implementation. */
+#define PA_FLAG_PLAIN 1u
+
+int pa_decode_partial(const pa_decode_args *args, const pa_plan_t *plan, pa_stream_t stream);
+
+/* Merge ([P1] Summary: stable split-softmax merge).  For each (s, h) with
+ * n_live = ceil(L_s / part_tokens) live partitions: M = max m_p over
+ * partitions with l_p > 0, w_p = l_p 2^(m_p - M), out = sum w_p o_p /
+ * sum w_p; partitions with l_p == 0 are skipped and no live partition gives
+ * 0.  Layouts as in pa_decode_args.  PA_ERR_INVALID for a direct plan
+ * (nothing to merge).  Indexing is 64-bit; PA_ERR_RANGE if the partial
+ * buffer exceeds 2^40 elements. */
+int pa_merge(const void *part_o, const float *part_ml, const int32_t *seq_lens, float *out,
+             uint32_t n_seqs, uint32_t hq, uint32_t d, const pa_plan_t *plan,
+             pa_stream_t stream);
+
+/* One full decode step on the device: pa_quantize_q (quantised K only, into
+ * q8_1_scratch of n_seqs*hq*d/32*36 bytes), pa_decode_partial, and pa_merge
+ * unless the plan is direct.  args->q must point at the float32 query; the
+ * call substitutes q8_1_scratch for the kernel.  Same errors as the parts. */
+int pa_decode_step(const pa_decode_args *args, const pa_plan_t *plan, void *q8_1_scratch,
+                   pa_stream_t stream);
+
+/* The same step with the query taken from and the output returned to HOST
+ * memory: copies q_host (float32 [n_seqs][hq][d]) into args->q (device),
+ * runs pa_decode_step, and copies args->out back into out_host, all on
+ * `stream` (page-locked host buffers make the copies asynchronous).  The
+ * caller synchronises before reading out_host. */
+int pa_decode_step_host(const float *q_host, float *out_host, const pa_decode_args *args,
+                        const pa_plan_t *plan, void *q8_1_scratch, pa_stream_t stream);
+
+/* Reads the status word into *host_out (synchronising `stream`); reset != 0
+ * clears it afterwards.  Returns PA_ERR_CORRUPT_TABLE if the corrupt-table
+ * bit is set, PA_OK otherwise, PA_ERR_CUDA on a runtime failure. */
+int pa_status_read(int32_t *dev_status, pa_stream_t stream, int32_t *host_out, int reset);
+
+/* Debug ([P4] Acceptance Criteria: the offsets must be 64-bit).  Writes the
+ * byte offset of every row the decode step reads into offsets, a device
+ * uint64 array [n_seqs][max_tokens][hkv]: entry (s, t, g) for t < L_s is the
+ * offset of that row in a pool of row_bytes-sized rows, computed by the same
+ * device routine the decode kernels use; other entries are UINT64_MAX.
+ * Out-of-pool block ids also give UINT64_MAX and set PA_STATUS_CORRUPT_TABLE. */
+int pa_debug_row_offsets(const int32_t *block_table, uint32_t table_stride,
+                         const int32_t *seq_lens, uint32_t n_seqs, uint32_t max_tokens,
+                         uint32_t block_size, uint32_t hkv, uint64_t row_bytes,
+                         uint64_t n_pool_blocks, uint64_t *offsets, int32_t *status,
+                         pa_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* PA_H */

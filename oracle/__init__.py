@@ -91,6 +91,9 @@ def lib():
                                    ctypes.c_int64, ctypes.c_uint32, ctypes.c_uint32,
                                    ctypes.c_void_p]
             L.or_merge.restype = ctypes.c_int
+            L.or_vmax_units.argtypes = [ctypes.POINTER(OrArgs), ctypes.c_void_p, ctypes.c_int64,
+                                        ctypes.POINTER(ctypes.c_double)]
+            L.or_vmax_units.restype = ctypes.c_int
             _lib = L
     return _lib
 
@@ -154,8 +157,44 @@ class OracleError(RuntimeError):
         self.rc = rc
 
 
-def decode(k_pool: np.ndarray, v_pool: np.ndarray, block_table: np.ndarray,
-           seq_lens: np.ndarray, q: np.ndarray, *, hkv: int, block_size: int,
+def _args(k_pool, v_pool, block_table, seq_lens, q, hkv, block_size, k_type, v_type, scale):
+    q = np.ascontiguousarray(q, dtype=np.float32)
+    S, hq, d = q.shape
+    k_pool = np.ascontiguousarray(k_pool).view(np.uint8)
+    v_pool = np.ascontiguousarray(v_pool).view(np.uint8)
+    bt = np.ascontiguousarray(block_table, dtype=np.int32)
+    sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    krb, vrb = row_bytes(k_type, d), row_bytes(v_type, d)
+    n_blocks = k_pool.size // (block_size * hkv * krb)
+    assert v_pool.size // (block_size * hkv * vrb) == n_blocks
+    a = OrArgs(k_pool=_ptr(k_pool), v_pool=_ptr(v_pool), n_pool_blocks=n_blocks,
+               block_table=_ptr(bt), table_stride=bt.shape[1] if bt.ndim == 2 else bt.size,
+               seq_lens=_ptr(sl), q=_ptr(q),
+               scale=float(1.0 / np.sqrt(d)) if scale is None else float(scale),
+               n_seqs=S, hq=hq, hkv=hkv, d=d, block_size=block_size,
+               k_type=int(k_type), v_type=int(v_type))
+    keep = (q, k_pool, v_pool, bt, sl)  # arrays the struct points into
+    return a, keep
+
+
+def vmax(k_pool, v_pool, block_table, seq_lens, q, *, hkv, block_size, k_type, v_type,
+         units=None) -> float:
+    """max |Vhat| over the live rows that the listed units (default: every
+    sequence and K/V head) read."""
+    a, keep = _args(k_pool, v_pool, block_table, seq_lens, q, hkv, block_size, k_type, v_type,
+                    None)
+    S, hq, _ = keep[0].shape
+    if units is None:
+        units = [(s, h) for s in range(S) for h in range(0, hq, hq // hkv)]
+    u = np.ascontiguousarray(np.asarray(units, dtype=np.int32).reshape(-1, 2))
+    out = ctypes.c_double(0.0)
+    rc = lib().or_vmax_units(ctypes.byref(a), _ptr(u), u.shape[0], ctypes.byref(out))
+    if rc != OR_OK:
+        raise OracleError(rc)
+    return float(out.value)
+
+
+def decode(k_pool, v_pool, block_table, seq_lens, q, *, hkv: int, block_size: int,
            k_type: int, v_type: int, scale: float | None = None, units=None,
            part_tokens: int = 0, n_threads: int | None = None) -> np.ndarray:
     """Float64 decode attention.
@@ -166,27 +205,14 @@ def decode(k_pool: np.ndarray, v_pool: np.ndarray, block_table: np.ndarray,
     (seq, head) pairs; default every pair.  Returns float64 [n_units][D]
     (or [S][Hq][D] when units is None).  part_tokens > 0 selects the
     partitioned-with-merge form of the same definition."""
-    q = np.ascontiguousarray(q, dtype=np.float32)
-    S, hq, d = q.shape
-    k_pool = np.ascontiguousarray(k_pool).view(np.uint8)
-    v_pool = np.ascontiguousarray(v_pool).view(np.uint8)
-    bt = np.ascontiguousarray(block_table, dtype=np.int32)
-    sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
-    krb, vrb = row_bytes(k_type, d), row_bytes(v_type, d)
-    per_block_k = block_size * hkv * krb
-    n_blocks = k_pool.size // per_block_k
-    assert v_pool.size // (block_size * hkv * vrb) == n_blocks
+    a, keep = _args(k_pool, v_pool, block_table, seq_lens, q, hkv, block_size, k_type, v_type,
+                    scale)
+    S, hq, d = keep[0].shape
     full = units is None
     if full:
         units = [(s, h) for s in range(S) for h in range(hq)]
     u = np.ascontiguousarray(np.asarray(units, dtype=np.int32).reshape(-1, 2))
     out = np.zeros((u.shape[0], d), dtype=np.float64)
-    a = OrArgs(k_pool=_ptr(k_pool), v_pool=_ptr(v_pool), n_pool_blocks=n_blocks,
-               block_table=_ptr(bt), table_stride=bt.shape[1] if bt.ndim == 2 else bt.size,
-               seq_lens=_ptr(sl), q=_ptr(q),
-               scale=float(1.0 / np.sqrt(d)) if scale is None else float(scale),
-               n_seqs=S, hq=hq, hkv=hkv, d=d, block_size=block_size,
-               k_type=int(k_type), v_type=int(v_type))
     if n_threads is None:
         n_threads = max(1, len(os.sched_getaffinity(0)))
     rc = lib().or_decode_units(ctypes.byref(a), _ptr(u), u.shape[0], int(part_tokens),

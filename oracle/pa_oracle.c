@@ -512,3 +512,35 @@ int or_merge(const uint16_t *o, const float *ml, const int32_t *n_live,
     }
     return OR_OK;
 }
+
+/* max |Vhat| over the live rows the listed (seq, head) units read: the scale
+ * of the accuracy gate (max|err| <= tol * max|V| over the live tokens). */
+int or_vmax_units(const or_args *a, const int32_t *units, int64_t n_units, double *vmax)
+{
+    int rc = check_args(a);
+    if (rc != OR_OK)
+        return rc;
+    double *row = (double *)malloc(sizeof(double) * a->d);
+    if (!row)
+        return OR_ERR_NOMEM;
+    uint64_t vrb = or_row_bytes(a->v_type, a->d);
+    double mx = 0.0;
+    for (int64_t u = 0; u < n_units; ++u) {
+        uint32_t s = (uint32_t)units[2 * u], h = (uint32_t)units[2 * u + 1];
+        uint32_t g = h / (a->hq / a->hkv);
+        int32_t L = a->seq_lens[s];
+        for (int32_t t = 0; t < L; ++t) {
+            uint64_t off;
+            if (token_row(a, s, (uint32_t)t, g, vrb, &off)) {
+                free(row);
+                return OR_ERR_CORRUPT;
+            }
+            or_dequant_row(a->v_type, a->v_pool + off, a->d, row);
+            for (uint32_t i = 0; i < a->d; ++i)
+                if (fabs(row[i]) > mx) mx = fabs(row[i]);
+        }
+    }
+    free(row);
+    *vmax = mx;
+    return OR_OK;
+}

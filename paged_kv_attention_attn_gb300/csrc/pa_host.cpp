@@ -1,0 +1,227 @@
+// pa_host.cpp -- host-only parts of the C ABI: error reporting, the fixed-block
+// allocator and the partition planner.  No device code and no allocation of
+// device memory here.
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "pa_internal.h"
+
+namespace pa {
+
+static thread_local char g_last_error[512] = "";
+
+int fail(int code, const char *entry, const char *fmt, ...)
+{
+    char msg[400];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(msg, sizeof msg, fmt, ap);
+    va_end(ap);
+    snprintf(g_last_error, sizeof g_last_error, "%s: %s", entry, msg);
+    return code;
+}
+
+int cuda_check(cudaError_t e, const char *entry, const char *what)
+{
+    if (e == cudaSuccess)
+        return PA_OK;
+    return fail(PA_ERR_CUDA, entry, "%s: %s", what, cudaGetErrorString(e));
+}
+
+}  // namespace pa
+
+using pa::fail;
+
+extern "C" const char *pa_strerror(int code)
+{
+    switch (code) {
+    case PA_OK: return "PA_OK";
+    case PA_ERR_INVALID: return "PA_ERR_INVALID";
+    case PA_ERR_NOMEM: return "PA_ERR_NOMEM";
+    case PA_ERR_STALE: return "PA_ERR_STALE";
+    case PA_ERR_CUDA: return "PA_ERR_CUDA";
+    case PA_ERR_CORRUPT_TABLE: return "PA_ERR_CORRUPT_TABLE";
+    case PA_ERR_RANGE: return "PA_ERR_RANGE";
+    default: return "PA_ERR_UNKNOWN";
+    }
+}
+
+extern "C" const char *pa_last_error(void) { return pa::g_last_error; }
+
+extern "C" uint64_t pa_row_bytes(pa_type type, uint32_t d)
+{
+    if (d == 0 || d % 32 != 0)
+        return 0;
+    switch (type) {
+    case PA_F16: return 2ull * d;
+    case PA_Q8_0: return (uint64_t)(d / 32) * 34ull;
+    case PA_Q4_0: return (uint64_t)(d / 32) * 18ull;
+    default: return 0;
+    }
+}
+
+// ------------------------------------------------------------------ allocator
+//
+// Fixed-block pool with transactional allocation, stale-handle detection and
+// immediate release ("feat: add paged-attention monolithic decode-only AR
+// foundation", lucebox pull 555, Summary).  LIFO free stack; handle =
+// (generation << 32) | id; generation starts at 1, advances on release and
+// skips 0 on wrap.
+
+struct pa_pool {
+    uint32_t n;
+    std::vector<uint32_t> gen;
+    std::vector<uint8_t> live;
+    std::vector<uint32_t> stack;  // back() is the next id handed out
+    std::vector<uint8_t> mark;    // scratch for duplicate detection in free
+};
+
+extern "C" int pa_pool_create(uint32_t n_blocks, pa_pool **out)
+{
+    static const char *E = "pa_pool_create";
+    if (!out)
+        return fail(PA_ERR_INVALID, E, "out is NULL");
+    *out = nullptr;
+    if (n_blocks == 0 || n_blocks > 0x7fffffffu)
+        return fail(PA_ERR_INVALID, E, "n_blocks %u outside [1, 2^31-1]", n_blocks);
+    pa_pool *p = new (std::nothrow) pa_pool;
+    if (!p)
+        return fail(PA_ERR_NOMEM, E, "host allocation failed");
+    try {
+        p->n = n_blocks;
+        p->gen.assign(n_blocks, 1u);
+        p->live.assign(n_blocks, 0);
+        p->mark.assign(n_blocks, 0);
+        p->stack.resize(n_blocks);
+        for (uint32_t i = 0; i < n_blocks; ++i)
+            p->stack[i] = n_blocks - 1 - i;
+    } catch (...) {
+        delete p;
+        return fail(PA_ERR_NOMEM, E, "host allocation failed");
+    }
+    *out = p;
+    return PA_OK;
+}
+
+extern "C" void pa_pool_destroy(pa_pool *pool) { delete pool; }
+
+extern "C" int pa_pool_alloc(pa_pool *pool, uint32_t n, pa_handle *out)
+{
+    static const char *E = "pa_pool_alloc";
+    if (!pool || (n && !out))
+        return fail(PA_ERR_INVALID, E, "NULL pool or out");
+    if (n > pool->stack.size())
+        return fail(PA_ERR_NOMEM, E, "%u blocks requested, %zu free", n, pool->stack.size());
+    for (uint32_t i = 0; i < n; ++i) {
+        uint32_t id = pool->stack.back();
+        pool->stack.pop_back();
+        pool->live[id] = 1;
+        out[i] = ((uint64_t)pool->gen[id] << 32) | id;
+    }
+    return PA_OK;
+}
+
+extern "C" int pa_pool_free(pa_pool *pool, uint32_t n, const pa_handle *h)
+{
+    static const char *E = "pa_pool_free";
+    if (!pool || (n && !h))
+        return fail(PA_ERR_INVALID, E, "NULL pool or handles");
+    // validate everything first; marks catch a handle listed twice
+    uint32_t bad = n;
+    for (uint32_t i = 0; i < n; ++i) {
+        uint64_t id = h[i] & 0xffffffffull;
+        uint32_t g = (uint32_t)(h[i] >> 32);
+        if (id >= pool->n || !pool->live[id] || pool->gen[id] != g || pool->mark[id]) {
+            bad = i;
+            break;
+        }
+        pool->mark[id] = 1;
+    }
+    for (uint32_t i = 0; i < bad; ++i)
+        pool->mark[h[i] & 0xffffffffull] = 0;
+    if (bad < n)
+        return fail(PA_ERR_STALE, E, "handle %u (0x%llx) is stale, out of range or repeated",
+                    bad, (unsigned long long)h[bad]);
+    for (uint32_t i = 0; i < n; ++i) {
+        uint32_t id = (uint32_t)(h[i] & 0xffffffffull);
+        pool->live[id] = 0;
+        uint32_t g = pool->gen[id] + 1;
+        pool->gen[id] = g ? g : 1;
+        pool->stack.push_back(id);
+    }
+    return PA_OK;
+}
+
+extern "C" int32_t pa_handle_block(pa_handle h) { return (int32_t)(uint32_t)(h & 0xffffffffull); }
+
+extern "C" uint32_t pa_pool_free_count(const pa_pool *pool)
+{
+    return pool ? (uint32_t)pool->stack.size() : 0;
+}
+
+extern "C" uint32_t pa_pool_capacity(const pa_pool *pool) { return pool ? pool->n : 0; }
+
+// -------------------------------------------------------------------- planner
+
+static uint64_t cdiv(uint64_t a, uint64_t b) { return (a + b - 1) / b; }
+static uint64_t roundup(uint64_t a, uint64_t b) { return cdiv(a, b) * b; }
+
+extern "C" int pa_plan(const pa_plan_in *in, pa_plan_t *out)
+{
+    static const char *E = "pa_plan";
+    const uint64_t TILE = 32, MIN_PART = 128;
+    if (!in || !out)
+        return fail(PA_ERR_INVALID, E, "NULL argument");
+    if (in->n_seqs < 1)
+        return fail(PA_ERR_INVALID, E, "n_seqs must be >= 1");
+    if (in->block_size != 16 && in->block_size != 32)
+        return fail(PA_ERR_INVALID, E, "block_size %u unsupported (16 or 32)", in->block_size);
+    if (in->hkv < 1 || in->hq < in->hkv || in->hq % in->hkv || in->hq / in->hkv > 8)
+        return fail(PA_ERR_INVALID, E, "hq %u / hkv %u: need hq %% hkv == 0 and a group <= 8",
+                    in->hq, in->hkv);
+    if (in->d != 128 && in->d != 256)
+        return fail(PA_ERR_INVALID, E, "d %u unsupported (128 or 256)", in->d);
+    if ((unsigned)in->k_type > 2u || (unsigned)in->v_type > 2u)
+        return fail(PA_ERR_INVALID, E, "unknown K/V type");
+    if (in->sm_count < 1 || in->ctas_per_sm < 1 || in->force_parts < 0)
+        return fail(PA_ERR_INVALID, E, "sm_count / ctas_per_sm / force_parts out of range");
+    if (in->total_len < in->max_len || in->total_len > (uint64_t)in->n_seqs * in->max_len)
+        return fail(PA_ERR_INVALID, E, "total_len inconsistent with max_len and n_seqs");
+    uint64_t part, n_parts;
+    if (in->max_len == 0) {
+        part = TILE;
+        n_parts = 1;
+    } else if (in->force_parts > 0) {
+        part = roundup(cdiv(in->max_len, (uint64_t)in->force_parts), TILE);
+        n_parts = cdiv(in->max_len, part);
+    } else {
+        uint64_t slots = (uint64_t)in->sm_count * (uint64_t)in->ctas_per_sm;
+        part = roundup(cdiv(in->total_len, slots), TILE);
+        if (part < MIN_PART) part = MIN_PART;
+        uint64_t cap = roundup(in->max_len, TILE);
+        if (part > cap) part = cap;
+        n_parts = cdiv(in->max_len, part);
+    }
+    pa_plan_t p;
+    memset(&p, 0, sizeof p);
+    p.part_tokens = (uint32_t)part;
+    p.n_parts = (uint32_t)n_parts;
+    p.direct = n_parts == 1;
+    if (p.direct) {
+        p.n_ctas = in->n_seqs;
+    } else {
+        uint64_t a = (uint64_t)in->n_seqs * n_parts;
+        uint64_t b = cdiv(in->total_len, part) + in->n_seqs;
+        uint64_t n = a < b ? a : b;
+        if (n > 0x7fffffffull)
+            return fail(PA_ERR_RANGE, E, "grid of %llu CTAs exceeds 2^31-1", (unsigned long long)n);
+        p.n_ctas = (uint32_t)n;
+        p.part_o_bytes = (uint64_t)in->n_seqs * in->hq * n_parts * in->d * 2ull;
+        p.part_ml_bytes = (uint64_t)in->n_seqs * in->hq * n_parts * 8ull;
+    }
+    *out = p;
+    return PA_OK;
+}
