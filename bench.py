@@ -1,0 +1,421 @@
+"""Benchmark of one paged decode-attention step on GB300.
+
+Workload (default): the uniform batch at Qwen attention dims -- 8 sequences
+of 131,072 tokens, D=256, Hq=24, Hkv=4, 16-token blocks, Q4_0 K/V from
+N(0,1), fp32 Q from N(0,1) quantised to q8_1, block tables randomly
+interleaved in one pool ("feat: add paged-attention monolithic decode-only AR
+foundation", lucebox pull 555, Benchmark results).  A step is the whole hot
+path: the q8_1 pre-pass, the decode kernel and the merge, on one stream.
+
+Prints ONE JSON line (rank 0).  `value` is achieved algorithmic HBM
+bandwidth in GB/s over all ranks (bytes every rank's steps must move / the
+slowest rank's time); `us_per_step` is the step time.  The roofline object
+reports the decode kernel alone, timed with CUDA events around its launch
+inside the timed loop.  `--impl reference` times the float64 CPU oracle on
+a bounded sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = ("paged decode-attn µs/step and achieved HBM GB/s vs GB300 peak "
+          "(Q4_0 K/V, 1 GPU)")
+WORKLOADS = {
+    "uniform-q4_0-b8x131072": lambda: synth.uniform_spec(8, 131072, synth.Q4_0),
+    "uniform-q4_0-b4x32768": lambda: synth.uniform_spec(4, 32768, synth.Q4_0),
+    "ragged-q4_0-128k+7x8k": lambda: synth.ragged_spec(synth.Q4_0),
+    "sweep-f16-b4x32768": lambda: synth.dtype_sweep_spec(synth.F16),
+    "sweep-q8_0-b4x32768": lambda: synth.dtype_sweep_spec(synth.Q8_0),
+    "sweep-q4_0-b4x32768": lambda: synth.dtype_sweep_spec(synth.Q4_0),
+}
+DEFAULT_WORKLOAD = "uniform-q4_0-b8x131072"
+L2_BYTES = 129 * 2**20
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def algorithmic_bytes(spec, plan) -> dict:
+    """Bytes the method must move in one step, by class."""
+    S, hq, d = spec.n_seqs, spec.hq, spec.d
+    krb, vrb = synth.row_bytes(spec.k_type, d), synth.row_bytes(spec.v_type, d)
+    lens = spec.seq_lens
+    kv = sum(lens) * spec.hkv * (krb + vrb)
+    table = sum(math.ceil(L / spec.block_size) for L in lens) * 4
+    q_f32 = S * hq * d * 4
+    q81 = S * hq * d // 32 * 36
+    quantised = spec.k_type != synth.F16
+    prepass = (q_f32 + q81) if quantised else 0
+    q_read = q81 if quantised else q_f32
+    out = S * hq * d * 4
+    if plan.direct:
+        part_w = part_r = 0
+        dec_out = out
+    else:
+        live = sum(math.ceil(L / plan.part_tokens) for L in lens)
+        part_w = part_r = live * hq * (2 * d + 8)
+        dec_out = part_w
+    merge = 0 if plan.direct else part_r + out + S * 4
+    decode = kv + table + q_read + dec_out + S * 4
+    return dict(kv=kv, table=table, prepass=prepass, decode=decode, merge=merge,
+                step=prepass + decode + merge)
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples while the timed region runs."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        mx = [num(r[2]) for r in rows if num(r[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4)
+                          if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def reduce_max(x: float, world: int, device) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def aggregate(bytes_per_step_per_rank: float, steps: int, world: int, max_seconds: float):
+    """Whole-job GB/s: bytes all ranks moved over the slowest rank's time."""
+    return bytes_per_step_per_rank * steps * world / max_seconds / 1e9
+
+
+def traffic_from_profiles(kernel_name: str):
+    """dram bytes per launch from a committed ncu summary, if it was taken on
+    the current kernel source; else None."""
+    p = os.path.join(ROOT, "profiles", "decode_traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p))
+    if d.get("kernel") != kernel_name or d.get("source_sha") != kernel_source_sha():
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+def kernel_source_sha() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "paged_kv_attention_attn_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh", ".h", ".cpp")):
+            h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+# ------------------------------------------------------------------ oracle
+
+def oracle_sample(case_host, spec, seqs, threads):
+    """Times the float64 oracle on sequences `seqs` (all query heads, full
+    context) of the workload; returns (seconds, algorithmic bytes)."""
+    import oracle
+    k, v, bt, sl, q = case_host
+    units = [(s, h) for s in seqs for h in range(spec.hq)]
+    t0 = time.perf_counter()
+    oracle.decode(k, v, bt, sl, q, hkv=spec.hkv, block_size=spec.block_size,
+                  k_type=spec.k_type, v_type=spec.v_type, units=units, n_threads=threads)
+    dt = time.perf_counter() - t0
+    krb, vrb = synth.row_bytes(spec.k_type, spec.d), synth.row_bytes(spec.v_type, spec.d)
+    nbytes = sum(spec.seq_lens[s] * spec.hkv * (krb + vrb) for s in seqs)
+    nbytes += len(seqs) * spec.hq * spec.d * 8
+    return dt, nbytes
+
+
+def host_copy(case):
+    return [case.k_pool.cpu().numpy(), case.v_pool.cpu().numpy(),
+            case.block_table.cpu().numpy(), case.seq_lens.cpu().numpy(), case.q.cpu().numpy()]
+
+
+def run_reference(a, world, rank):
+    """The reference arm: the oracle as it stands, on the host cores."""
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    spec = WORKLOADS[a.workload]()
+    dev = "cuda:0" if torch.cuda.is_available() else "cpu"
+    case = synth.build_case(spec, seed=a.seed, device=dev)
+    host = host_copy(case)
+    del case
+    threads = len(os.sched_getaffinity(0))
+    seqs = [0]  # one sequence, every query head, full context: a bounded sample
+    for _ in range(a.ref_warmup):
+        oracle_sample(host, spec, seqs, threads)
+    tot_t, tot_b = 0.0, 0
+    for _ in range(a.ref_steps):
+        dt, nb = oracle_sample(host, spec, seqs, threads)
+        tot_t += dt
+        tot_b += nb
+    gbs = tot_b / tot_t / 1e9
+    sample = (f"sequence 0 of {spec.n_seqs}, all {spec.hq} query heads, "
+              f"{spec.seq_lens[0]} tokens, per step")
+    line = {"impl": "reference", "metric": METRIC, "value": gbs, "unit": "GB/s",
+            "n_gpus": world, "steps": a.ref_steps, "warmup": a.ref_warmup,
+            "ms_per_step": tot_t / a.ref_steps * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": a.workload, "sample": sample},
+            "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": threads, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------- ours
+
+def run_ours(a, world, rank, local):
+    import paged_kv_attention_attn_gb300 as pa
+    from paged_kv_attention_attn_gb300 import build as pa_build
+    pa_build.build()
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    spec = WORKLOADS[a.workload]()
+    case = synth.build_case(spec, seed=a.seed + 1000 * rank, device=dev)
+    flags = pa.PA_FLAG_PLAIN if a.plain else 0
+    pl = pa.plan(seq_lens=spec.seq_lens, block_size=spec.block_size, hq=spec.hq, hkv=spec.hkv,
+                 d=spec.d, k_type=spec.k_type, v_type=spec.v_type)
+    ws = pa.workspace(pl, n_seqs=spec.n_seqs, hq=spec.hq, d=spec.d, device=dev)
+    args = pa.make_args(k_pool=case.k_pool, v_pool=case.v_pool, block_table=case.block_table,
+                        seq_lens=case.seq_lens, q=case.q, ws=ws, hkv=spec.hkv,
+                        block_size=spec.block_size, k_type=spec.k_type, v_type=spec.v_type,
+                        flags=flags)
+    quantised = spec.k_type != synth.F16
+    dec_args = pa.make_args(k_pool=case.k_pool, v_pool=case.v_pool,
+                            block_table=case.block_table, seq_lens=case.seq_lens,
+                            q=ws.q8_1 if quantised else case.q, ws=ws, hkv=spec.hkv,
+                            block_size=spec.block_size, k_type=spec.k_type,
+                            v_type=spec.v_type, flags=flags)
+    nb = algorithmic_bytes(spec, pl)
+    stream = torch.cuda.current_stream()
+    L = pa.lib()
+    import ctypes
+    p_args, p_plan = ctypes.byref(dec_args), ctypes.byref(pl)
+    sh = stream.cuda_stream
+
+    def step(ev0=None, ev1=None):
+        if quantised:
+            L.pa_quantize_q(case.q.data_ptr(), ws.q8_1.data_ptr(), spec.n_seqs * spec.hq,
+                            spec.d, sh)
+        if ev0 is not None:
+            ev0.record(stream)
+        rc = L.pa_decode_partial(p_args, p_plan, sh)
+        if ev1 is not None:
+            ev1.record(stream)
+        if not pl.direct:
+            L.pa_merge(ws.part_o.data_ptr(), ws.part_ml.data_ptr(), case.seq_lens.data_ptr(),
+                       ws.out.data_ptr(), spec.n_seqs, spec.hq, spec.d, p_plan, sh)
+        return rc
+
+    # correctness of the configuration before timing
+    if step() != 0:
+        raise RuntimeError(L.pa_last_error().decode())
+    torch.cuda.synchronize()
+    assert pa.status_read(ws.status) == 0
+    for _ in range(a.warmup):
+        step()
+    torch.cuda.synchronize()
+
+    K = a.steps
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(K)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    start.record(stream)
+    for k in range(K):
+        step(*evs[k])
+    end.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    total_ms = start.elapsed_time(end)
+    dec_ms = [e0.elapsed_time(e1) for e0, e1 in evs]
+    max_s = reduce_max(total_ms / 1e3, world, dev)
+    value = aggregate(nb["step"], K, world, max_s)
+    ms_per_step = max_s * 1e3 / K
+    dec_avg_ms = sum(dec_ms) / K
+    peak, peak_kind = load_peaks()
+    dec_achieved = nb["decode"] / (dec_avg_ms / 1e3) / 1e9
+
+    # end to end through the public C call with host buffers
+    q_host = case.q.cpu().pin_memory()
+    out_host = torch.empty(ws.out.shape, dtype=torch.float32).pin_memory()
+    qdev = torch.empty_like(case.q)
+    e2e_args = pa.make_args(k_pool=case.k_pool, v_pool=case.v_pool,
+                            block_table=case.block_table, seq_lens=case.seq_lens, q=qdev,
+                            ws=ws, hkv=spec.hkv, block_size=spec.block_size,
+                            k_type=spec.k_type, v_type=spec.v_type, flags=flags)
+    for _ in range(a.warmup):
+        pa.decode_step_host(q_host, out_host, e2e_args, ws)
+    torch.cuda.synchronize()
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(K):
+        pa.decode_step_host(q_host, out_host, e2e_args, ws)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    e2e_s = reduce_max(e0.elapsed_time(e1) / 1e3, world, dev)
+    h2d = q_host.numel() * 4
+    d2h = out_host.numel() * 4
+    e2e = {"value": aggregate(nb["step"], K, world, e2e_s), "unit": "GB/s",
+           "us_per_step": e2e_s * 1e6 / K, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+    cpu = None
+    if world == 1 and not a.no_cpu_baseline:
+        host = host_copy(case)
+        threads = len(os.sched_getaffinity(0))
+        seqs = list(range(min(2, spec.n_seqs)))
+        dt, cb = oracle_sample(host, spec, seqs, threads)
+        cpu = {"value": cb / dt / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
+               "sample": f"sequences {seqs} of {spec.n_seqs}, all {spec.hq} query heads, "
+                         f"full context ({sum(spec.seq_lens[s] for s in seqs)} tokens), "
+                         f"{dt:.2f} s wall"}
+
+    kname = pa.decode_kernel_name(k_type=spec.k_type, v_type=spec.v_type, d=spec.d,
+                                  hq=spec.hq, hkv=spec.hkv, block_size=spec.block_size,
+                                  flags=flags)
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K,
+        "warmup": a.warmup, "ms_per_step": ms_per_step, "us_per_step": ms_per_step * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded N(0,1), see synth/)",
+        "config": {"workload": a.workload, "batch": spec.n_seqs,
+                   "context": max(spec.seq_lens), "d": spec.d, "hq": spec.hq,
+                   "hkv": spec.hkv, "block_size": spec.block_size,
+                   "kv_type": synth.TYPE_LABEL[spec.k_type],
+                   "l2": f"inputs larger than L2: {nb['kv'] / 1e9:.3f} GB of K/V per step",
+                   "kernel": kname, "plan": pl.as_dict(),
+                   "bytes_per_step": nb},
+        "roofline": {"bound": "hbm", "achieved": dec_achieved, "peak": peak, "unit": "GB/s",
+                     "frac": dec_achieved / peak, "peak_kind": peak_kind,
+                     "kernel": kname, "kernel_us": dec_avg_ms * 1e3,
+                     "bytes_per_launch": nb["decode"],
+                     "traffic": traffic_from_profiles(kname)},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": K * ((2 if quantised else 1) + (0 if pl.direct else 1)),
+        "clocks": clk,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD)
+    ap.add_argument("--seed", type=int, default=2001)
+    ap.add_argument("--plain", action="store_true", help="force the plain decode kernel")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ref-steps", type=int, default=None)
+    ap.add_argument("--ref-warmup", type=int, default=None)
+    a = ap.parse_args()
+    a.warmup = max(a.warmup, 3)
+    a.ref_steps = a.ref_steps if a.ref_steps is not None else min(a.steps, 10)
+    a.ref_warmup = a.ref_warmup if a.ref_warmup is not None else min(a.warmup, 3)
+    world, rank, local = dist_setup()
+    if a.impl == "reference":
+        run_reference(a, world, rank)
+    else:
+        run_ours(a, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -198,6 +198,12 @@ typedef struct {
 
 int pa_decode_partial(const pa_decode_args *args, const pa_plan_t *plan, pa_stream_t stream);
 
+/* Name of the decode kernel pa_decode_partial launches for these shapes and
+ * flags ("fast_decode_kernel" or "plain_decode_kernel"); NULL for shapes no
+ * kernel supports.  Host only, no device work. */
+const char *pa_decode_kernel_name(pa_type k_type, pa_type v_type, uint32_t d, uint32_t hq,
+                                  uint32_t hkv, uint32_t block_size, uint32_t flags);
+
 /* Merge ([P1] Summary: stable split-softmax merge).  For each (s, h) with
  * n_live = ceil(L_s / part_tokens) live partitions: M = max m_p over
  * partitions with l_p > 0, w_p = l_p 2^(m_p - M), out = sum w_p o_p /

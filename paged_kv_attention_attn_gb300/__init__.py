@@ -85,6 +85,8 @@ _SIGNATURES = {
                             ctypes.POINTER(_i32)], ctypes.c_int),
     "pa_decode_partial": ([ctypes.POINTER(DecodeArgs), ctypes.POINTER(Plan), _vp],
                           ctypes.c_int),
+    "pa_decode_kernel_name": ([ctypes.c_int, ctypes.c_int, _u32, _u32, _u32, _u32, _u32],
+                              ctypes.c_char_p),
     "pa_merge": ([_vp, _vp, _vp, _vp, _u32, _u32, _u32, ctypes.POINTER(Plan), _vp],
                  ctypes.c_int),
     "pa_decode_step": ([ctypes.POINTER(DecodeArgs), ctypes.POINTER(Plan), _vp, _vp],
@@ -262,6 +264,12 @@ def make_args(*, k_pool, v_pool, block_table, seq_lens, q, ws: Workspace, hkv, b
 
 def decode_partial(args: DecodeArgs, pl: Plan, stream=None) -> None:
     _check(lib().pa_decode_partial(ctypes.byref(args), ctypes.byref(pl), _stream(stream)))
+
+
+def decode_kernel_name(*, k_type, v_type, d, hq, hkv, block_size, flags=0) -> str | None:
+    """Which decode kernel pa_decode_partial would launch for these shapes."""
+    r = lib().pa_decode_kernel_name(k_type, v_type, d, hq, hkv, block_size, flags)
+    return r.decode() if r else None
 
 
 def merge(ws: Workspace, seq_lens: torch.Tensor, stream=None) -> None:

@@ -166,6 +166,16 @@ extern "C" int pa_decode_partial(const pa_decode_args *args, const pa_plan_t *pl
     return launch_decode(args, p, pa::stream_of(stream), E);
 }
 
+extern "C" const char *pa_decode_kernel_name(pa_type kt, pa_type vt, uint32_t d, uint32_t hq,
+                                             uint32_t hkv, uint32_t block_size, uint32_t flags)
+{
+    if (check_shapes(1, hq, hkv, d, block_size, kt, vt, "pa_decode_kernel_name"))
+        return nullptr;
+    if (!(flags & PA_FLAG_PLAIN) && pa::fast_decode_supported(kt, vt, d, hq, hkv, block_size))
+        return "fast_decode_kernel";
+    return "plain_decode_kernel";
+}
+
 extern "C" int pa_merge(const void *part_o, const float *part_ml, const int32_t *seq_lens,
                         float *out, uint32_t n_seqs, uint32_t hq, uint32_t d,
                         const pa_plan_t *plan, pa_stream_t stream)

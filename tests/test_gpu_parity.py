@@ -1,0 +1,224 @@
+"""GPU parity tests at oracle-sized inputs: the CUDA path through the C ABI
+against the float64 oracle, element by element.
+
+Covered: the q8_1 pre-pass bit for bit; the tiny F16 workload; every K/V
+type pair in direct, forced-single, planner and forced-many modes, on both
+kernels; block-boundary lengths including empty sequences; paged ==
+contiguous bit for bit under a shuffled table with poisoned junk blocks;
+run-to-run determinism; the corrupt-table guard; a red control; the 64-bit
+row offsets bit for bit; the merge kernel alone; the host-buffer step."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_attention_attn_gb300 as pa
+import synth
+from tests import helpers as H
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+KERNELS = {"fast": 0, "plain": pa.PA_FLAG_PLAIN}
+TYPES = [synth.F16, synth.Q8_0, synth.Q4_0]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from paged_kv_attention_attn_gb300 import build
+    build.build()
+    oracle.build()
+
+
+def test_quantize_q_bit_exact():
+    g = torch.Generator().manual_seed(3)
+    x = torch.randn(37, 256, generator=g) * torch.rand(37, 1, generator=g) * 50
+    x[0, :32] = 0.0                                 # zero block
+    x[1, :32] = torch.arange(32) - 15.5             # ties after scaling
+    x[2, 0], x[2, 1:32] = 127.0, 2.5                # d = 1: x/d ties round away
+    x[3, 32:64] = 1e-30                             # tiny values
+    got = pa.quantize_q(x.to(DEV)).cpu().numpy()
+    ref = oracle.quantize_q8_1(x.numpy())
+    assert np.array_equal(got, ref)
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("force", [0, 1, 7])
+def test_tiny_f16(kernel, force):
+    case = synth.build_case(synth.tiny_spec(), seed=1000, device=DEV)
+    out, ws, pl, tails = H.run(case, force_parts=force, flags=KERNELS[kernel], canary=True)
+    assert pa.status_read(ws.status) == 0
+    H.check_canaries(tails)
+    H.assert_close(case, out, H.oracle_out(case), H.oracle_vmax(case))
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("kt", TYPES)
+@pytest.mark.parametrize("vt", TYPES)
+@pytest.mark.parametrize("force", [0, 1, 5])
+def test_type_pairs_and_modes(kernel, kt, vt, force):
+    spec = synth.CaseSpec(seq_lens=[600, 37, 0, 257], k_type=kt, v_type=vt, junk=11,
+                          outliers=True, name=f"pair-{kt}{vt}")
+    case = synth.build_case(spec, seed=1100 + 3 * kt + vt, device=DEV)
+    out, ws, pl, tails = H.run(case, force_parts=force, flags=KERNELS[kernel], canary=True)
+    assert pa.status_read(ws.status) == 0
+    H.check_canaries(tails)
+    H.assert_close(case, out, H.oracle_out(case), H.oracle_vmax(case))
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("shape", [dict(d=128, hq=32, hkv=8, block_size=32),
+                                   dict(d=256, hq=8, hkv=8, block_size=16),
+                                   dict(d=128, hq=8, hkv=1, block_size=16)])
+def test_other_head_shapes(kernel, shape):
+    spec = synth.CaseSpec(seq_lens=[333, 64, 1], k_type=synth.F16, v_type=synth.F16, junk=5,
+                          **shape)
+    case = synth.build_case(spec, seed=1200, device=DEV)
+    for force in (0, 3):
+        out, ws, _, _ = H.run(case, force_parts=force, flags=KERNELS[kernel])
+        H.assert_close(case, out, H.oracle_out(case), H.oracle_vmax(case))
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_block_boundary_lengths(kernel):
+    lens = [0, 1, 15, 16, 17, 31, 32, 33, 200, 127, 128, 129, 255, 256, 257]
+    spec = synth.CaseSpec(seq_lens=lens, k_type=synth.Q4_0, v_type=synth.Q4_0, junk=13)
+    case = synth.build_case(spec, seed=1300, device=DEV)
+    for force in (0, 2):
+        out, ws, _, tails = H.run(case, force_parts=force, flags=KERNELS[kernel], canary=True)
+        H.check_canaries(tails)
+        got = out.cpu().numpy()
+        assert np.all(got[0] == 0.0)  # empty sequence
+        H.assert_close(case, out, H.oracle_out(case), H.oracle_vmax(case))
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("t", TYPES)
+def test_paged_equals_contiguous_bit_for_bit(kernel, t):
+    spec = synth.CaseSpec(seq_lens=[1000, 77, 300, 16], k_type=t, v_type=t, junk=40)
+    case = synth.build_case(spec, seed=1400 + t, device=DEV)
+    twin = synth.contiguous_twin(case)
+    for force in (0, 1, 4):
+        a, _, pa_, _ = H.run(case, force_parts=force, flags=KERNELS[kernel])
+        b, _, pb_, _ = H.run(twin, force_parts=force, flags=KERNELS[kernel])
+        assert pa_.as_dict() == pb_.as_dict()
+        assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_run_to_run_deterministic(kernel):
+    spec = synth.CaseSpec(seq_lens=[2000, 500], k_type=synth.Q4_0, v_type=synth.Q4_0, junk=3)
+    case = synth.build_case(spec, seed=1500, device=DEV)
+    a, _, _, _ = H.run(case, flags=KERNELS[kernel])
+    b, _, _, _ = H.run(case, flags=KERNELS[kernel])
+    assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_corrupt_table_is_guarded(kernel):
+    spec = synth.CaseSpec(seq_lens=[100, 50], k_type=synth.Q4_0, v_type=synth.Q4_0, junk=2)
+    case = synth.build_case(spec, seed=1600, device=DEV)
+    case.block_table[0, 3] = case.n_blocks + 1000   # past the pool
+    case.block_table[1, 0] = -7
+    out, ws, _, _ = H.run(case, flags=KERNELS[kernel])
+    assert pa.status_read(ws.status) & pa.PA_STATUS_CORRUPT_TABLE
+    assert pa.status_read(ws.status) == 0  # the read above reset it
+    assert torch.isfinite(out).all()
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_red_control_wrong_in_range_table_fails_parity(kernel):
+    """A table whose first entry names a later block of the sequence: the
+    kernel reads valid data and sets no status bit, but the comparison with
+    the oracle (given the true table) must fail."""
+    spec = synth.CaseSpec(seq_lens=[160], k_type=synth.F16, v_type=synth.F16, junk=4)
+    case = synth.build_case(spec, seed=1700, device=DEV)
+    ref, vmax = H.oracle_out(case), H.oracle_vmax(case)
+    case.block_table[0, 0] = case.block_table[0, 5]
+    out, ws, _, _ = H.run(case, flags=KERNELS[kernel])
+    assert pa.status_read(ws.status) == 0
+    with pytest.raises(AssertionError):
+        H.assert_close(case, out, ref, vmax)
+
+
+def test_row_offsets_bit_exact():
+    spec = synth.CaseSpec(seq_lens=[70, 0, 33, 16], k_type=synth.Q4_0, v_type=synth.Q4_0,
+                          junk=6, block_size=32)
+    case = synth.build_case(spec, seed=1800, device=DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    rb = pa.row_bytes(synth.Q4_0, spec.d)
+    maxt = 80
+    got = pa.debug_row_offsets(case.block_table, case.seq_lens, max_tokens=maxt,
+                               block_size=32, hkv=spec.hkv, row_bytes_=rb,
+                               n_pool_blocks=case.n_blocks, status=status).cpu().numpy()
+    bt = case.block_table.cpu().numpy()
+    for s, L in enumerate(spec.seq_lens):
+        for t in range(maxt):
+            for g in range(spec.hkv):
+                v = int(got[s, t, g]) & 0xFFFFFFFFFFFFFFFF
+                if t < L:
+                    assert v == oracle.row_offset(int(bt[s, t // 32]), t % 32, g, 32, spec.hkv, rb)
+                else:
+                    assert v == 0xFFFFFFFFFFFFFFFF
+
+
+def test_row_offsets_past_2_to_the_32():
+    """Offsets of blocks around the 2^32-element wrap point of a [32, 8, 128]
+    f16 pool, computed by the kernels' device routine, equal the oracle's; no
+    pool memory is needed for this."""
+    B, hkv, d = 32, 8, 128
+    rb = 2 * d
+    ids = torch.tensor([[0, 131071, 131072, 131073, 163839, 2**31 - 1]], dtype=torch.int32)
+    lens = torch.tensor([6 * B], dtype=torch.int32)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    got = pa.debug_row_offsets(ids.to(DEV), lens.to(DEV), max_tokens=6 * B, block_size=B,
+                               hkv=hkv, row_bytes_=rb, n_pool_blocks=2**31,
+                               status=status).cpu().numpy()
+    for t in range(6 * B):
+        for g in range(hkv):
+            want = oracle.row_offset(int(ids[0, t // B]), t % B, g, B, hkv, rb)
+            assert int(got[0, t, g]) == want
+    assert int(got[0, 2 * B, 0]) == 2**32 * 2  # element offset exactly 2^32
+
+
+def test_merge_kernel_against_oracle_merge():
+    rng = np.random.default_rng(5)
+    S, hq, d, P, part = 3, 4, 128, 6, 64
+    lens = [P * part, 2 * part + 5, 0]
+    o = rng.standard_normal((S, hq, P, d)).astype(np.float16)
+    ml = np.zeros((S, hq, P, 2), dtype=np.float32)
+    ml[..., 0] = rng.uniform(-20, 20, (S, hq, P))
+    ml[..., 1] = rng.uniform(0.5, 40, (S, hq, P))
+    ml[0, 1, 2, 1] = 0.0               # a dead partition inside a live sequence
+    o[0, 1, 2] = np.float16(np.nan)    # whose o must not be read
+    pl = pa.Plan(part_tokens=part, n_parts=P, direct=0, n_ctas=S * P)
+    ws = pa.workspace(pl, n_seqs=S, hq=hq, d=d, device=DEV)
+    ws.part_o.copy_(torch.from_numpy(o))
+    ws.part_ml.copy_(torch.from_numpy(ml))
+    seq_lens = torch.tensor(lens, dtype=torch.int32, device=DEV)
+    pa.merge(ws, seq_lens)
+    torch.cuda.synchronize()
+    got = ws.out.cpu().double().numpy().reshape(S * hq, d)
+    n_live = np.repeat([-(-L // part) for L in lens], hq).astype(np.int32)
+    ref = oracle.merge(o.view(np.uint16).reshape(S * hq, P, d), ml.reshape(S * hq, P, 2), n_live)
+    assert np.isfinite(got).all()
+    np.testing.assert_allclose(got, ref, rtol=0, atol=2e-5 * np.abs(o.astype(np.float64)[
+        np.isfinite(o.astype(np.float64))]).max())
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_host_buffer_step_equals_device_step(kernel):
+    spec = synth.CaseSpec(seq_lens=[700, 90], k_type=synth.Q4_0, v_type=synth.Q4_0, junk=3)
+    case = synth.build_case(spec, seed=1900, device=DEV)
+    dev_out, _, _, _ = H.run(case, flags=KERNELS[kernel])
+    pl = pa.plan(seq_lens=spec.seq_lens, block_size=16, hq=24, hkv=4, d=256,
+                 k_type=spec.k_type, v_type=spec.v_type)
+    ws = pa.workspace(pl, n_seqs=2, hq=24, d=256, device=DEV)
+    qdev = torch.empty_like(case.q)
+    args = pa.make_args(k_pool=case.k_pool, v_pool=case.v_pool, block_table=case.block_table,
+                        seq_lens=case.seq_lens, q=qdev, ws=ws, hkv=4, block_size=16,
+                        k_type=spec.k_type, v_type=spec.v_type, flags=KERNELS[kernel])
+    q_host = case.q.cpu().pin_memory()
+    out_host = torch.empty(2, 24, 256, dtype=torch.float32).pin_memory()
+    pa.decode_step_host(q_host, out_host, args, ws)
+    torch.cuda.synchronize()
+    assert torch.equal(out_host.view(torch.int32), dev_out.cpu().view(torch.int32))
