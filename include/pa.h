@@ -230,6 +230,33 @@ int pa_decode_step(const pa_decode_args *args, const pa_plan_t *plan, void *q8_1
 int pa_decode_step_host(const float *q_host, float *out_host, const pa_decode_args *args,
                         const pa_plan_t *plan, void *q8_1_scratch, pa_stream_t stream);
 
+/* The same device step for callers that cannot allocate device memory.
+ * The pages have no counterpart to this call; it exists for users of this
+ * library whose code may not call cudaMalloc at decode time (for example a
+ * component that runs inside a host callback, or a serving engine whose
+ * memory is owned by another allocator or capped by a fixed budget) and so
+ * cannot supply the q8_1 and partial buffers that pa_decode_step takes.
+ * Here that scratch lives in one static device array of the library,
+ * PA_NOALLOC_SCRATCH_BYTES long, which every GPU that loads the library
+ * holds until the process exits.  The caller still passes every input and
+ * output in *args (pools, table, lengths, the float32 query in args->q, out
+ * and the status word); args->part_o and args->part_ml are ignored.
+ *  - The first call on a device looks up the array's device address with
+ *    that device current (cudaGetSymbolAddress), once per device; make that
+ *    first call before any stream capture.
+ *  - A step whose scratch (q8_1 rows plus partials, each rounded up to 256
+ *    bytes) exceeds PA_NOALLOC_SCRATCH_BYTES is refused with PA_ERR_RANGE
+ *    and the size it would need; nothing is launched.
+ *  - No allocation happens: no cudaMalloc, cudaFree or allocating routine.
+ *  - Every call shares the one array and finds the previous call's bytes in
+ *    it; nothing in it needs to start at zero.  Calls whose kernels overlap
+ *    on the GPU (different streams, or different host threads without
+ *    ordering) race on the array: order them on one stream.
+ * Errors as pa_decode_step. */
+#define PA_NOALLOC_SCRATCH_BYTES (16ull << 20)
+int pa_decode_step_noalloc(const pa_decode_args *args, const pa_plan_t *plan,
+                           pa_stream_t stream);
+
 /* Reads the status word into *host_out (synchronising `stream`); reset != 0
  * clears it afterwards.  Returns PA_ERR_CORRUPT_TABLE if the corrupt-table
  * bit is set, PA_OK otherwise, PA_ERR_CUDA on a runtime failure. */

@@ -93,6 +93,8 @@ _SIGNATURES = {
                        ctypes.c_int),
     "pa_decode_step_host": ([_vp, _vp, ctypes.POINTER(DecodeArgs), ctypes.POINTER(Plan),
                              _vp, _vp], ctypes.c_int),
+    "pa_decode_step_noalloc": ([ctypes.POINTER(DecodeArgs), ctypes.POINTER(Plan), _vp],
+                               ctypes.c_int),
     "pa_status_read": ([_vp, _vp, ctypes.POINTER(_i32), ctypes.c_int], ctypes.c_int),
     "pa_debug_row_offsets": ([_vp, _u32, _vp, _u32, _u32, _u32, _u32, _u64, _u64, _vp,
                               _vp, _vp], ctypes.c_int),
@@ -291,6 +293,17 @@ def decode_step_host(q_host: torch.Tensor, out_host: torch.Tensor, args: DecodeA
     assert not q_host.is_cuda and not out_host.is_cuda
     _check(lib().pa_decode_step_host(_ptr(q_host), _ptr(out_host), ctypes.byref(args),
                                      ctypes.byref(ws.plan), _ptr(ws.q8_1), _stream(stream)))
+
+
+NOALLOC_SCRATCH_BYTES = 16 << 20
+
+
+def decode_step_noalloc(args: DecodeArgs, pl: Plan, stream=None) -> None:
+    """pa_decode_step_noalloc: the decode step with the library's static
+    scratch instead of caller buffers, for callers that cannot allocate
+    device memory.  args.q must point at the float32 query; args.part_o and
+    args.part_ml are ignored."""
+    _check(lib().pa_decode_step_noalloc(ctypes.byref(args), ctypes.byref(pl), _stream(stream)))
 
 
 def status_read(status: torch.Tensor, reset: bool = True, stream=None) -> int:
