@@ -66,9 +66,11 @@ typedef struct CUstream_st *pa_stream_t;
 #define PA_ERR_CUDA (-4)          /* a CUDA runtime call or launch failed */
 #define PA_ERR_CORRUPT_TABLE (-5) /* device guard saw a block id outside the pool */
 #define PA_ERR_RANGE (-6)         /* a size beyond a documented limit */
+#define PA_ERR_TIMEOUT (-7)       /* a kernel gave up a bounded wait (see pa_status_read) */
 
 /* Device status word bits (written by the kernels with atomicOr). */
 #define PA_STATUS_CORRUPT_TABLE 1 /* a block id outside [0, n_pool_blocks) */
+#define PA_STATUS_TIMEOUT 2       /* a pipeline wait exceeded its bound (2 s); output invalid */
 
 typedef enum { PA_F16 = 0, PA_Q8_0 = 1, PA_Q4_0 = 2 } pa_type;
 
@@ -258,8 +260,9 @@ int pa_decode_step_noalloc(const pa_decode_args *args, const pa_plan_t *plan,
                            pa_stream_t stream);
 
 /* Reads the status word into *host_out (synchronising `stream`); reset != 0
- * clears it afterwards.  Returns PA_ERR_CORRUPT_TABLE if the corrupt-table
- * bit is set, PA_OK otherwise, PA_ERR_CUDA on a runtime failure. */
+ * clears it afterwards.  Returns PA_ERR_TIMEOUT if the timeout bit is set,
+ * else PA_ERR_CORRUPT_TABLE if the corrupt-table bit is set, PA_OK
+ * otherwise, PA_ERR_CUDA on a runtime failure. */
 int pa_status_read(int32_t *dev_status, pa_stream_t stream, int32_t *host_out, int reset);
 
 /* Debug ([P4] Acceptance Criteria: the offsets must be 64-bit).  Writes the

@@ -45,6 +45,7 @@ extern "C" const char *pa_strerror(int code)
     case PA_ERR_CUDA: return "PA_ERR_CUDA";
     case PA_ERR_CORRUPT_TABLE: return "PA_ERR_CORRUPT_TABLE";
     case PA_ERR_RANGE: return "PA_ERR_RANGE";
+    case PA_ERR_TIMEOUT: return "PA_ERR_TIMEOUT";
     default: return "PA_ERR_UNKNOWN";
     }
 }
