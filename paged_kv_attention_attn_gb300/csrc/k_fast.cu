@@ -126,6 +126,19 @@ __device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// d = a * b + c with c in separate registers (no copy into the accumulator)
+__device__ __forceinline__ void mma16816_c(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                           uint32_t a3, uint32_t b0, uint32_t b1, float c0,
+                                           float c1, float c2, float c3)
+{
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%10,%11,%12,%13};"
+        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(c0), "f"(c1), "f"(c2),
+          "f"(c3));
+}
+
 __device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], uint32_t addr)
 {
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
@@ -143,163 +156,252 @@ __device__ __forceinline__ void ldsm_x4_trans(uint32_t (&r)[4], uint32_t addr)
 __device__ __forceinline__ uint32_t h2_bits(__half2 h) { return *reinterpret_cast<uint32_t *>(&h); }
 __device__ __forceinline__ __half2 bits_h2(uint32_t u) { return *reinterpret_cast<__half2 *>(&u); }
 
-__device__ __forceinline__ uint32_t hsub2_bits(uint32_t x, uint32_t y)
-{
-    return h2_bits(__hsub2(bits_h2(x), bits_h2(y)));
-}
-
 __device__ __forceinline__ uint32_t hmul2_bits(uint32_t x, uint32_t y)
 {
     return h2_bits(__hmul2(bits_h2(x), bits_h2(y)));
 }
 
+// Shared-memory accesses by 32-bit shared-window address.
+__device__ __forceinline__ uint32_t lds_u32(uint32_t a)
+{
+    uint32_t v;
+    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(a));
+    return v;
+}
+
+__device__ __forceinline__ uint32_t lds_u16(uint32_t a)
+{
+    uint32_t v;  // zero-extended into a 32-bit register
+    asm volatile("ld.shared.u16 %0, [%1];" : "=r"(v) : "r"(a));
+    return v;
+}
+
+__device__ __forceinline__ float2 lds_f2(uint32_t a)
+{
+    float2 v;
+    asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(a));
+    return v;
+}
+
+__device__ __forceinline__ void sts_f32(uint32_t a, float v)
+{
+    asm volatile("st.shared.f32 [%0], %1;" ::"r"(a), "f"(v));
+}
+
+__device__ __forceinline__ void sts_u16(uint32_t a, uint32_t v)
+{
+    asm volatile("st.shared.u16 [%0], %1;" ::"r"(a), "r"(v));  // low 16 bits stored
+}
+
+// A 32-bit constant the compiler cannot fold back into immediates, so it is
+// materialised once and kept in a register.
+__device__ __forceinline__ uint32_t opaque(uint32_t v)
+{
+    uint32_t r;
+    asm volatile("mov.b32 %0, %1;" : "=r"(r) : "r"(v));
+    return r;
+}
+
+// (x & m) | c in one LOP3.
+__device__ __forceinline__ uint32_t and_or(uint32_t x, uint32_t m, uint32_t c)
+{
+    uint32_t r;
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(r) : "r"(x), "r"(m), "r"(c));
+    return r;
+}
+
+// Register constants of the Q4_0 nibble expansion: masks and f16 biases.
+struct NibbleConsts {
+    uint32_t mlo, mhi, blo, bhi;  // 0x000F000F, 0x00F000F0, f16 1024 | 1024, f16 64 | 64
+    uint32_t nlo[4], nhi[4];      // A quads of -1032 and -72 (f16 pairs)
+    __device__ __forceinline__ void init()
+    {
+        mlo = opaque(0x000F000Fu);
+        mhi = opaque(0x00F000F0u);
+        blo = opaque(0x64006400u);
+        bhi = opaque(0x54005400u);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            nlo[i] = opaque(0xE408E408u);
+            nhi[i] = opaque(0xD480D480u);
+        }
+    }
+};
+
+// Transposes an 8x8 matrix of 16-bit values held in mma fragment layout.
+__device__ __forceinline__ uint32_t movmatrix_t(uint32_t x)
+{
+    uint32_t y;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+    return y;
+}
+
 // ------------------------------------------------------------ per-type code
 //
-// Each type provides the shared-memory layout of one stage and, for one
-// consumer warp, the query fragments, the scores of one tile and the PV update
-// of one tile.  Thread roles follow the m16n8k16 fragment layout: gid = lane/4,
-// tig = lane%4.  QK: A = query heads (row gid; rows >= G and gid+8 are zero),
-// B = keys (column gid = token).  PV: A = values (rows = dimensions), B =
-// probabilities (column gid = query head), C = O[dimension][head].
+// Each type provides the layout of one ring slot and, for one warp, the
+// query fragments, the scores of one 16-token tile and the PV update of one
+// tile.  Thread roles follow the m16n8k16 fragment layout: gid = lane/4,
+// tig = lane%4.
+//  QK: A = keys (row = token of the tile), B = queries (column gid = query
+//      head of the group; columns >= G are zero), C = S[token][head].  Each
+//      thread ends with the scores of tokens gid, gid+8 for heads 2tig, 2tig+1
+//      in log2 units.
+//  PV: A = values (row = head dimension), B = probabilities (column gid =
+//      query head), C = O[dimension][head]: columns 2tig, 2tig+1 are again this
+//      thread's heads.
 
 // --- Q4_0, D = 256 --------------------------------------------------------
-struct Q40 {
+template <uint32_t KMAXW>
+struct Q40T {
     static constexpr int D = 256;
     static constexpr int NB = D / 32;       // 32-value blocks per row
     static constexpr int RB = NB * 18;      // row bytes
     static constexpr int MT = D / 16;       // PV m-tiles
-    static constexpr int SCRATCH = NB * kTile * 4 + NB * kTile * 2;  // dk f32, dv f16
+    static constexpr int DK = 0, DV = NB * kTile * 4;  // scratch: dk f32, dv f16
+    static constexpr int SCRATCH = NB * kTile * 4 + NB * kTile * 2;
     static constexpr bool kZeroInvalidV = false;
     static constexpr uint32_t kTmaX = 1;    // TMA boxes per (side, head)
+    static constexpr uint32_t kMaxWarps = KMAXW;
 
     static __host__ __device__ constexpr uint32_t side_bytes(uint32_t hkv)
     {
         return hkv * kTile * RB;
     }
 
+    // Query fragments live in shared memory, one 32-byte record per (block,
+    // lane) of each K/V head: the four B registers, then the C quad that
+    // starts the accumulator at minus the bias contribution (heads 2tig, 2tig+1).
+    static constexpr int QREC = 16;                     // one uint4 per (block, lane)
+    static constexpr int QCORR = NB * 32 * QREC;         // offset of the C quads
+    static constexpr int QBYTES = 2 * NB * 32 * QREC;    // per K/V head
     struct Frag {
-        uint32_t qa[NB][4];  // per block: low-dims a0, a2; high-dims a0, a2
-        float ncorr[NB];     // minus the bias contribution of the block (exact)
-        float dqs[NB];       // d_q * scale * log2(e)
+        uint32_t q;  // shared address of this lane's records (block 0)
     };
 
-    // Query head row gid of group g: q8_1 bytes -> exact f16 integers in the
-    // dimension order the nibble expansion produces (see qk_block).
-    __device__ static void load_q(const DecodeParams &p, uint32_t s, uint32_t h0, uint32_t G,
-                                  int gid, int tig, Frag &f)
+    // Writes the fragments of query head gid of the group: qhat = f16(q * d_q
+    // * scale * log2 e), in the dimension order the nibble expansion produces
+    // (see block()).  One warp per K/V head calls this.
+    __device__ static void store_q(const DecodeParams &p, uint32_t s, uint32_t h0, uint32_t G,
+                                   int gid, int tig, uint32_t qsm)
     {
+        const int lane = gid * 4 + tig;
         const bool live = (uint32_t)gid < G;
         const uint8_t *row = static_cast<const uint8_t *>(p.q) +
                              ((uint64_t)s * p.hq + h0 + (live ? gid : 0)) * NB * 36;
 #pragma unroll
         for (int b = 0; b < NB; ++b) {
             const uint8_t *blk = row + 36 * b;
-            int q[8];
+            const float d = live ? half_bits_to_float(load_u16(blk)) * p.scale_log2 : 0.0f;
+            __half qh[8];
+            float corr = 0.0f;
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                q[j] = live ? (int)(int8_t)blk[4 + 4 * tig + j] : 0;       // dims 4tig+j
-                q[4 + j] = live ? (int)(int8_t)blk[20 + 4 * tig + j] : 0;  // dims 16+4tig+j
+            for (int j = 0; j < 8; ++j) {
+                const int off = j < 4 ? 4 + 4 * tig + j : 20 + 4 * tig + (j - 4);
+                qh[j] = __float2half_rn((float)(int8_t)blk[off] * d);
+                // low nibbles read as 1024 + n, high as 64 + n; the value is n - 8
+                corr += __half2float(qh[j]) * (j < 4 ? 1032.0f : 72.0f);
             }
-            f.qa[b][0] = h2_bits(__halves2half2(__int2half_rn(q[0]), __int2half_rn(q[2])));
-            f.qa[b][1] = h2_bits(__halves2half2(__int2half_rn(q[1]), __int2half_rn(q[3])));
-            f.qa[b][2] = h2_bits(__halves2half2(__int2half_rn(q[4]), __int2half_rn(q[6])));
-            f.qa[b][3] = h2_bits(__halves2half2(__int2half_rn(q[5]), __int2half_rn(q[7])));
-            int lo = q[0] + q[1] + q[2] + q[3], hi = q[4] + q[5] + q[6] + q[7];
-            lo += __shfl_xor_sync(0xffffffffu, lo, 1);
-            lo += __shfl_xor_sync(0xffffffffu, lo, 2);
-            hi += __shfl_xor_sync(0xffffffffu, hi, 1);
-            hi += __shfl_xor_sync(0xffffffffu, hi, 2);
-            // low nibbles read as 1024 + n, high nibbles as 64 + n; the value is n - 8
-            f.ncorr[b] = -(float)(1032 * lo + 72 * hi);
-            f.dqs[b] = live ? half_bits_to_float(load_u16(blk)) * p.scale_log2 : 0.0f;
+            corr += __shfl_xor_sync(0xffffffffu, corr, 1);
+            corr += __shfl_xor_sync(0xffffffffu, corr, 2);
+            const float n0 = -__shfl_sync(0xffffffffu, corr, 8 * tig);
+            const float n1 = -__shfl_sync(0xffffffffu, corr, 8 * tig + 4);
+            const uint32_t r = qsm + (b * 32 + lane) * QREC;
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(r),
+                         "r"(h2_bits(__halves2half2(qh[0], qh[2]))),
+                         "r"(h2_bits(__halves2half2(qh[1], qh[3]))),
+                         "r"(h2_bits(__halves2half2(qh[4], qh[6]))),
+                         "r"(h2_bits(__halves2half2(qh[5], qh[7]))));
+            asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(r + QCORR), "f"(n0),
+                         "f"(n1), "f"(n0), "f"(n1));
         }
     }
 
-    // Copies the tile's block scales of head g into the warp's scratch:
-    // dk float [NB][16] and dv half [NB][16], zero for invalid tokens.
-    __device__ static void extract(const uint8_t *kh, const uint8_t *vh, uint8_t *scr,
-                                   int nvalid, int lane)
+    __device__ static void load_q(uint32_t qsm, int lane, Frag &f) { f.q = qsm + lane * QREC; }
+
+    // Block scales of the tile into the warp's scratch: dk as float with the
+    // pair (t, t+8) adjacent, dv as half in token order; zero for invalid tokens.
+    __device__ static void extract(uint32_t kh, uint32_t vh, uint32_t scr, int nvalid, int lane)
     {
-        float *dk = reinterpret_cast<float *>(scr);
-        uint16_t *dv = reinterpret_cast<uint16_t *>(scr + NB * kTile * 4);
 #pragma unroll
         for (int k = 0; k < NB * kTile / 32; ++k) {
             const int e = lane + 32 * k, t = e & 15, b = e >> 4;
             const bool v = t < nvalid;
-            const uint16_t kd = load_u16(kh + t * RB + 18 * b);
-            const uint16_t vd = load_u16(vh + t * RB + 18 * b);
-            dk[e] = v ? half_bits_to_float(kd) : 0.0f;
-            dv[e] = v ? vd : (uint16_t)0;
+            const uint32_t kd = lds_u16(kh + t * RB + 18 * b);
+            const uint32_t vd = lds_u16(vh + t * RB + 18 * b);
+            sts_f32(scr + DK + 4 * (b * kTile + 2 * (t & 7) + (t >> 3)),
+                    v ? half_bits_to_float((uint16_t)kd) : 0.0f);
+            sts_u16(scr + DV + 2 * (b * kTile + t), v ? vd : 0u);
         }
     }
 
-    // QK of one 32-value block for the 8 tokens of this n-tile; w holds the
-    // 8 nibbles of dims 4tig..4tig+3 (low) and 16+4tig..19+4tig (high).
-    __device__ static __forceinline__ void qk_block(const Frag &f, int b, uint32_t w, float dk0,
-                                                    float dk1, float &s0, float &s1)
+    // One 32-value block: x0 / x1 are the nibble words of tokens gid / gid+8
+    // holding dims 4tig..4tig+3 (low nibbles) and 16+4tig..19+4tig (high).
+    __device__ static __forceinline__ void block(const NibbleConsts &K, uint32_t qrec, uint32_t x0,
+                                                 uint32_t x1, float2 dk, float (&s)[4])
     {
-        const uint32_t x = w >> 8;
-        const uint32_t blo0 = (w & 0x000F000Fu) | 0x64006400u;  // dims 4tig, 4tig+2
-        const uint32_t blo1 = (x & 0x000F000Fu) | 0x64006400u;  // dims 4tig+1, 4tig+3
-        const uint32_t bhi0 = (w & 0x00F000F0u) | 0x54005400u;
-        const uint32_t bhi1 = (x & 0x00F000F0u) | 0x54005400u;
-        float c[4] = {f.ncorr[b], f.ncorr[b], 0.0f, 0.0f};
-        mma16816(c, f.qa[b][0], 0u, f.qa[b][1], 0u, blo0, blo1);
-        mma16816(c, f.qa[b][2], 0u, f.qa[b][3], 0u, bhi0, bhi1);
-        s0 = fmaf(c[0] * dk0, f.dqs[b], s0);
-        s1 = fmaf(c[1] * dk1, f.dqs[b], s1);
+        uint32_t qb0, qb1, qb2, qb3;
+        float c[4];
+        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(qb0), "=r"(qb1), "=r"(qb2), "=r"(qb3)
+                     : "r"(qrec));
+        asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                     : "=f"(c[0]), "=f"(c[1]), "=f"(c[2]), "=f"(c[3])
+                     : "r"(qrec + QCORR));
+        const uint32_t y0 = x0 >> 8, y1 = x1 >> 8;
+        mma16816(c, and_or(x0, K.mlo, K.blo), and_or(x1, K.mlo, K.blo), and_or(y0, K.mlo, K.blo),
+                 and_or(y1, K.mlo, K.blo), qb0, qb1);
+        mma16816(c, and_or(x0, K.mhi, K.bhi), and_or(x1, K.mhi, K.bhi), and_or(y0, K.mhi, K.bhi),
+                 and_or(y1, K.mhi, K.bhi), qb2, qb3);
+        s[0] = fmaf(c[0], dk.x, s[0]);
+        s[1] = fmaf(c[1], dk.x, s[1]);
+        s[2] = fmaf(c[2], dk.y, s[2]);
+        s[3] = fmaf(c[3], dk.y, s[3]);
     }
 
-    // Scores (log2 units, unmasked) of tokens nt*8 + 2tig + {0, 1}.
-    __device__ static void scores(const Frag &f, const uint8_t *kh, const uint8_t *scr, int gid,
-                                  int tig, float (&sc)[2][2])
+    __device__ static void scores(const NibbleConsts &K, const Frag &f, uint32_t kh, uint32_t scr,
+                                  int gid, int tig, float (&s)[4])
     {
-        const float *dk = reinterpret_cast<const float *>(scr);
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-            const uint32_t *wr = reinterpret_cast<const uint32_t *>(kh + (nt * 8 + gid) * RB);
-            float s0 = 0.0f, s1 = 0.0f;
-#pragma unroll
-            for (int pb = 0; pb < NB / 2; ++pb) {
-                // blocks 2pb and 2pb+1 share 36 bytes = 9 aligned words
-                const uint32_t w0 = wr[9 * pb + tig], w1 = wr[9 * pb + tig + 1];
-                const uint32_t w2 = wr[9 * pb + 5 + tig];
-                const uint32_t wa = __funnelshift_r(w0, w1, 16);
-                const float2 k0 = *reinterpret_cast<const float2 *>(dk + (2 * pb) * kTile + nt * 8 + 2 * tig);
-                const float2 k1 = *reinterpret_cast<const float2 *>(dk + (2 * pb + 1) * kTile + nt * 8 + 2 * tig);
-                qk_block(f, 2 * pb, wa, k0.x, k0.y, s0, s1);
-                qk_block(f, 2 * pb + 1, w2, k1.x, k1.y, s0, s1);
-            }
-            sc[nt][0] = s0;
-            sc[nt][1] = s1;
+        const uint32_t r0 = kh + gid * RB + 4 * tig, r1 = r0 + 8 * RB;
+        const uint32_t dk = scr + DK + 8 * gid;
+        s[0] = s[1] = s[2] = s[3] = 0.0f;
+#pragma unroll 1
+        for (int pb = 0; pb < NB / 2; ++pb) {
+            // blocks 2pb and 2pb+1 share 36 bytes = 9 aligned words
+            const uint32_t a0 = lds_u32(r0 + 36 * pb), a1 = lds_u32(r0 + 36 * pb + 4);
+            const uint32_t a2 = lds_u32(r0 + 36 * pb + 20);
+            const uint32_t b0 = lds_u32(r1 + 36 * pb), b1 = lds_u32(r1 + 36 * pb + 4);
+            const uint32_t b2 = lds_u32(r1 + 36 * pb + 20);
+            const float2 k0 = lds_f2(dk + 4 * (2 * pb) * kTile);
+            const float2 k1 = lds_f2(dk + 4 * (2 * pb + 1) * kTile);
+            const uint32_t qr = f.q + (2 * pb) * 32 * QREC;
+            block(K, qr, __funnelshift_r(a0, a1, 16), __funnelshift_r(b0, b1, 16), k0, s);
+            block(K, qr + 32 * QREC, a2, b2, k1, s);
         }
     }
 
-    // O += V^T P' over the tile; P' = P * d_v per block.
-    __device__ static void pv(float (&o)[MT][4], const uint8_t *vh, const uint8_t *scr, uint32_t p0,
-                              uint32_t p1, int gid, int tig)
+    // O += V^T P' over the tile, P' = P * d_v per block.  The V operand is the
+    // nibble read as 1024 + n (low nibbles) or 64 + n (high nibbles); a second
+    // MMA with every A entry -1032 (or -72) adds -(bias + 8) * sum_t P', so the
+    // two together contribute sum_t (n - 8) P'.
+    __device__ static void pv(const NibbleConsts &K, float (&o)[MT][4], uint32_t vh, uint32_t scr,
+                              uint32_t p0, uint32_t p1, int gid, int tig)
     {
-        const uint16_t *dv = reinterpret_cast<const uint16_t *>(scr + NB * kTile * 4);
-        const uint8_t *ra = vh + (2 * tig) * RB + 2 + 2 * gid;
-        const uint8_t *rc = vh + (2 * tig + 8) * RB + 2 + 2 * gid;
-        const uint32_t kLo = 0x64086408u;  // 1032
-        const uint32_t kHi = 0x54805480u;  // 72
+        const uint32_t ra = vh + (2 * tig) * RB + 2 + 2 * gid;
+        const uint32_t rc = ra + 8 * RB;
 #pragma unroll
         for (int b = 0; b < NB; ++b) {
-            const uint32_t ua = load_u16(ra + 18 * b), ub = load_u16(ra + RB + 18 * b);
-            const uint32_t uc = load_u16(rc + 18 * b), ud = load_u16(rc + RB + 18 * b);
+            const uint32_t ua = lds_u16(ra + 18 * b), ub = lds_u16(ra + RB + 18 * b);
+            const uint32_t uc = lds_u16(rc + 18 * b), ud = lds_u16(rc + RB + 18 * b);
             const uint32_t xab = __byte_perm(ua, ub, 0x5410), yab = xab >> 8;
             const uint32_t xcd = __byte_perm(uc, ud, 0x5410), ycd = xcd >> 8;
-            const uint32_t b0 = hmul2_bits(p0, *reinterpret_cast<const uint32_t *>(dv + b * kTile + 2 * tig));
-            const uint32_t b1 = hmul2_bits(p1, *reinterpret_cast<const uint32_t *>(dv + b * kTile + 8 + 2 * tig));
-            mma16816(o[2 * b], hsub2_bits((xab & 0x000F000Fu) | 0x64006400u, kLo),
-                     hsub2_bits((yab & 0x000F000Fu) | 0x64006400u, kLo),
-                     hsub2_bits((xcd & 0x000F000Fu) | 0x64006400u, kLo),
-                     hsub2_bits((ycd & 0x000F000Fu) | 0x64006400u, kLo), b0, b1);
-            mma16816(o[2 * b + 1], hsub2_bits((xab & 0x00F000F0u) | 0x54005400u, kHi),
-                     hsub2_bits((yab & 0x00F000F0u) | 0x54005400u, kHi),
-                     hsub2_bits((xcd & 0x00F000F0u) | 0x54005400u, kHi),
-                     hsub2_bits((ycd & 0x00F000F0u) | 0x54005400u, kHi), b0, b1);
+            const uint32_t b0 = hmul2_bits(p0, lds_u32(scr + DV + 2 * (b * kTile + 2 * tig)));
+            const uint32_t b1 = hmul2_bits(p1, lds_u32(scr + DV + 2 * (b * kTile + 8 + 2 * tig)));
+            mma16816(o[2 * b], and_or(xab, K.mlo, K.blo), and_or(yab, K.mlo, K.blo),
+                     and_or(xcd, K.mlo, K.blo), and_or(ycd, K.mlo, K.blo), b0, b1);
+            mma16816(o[2 * b], K.nlo[0], K.nlo[1], K.nlo[2], K.nlo[3], b0, b1);
+            mma16816(o[2 * b + 1], and_or(xab, K.mhi, K.bhi), and_or(yab, K.mhi, K.bhi),
+                     and_or(xcd, K.mhi, K.bhi), and_or(ycd, K.mhi, K.bhi), b0, b1);
+            mma16816(o[2 * b + 1], K.nhi[0], K.nhi[1], K.nhi[2], K.nhi[3], b0, b1);
         }
     }
 
@@ -310,10 +412,12 @@ struct Q40 {
     }
 };
 
+using Q40 = Q40T<12>;
+
 // --- F16, D = 128 or 256 ----------------------------------------------------
-// Stage layout per side: [head][64-dim chunk][16 tokens][128 B], written by
-// TMA with the 128-byte swizzle (16-byte chunk c of row t stored at c ^ (t&7)),
-// read with ldmatrix without bank conflicts.
+// Slot layout per side: [64-dim chunk][16 tokens][128 B], written by TMA with
+// the 128-byte swizzle (16-byte chunk c of row t stored at c ^ (t & 7)), read
+// with ldmatrix without bank conflicts.
 template <int D_>
 struct F16T {
     static constexpr int D = D_;
@@ -323,16 +427,22 @@ struct F16T {
     static constexpr int SCRATCH = 0;
     static constexpr bool kZeroInvalidV = true;
     static constexpr uint32_t kTmaX = NC;
+    static constexpr uint32_t kMaxWarps = 8;
 
     static __host__ __device__ constexpr uint32_t side_bytes(uint32_t hkv)
     {
         return hkv * kTile * D * 2;
     }
 
+    static constexpr int QBYTES = 0;
     struct Frag {
-        uint32_t qa[KS][2];  // a0, a2 of each k-step
-        float scale;
+        uint32_t qb[KS][2];  // B fragments (query column gid) of each k-step
     };
+
+    __device__ static void store_q(const DecodeParams &, uint32_t, uint32_t, uint32_t, int, int,
+                                   uint32_t)
+    {
+    }
 
     __device__ static void load_q(const DecodeParams &p, uint32_t s, uint32_t h0, uint32_t G,
                                   int gid, int tig, Frag &f)
@@ -340,21 +450,19 @@ struct F16T {
         const bool live = (uint32_t)gid < G;
         const float *row = static_cast<const float *>(p.q) +
                            ((uint64_t)s * p.hq + h0 + (live ? gid : 0)) * D;
+        const float sc = live ? p.scale_log2 : 0.0f;
 #pragma unroll
         for (int j = 0; j < KS; ++j) {
-            const float2 x = live ? *reinterpret_cast<const float2 *>(row + 16 * j + 2 * tig)
-                                  : make_float2(0.f, 0.f);
-            const float2 y = live ? *reinterpret_cast<const float2 *>(row + 16 * j + 8 + 2 * tig)
-                                  : make_float2(0.f, 0.f);
-            f.qa[j][0] = h2_bits(__floats2half2_rn(x.x, x.y));
-            f.qa[j][1] = h2_bits(__floats2half2_rn(y.x, y.y));
+            const float2 x = *reinterpret_cast<const float2 *>(row + 16 * j + 2 * tig);
+            const float2 y = *reinterpret_cast<const float2 *>(row + 16 * j + 8 + 2 * tig);
+            f.qb[j][0] = h2_bits(__floats2half2_rn(x.x * sc, x.y * sc));
+            f.qb[j][1] = h2_bits(__floats2half2_rn(y.x * sc, y.y * sc));
         }
-        f.scale = p.scale_log2;
     }
 
-    __device__ static __forceinline__ uint32_t chunk_addr(const uint8_t *sub, int token, int c16)
+    __device__ static __forceinline__ uint32_t chunk_addr(uint32_t sub, int token, int c16)
     {
-        return smem_u32(sub + token * 128 + ((c16 ^ (token & 7)) << 4));
+        return sub + token * 128 + ((c16 ^ (token & 7)) << 4);
     }
 
     // Zero V rows of tokens >= nvalid (their bytes may be anything).
@@ -368,30 +476,27 @@ struct F16T {
         }
     }
 
-    __device__ static void scores(const Frag &f, const uint8_t *kh, const uint8_t *, int gid,
-                                  int tig, float (&sc)[2][2])
+    __device__ static void scores(const NibbleConsts &, const Frag &f, uint32_t kh, uint32_t,
+                                  int gid, int tig, float (&s)[4])
     {
         const int lane = gid * 4 + tig;
         const int mi = lane >> 3, r = lane & 7;
+        const int token = (mi & 1) * 8 + r;
+        float c[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-            float c[4] = {0.f, 0.f, 0.f, 0.f};
-            const int token = nt * 8 + r;
-#pragma unroll
-            for (int j2 = 0; j2 < KS / 2; ++j2) {
-                uint32_t bq[4];
-                const uint8_t *sub = kh + (j2 >> 1) * kTile * 128;
-                ldsm_x4(bq, chunk_addr(sub, token, (j2 & 1) * 4 + mi));
-                mma16816(c, f.qa[2 * j2][0], 0u, f.qa[2 * j2][1], 0u, bq[0], bq[1]);
-                mma16816(c, f.qa[2 * j2 + 1][0], 0u, f.qa[2 * j2 + 1][1], 0u, bq[2], bq[3]);
-            }
-            sc[nt][0] = c[0] * f.scale;
-            sc[nt][1] = c[1] * f.scale;
+        for (int j = 0; j < KS; ++j) {
+            uint32_t a[4];
+            ldsm_x4(a, chunk_addr(kh + (j >> 2) * kTile * 128, token, 2 * (j & 3) + (mi >> 1)));
+            mma16816(c, a[0], a[1], a[2], a[3], f.qb[j][0], f.qb[j][1]);
         }
+        s[0] = c[0];
+        s[1] = c[1];
+        s[2] = c[2];
+        s[3] = c[3];
     }
 
-    __device__ static void pv(float (&o)[MT][4], const uint8_t *vh, const uint8_t *, uint32_t p0,
-                              uint32_t p1, int gid, int tig)
+    __device__ static void pv(const NibbleConsts &, float (&o)[MT][4], uint32_t vh, uint32_t,
+                              uint32_t p0, uint32_t p1, int gid, int tig)
     {
         const int lane = gid * 4 + tig;
         const int mi = lane >> 3, r = lane & 7;
@@ -399,8 +504,7 @@ struct F16T {
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt) {
             uint32_t a[4];
-            const uint8_t *sub = vh + (mt >> 2) * kTile * 128;
-            ldsm_x4_trans(a, chunk_addr(sub, token, (mt & 3) * 2 + (mi & 1)));
+            ldsm_x4_trans(a, chunk_addr(vh + (mt >> 2) * kTile * 128, token, (mt & 3) * 2 + (mi & 1)));
             mma16816(o[mt], a[0], a[1], a[2], a[3], p0, p1);
         }
     }
@@ -421,23 +525,26 @@ struct F16T {
 // heads are fetched by the other warps at about the same time; the whole
 // 16-token block is one contiguous range of the pool.
 
+constexpr float kHeadroom = 4.0f;  // log2 units kept between the reference and the max
+
 template <class T>
-__global__ void __launch_bounds__(256, 1) fast_decode_kernel(const __grid_constant__ FastArgs a)
+__global__ void __launch_bounds__(T::kMaxWarps * 32, 1)
+    fast_decode_kernel(const __grid_constant__ FastArgs a)
 {
     const DecodeParams &p = a.p;
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                                ~uintptr_t(1023));
+    extern __shared__ __align__(16) uint8_t smem_raw[];
+    uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const uint32_t NSW = a.n_slots, SLOT = a.slot_bytes, nwarps = blockDim.x >> 5;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t hkv = p.hkv, G = p.hq / p.hkv, wph = nwarps / hkv;
     uint8_t *ring = smem + (size_t)warp * NSW * SLOT;
+    const uint32_t ring_u = smem_u32(ring);
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + a.region_bytes) + warp * NSW;
     int *slot_ok = reinterpret_cast<int *>(reinterpret_cast<uint64_t *>(smem + a.region_bytes) +
                                            nwarps * NSW) + warp * NSW;
-    uint8_t *scr = reinterpret_cast<uint8_t *>(
-        (reinterpret_cast<uintptr_t>(slot_ok + (nwarps - warp) * NSW) + 15) & ~uintptr_t(15)) +
-        warp * T::SCRATCH;
+    const uint32_t scr_base = (smem_u32(slot_ok + (nwarps - warp) * NSW) + 15u) & ~15u;
+    const uint32_t scr_u = scr_base + warp * T::SCRATCH;
+    const uint32_t qsm_base = scr_base + nwarps * T::SCRATCH;  // per K/V head: T::QBYTES
 
     if (lane == 0) {
         for (uint32_t s = 0; s < NSW; ++s)
@@ -463,21 +570,21 @@ __global__ void __launch_bounds__(256, 1) fast_decode_kernel(const __grid_consta
     const int32_t *bt = p.block_table + (uint64_t)seq * p.table_stride;
     const CUtensorMap *tmk = &a.tm[0][g], *tmv = &a.tm[1][g];
     const uint32_t side = SLOT / 2;
+    const uint32_t bshift = p.block_size == 32 ? 5 : 4, bmask = p.block_size - 1;
 
     // block ids of my tiles k0 .. k0+31, one per lane
     auto fetch_ids = [&](uint32_t k0) -> int32_t {
         const uint32_t k = k0 + lane;
-        return k < n_my ? bt[(t0 + kTile * (sub + k * wph)) / p.block_size] : 0;
+        return k < n_my ? bt[(t0 + kTile * (sub + k * wph)) >> bshift] : 0;
     };
-    // lane 0: start the copy of my tile k (block id blk) into its slot
-    auto issue = [&](uint32_t k, int32_t blk) {
-        const uint32_t s = k % NSW;
+    // lane 0: start the copy of my tile k (block id blk) into slot s
+    auto issue = [&](uint32_t k, uint32_t s, int32_t blk) {
         const uint32_t tok = t0 + kTile * (sub + k * wph);
         const bool ok = block_in_pool(blk, p.n_pool_blocks);
         slot_ok[s] = ok;
         if (ok) {
             uint8_t *dst = ring + (size_t)s * SLOT;
-            const int y = blk * (int)p.block_size + (int)(tok % p.block_size);
+            const int y = (blk << bshift) + (int)(tok & bmask);
             fence_proxy_async();  // earlier generic reads of this slot come first
             mbar_arrive_expect_tx(&full[s], SLOT);
 #pragma unroll
@@ -496,27 +603,39 @@ __global__ void __launch_bounds__(256, 1) fast_decode_kernel(const __grid_consta
     for (uint32_t k = 0; k < pro; ++k) {
         const int32_t b = __shfl_sync(0xffffffffu, ids, k);
         if (lane == 0)
-            issue(k, b);
+            issue(k, k, b);
     }
     __syncwarp();
 
+    NibbleConsts K;
+    if constexpr (T::kZeroInvalidV == false)
+        K.init();
     typename T::Frag f;
-    T::load_q(p, seq, g * G, G, gid, tig, f);
+    if constexpr (T::QBYTES > 0) {
+        if (sub == 0)
+            T::store_q(p, seq, g * G, G, gid, tig, qsm_base + g * T::QBYTES);
+        __syncthreads();
+        T::load_q(qsm_base + g * T::QBYTES, lane, f);
+    } else {
+        T::load_q(p, seq, g * G, G, gid, tig, f);
+    }
     float o[T::MT][4];
 #pragma unroll
     for (int mt = 0; mt < T::MT; ++mt)
         o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.0f;
-    float m_run = -INFINITY, l_run = 0.0f;
+    // softmax state of this thread's heads 2tig and 2tig+1: reference max
+    // (>= every score seen) and the partial sum over its tokens
+    float mref0 = -INFINITY, mref1 = -INFINITY, l0 = 0.0f, l1 = 0.0f;
     bool aborted = false;
     uint32_t issued = pro;
 
+    uint32_t s = 0, phase = 0;  // slot of tile k and the parity of its current use
     for (uint32_t k = 0; k < n_my; ++k) {
-        const uint32_t s = k % NSW;
         // every lane waits (bounded) and so acquires the slot's TMA writes itself
-        bool done = mbar_try_wait(&full[s], (k / NSW) & 1);
+        bool done = mbar_try_wait(&full[s], phase);
         if (!done) {
             const uint64_t tw = global_ns();
-            while (!(done = mbar_try_wait(&full[s], (k / NSW) & 1)) && global_ns() - tw < kWaitNs) {
+            while (!(done = mbar_try_wait(&full[s], phase)) && global_ns() - tw < kWaitNs) {
             }
         }
         if (!__all_sync(0xffffffffu, done)) {
@@ -527,36 +646,35 @@ __global__ void __launch_bounds__(256, 1) fast_decode_kernel(const __grid_consta
         }
         const uint32_t i = sub + k * wph;
         const int nvalid = slot_ok[s] ? (int)min(16u, t1 - (t0 + kTile * i)) : 0;
-        uint8_t *kh = ring + (size_t)s * SLOT;
-        uint8_t *vh = kh + side;
+        const uint32_t kh = ring_u + s * SLOT, vh = kh + side;
         if constexpr (T::kZeroInvalidV) {
             if (nvalid < kTile) {
-                T::zero_invalid_v(vh, nvalid, lane);
+                T::zero_invalid_v(ring + (size_t)s * SLOT + side, nvalid, lane);
                 __syncwarp();
             }
         } else {
-            T::extract(kh, vh, scr, nvalid, lane);
+            T::extract(kh, vh, scr_u, nvalid, lane);
             __syncwarp();
         }
-        float sc[2][2];
-        T::scores(f, kh, scr, gid, tig, sc);
-        // online softmax over the tile, log2 domain; rescale only on a new max
-        float tmax = -INFINITY;
+        float sc[4];
+        T::scores(K, f, kh, scr_u, gid, tig, sc);
+        // online softmax over the tile (log2 domain); the reference max moves,
+        // and the accumulators are rescaled, only when a score passes it
+        if (gid >= nvalid)
+            sc[0] = sc[1] = -INFINITY;
+        if (gid + 8 >= nvalid)
+            sc[2] = sc[3] = -INFINITY;
+        float t0m = fmaxf(sc[0], sc[2]), t1m = fmaxf(sc[1], sc[3]);
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                if (nt * 8 + 2 * tig + j >= nvalid)
-                    sc[nt][j] = -INFINITY;
-                tmax = fmaxf(tmax, sc[nt][j]);
-            }
-        tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 1));
-        tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 2));
-        if (__any_sync(0xffffffffu, tmax > m_run)) {
-            const float m_new = fmaxf(m_run, tmax);
-            const float alpha = m_run == -INFINITY ? 0.0f : exp2f(m_run - m_new);
-            const float a0 = __shfl_sync(0xffffffffu, alpha, 8 * tig);
-            const float a1 = __shfl_sync(0xffffffffu, alpha, 8 * tig + 4);
+        for (int off = 4; off < 32; off <<= 1) {
+            t0m = fmaxf(t0m, __shfl_xor_sync(0xffffffffu, t0m, off));
+            t1m = fmaxf(t1m, __shfl_xor_sync(0xffffffffu, t1m, off));
+        }
+        if (__any_sync(0xffffffffu, t0m > mref0 || t1m > mref1)) {
+            const float n0 = t0m > mref0 ? t0m + kHeadroom : mref0;
+            const float n1 = t1m > mref1 ? t1m + kHeadroom : mref1;
+            const float a0 = mref0 == -INFINITY ? 0.0f : exp2f(mref0 - n0);
+            const float a1 = mref1 == -INFINITY ? 0.0f : exp2f(mref1 - n1);
 #pragma unroll
             for (int mt = 0; mt < T::MT; ++mt) {
                 o[mt][0] *= a0;
@@ -564,21 +682,21 @@ __global__ void __launch_bounds__(256, 1) fast_decode_kernel(const __grid_consta
                 o[mt][2] *= a0;
                 o[mt][3] *= a1;
             }
-            l_run *= alpha;
-            m_run = m_new;
+            l0 *= a0;
+            l1 *= a1;
+            mref0 = n0;
+            mref1 = n1;
         }
-        const float ms = m_run == -INFINITY ? 0.0f : m_run;
-        float pr[2][2];
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                pr[nt][j] = exp2f(sc[nt][j] - ms);
-                l_run += pr[nt][j];
-            }
-        const uint32_t p0 = h2_bits(__floats2half2_rn(pr[0][0], pr[0][1]));
-        const uint32_t p1 = h2_bits(__floats2half2_rn(pr[1][0], pr[1][1]));
-        T::pv(o, vh, scr, p0, p1, gid, tig);
+        const float ms0 = mref0 == -INFINITY ? 0.0f : mref0;
+        const float ms1 = mref1 == -INFINITY ? 0.0f : mref1;
+        const float q00 = exp2f(sc[0] - ms0), q01 = exp2f(sc[1] - ms1);
+        const float q10 = exp2f(sc[2] - ms0), q11 = exp2f(sc[3] - ms1);
+        l0 += q00 + q10;
+        l1 += q01 + q11;
+        // P[token][head] as two 8x8 blocks (tokens 0-7, 8-15) -> PV B operand
+        const uint32_t p0 = movmatrix_t(h2_bits(__floats2half2_rn(q00, q01)));
+        const uint32_t p1 = movmatrix_t(h2_bits(__floats2half2_rn(q10, q11)));
+        T::pv(K, o, vh, scr_u, p0, p1, gid, tig);
         __syncwarp();  // all reads of this slot are done
         // refill the slot with my tile k + NSW
         const uint32_t kn = k + NSW;
@@ -589,10 +707,14 @@ __global__ void __launch_bounds__(256, 1) fast_decode_kernel(const __grid_consta
             }
             const int32_t b = __shfl_sync(0xffffffffu, ids, kn & 31);
             if (lane == 0)
-                issue(kn, b);
+                issue(kn, s, b);
             issued = kn + 1;
         }
         __syncwarp();
+        if (++s == NSW) {
+            s = 0;
+            phase ^= 1;
+        }
     }
     if (aborted && lane == 0) {
         // let my copies still in flight land (bounded) before the CTA moves on
@@ -602,8 +724,11 @@ __global__ void __launch_bounds__(256, 1) fast_decode_kernel(const __grid_consta
             }
         }
     }
-    l_run += __shfl_xor_sync(0xffffffffu, l_run, 1);
-    l_run += __shfl_xor_sync(0xffffffffu, l_run, 2);
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+        l0 += __shfl_xor_sync(0xffffffffu, l0, off);
+        l1 += __shfl_xor_sync(0xffffffffu, l1, off);
+    }
 
     // park (m, l, O) of every warp in the now idle rings, then the first warp
     // of each head combines them
@@ -611,9 +736,11 @@ __global__ void __launch_bounds__(256, 1) fast_decode_kernel(const __grid_consta
     float *park = reinterpret_cast<float *>(smem);
     const int per_warp = 16 + 32 * 4 * T::MT;
     float *mine = park + warp * per_warp;
-    if (tig == 0) {
-        mine[gid] = m_run;
-        mine[8 + gid] = l_run;
+    if (gid == 0) {
+        mine[2 * tig] = mref0;
+        mine[2 * tig + 1] = mref1;
+        mine[8 + 2 * tig] = l0;
+        mine[8 + 2 * tig + 1] = l1;
     }
 #pragma unroll
     for (int mt = 0; mt < T::MT; ++mt)
@@ -623,7 +750,7 @@ __global__ void __launch_bounds__(256, 1) fast_decode_kernel(const __grid_consta
     __syncthreads();
     if (sub != 0)
         return;
-    float M[2], l[2], fk[8][2];
+    float M[2], l[2], fk[12][2];
 #pragma unroll
     for (int c = 0; c < 2; ++c) {
         const int h = 2 * tig + c;
@@ -633,7 +760,7 @@ __global__ void __launch_bounds__(256, 1) fast_decode_kernel(const __grid_consta
         l[c] = 0.0f;
         for (uint32_t k = 0; k < wph; ++k) {
             const float mk = park[(g + k * hkv) * per_warp + h];
-            const float f2 = M[c] == -INFINITY ? 0.0f : exp2f(mk - M[c]);
+            const float f2 = (M[c] == -INFINITY || mk == -INFINITY) ? 0.0f : exp2f(mk - M[c]);
             fk[k][c] = f2;
             l[c] += park[(g + k * hkv) * per_warp + 8 + h] * f2;
         }
@@ -703,9 +830,10 @@ Geometry geometry(uint32_t hkv)
     Geometry gm;
     const size_t slot = 2 * (size_t)T::side_bytes(1);
     const size_t park_per_warp = (16 + 32 * 4 * T::MT) * 4;
-    for (uint32_t wph = 8 / hkv; wph >= 1; wph /= 2) {
+    for (uint32_t wph = T::kMaxWarps / hkv; wph >= 1; --wph) {
         const uint32_t warps = wph * hkv;
-        const size_t fixed = 1024 + warps * (size_t)T::SCRATCH + warps * 16 * 12 + 64;
+        const size_t fixed = 1024 + warps * (size_t)T::SCRATCH + warps * 16 * 12 + 64 +
+                             hkv * (size_t)T::QBYTES;
         if (fixed >= kSmemBudget)
             continue;
         size_t ns = (kSmemBudget - fixed) / (warps * slot);
@@ -718,7 +846,8 @@ Geometry geometry(uint32_t hkv)
             gm.slot_bytes = (uint32_t)slot;
             size_t ring = warps * ns * slot, park = warps * park_per_warp;
             gm.region = (uint32_t)(ring > park ? ring : park);
-            gm.smem = 1024 + gm.region + warps * ns * (8 + 4) + 16 + warps * (size_t)T::SCRATCH;
+            gm.smem = 1024 + gm.region + warps * ns * (8 + 4) + 16 + warps * (size_t)T::SCRATCH +
+                      hkv * (size_t)T::QBYTES;
             return gm;
         }
         if (wph == 1)
@@ -776,6 +905,46 @@ cudaError_t allow_smem()
     return cudaSuccess;
 }
 
+// The tensor maps depend only on the pools, their size and the head layout;
+// a few recent encodings are kept so that repeated steps skip the encoding.
+struct MapKey {
+    const void *k, *v;
+    uint64_t n_blocks;
+    uint32_t block_size, hkv, d, type;
+    bool operator==(const MapKey &o) const
+    {
+        return k == o.k && v == o.v && n_blocks == o.n_blocks && block_size == o.block_size &&
+               hkv == o.hkv && d == o.d && type == o.type;
+    }
+};
+
+template <class T>
+int cached_maps(const DecodeParams &p, FastArgs &a, const char *entry)
+{
+    constexpr int kSlots = 8;
+    static std::mutex mu;
+    static MapKey keys[kSlots];
+    static CUtensorMap maps[kSlots][2][kMaxHkv];
+    static bool used[kSlots] = {};
+    static int next = 0;
+    const MapKey key{p.k_pool, p.v_pool, p.n_pool_blocks, p.block_size, p.hkv, (uint32_t)T::D,
+                     (uint32_t)T::kTmaX};
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < kSlots; ++i)
+        if (used[i] && keys[i] == key) {
+            memcpy(a.tm, maps[i], sizeof a.tm);
+            return PA_OK;
+        }
+    int rc = encode_maps<T>(p, a, entry);
+    if (rc)
+        return rc;
+    keys[next] = key;
+    memcpy(maps[next], a.tm, sizeof a.tm);
+    used[next] = true;
+    next = (next + 1) % kSlots;
+    return PA_OK;
+}
+
 template <class T>
 int launch_t(const DecodeParams &p, cudaStream_t st, const char *entry)
 {
@@ -784,7 +953,7 @@ int launch_t(const DecodeParams &p, cudaStream_t st, const char *entry)
         return fail(PA_ERR_INVALID, entry, "fast kernel: a tile does not fit shared memory");
     FastArgs a;
     memset(&a, 0, sizeof a);
-    int rc = encode_maps<T>(p, a, entry);
+    int rc = cached_maps<T>(p, a, entry);
     if (rc)
         return rc;
     a.p = p;
