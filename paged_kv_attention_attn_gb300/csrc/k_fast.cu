@@ -322,15 +322,18 @@ struct Q40T {
     // pair (t, t+8) adjacent, dv as half in token order; zero for invalid tokens.
     __device__ static void extract(uint32_t kh, uint32_t vh, uint32_t scr, int nvalid, int lane)
     {
+        // lane covers token t = lane % 16 of blocks lane / 16 + 2k, k = 0..3
+        const int t = lane & 15, b0 = lane >> 4;
+        const bool v = t < nvalid;
+        const uint32_t ka = kh + t * RB + 18 * b0, va = vh + t * RB + 18 * b0;
+        const uint32_t sk = scr + DK + 4 * (b0 * kTile + 2 * (t & 7) + (t >> 3));
+        const uint32_t sv = scr + DV + 2 * (b0 * kTile + t);
 #pragma unroll
-        for (int k = 0; k < NB * kTile / 32; ++k) {
-            const int e = lane + 32 * k, t = e & 15, b = e >> 4;
-            const bool v = t < nvalid;
-            const uint32_t kd = lds_u16(kh + t * RB + 18 * b);
-            const uint32_t vd = lds_u16(vh + t * RB + 18 * b);
-            sts_f32(scr + DK + 4 * (b * kTile + 2 * (t & 7) + (t >> 3)),
-                    v ? half_bits_to_float((uint16_t)kd) : 0.0f);
-            sts_u16(scr + DV + 2 * (b * kTile + t), v ? vd : 0u);
+        for (int k = 0; k < NB / 2; ++k) {
+            const uint32_t kd = lds_u16(ka + 36 * k);
+            const uint32_t vd = lds_u16(va + 36 * k);
+            sts_f32(sk + 128 * k, v ? half_bits_to_float((uint16_t)kd) : 0.0f);
+            sts_u16(sv + 64 * k, v ? vd : 0u);
         }
     }
 
@@ -361,21 +364,23 @@ struct Q40T {
     __device__ static void scores(const NibbleConsts &K, const Frag &f, uint32_t kh, uint32_t scr,
                                   int gid, int tig, float (&s)[4])
     {
-        const uint32_t r0 = kh + gid * RB + 4 * tig, r1 = r0 + 8 * RB;
-        const uint32_t dk = scr + DK + 8 * gid;
+        uint32_t r0 = kh + gid * RB + 4 * tig;
+        uint32_t dk = scr + DK + 8 * gid;
+        uint32_t qr = f.q;
         s[0] = s[1] = s[2] = s[3] = 0.0f;
-#pragma unroll 1
+#pragma unroll
         for (int pb = 0; pb < NB / 2; ++pb) {
             // blocks 2pb and 2pb+1 share 36 bytes = 9 aligned words
-            const uint32_t a0 = lds_u32(r0 + 36 * pb), a1 = lds_u32(r0 + 36 * pb + 4);
-            const uint32_t a2 = lds_u32(r0 + 36 * pb + 20);
-            const uint32_t b0 = lds_u32(r1 + 36 * pb), b1 = lds_u32(r1 + 36 * pb + 4);
-            const uint32_t b2 = lds_u32(r1 + 36 * pb + 20);
-            const float2 k0 = lds_f2(dk + 4 * (2 * pb) * kTile);
-            const float2 k1 = lds_f2(dk + 4 * (2 * pb + 1) * kTile);
-            const uint32_t qr = f.q + (2 * pb) * 32 * QREC;
+            const uint32_t a0 = lds_u32(r0), a1 = lds_u32(r0 + 4), a2 = lds_u32(r0 + 20);
+            const uint32_t b0 = lds_u32(r0 + 8 * RB), b1 = lds_u32(r0 + 8 * RB + 4);
+            const uint32_t b2 = lds_u32(r0 + 8 * RB + 20);
+            const float2 k0 = lds_f2(dk);
+            const float2 k1 = lds_f2(dk + 4 * kTile);
             block(K, qr, __funnelshift_r(a0, a1, 16), __funnelshift_r(b0, b1, 16), k0, s);
             block(K, qr + 32 * QREC, a2, b2, k1, s);
+            r0 += 36;
+            dk += 2 * 4 * kTile;
+            qr += 2 * 32 * QREC;
         }
     }
 
@@ -670,7 +675,7 @@ __global__ void __launch_bounds__(T::kMaxWarps * 32, 1)
             t0m = fmaxf(t0m, __shfl_xor_sync(0xffffffffu, t0m, off));
             t1m = fmaxf(t1m, __shfl_xor_sync(0xffffffffu, t1m, off));
         }
-        if (__any_sync(0xffffffffu, t0m > mref0 || t1m > mref1)) {
+        if (__builtin_expect(__any_sync(0xffffffffu, t0m > mref0 || t1m > mref1), 0)) {
             const float n0 = t0m > mref0 ? t0m + kHeadroom : mref0;
             const float n1 = t1m > mref1 ? t1m + kHeadroom : mref1;
             const float a0 = mref0 == -INFINITY ? 0.0f : exp2f(mref0 - n0);
@@ -750,7 +755,7 @@ __global__ void __launch_bounds__(T::kMaxWarps * 32, 1)
     __syncthreads();
     if (sub != 0)
         return;
-    float M[2], l[2], fk[12][2];
+    float M[2], l[2], fk[16][2];
 #pragma unroll
     for (int c = 0; c < 2; ++c) {
         const int h = 2 * tig + c;
