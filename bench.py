@@ -57,8 +57,9 @@ def load_peaks():
     return 6800.0, "fallback"
 
 
-def algorithmic_bytes(spec, plan) -> dict:
-    """Bytes the method must move in one step, by class."""
+def algorithmic_bytes(spec, plan, fused: bool = True) -> dict:
+    """Bytes the method must move in one step, by class.  With the fused
+    merge the decode launch also reads the partials back and writes out."""
     S, hq, d = spec.n_seqs, spec.hq, spec.d
     krb, vrb = synth.row_bytes(spec.k_type, d), synth.row_bytes(spec.v_type, d)
     lens = spec.seq_lens
@@ -79,6 +80,9 @@ def algorithmic_bytes(spec, plan) -> dict:
         dec_out = part_w
     merge = 0 if plan.direct else part_r + out + S * 4
     decode = kv + table + q_read + dec_out + S * 4
+    if fused and not plan.direct:
+        decode += merge
+        merge = 0
     return dict(kv=kv, table=table, prepass=prepass, decode=decode, merge=merge,
                 step=prepass + decode + merge)
 
@@ -271,12 +275,15 @@ def run_ours(a, world, rank, local):
                             q=ws.q8_1 if quantised else case.q, ws=ws, hkv=spec.hkv,
                             block_size=spec.block_size, k_type=spec.k_type,
                             v_type=spec.v_type, flags=flags)
-    nb = algorithmic_bytes(spec, pl)
+    nb = algorithmic_bytes(spec, pl, fused=not a.unfused)
     stream = torch.cuda.current_stream()
     L = pa.lib()
     import ctypes
     p_args, p_plan = ctypes.byref(dec_args), ctypes.byref(pl)
     sh = stream.cuda_stream
+
+    fused = not a.unfused
+    counters = ws.counters.data_ptr()
 
     def step(ev0=None, ev1=None):
         if quantised:
@@ -284,10 +291,13 @@ def run_ours(a, world, rank, local):
                             spec.d, sh)
         if ev0 is not None:
             ev0.record(stream)
-        rc = L.pa_decode_partial(p_args, p_plan, sh)
+        if fused:  # merge inside the decode launch
+            rc = L.pa_decode_fused(p_args, p_plan, counters, sh)
+        else:
+            rc = L.pa_decode_partial(p_args, p_plan, sh)
         if ev1 is not None:
             ev1.record(stream)
-        if not pl.direct:
+        if not fused and not pl.direct:
             L.pa_merge(ws.part_o.data_ptr(), ws.part_ml.data_ptr(), case.seq_lens.data_ptr(),
                        ws.out.data_ptr(), spec.n_seqs, spec.hq, spec.d, p_plan, sh)
         return rc
@@ -330,18 +340,19 @@ def run_ours(a, world, rank, local):
     q_host = case.q.cpu().pin_memory()
     out_host = torch.empty(ws.out.shape, dtype=torch.float32).pin_memory()
     qdev = torch.empty_like(case.q)
+    e2e_call = pa.decode_step_host if a.unfused else pa.decode_step_fused_host
     e2e_args = pa.make_args(k_pool=case.k_pool, v_pool=case.v_pool,
                             block_table=case.block_table, seq_lens=case.seq_lens, q=qdev,
                             ws=ws, hkv=spec.hkv, block_size=spec.block_size,
                             k_type=spec.k_type, v_type=spec.v_type, flags=flags)
     for _ in range(a.warmup):
-        pa.decode_step_host(q_host, out_host, e2e_args, ws)
+        e2e_call(q_host, out_host, e2e_args, ws)
     torch.cuda.synchronize()
     barrier(world)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(K):
-        pa.decode_step_host(q_host, out_host, e2e_args, ws)
+        e2e_call(q_host, out_host, e2e_args, ws)
     e1.record(stream)
     torch.cuda.synchronize()
     barrier(world)
@@ -376,6 +387,8 @@ def run_ours(a, world, rank, local):
                    "kv_type": synth.TYPE_LABEL[spec.k_type],
                    "l2": f"inputs larger than L2: {nb['kv'] / 1e9:.3f} GB of K/V per step",
                    "kernel": kname, "plan": pl.as_dict(),
+                   "step": ("q8_1 pre-pass + decode with in-launch merge" if fused else
+                            "q8_1 pre-pass + decode + merge kernel"),
                    "bytes_per_step": nb},
         "roofline": {"bound": "hbm", "achieved": dec_achieved, "peak": peak, "unit": "GB/s",
                      "frac": dec_achieved / peak, "peak_kind": peak_kind,
@@ -384,7 +397,7 @@ def run_ours(a, world, rank, local):
                      "traffic": traffic_from_profiles(kname)},
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": K * ((2 if quantised else 1) + (0 if pl.direct else 1)),
+        "gpu_launches": K * ((2 if quantised else 1) + (0 if (pl.direct or fused) else 1)),
         "clocks": clk,
     }
     if rank == 0:
@@ -400,6 +413,8 @@ def main():
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD)
     ap.add_argument("--seed", type=int, default=2001)
     ap.add_argument("--plain", action="store_true", help="force the plain decode kernel")
+    ap.add_argument("--unfused", action="store_true",
+                    help="time the three-launch step (separate merge) instead of the fused one")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-steps", type=int, default=None)
     ap.add_argument("--ref-warmup", type=int, default=None)

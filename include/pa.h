@@ -186,7 +186,8 @@ typedef struct {
     float scale;                     /* softmax scale; callers pass 1/sqrt(d) */
     void *part_o;                    /* device f16 [n_seqs][hq][n_parts][d] (unused if direct) */
     float *part_ml;                  /* device float32 [n_seqs][hq][n_parts][2] */
-    float *out;                      /* device float32 [n_seqs][hq][d] (written if direct) */
+    float *out;                      /* device float32 [n_seqs][hq][d], 16-byte aligned
+                                        (written if direct or fused) */
     int32_t *status;                 /* device int32 status word (required) */
     uint32_t n_seqs, hq, hkv, d, block_size;
     pa_type k_type, v_type;
@@ -216,6 +217,28 @@ const char *pa_decode_kernel_name(pa_type k_type, pa_type v_type, uint32_t d, ui
 int pa_merge(const void *part_o, const float *part_ml, const int32_t *seq_lens, float *out,
              uint32_t n_seqs, uint32_t hq, uint32_t d, const pa_plan_t *plan,
              pa_stream_t stream);
+
+/* pa_decode_partial with the merge done inside the same launch ("HRX:
+ * multi-pass KV-block reduction for flash-attention decode-split", llama.cpp
+ * fork pull 13, Changes: an atomic completion counter lets the reduction run
+ * in the decode launch itself, with no second dispatch).  Every CTA writes its
+ * partial as pa_decode_partial does, then counts it in counters[s]; the CTA
+ * that completes sequence s merges that sequence's partials into out exactly
+ * as pa_merge would, and resets counters[s] to 0.  No CTA ever waits for
+ * another.
+ * counters: device int32 [n_seqs], caller-owned, all zero before the first
+ * call; every completed call leaves them zero.  After a call that reported
+ * PA_STATUS_TIMEOUT the caller zeroes them again.  Calls that share a counter
+ * array must not overlap on the GPU.  Direct plans ignore counters (may be
+ * NULL) and behave as pa_decode_partial.  part_o / part_ml / out are required
+ * for partitioned plans. */
+int pa_decode_fused(const pa_decode_args *args, const pa_plan_t *plan, int32_t *counters,
+                    pa_stream_t stream);
+
+/* pa_decode_step with the fused merge: pa_quantize_q (quantised K) and
+ * pa_decode_fused, two launches on `stream`. */
+int pa_decode_step_fused(const pa_decode_args *args, const pa_plan_t *plan, void *q8_1_scratch,
+                         int32_t *counters, pa_stream_t stream);
 
 /* One full decode step on the device: pa_quantize_q (quantised K only, into
  * q8_1_scratch of n_seqs*hq*d/32*36 bytes), pa_decode_partial, and pa_merge
@@ -258,6 +281,12 @@ int pa_decode_step_host(const float *q_host, float *out_host, const pa_decode_ar
 #define PA_NOALLOC_SCRATCH_BYTES (16ull << 20)
 int pa_decode_step_noalloc(const pa_decode_args *args, const pa_plan_t *plan,
                            pa_stream_t stream);
+
+/* pa_decode_step_host with the fused merge: host q in, host out back, with
+ * pa_decode_step_fused in between, all on `stream`. */
+int pa_decode_step_fused_host(const float *q_host, float *out_host, const pa_decode_args *args,
+                              const pa_plan_t *plan, void *q8_1_scratch, int32_t *counters,
+                              pa_stream_t stream);
 
 /* Reads the status word into *host_out (synchronising `stream`); reset != 0
  * clears it afterwards.  Returns PA_ERR_TIMEOUT if the timeout bit is set,

@@ -87,6 +87,10 @@ _SIGNATURES = {
                           ctypes.c_int),
     "pa_decode_kernel_name": ([ctypes.c_int, ctypes.c_int, _u32, _u32, _u32, _u32, _u32],
                               ctypes.c_char_p),
+    "pa_decode_fused": ([ctypes.POINTER(DecodeArgs), ctypes.POINTER(Plan), _vp, _vp],
+                        ctypes.c_int),
+    "pa_decode_step_fused": ([ctypes.POINTER(DecodeArgs), ctypes.POINTER(Plan), _vp, _vp, _vp],
+                             ctypes.c_int),
     "pa_merge": ([_vp, _vp, _vp, _vp, _u32, _u32, _u32, ctypes.POINTER(Plan), _vp],
                  ctypes.c_int),
     "pa_decode_step": ([ctypes.POINTER(DecodeArgs), ctypes.POINTER(Plan), _vp, _vp],
@@ -95,6 +99,8 @@ _SIGNATURES = {
                              _vp, _vp], ctypes.c_int),
     "pa_decode_step_noalloc": ([ctypes.POINTER(DecodeArgs), ctypes.POINTER(Plan), _vp],
                                ctypes.c_int),
+    "pa_decode_step_fused_host": ([_vp, _vp, ctypes.POINTER(DecodeArgs), ctypes.POINTER(Plan),
+                                   _vp, _vp, _vp], ctypes.c_int),
     "pa_status_read": ([_vp, _vp, ctypes.POINTER(_i32), ctypes.c_int], ctypes.c_int),
     "pa_debug_row_offsets": ([_vp, _u32, _vp, _u32, _u32, _u32, _u32, _u64, _u64, _vp,
                               _vp, _vp], ctypes.c_int),
@@ -238,6 +244,7 @@ class Workspace:
     part_ml: torch.Tensor   # float32 [S, hq, n_parts, 2]
     status: torch.Tensor    # int32 [1]
     q8_1: torch.Tensor      # uint8 [S, hq, d/32*36]
+    counters: torch.Tensor  # int32 [S], zero: fused-merge completion counters
 
 
 def workspace(pl: Plan, *, n_seqs, hq, d, device) -> Workspace:
@@ -248,7 +255,8 @@ def workspace(pl: Plan, *, n_seqs, hq, d, device) -> Workspace:
         part_o=torch.empty((n_seqs, hq, P, d), dtype=torch.float16, device=device),
         part_ml=torch.empty((n_seqs, hq, P, 2), dtype=torch.float32, device=device),
         status=torch.zeros(1, dtype=torch.int32, device=device),
-        q8_1=torch.empty((n_seqs, hq, d // 32 * 36), dtype=torch.uint8, device=device))
+        q8_1=torch.empty((n_seqs, hq, d // 32 * 36), dtype=torch.uint8, device=device),
+        counters=torch.zeros(n_seqs, dtype=torch.int32, device=device))
 
 
 def make_args(*, k_pool, v_pool, block_table, seq_lens, q, ws: Workspace, hkv, block_size,
@@ -272,6 +280,19 @@ def decode_kernel_name(*, k_type, v_type, d, hq, hkv, block_size, flags=0) -> st
     """Which decode kernel pa_decode_partial would launch for these shapes."""
     r = lib().pa_decode_kernel_name(k_type, v_type, d, hq, hkv, block_size, flags)
     return r.decode() if r else None
+
+
+def decode_fused(args: DecodeArgs, ws: Workspace, stream=None) -> None:
+    """pa_decode_fused: decode with the merge inside the same launch."""
+    _check(lib().pa_decode_fused(ctypes.byref(args), ctypes.byref(ws.plan), _ptr(ws.counters),
+                                 _stream(stream)))
+
+
+def decode_step_fused(args: DecodeArgs, ws: Workspace, stream=None) -> None:
+    """pa_decode_step_fused: q8_1 pre-pass and the fused decode (args.q is
+    the float32 query)."""
+    _check(lib().pa_decode_step_fused(ctypes.byref(args), ctypes.byref(ws.plan), _ptr(ws.q8_1),
+                                      _ptr(ws.counters), _stream(stream)))
 
 
 def merge(ws: Workspace, seq_lens: torch.Tensor, stream=None) -> None:
@@ -304,6 +325,15 @@ def decode_step_noalloc(args: DecodeArgs, pl: Plan, stream=None) -> None:
     device memory.  args.q must point at the float32 query; args.part_o and
     args.part_ml are ignored."""
     _check(lib().pa_decode_step_noalloc(ctypes.byref(args), ctypes.byref(pl), _stream(stream)))
+
+
+def decode_step_fused_host(q_host: torch.Tensor, out_host: torch.Tensor, args: DecodeArgs,
+                           ws: Workspace, stream=None) -> None:
+    """pa_decode_step_fused_host: host q in, fused decode, host out back."""
+    assert not q_host.is_cuda and not out_host.is_cuda
+    _check(lib().pa_decode_step_fused_host(_ptr(q_host), _ptr(out_host), ctypes.byref(args),
+                                           ctypes.byref(ws.plan), _ptr(ws.q8_1),
+                                           _ptr(ws.counters), _stream(stream)))
 
 
 def status_read(status: torch.Tensor, reset: bool = True, stream=None) -> int:

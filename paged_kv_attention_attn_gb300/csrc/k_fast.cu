@@ -533,6 +533,12 @@ struct F16T {
 constexpr float kHeadroom = 4.0f;  // log2 units kept between the reference and the max
 
 template <class T>
+__device__ __forceinline__ void combine_and_write(const DecodeParams &p, const float *park,
+                                                  int per_warp, uint32_t g, uint32_t hkv,
+                                                  uint32_t wph, uint32_t G, uint32_t seq,
+                                                  uint32_t part, int gid, int tig, int lane);
+
+template <class T>
 __global__ void __launch_bounds__(T::kMaxWarps * 32, 1)
     fast_decode_kernel(const __grid_constant__ FastArgs a)
 {
@@ -753,8 +759,20 @@ __global__ void __launch_bounds__(T::kMaxWarps * 32, 1)
         for (int e = 0; e < 4; ++e)
             mine[16 + (mt * 4 + e) * 32 + lane] = o[mt][e];
     __syncthreads();
-    if (sub != 0)
-        return;
+    if (sub == 0)
+        combine_and_write<T>(p, park, per_warp, g, hkv, wph, G, seq, part, gid, tig, lane);
+    if (p.counters && !p.direct)
+        fused_merge_tail(p, seq, warp, nwarps);
+}
+
+// The first warp of head group g combines the parked (m, l, O) of the wph
+// warps of that group and writes the partial (or, direct, the output).
+template <class T>
+__device__ __forceinline__ void combine_and_write(const DecodeParams &p, const float *park,
+                                                  int per_warp, uint32_t g, uint32_t hkv,
+                                                  uint32_t wph, uint32_t G, uint32_t seq,
+                                                  uint32_t part, int gid, int tig, int lane)
+{
     float M[2], l[2], fk[16][2];
 #pragma unroll
     for (int c = 0; c < 2; ++c) {

@@ -300,6 +300,8 @@ __global__ void __launch_bounds__(kPlainWarps * 32) plain_decode_kernel(const De
         }
         __syncwarp();
     }
+    if (p.counters && !p.direct)
+        fused_merge_tail(p, s, threadIdx.x >> 5, blockDim.x >> 5);
 }
 
 template <int KT, int VT, int D>
@@ -359,54 +361,23 @@ int launch_plain_decode(const DecodeParams &p, pa_type kt, pa_type vt, cudaStrea
 }
 
 // -------------------------------------------------------------------- merge
-// Stable split-softmax merge of the stored f16 partials ("feat: add
-// paged-attention monolithic decode-only AR foundation", lucebox pull 555,
-// Summary): M = max m_p, w_p = l_p 2^(m_p - M), out = sum w_p o_p / sum w_p.
-// One CTA per (sequence, query head); dead partitions (l_p == 0) get weight 0.
+// Stable split-softmax merge of the stored f16 partials: one warp per
+// (sequence, query head) row, the same routine the fused decode uses.
 __global__ void __launch_bounds__(128) merge_kernel(const __half *__restrict__ po,
                                                     const float2 *__restrict__ pml,
                                                     const int32_t *__restrict__ seq_lens,
                                                     float *__restrict__ out, uint32_t hq,
                                                     uint32_t D, uint32_t n_parts,
-                                                    uint32_t part_tokens)
+                                                    uint32_t part_tokens, uint64_t units)
 {
-    extern __shared__ float w[];  // [n_parts] weights, then the weight sum
-    const uint64_t sh = blockIdx.x;
-    const uint32_t s = (uint32_t)(sh / hq);
-    const int32_t L = seq_lens[s];
+    const uint64_t sh = (uint64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (sh >= units)
+        return;
+    const int32_t L = seq_lens[sh / hq];
     uint32_t n_live = L > 0 ? ((uint32_t)L + part_tokens - 1) / part_tokens : 0;
     if (n_live > n_parts)
         n_live = n_parts;
-    const uint64_t base = sh * n_parts;
-    if (threadIdx.x < 32) {
-        float M = -INFINITY;
-        for (uint32_t p = threadIdx.x; p < n_live; p += 32) {
-            float2 ml = pml[base + p];
-            if (ml.y > 0.0f)
-                M = fmaxf(M, ml.x);
-        }
-        M = warp_max(M);
-        float ws = 0.0f;
-        for (uint32_t p = threadIdx.x; p < n_live; p += 32) {
-            float2 ml = pml[base + p];
-            float wp = ml.y > 0.0f ? ml.y * exp2f(ml.x - M) : 0.0f;
-            w[p] = wp;
-            ws += wp;
-        }
-        ws = warp_sum(ws);
-        if (threadIdx.x == 0)
-            w[n_parts] = ws;
-    }
-    __syncthreads();
-    const float ws = w[n_parts];
-    const float inv = ws > 0.0f ? 1.0f / ws : 0.0f;
-    for (uint32_t i = threadIdx.x; i < D; i += blockDim.x) {
-        float acc = 0.0f;
-        for (uint32_t p = 0; p < n_live; ++p)
-            if (w[p] > 0.0f)
-                acc = fmaf(w[p], __half2float(po[(base + p) * D + i]), acc);
-        out[sh * D + i] = acc * inv;
-    }
+    merge_row_warp(po + sh * n_parts * D, pml + sh * n_parts, out + sh * D, n_live, D);
 }
 
 int launch_merge(const void *part_o, const float *part_ml, const int32_t *seq_lens, float *out,
@@ -416,14 +387,13 @@ int launch_merge(const void *part_o, const float *part_ml, const int32_t *seq_le
     uint64_t units = (uint64_t)n_seqs * hq;
     if (units == 0)
         return PA_OK;
-    if (units > 0x7fffffffull)
-        return fail(PA_ERR_RANGE, entry, "n_seqs * hq exceeds 2^31-1");
-    size_t smem = (size_t)(n_parts + 1) * sizeof(float);
-    if (smem > 48 * 1024)
-        return fail(PA_ERR_RANGE, entry, "n_parts %u too large for the merge", n_parts);
-    merge_kernel<<<(unsigned)units, 128, smem, st>>>(
+    if ((units + 3) / 4 > 0x7fffffffull)
+        return fail(PA_ERR_RANGE, entry, "n_seqs * hq too large for the merge grid");
+    if (d != 128 && d != 256)
+        return fail(PA_ERR_INVALID, entry, "d %u unsupported by the merge (128 or 256)", d);
+    merge_kernel<<<(unsigned)((units + 3) / 4), 128, 0, st>>>(
         static_cast<const __half *>(part_o), reinterpret_cast<const float2 *>(part_ml), seq_lens,
-        out, hq, d, n_parts, part_tokens);
+        out, hq, d, n_parts, part_tokens, units);
     return cuda_check(cudaGetLastError(), entry, "merge_kernel launch");
 }
 

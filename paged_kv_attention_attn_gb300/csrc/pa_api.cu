@@ -61,6 +61,8 @@ int resolve(const pa_decode_args *a, const pa_plan_t *plan, const char *E, pa::D
                                                     : "partitioned plan needs part_o and part_ml");
     if (!plan->direct && (!aligned16(a->part_o) || (reinterpret_cast<uintptr_t>(a->part_ml) & 7)))
         return fail(PA_ERR_INVALID, E, "part_o must be 16-byte and part_ml 8-byte aligned");
+    if (a->out && (reinterpret_cast<uintptr_t>(a->out) & 15))
+        return fail(PA_ERR_INVALID, E, "out must be 16-byte aligned");
     if (plan->direct && plan->n_ctas != a->n_seqs)
         return fail(PA_ERR_INVALID, E, "direct plan must have n_ctas == n_seqs");
     if (a->table_stride == 0)
@@ -92,6 +94,7 @@ int resolve(const pa_decode_args *a, const pa_plan_t *plan, const char *E, pa::D
     p->n_ctas = plan->n_ctas;
     p->k_row_bytes = pa_row_bytes(a->k_type, a->d);
     p->v_row_bytes = pa_row_bytes(a->v_type, a->d);
+    p->counters = nullptr;
     return PA_OK;
 }
 
@@ -176,6 +179,52 @@ extern "C" const char *pa_decode_kernel_name(pa_type kt, pa_type vt, uint32_t d,
     return "plain_decode_kernel";
 }
 
+extern "C" int pa_decode_fused(const pa_decode_args *args, const pa_plan_t *plan,
+                               int32_t *counters, pa_stream_t stream)
+{
+    static const char *E = "pa_decode_fused";
+    pa::DecodeParams p;
+    int rc = resolve(args, plan, E, &p);
+    if (rc)
+        return rc;
+    if (!plan->direct) {
+        if (!counters || (reinterpret_cast<uintptr_t>(counters) & 3))
+            return fail(PA_ERR_INVALID, E, "a partitioned plan needs 4-byte aligned counters");
+        if (!args->out)
+            return fail(PA_ERR_INVALID, E, "out is NULL");
+        p.counters = counters;
+    }
+    return launch_decode(args, p, pa::stream_of(stream), E);
+}
+
+extern "C" int pa_decode_step_fused(const pa_decode_args *args, const pa_plan_t *plan,
+                                    void *q8_1_scratch, int32_t *counters, pa_stream_t stream)
+{
+    static const char *E = "pa_decode_step_fused";
+    pa::DecodeParams p;
+    int rc = resolve(args, plan, E, &p);
+    if (rc)
+        return rc;
+    if (!plan->direct) {
+        if (!counters || (reinterpret_cast<uintptr_t>(counters) & 3))
+            return fail(PA_ERR_INVALID, E, "a partitioned plan needs 4-byte aligned counters");
+        if (!args->out)
+            return fail(PA_ERR_INVALID, E, "out is NULL");
+        p.counters = counters;
+    }
+    cudaStream_t st = pa::stream_of(stream);
+    if (args->k_type != PA_F16) {
+        if (!q8_1_scratch || (reinterpret_cast<uintptr_t>(q8_1_scratch) & 15))
+            return fail(PA_ERR_INVALID, E, "quantised K needs a 16-byte aligned q8_1_scratch");
+        rc = pa::launch_quantize_q(static_cast<const float *>(args->q), q8_1_scratch,
+                                   args->n_seqs * args->hq, args->d, st, E);
+        if (rc)
+            return rc;
+        p.q = q8_1_scratch;
+    }
+    return launch_decode(args, p, st, E);
+}
+
 extern "C" int pa_merge(const void *part_o, const float *part_ml, const int32_t *seq_lens,
                         float *out, uint32_t n_seqs, uint32_t hq, uint32_t d,
                         const pa_plan_t *plan, pa_stream_t stream)
@@ -188,7 +237,10 @@ extern "C" int pa_merge(const void *part_o, const float *part_ml, const int32_t 
         return fail(PA_ERR_INVALID, E, "a direct plan has no partials to merge");
     if (!part_o || !part_ml || !seq_lens || !out)
         return fail(PA_ERR_INVALID, E, "NULL device pointer");
-    if (n_seqs == 0 || hq == 0 || d == 0 || d % 32)
+    if (!aligned16(part_o) || (reinterpret_cast<uintptr_t>(part_ml) & 7) ||
+        (reinterpret_cast<uintptr_t>(out) & 15))
+        return fail(PA_ERR_INVALID, E, "part_o and out must be 16-byte, part_ml 8-byte aligned");
+    if (n_seqs == 0 || hq == 0 || (d != 128 && d != 256))
         return fail(PA_ERR_INVALID, E, "bad shape (n_seqs %u, hq %u, d %u)", n_seqs, hq, d);
     const uint64_t elems = (uint64_t)n_seqs * hq * plan->n_parts * d;
     if (elems > (1ull << 40))
@@ -243,6 +295,34 @@ extern "C" int pa_decode_step_host(const float *q_host, float *out_host,
     if (rc)
         return rc;
     rc = pa_decode_step(args, plan, q8_1_scratch, stream);
+    if (rc)
+        return rc;
+    return cuda_check(cudaMemcpyAsync(out_host, args->out, bytes, cudaMemcpyDeviceToHost, st), E,
+                      "copy of out to the host");
+}
+
+extern "C" int pa_decode_step_fused_host(const float *q_host, float *out_host,
+                                         const pa_decode_args *args, const pa_plan_t *plan,
+                                         void *q8_1_scratch, int32_t *counters,
+                                         pa_stream_t stream)
+{
+    static const char *E = "pa_decode_step_fused_host";
+    if (!q_host || !out_host || !args || !args->q || !args->out)
+        return fail(PA_ERR_INVALID, E, "NULL host or device pointer");
+    pa::DecodeParams p;
+    int rc = resolve(args, plan, E, &p);  // refuse before copying anything
+    if (rc)
+        return rc;
+    if (!plan->direct && !counters)
+        return fail(PA_ERR_INVALID, E, "a partitioned plan needs counters");
+    const size_t bytes = (size_t)args->n_seqs * args->hq * args->d * sizeof(float);
+    cudaStream_t st = pa::stream_of(stream);
+    rc = cuda_check(cudaMemcpyAsync(const_cast<void *>(args->q), q_host, bytes,
+                                    cudaMemcpyHostToDevice, st),
+                    E, "copy of q to the device");
+    if (rc)
+        return rc;
+    rc = pa_decode_step_fused(args, plan, q8_1_scratch, counters, stream);
     if (rc)
         return rc;
     return cuda_check(cudaMemcpyAsync(out_host, args->out, bytes, cudaMemcpyDeviceToHost, st), E,

@@ -95,4 +95,129 @@ __device__ __forceinline__ bool cta_work(const int32_t *seq_lens, uint32_t n_seq
     return false;
 }
 
+// Stable split-softmax merge of the stored partials of one (sequence, query
+// head) row, executed by one warp ("feat: add paged-attention monolithic
+// decode-only AR foundation", lucebox pull 555, Summary): M = max m_p over
+// partials with l_p > 0, w_p = l_p 2^(m_p - M), out = sum_p w_p o_p / sum_p w_p;
+// partials with l_p == 0 are skipped and none gives 0.  po / pml point at the
+// row's n_parts partials; loads go through L2 (.cg) so that partials written by
+// other CTAs of the same launch are seen.  D is a multiple of 32.
+template <int VEC>
+__device__ __forceinline__ void merge_row_warp_v(const __half *po, const float2 *pml, float *out,
+                                                 uint32_t n_live, uint32_t D)
+{
+    const int lane = threadIdx.x & 31;
+    // reference maximum over live partials
+    float M = -INFINITY;
+    for (uint32_t p = lane; p < n_live; p += 32) {
+        const float2 ml = __ldcg(pml + p);
+        if (ml.y > 0.0f)
+            M = fmaxf(M, ml.x);
+    }
+    M = warp_max(M);
+    float acc[VEC];
+#pragma unroll
+    for (int j = 0; j < VEC; ++j)
+        acc[j] = 0.0f;
+    float ws = 0.0f;  // lane-partial sum of the weights
+    for (uint32_t c = 0; c < n_live; c += 32) {
+        // lane p holds the weight of partial c + p (0 for dead or absent ones)
+        float w = 0.0f;
+        if (c + lane < n_live) {
+            const float2 ml = __ldcg(pml + c + lane);
+            if (ml.y > 0.0f)
+                w = ml.y * exp2f(ml.x - M);
+        }
+        ws += w;
+        const uint32_t cnt = min(32u, n_live - c);
+        for (uint32_t q0 = 0; q0 < cnt; q0 += 8) {
+            // eight partial rows in flight at once; this lane's VEC values each
+            uint4 raw[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const uint32_t pk = c + q0 + k;
+                if (q0 + k < cnt) {
+                    const __half *src = po + (uint64_t)pk * D + VEC * lane;
+                    if constexpr (VEC == 8) {
+                        raw[k] = __ldcg(reinterpret_cast<const uint4 *>(src));
+                    } else {
+                        const uint2 r2 = __ldcg(reinterpret_cast<const uint2 *>(src));
+                        raw[k] = make_uint4(r2.x, r2.y, 0u, 0u);
+                    }
+                }
+            }
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const float wk = __shfl_sync(0xffffffffu, w, (q0 + k) & 31);
+                if (q0 + k < cnt && wk > 0.0f) {
+                    const __half2 *h2 = reinterpret_cast<const __half2 *>(&raw[k]);
+#pragma unroll
+                    for (int j = 0; j < VEC / 2; ++j) {
+                        const float2 f = __half22float2(h2[j]);
+                        acc[2 * j] = fmaf(wk, f.x, acc[2 * j]);
+                        acc[2 * j + 1] = fmaf(wk, f.y, acc[2 * j + 1]);
+                    }
+                }
+            }
+        }
+    }
+    ws = warp_sum(ws);
+    const float inv = ws > 0.0f ? 1.0f / ws : 0.0f;
+    float *o = out + VEC * lane;
+#pragma unroll
+    for (int j = 0; j < VEC; ++j)
+        o[j] = acc[j] * inv;
+}
+
+// Stable split-softmax merge of the stored partials of one (sequence, query
+// head) row, executed by one warp ("feat: add paged-attention monolithic
+// decode-only AR foundation", lucebox pull 555, Summary): M = max m_p over
+// partials with l_p > 0, w_p = l_p 2^(m_p - M), out = sum_p w_p o_p / sum_p w_p
+// (summed in partition order); partials with l_p == 0 are skipped and none
+// gives 0.  po / pml point at the row's partials; loads go through L2 (.cg) so
+// that partials written by other CTAs of the same launch are seen.  Lane i owns
+// dims [D/32 * i, D/32 * (i+1)); D is 128 or 256.
+__device__ __forceinline__ void merge_row_warp(const __half *po, const float2 *pml, float *out,
+                                               uint32_t n_live, uint32_t D)
+{
+    if (D == 256)
+        merge_row_warp_v<8>(po, pml, out, n_live, D);
+    else
+        merge_row_warp_v<4>(po, pml, out, n_live, D);
+}
+
+// In-launch merge ("HRX: multi-pass KV-block reduction for flash-attention
+// decode-split", llama.cpp fork pull 13, Changes: the reduction runs in the
+// same launch through an atomic completion counter, with no second dispatch and
+// no waiting).  Called by every thread of a CTA after it has written the
+// partials of (sequence seq, its partition): the CTA that completes the
+// sequence's count merges all its rows into out and resets the counter to 0.
+// Nothing ever waits on another CTA.
+template <class P>
+__device__ inline void fused_merge_tail(const P &p, uint32_t seq, uint32_t warp, uint32_t nwarps)
+{
+    __shared__ int last;
+    __threadfence();  // this thread's partial writes before the count
+    __syncthreads();
+    const int32_t L = p.seq_lens[seq];
+    const uint32_t n_live = L > 0 ? ((uint32_t)L + p.part_tokens - 1) / p.part_tokens : 0;
+    if (threadIdx.x == 0) {
+        const int old = atomicAdd(&p.counters[seq], 1);
+        last = (uint32_t)(old + 1) == n_live;
+        if (last)
+            p.counters[seq] = 0;  // every partition of this launch has counted
+    }
+    __syncthreads();
+    if (!last)
+        return;
+    __threadfence();  // the other CTAs' partials are visible past their counts
+    const __half *po = static_cast<const __half *>(p.part_o);
+    const float2 *pml = reinterpret_cast<const float2 *>(p.part_ml);
+    for (uint32_t h = warp; h < p.hq; h += nwarps) {
+        const uint64_t sh = (uint64_t)seq * p.hq + h;
+        merge_row_warp(po + sh * p.n_parts * p.d, pml + sh * p.n_parts, p.out + sh * p.d, n_live,
+                       p.d);
+    }
+}
+
 }  // namespace pa

@@ -31,6 +31,7 @@ struct DecodeParams {
     uint32_t n_seqs, hq, hkv, d, block_size;
     uint32_t part_tokens, n_parts, direct, n_ctas;
     uint64_t k_row_bytes, v_row_bytes;
+    int32_t *counters;      // fused merge: per-sequence completion counters, or null
 };
 
 // Launchers (each returns PA_OK or an error already recorded for `entry`).

@@ -45,7 +45,8 @@ def with_canary(t: torch.Tensor, extra_bytes: int = 4096):
     return view, buf[nbytes:]
 
 
-def run(case, *, force_parts=0, flags=0, plan=None, canary=False, step=True, stream=None):
+def run(case, *, force_parts=0, flags=0, plan=None, canary=False, step=True, stream=None,
+        fused=False):
     """One decode step of `case` through the C ABI.  Returns (out float32
     tensor, workspace, plan, canary tails)."""
     sp = case.spec
@@ -63,7 +64,9 @@ def run(case, *, force_parts=0, flags=0, plan=None, canary=False, step=True, str
                         seq_lens=case.seq_lens, q=case.q, ws=ws, hkv=sp.hkv,
                         block_size=sp.block_size, k_type=sp.k_type, v_type=sp.v_type,
                         flags=flags)
-    if step:
+    if fused:
+        pa.decode_step_fused(args, ws, stream=stream)
+    elif step:
         pa.decode_step(args, ws, stream=stream)
     else:
         if sp.k_type != synth.F16:

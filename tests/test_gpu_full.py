@@ -50,6 +50,9 @@ def test_uniform_q4_0(kernel, batch, ctx):
     assert pa.status_read(ws.status) == 0
     units = [(0, 0), (batch - 1, 23), (batch // 2, 11)]
     sampled_check(case, out, units)
+    fused, ws2, _, _ = H.run(case, flags=KERNELS[kernel], fused=True)
+    assert torch.equal(fused.view(torch.int32), out.view(torch.int32))
+    assert int(ws2.counters.abs().sum()) == 0
 
 
 @pytest.mark.parametrize("kernel", KERNELS)

@@ -222,3 +222,46 @@ def test_host_buffer_step_equals_device_step(kernel):
     pa.decode_step_host(q_host, out_host, args, ws)
     torch.cuda.synchronize()
     assert torch.equal(out_host.view(torch.int32), dev_out.cpu().view(torch.int32))
+    out_host.zero_()
+    pa.decode_step_fused_host(q_host, out_host, args, ws)
+    torch.cuda.synchronize()
+    assert torch.equal(out_host.view(torch.int32), dev_out.cpu().view(torch.int32))
+
+
+# ------------------------------------------------------------- fused merge
+
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("t", TYPES)
+@pytest.mark.parametrize("force", [0, 1, 6])
+def test_fused_merge_equals_separate_merge(kernel, t, force):
+    """The in-launch merge runs the same merge routine as pa_merge, so the
+    two paths give the same bits; the counters are left at zero."""
+    spec = synth.CaseSpec(seq_lens=[1500, 33, 0, 700, 16], k_type=t, v_type=t, junk=7,
+                          outliers=True)
+    case = synth.build_case(spec, seed=2600 + t, device=DEV)
+    a, _, pl, _ = H.run(case, force_parts=force, flags=KERNELS[kernel])
+    b, ws, pl2, tails = H.run(case, force_parts=force, flags=KERNELS[kernel], fused=True,
+                              canary=True)
+    H.check_canaries(tails)
+    assert pl.as_dict() == pl2.as_dict()
+    assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+    assert int(ws.counters.abs().sum()) == 0
+    assert pa.status_read(ws.status) == 0
+    H.assert_close(case, b, H.oracle_out(case), H.oracle_vmax(case))
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_fused_merge_repeated_calls_reuse_counters(kernel):
+    spec = synth.CaseSpec(seq_lens=[2000, 300], k_type=synth.Q4_0, v_type=synth.Q4_0, junk=3)
+    case = synth.build_case(spec, seed=2700, device=DEV)
+    ref, _, pl, _ = H.run(case, force_parts=5, flags=KERNELS[kernel])
+    ws = pa.workspace(pl, n_seqs=2, hq=24, d=256, device=DEV)
+    args = pa.make_args(k_pool=case.k_pool, v_pool=case.v_pool, block_table=case.block_table,
+                        seq_lens=case.seq_lens, q=case.q, ws=ws, hkv=4, block_size=16,
+                        k_type=spec.k_type, v_type=spec.v_type, flags=KERNELS[kernel])
+    for _ in range(3):
+        ws.out.fill_(float("nan"))
+        pa.decode_step_fused(args, ws)
+        torch.cuda.synchronize()
+        assert torch.equal(ws.out.view(torch.int32), ref.view(torch.int32))
+        assert int(ws.counters.abs().sum()) == 0

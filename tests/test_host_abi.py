@@ -156,3 +156,13 @@ def test_merge_and_plan_refusals():
         pa.PA_ERR_RANGE
     assert b"pa_merge" in L.pa_last_error()
     assert L.pa_quantize_q(16, 16, 1, 48, None) == pa.PA_ERR_INVALID
+
+
+def test_fused_refuses_missing_counters():
+    pl = pa.Plan(part_tokens=128, n_parts=2, direct=0, n_ctas=2, part_o_bytes=0, part_ml_bytes=0)
+    a = _dummy_args()
+    assert pa.lib().pa_decode_fused(ctypes.byref(a), ctypes.byref(pl), None, None) == \
+        pa.PA_ERR_INVALID
+    assert pa.lib().pa_last_error().startswith(b"pa_decode_fused: ")
+    assert pa.lib().pa_decode_step_fused(ctypes.byref(a), ctypes.byref(pl), 16, 2, None) == \
+        pa.PA_ERR_INVALID
