@@ -38,12 +38,17 @@ import synth  # noqa: E402
 METRIC = ("paged decode-attn µs/step and achieved HBM GB/s vs GB300 peak "
           "(Q4_0 K/V, 1 GPU)")
 WORKLOADS = {
-    "uniform-q4_0-b8x131072": lambda: synth.uniform_spec(8, 131072, synth.Q4_0),
-    "uniform-q4_0-b4x32768": lambda: synth.uniform_spec(4, 32768, synth.Q4_0),
+    # uniform batches 1/2/4/8 x 4K/32K/128K, Q4_0
+    **{f"uniform-q4_0-b{b}x{c}": (lambda b=b, c=c: synth.uniform_spec(b, c, synth.Q4_0))
+       for b in (1, 2, 4, 8) for c in (4096, 32768, 131072)},
     "ragged-q4_0-128k+7x8k": lambda: synth.ragged_spec(synth.Q4_0),
-    "sweep-f16-b4x32768": lambda: synth.dtype_sweep_spec(synth.F16),
-    "sweep-q8_0-b4x32768": lambda: synth.dtype_sweep_spec(synth.Q8_0),
-    "sweep-q4_0-b4x32768": lambda: synth.dtype_sweep_spec(synth.Q4_0),
+    # the same rows in the padded contiguous layout (identity tables)
+    "ragged-q4_0-128k+7x8k-contiguous": lambda: synth.ragged_spec(synth.Q4_0),
+    **{f"sweep-{n}-{tag}": (lambda t=t, sh=sh: synth.dtype_sweep_spec(t, short=sh))
+       for n, t in (("f16", synth.F16), ("q8_0", synth.Q8_0), ("q4_0", synth.Q4_0))
+       for tag, sh in (("b4x32768", False), ("short", True))},
+    "tiny-f16-L200": synth.tiny_spec,
+    "largepool-f16-b16x300000": synth.large_pool_spec,
 }
 DEFAULT_WORKLOAD = "uniform-q4_0-b8x131072"
 L2_BYTES = 129 * 2**20
@@ -260,7 +265,9 @@ def run_ours(a, world, rank, local):
     dev = torch.device(f"cuda:{local}")
     torch.cuda.set_device(dev)
     spec = WORKLOADS[a.workload]()
-    case = synth.build_case(spec, seed=a.seed + 1000 * rank, device=dev)
+    case = synth.build_case(spec, seed=a.seed + 1000 * rank, device=dev, chunk_blocks=1024)
+    if a.workload.endswith("-contiguous"):
+        case = synth.contiguous_twin(case)
     flags = pa.PA_FLAG_PLAIN if a.plain else 0
     pl = pa.plan(seq_lens=spec.seq_lens, block_size=spec.block_size, hq=spec.hq, hkv=spec.hkv,
                  d=spec.d, k_type=spec.k_type, v_type=spec.v_type)

@@ -126,19 +126,6 @@ __device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// d = a * b + c with c in separate registers (no copy into the accumulator)
-__device__ __forceinline__ void mma16816_c(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
-                                           uint32_t a3, uint32_t b0, uint32_t b1, float c0,
-                                           float c1, float c2, float c3)
-{
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-        "{%8,%9}, {%10,%11,%12,%13};"
-        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(c0), "f"(c1), "f"(c2),
-          "f"(c3));
-}
-
 __device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], uint32_t addr)
 {
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
@@ -532,11 +519,19 @@ struct F16T {
 
 constexpr float kHeadroom = 4.0f;  // log2 units kept between the reference and the max
 
+// Parked (m, l, O) of one warp: m of its 8 head columns, then l, then O as
+// 8 rows of D floats (row stride D + 4, so that the fragment stores of the
+// four tig lanes fall in different banks).
+template <class T>
+struct Park {
+    static constexpr int kRow = T::D + 4;
+    static constexpr int kWarp = 16 + 8 * kRow;
+};
+
 template <class T>
 __device__ __forceinline__ void combine_and_write(const DecodeParams &p, const float *park,
-                                                  int per_warp, uint32_t g, uint32_t hkv,
-                                                  uint32_t wph, uint32_t G, uint32_t seq,
-                                                  uint32_t part, int gid, int tig, int lane);
+                                                  uint32_t hkv, uint32_t wph, uint32_t G,
+                                                  uint32_t seq, uint32_t part);
 
 template <class T>
 __global__ void __launch_bounds__(T::kMaxWarps * 32, 1)
@@ -741,12 +736,11 @@ __global__ void __launch_bounds__(T::kMaxWarps * 32, 1)
         l1 += __shfl_xor_sync(0xffffffffu, l1, off);
     }
 
-    // park (m, l, O) of every warp in the now idle rings, then the first warp
-    // of each head combines them
+    // park (m, l, O) of every warp in the now idle rings, head-major, then
+    // all warps of the CTA combine them
     __syncthreads();
     float *park = reinterpret_cast<float *>(smem);
-    const int per_warp = 16 + 32 * 4 * T::MT;
-    float *mine = park + warp * per_warp;
+    float *mine = park + warp * Park<T>::kWarp;
     if (gid == 0) {
         mine[2 * tig] = mref0;
         mine[2 * tig + 1] = mref1;
@@ -757,69 +751,74 @@ __global__ void __launch_bounds__(T::kMaxWarps * 32, 1)
     for (int mt = 0; mt < T::MT; ++mt)
 #pragma unroll
         for (int e = 0; e < 4; ++e)
-            mine[16 + (mt * 4 + e) * 32 + lane] = o[mt][e];
+            mine[16 + (2 * tig + (e & 1)) * Park<T>::kRow + T::dim_of(mt, gid, e >> 1)] = o[mt][e];
     __syncthreads();
-    if (sub == 0)
-        combine_and_write<T>(p, park, per_warp, g, hkv, wph, G, seq, part, gid, tig, lane);
+    combine_and_write<T>(p, park, hkv, wph, G, seq, part);
     if (p.counters && !p.direct)
         fused_merge_tail(p, seq, warp, nwarps);
 }
 
-// The first warp of head group g combines the parked (m, l, O) of the wph
-// warps of that group and writes the partial (or, direct, the output).
+// Combine of the parked (m, l, O) of the wph warps of every head group into
+// the partition's result: for each query head, M = max of the warps'
+// reference maxima, f_k = 2^(m_k - M), O = sum f_k O_k / sum f_k l_k.  Every
+// thread of the CTA takes 8-dim chunks of the output rows, so the partial
+// rows are written with coalesced 16-byte stores (f16 partials) or 32-byte
+// stores (the f32 output of a direct plan).
 template <class T>
 __device__ __forceinline__ void combine_and_write(const DecodeParams &p, const float *park,
-                                                  int per_warp, uint32_t g, uint32_t hkv,
-                                                  uint32_t wph, uint32_t G, uint32_t seq,
-                                                  uint32_t part, int gid, int tig, int lane)
+                                                  uint32_t hkv, uint32_t wph, uint32_t G,
+                                                  uint32_t seq, uint32_t part)
 {
-    float M[2], l[2], fk[16][2];
+    constexpr uint32_t NQ = T::D / 8;
+    const uint32_t n_chunks = hkv * G * NQ;
+    for (uint32_t c = threadIdx.x; c < n_chunks; c += blockDim.x) {
+        const uint32_t hg = c / NQ, q = c % NQ;
+        const uint32_t g = hg / G, h = hg - g * G;
+        float M = -INFINITY;
 #pragma unroll
-    for (int c = 0; c < 2; ++c) {
-        const int h = 2 * tig + c;
-        M[c] = -INFINITY;
-        for (uint32_t k = 0; k < wph; ++k)
-            M[c] = fmaxf(M[c], park[(g + k * hkv) * per_warp + h]);
-        l[c] = 0.0f;
-        for (uint32_t k = 0; k < wph; ++k) {
-            const float mk = park[(g + k * hkv) * per_warp + h];
-            const float f2 = (M[c] == -INFINITY || mk == -INFINITY) ? 0.0f : exp2f(mk - M[c]);
-            fk[k][c] = f2;
-            l[c] += park[(g + k * hkv) * per_warp + 8 + h] * f2;
-        }
-    }
-    float inv[2];
+        for (uint32_t k = 0; k < T::kMaxWarps; ++k)
+            if (k < wph)
+                M = fmaxf(M, park[(g + k * hkv) * Park<T>::kWarp + h]);
+        float l = 0.0f, acc[8];
 #pragma unroll
-    for (int c = 0; c < 2; ++c)
-        inv[c] = l[c] > 0.0f ? 1.0f / l[c] : 0.0f;
-    const uint64_t sh0 = (uint64_t)seq * p.hq + g * G;
+        for (int j = 0; j < 8; ++j)
+            acc[j] = 0.0f;
 #pragma unroll
-    for (int mt = 0; mt < T::MT; ++mt) {
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const int c = e & 1, upper = e >> 1;
-            float v = 0.0f;
-            for (uint32_t k = 0; k < wph; ++k)
-                v += park[(g + k * hkv) * per_warp + 16 + (mt * 4 + e) * 32 + lane] * fk[k][c];
-            const uint32_t h = 2 * tig + c;
-            if (h >= G)
-                continue;
-            const int dim = T::dim_of(mt, gid, upper);
-            if (p.direct) {
-                p.out[(sh0 + h) * T::D + dim] = v * inv[c];
-            } else {
-                __half *po = static_cast<__half *>(p.part_o);
-                po[((sh0 + h) * p.n_parts + part) * T::D + dim] = __float2half_rn(v * inv[c]);
+        for (uint32_t k = 0; k < T::kMaxWarps; ++k) {
+            if (k < wph) {
+                const float *w = park + (g + k * hkv) * Park<T>::kWarp;
+                const float mk = w[h];
+                const float f = mk == -INFINITY ? 0.0f : exp2f(mk - M);
+                l = fmaf(w[8 + h], f, l);
+                const float4 *src = reinterpret_cast<const float4 *>(w + 16 + h * Park<T>::kRow + 8 * q);
+                const float4 a = src[0], b = src[1];
+                acc[0] = fmaf(f, a.x, acc[0]);
+                acc[1] = fmaf(f, a.y, acc[1]);
+                acc[2] = fmaf(f, a.z, acc[2]);
+                acc[3] = fmaf(f, a.w, acc[3]);
+                acc[4] = fmaf(f, b.x, acc[4]);
+                acc[5] = fmaf(f, b.y, acc[5]);
+                acc[6] = fmaf(f, b.z, acc[6]);
+                acc[7] = fmaf(f, b.w, acc[7]);
             }
         }
-    }
-    if (!p.direct && gid == 0) {
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {
-            const uint32_t h = 2 * tig + c;
-            if (h < G)
-                reinterpret_cast<float2 *>(p.part_ml)[(sh0 + h) * p.n_parts + part] =
-                    make_float2(l[c] > 0.0f ? M[c] : -INFINITY, l[c]);
+        const float inv = l > 0.0f ? 1.0f / l : 0.0f;
+        const uint64_t row = (uint64_t)seq * p.hq + hg;
+        if (p.direct) {
+            float4 *dst = reinterpret_cast<float4 *>(p.out + row * T::D + 8 * q);
+            dst[0] = make_float4(acc[0] * inv, acc[1] * inv, acc[2] * inv, acc[3] * inv);
+            dst[1] = make_float4(acc[4] * inv, acc[5] * inv, acc[6] * inv, acc[7] * inv);
+        } else {
+            uint4 v;
+            v.x = h2_bits(__floats2half2_rn(acc[0] * inv, acc[1] * inv));
+            v.y = h2_bits(__floats2half2_rn(acc[2] * inv, acc[3] * inv));
+            v.z = h2_bits(__floats2half2_rn(acc[4] * inv, acc[5] * inv));
+            v.w = h2_bits(__floats2half2_rn(acc[6] * inv, acc[7] * inv));
+            __half *po = static_cast<__half *>(p.part_o);
+            *reinterpret_cast<uint4 *>(po + (row * p.n_parts + part) * T::D + 8 * q) = v;
+            if (q == 0)
+                reinterpret_cast<float2 *>(p.part_ml)[row * p.n_parts + part] =
+                    make_float2(l > 0.0f ? M : -INFINITY, l);
         }
     }
 }
@@ -852,7 +851,7 @@ Geometry geometry(uint32_t hkv)
 {
     Geometry gm;
     const size_t slot = 2 * (size_t)T::side_bytes(1);
-    const size_t park_per_warp = (16 + 32 * 4 * T::MT) * 4;
+    const size_t park_per_warp = Park<T>::kWarp * 4;
     for (uint32_t wph = T::kMaxWarps / hkv; wph >= 1; --wph) {
         const uint32_t warps = wph * hkv;
         const size_t fixed = 1024 + warps * (size_t)T::SCRATCH + warps * 16 * 12 + 64 +

@@ -96,12 +96,114 @@ __device__ __forceinline__ bool cta_work(const int32_t *seq_lens, uint32_t n_seq
 }
 
 // Stable split-softmax merge of the stored partials of one (sequence, query
-// head) row, executed by one warp ("feat: add paged-attention monolithic
+// head) row, NR rows at once by one warp ("feat: add paged-attention monolithic
 // decode-only AR foundation", lucebox pull 555, Summary): M = max m_p over
 // partials with l_p > 0, w_p = l_p 2^(m_p - M), out = sum_p w_p o_p / sum_p w_p;
-// partials with l_p == 0 are skipped and none gives 0.  po / pml point at the
-// row's n_parts partials; loads go through L2 (.cg) so that partials written by
-// other CTAs of the same launch are seen.  D is a multiple of 32.
+// partials with l_p == 0 are skipped and none gives 0.  po[r] / pml[r] point
+// at row r's partials (rows r >= nr are skipped); loads go through L2 (.cg) so
+// that partials written by other CTAs of the same launch are seen.  D is a
+// multiple of 32.
+template <int VEC, int NR>
+__device__ __forceinline__ void merge_rows_warp_v(const __half *const *po, const float2 *const *pml,
+                                                  float *const *out, int nr, uint32_t n_live,
+                                                  uint32_t D)
+{
+    const int lane = threadIdx.x & 31;
+    // reference maximum over live partials, per row
+    float M[NR];
+#pragma unroll
+    for (int r = 0; r < NR; ++r)
+        M[r] = -INFINITY;
+    for (uint32_t p = lane; p < n_live; p += 32) {
+#pragma unroll
+        for (int r = 0; r < NR; ++r) {
+            if (r < nr) {
+                const float2 ml = __ldcg(pml[r] + p);
+                if (ml.y > 0.0f)
+                    M[r] = fmaxf(M[r], ml.x);
+            }
+        }
+    }
+    float acc[NR][VEC], ws[NR];  // ws: lane-partial sum of the weights
+#pragma unroll
+    for (int r = 0; r < NR; ++r) {
+        M[r] = warp_max(M[r]);
+        ws[r] = 0.0f;
+#pragma unroll
+        for (int j = 0; j < VEC; ++j)
+            acc[r][j] = 0.0f;
+    }
+    for (uint32_t c = 0; c < n_live; c += 32) {
+        // lane p holds the weight of partial c + p (0 for dead or absent ones)
+        float w[NR];
+#pragma unroll
+        for (int r = 0; r < NR; ++r) {
+            w[r] = 0.0f;
+            if (r < nr && c + lane < n_live) {
+                const float2 ml = __ldcg(pml[r] + c + lane);
+                if (ml.y > 0.0f)
+                    w[r] = ml.y * exp2f(ml.x - M[r]);
+            }
+            ws[r] += w[r];
+        }
+        const uint32_t cnt = min(32u, n_live - c);
+        for (uint32_t q0 = 0; q0 < cnt; q0 += 8) {
+            // eight partial rows of every row in flight at once; VEC values each
+            uint4 raw[NR][8];
+#pragma unroll
+            for (int r = 0; r < NR; ++r) {
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    if (r < nr && q0 + k < cnt) {
+                        const __half *src = po[r] + (uint64_t)(c + q0 + k) * D + VEC * lane;
+                        if constexpr (VEC == 8) {
+                            raw[r][k] = __ldcg(reinterpret_cast<const uint4 *>(src));
+                        } else {
+                            const uint2 r2 = __ldcg(reinterpret_cast<const uint2 *>(src));
+                            raw[r][k] = make_uint4(r2.x, r2.y, 0u, 0u);
+                        }
+                    }
+                }
+            }
+#pragma unroll
+            for (int r = 0; r < NR; ++r) {
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const float wk = __shfl_sync(0xffffffffu, w[r], (q0 + k) & 31);
+                    if (r < nr && q0 + k < cnt && wk > 0.0f) {
+                        const __half2 *h2 = reinterpret_cast<const __half2 *>(&raw[r][k]);
+#pragma unroll
+                        for (int j = 0; j < VEC / 2; ++j) {
+                            const float2 f = __half22float2(h2[j]);
+                            acc[r][2 * j] = fmaf(wk, f.x, acc[r][2 * j]);
+                            acc[r][2 * j + 1] = fmaf(wk, f.y, acc[r][2 * j + 1]);
+                        }
+                    }
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int r = 0; r < NR; ++r) {
+        const float s = warp_sum(ws[r]);
+        const float inv = s > 0.0f ? 1.0f / s : 0.0f;
+        if (r < nr) {
+            float *o = out[r] + VEC * lane;
+#pragma unroll
+            for (int j = 0; j < VEC; ++j)
+                o[j] = acc[r][j] * inv;
+        }
+    }
+}
+
+// Stable split-softmax merge of the stored partials of one (sequence, query
+// head) row, NR rows at once by one warp ("feat: add paged-attention monolithic
+// decode-only AR foundation", lucebox pull 555, Summary): M = max m_p over
+// partials with l_p > 0, w_p = l_p 2^(m_p - M), out = sum_p w_p o_p / sum_p w_p;
+// partials with l_p == 0 are skipped and none gives 0.  po[r] / pml[r] point
+// at row r's partials (rows r >= nr are skipped); loads go through L2 (.cg) so
+// that partials written by other CTAs of the same launch are seen.  D is a
+// multiple of 32.
 template <int VEC>
 __device__ __forceinline__ void merge_row_warp_v(const __half *po, const float2 *pml, float *out,
                                                  uint32_t n_live, uint32_t D)
@@ -170,7 +272,7 @@ __device__ __forceinline__ void merge_row_warp_v(const __half *po, const float2 
 }
 
 // Stable split-softmax merge of the stored partials of one (sequence, query
-// head) row, executed by one warp ("feat: add paged-attention monolithic
+// head) row, NR rows at once by one warp ("feat: add paged-attention monolithic
 // decode-only AR foundation", lucebox pull 555, Summary): M = max m_p over
 // partials with l_p > 0, w_p = l_p 2^(m_p - M), out = sum_p w_p o_p / sum_p w_p
 // (summed in partition order); partials with l_p == 0 are skipped and none
@@ -181,9 +283,22 @@ __device__ __forceinline__ void merge_row_warp(const __half *po, const float2 *p
                                                uint32_t n_live, uint32_t D)
 {
     if (D == 256)
-        merge_row_warp_v<8>(po, pml, out, n_live, D);
+        merge_rows_warp_v<8, 1>(&po, &pml, &out, 1, n_live, D);
     else
-        merge_row_warp_v<4>(po, pml, out, n_live, D);
+        merge_rows_warp_v<4, 1>(&po, &pml, &out, 1, n_live, D);
+}
+
+// Two rows at once, with the same arithmetic per row as merge_row_warp (the
+// loads of both rows are in flight together); row 1 is skipped when nr == 1.
+__device__ __forceinline__ void merge_row_pair_warp(const __half *const po[2],
+                                                    const float2 *const pml[2],
+                                                    float *const out[2], int nr,
+                                                    uint32_t n_live, uint32_t D)
+{
+    if (D == 256)
+        merge_rows_warp_v<8, 2>(po, pml, out, nr, n_live, D);
+    else
+        merge_rows_warp_v<4, 2>(po, pml, out, nr, n_live, D);
 }
 
 // In-launch merge ("HRX: multi-pass KV-block reduction for flash-attention
@@ -213,10 +328,14 @@ __device__ inline void fused_merge_tail(const P &p, uint32_t seq, uint32_t warp,
     __threadfence();  // the other CTAs' partials are visible past their counts
     const __half *po = static_cast<const __half *>(p.part_o);
     const float2 *pml = reinterpret_cast<const float2 *>(p.part_ml);
-    for (uint32_t h = warp; h < p.hq; h += nwarps) {
-        const uint64_t sh = (uint64_t)seq * p.hq + h;
-        merge_row_warp(po + sh * p.n_parts * p.d, pml + sh * p.n_parts, p.out + sh * p.d, n_live,
-                       p.d);
+    // rows h and h + nwarps together, so that a warp has both rows' loads in flight
+    for (uint32_t h = warp; h < p.hq; h += 2 * nwarps) {
+        const uint64_t s0 = (uint64_t)seq * p.hq + h;
+        const uint64_t s1 = h + nwarps < p.hq ? s0 + nwarps : s0;
+        const __half *rpo[2] = {po + s0 * p.n_parts * p.d, po + s1 * p.n_parts * p.d};
+        const float2 *rml[2] = {pml + s0 * p.n_parts, pml + s1 * p.n_parts};
+        float *rout[2] = {p.out + s0 * p.d, p.out + s1 * p.d};
+        merge_row_pair_warp(rpo, rml, rout, h + nwarps < p.hq ? 2 : 1, n_live, p.d);
     }
 }
 
