@@ -71,6 +71,8 @@ typedef struct CUstream_st *pa_stream_t;
 /* Device status word bits (written by the kernels with atomicOr). */
 #define PA_STATUS_CORRUPT_TABLE 1 /* a block id outside [0, n_pool_blocks) */
 #define PA_STATUS_TIMEOUT 2       /* a pipeline wait exceeded its bound (2 s); output invalid */
+#define PA_STATUS_LEN_OVER_PLAN 4 /* a sequence longer than the plan's n_parts * part_tokens:
+                                     its tokens past that were left out; output invalid */
 
 typedef enum { PA_F16 = 0, PA_Q8_0 = 1, PA_Q4_0 = 2 } pa_type;
 
@@ -135,7 +137,9 @@ int pa_quantize_q(const float *q, void *q8_1, uint32_t n_rows, uint32_t d, pa_st
  *  - n_ctas = n_seqs when direct, else min(n_seqs * n_parts,
  *    ceil(total_len / part_tokens) + n_seqs) (>= the live partitions);
  *  - partial buffers: part_o f16 [n_seqs][hq][n_parts][d] and part_ml
- *    float32 [n_seqs][hq][n_parts][2] (0 bytes when direct).
+ *    float32 [n_seqs][hq][n_parts][2] (0 bytes when direct);
+ *  - counter_bytes = 4 * n_seqs * (1 + ceil(sqrt(n_parts))), the int32
+ *    completion counters of the fused merge (0 when direct).
  * Limits: block_size 16 or 32, d 128 or 256, hq a multiple of hkv with
  * hq / hkv <= 8, total_len <= n_seqs * max_len.  PA_ERR_INVALID otherwise. */
 typedef struct {
@@ -150,6 +154,7 @@ typedef struct {
 typedef struct {
     uint32_t part_tokens, n_parts, direct, n_ctas;
     uint64_t part_o_bytes, part_ml_bytes;
+    uint64_t counter_bytes;      /* completion counters of pa_decode_fused (0 when direct) */
 } pa_plan_t;
 
 int pa_plan(const pa_plan_in *in, pa_plan_t *out);
@@ -208,12 +213,16 @@ const char *pa_decode_kernel_name(pa_type k_type, pa_type v_type, uint32_t d, ui
                                   uint32_t hkv, uint32_t block_size, uint32_t flags);
 
 /* Merge ([P1] Summary: stable split-softmax merge).  For each (s, h) with
- * n_live = ceil(L_s / part_tokens) live partitions: M = max m_p over
- * partitions with l_p > 0, w_p = l_p 2^(m_p - M), out = sum w_p o_p /
- * sum w_p; partitions with l_p == 0 are skipped and no live partition gives
- * 0.  Layouts as in pa_decode_args.  PA_ERR_INVALID for a direct plan
- * (nothing to merge).  Indexing is 64-bit; PA_ERR_RANGE if the partial
- * buffer exceeds 2^40 elements. */
+ * n_live = min(ceil(L_s / part_tokens), n_parts) live partitions: M = max
+ * m_p over partitions with l_p > 0, w_p = l_p 2^(m_p - M), out = sum w_p o_p
+ * / sum w_p; partitions with l_p == 0 are skipped and no live partition gives
+ * 0.  More than 8 live partitions are merged in two passes ([P3] What:
+ * hierarchical reduction): groups of gs = ceil(sqrt(n_live)) consecutive
+ * partitions are merged into f16 partials of the same form, then those; the
+ * same as the flat merge up to rounding.  Reads the partials only.  Layouts
+ * as in pa_decode_args.  PA_ERR_INVALID for a direct plan (nothing to
+ * merge).  Indexing is 64-bit; PA_ERR_RANGE if the partial buffer exceeds
+ * 2^40 elements. */
 int pa_merge(const void *part_o, const float *part_ml, const int32_t *seq_lens, float *out,
              uint32_t n_seqs, uint32_t hq, uint32_t d, const pa_plan_t *plan,
              pa_stream_t stream);
@@ -222,21 +231,28 @@ int pa_merge(const void *part_o, const float *part_ml, const int32_t *seq_lens, 
  * multi-pass KV-block reduction for flash-attention decode-split", llama.cpp
  * fork pull 13, Changes: an atomic completion counter lets the reduction run
  * in the decode launch itself, with no second dispatch).  Every CTA writes its
- * partial as pa_decode_partial does, then counts it in counters[s]; the CTA
- * that completes sequence s merges that sequence's partials into out exactly
- * as pa_merge would, and resets counters[s] to 0.  No CTA ever waits for
- * another.
- * counters: device int32 [n_seqs], caller-owned, all zero before the first
- * call; every completed call leaves them zero.  After a call that reported
- * PA_STATUS_TIMEOUT the caller zeroes them again.  Calls that share a counter
- * array must not overlap on the GPU.  Direct plans ignore counters (may be
+ * partial as pa_decode_partial does and counts it; the CTA that completes a
+ * count merges: for a one-pass sequence all its partials into out, for a
+ * two-pass one (see pa_merge) its group's partials into the group's first
+ * partial slot, and the CTA that completes the last group the group results
+ * into out.  The result is pa_merge's bit for bit.  Every count is reset to 0
+ * by the CTA that completes it.  No CTA ever waits for another.
+ * counters: device int32 [plan->counter_bytes / 4], caller-owned, all zero
+ * before the first call; every completed call leaves them zero.  After a call
+ * that reported PA_STATUS_TIMEOUT the caller zeroes them again.  Calls that
+ * share a counter array must not overlap on the GPU.  The partials are
+ * overwritten by the group results.  Direct plans ignore counters (may be
  * NULL) and behave as pa_decode_partial.  part_o / part_ml / out are required
  * for partitioned plans. */
 int pa_decode_fused(const pa_decode_args *args, const pa_plan_t *plan, int32_t *counters,
                     pa_stream_t stream);
 
-/* pa_decode_step with the fused merge: pa_quantize_q (quantised K) and
- * pa_decode_fused, two launches on `stream`. */
+/* pa_decode_step with the fused merge, args->q the float32 query.  Where the
+ * fast kernel serves the shapes and K is quantised, it quantises the query
+ * rows itself with pa_quantize_q's arithmetic (the same q8_1 codes) and the
+ * step is one launch; otherwise pa_quantize_q (quantised K) into
+ * q8_1_scratch, then pa_decode_fused.  q8_1_scratch (n_seqs*hq*d/32*36 bytes,
+ * 16-byte aligned) is required for quantised K either way. */
 int pa_decode_step_fused(const pa_decode_args *args, const pa_plan_t *plan, void *q8_1_scratch,
                          int32_t *counters, pa_stream_t stream);
 

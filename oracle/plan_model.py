@@ -21,8 +21,12 @@ frozen here so that the C++ planner can be compared with it exactly:
 - the decode grid has n_ctas = S in direct mode, otherwise
   min(S * n_parts, ceil(total_len / part_tokens) + S) CTAs, an upper bound
   on the live (sequence, partition) pairs;
-- an empty batch (max_len == 0) is direct with part_tokens = 32.
+- an empty batch (max_len == 0) is direct with part_tokens = 32;
+- the fused merge keeps 1 + ceil(sqrt(n_parts)) int32 completion counters
+  per sequence (one for the last pass, one per group of the two-pass merge):
+  counter_bytes = 4 * S * (1 + ceil(sqrt(n_parts))), 0 when direct.
 """
+import math
 
 TILE = 32
 MIN_PART = 128
@@ -41,7 +45,7 @@ def _roundup(a: int, b: int) -> int:
 def plan(*, n_seqs, max_len, total_len, block_size, hq, hkv, d, k_type, v_type,
          sm_count, ctas_per_sm, force_parts=0):
     """Returns (rc, dict).  dict keys: part_tokens, n_parts, direct, n_ctas,
-    part_o_bytes, part_ml_bytes."""
+    part_o_bytes, part_ml_bytes, counter_bytes."""
     if (n_seqs < 1 or block_size not in (16, 32) or hkv < 1 or hq < hkv or hq % hkv
             or hq // hkv > 8 or d not in (128, 256) or k_type not in (0, 1, 2)
             or v_type not in (0, 1, 2) or sm_count < 1 or ctas_per_sm < 1
@@ -61,10 +65,11 @@ def plan(*, n_seqs, max_len, total_len, block_size, hq, hkv, d, k_type, v_type,
     direct = 1 if n_parts == 1 else 0
     if direct:
         n_ctas = n_seqs
-        po = pm = 0
+        po = pm = cb = 0
     else:
         n_ctas = min(n_seqs * n_parts, _cdiv(total_len, part) + n_seqs)
         po = n_seqs * hq * n_parts * d * 2
         pm = n_seqs * hq * n_parts * 8
+        cb = 4 * n_seqs * (1 + math.isqrt(n_parts - 1) + 1)
     return OK, dict(part_tokens=part, n_parts=n_parts, direct=direct, n_ctas=n_ctas,
-                    part_o_bytes=po, part_ml_bytes=pm)
+                    part_o_bytes=po, part_ml_bytes=pm, counter_bytes=cb)

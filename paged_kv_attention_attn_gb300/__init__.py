@@ -44,7 +44,8 @@ class PlanIn(ctypes.Structure):
 class Plan(ctypes.Structure):
     _fields_ = [("part_tokens", ctypes.c_uint32), ("n_parts", ctypes.c_uint32),
                 ("direct", ctypes.c_uint32), ("n_ctas", ctypes.c_uint32),
-                ("part_o_bytes", ctypes.c_uint64), ("part_ml_bytes", ctypes.c_uint64)]
+                ("part_o_bytes", ctypes.c_uint64), ("part_ml_bytes", ctypes.c_uint64),
+                ("counter_bytes", ctypes.c_uint64)]
 
     def as_dict(self):
         return {k: int(getattr(self, k)) for k, _ in self._fields_}
@@ -256,7 +257,8 @@ def workspace(pl: Plan, *, n_seqs, hq, d, device) -> Workspace:
         part_ml=torch.empty((n_seqs, hq, P, 2), dtype=torch.float32, device=device),
         status=torch.zeros(1, dtype=torch.int32, device=device),
         q8_1=torch.empty((n_seqs, hq, d // 32 * 36), dtype=torch.uint8, device=device),
-        counters=torch.zeros(n_seqs, dtype=torch.int32, device=device))
+        counters=torch.zeros(max(1, int(pl.counter_bytes) // 4), dtype=torch.int32,
+                             device=device))
 
 
 def make_args(*, k_pool, v_pool, block_table, seq_lens, q, ws: Workspace, hkv, block_size,

@@ -265,26 +265,78 @@ struct Q40T {
         uint32_t q;  // shared address of this lane's records (block 0)
     };
 
+    // This lane's eight query values of each block of query head gid of the
+    // group (dims 4tig..4tig+3 and 16+4tig..19+4tig): float32 when the kernel
+    // quantises the query itself, else the q8_1 codes and scale.  Fetched
+    // before the first K/V copies are issued, so that these loads do not
+    // queue behind them.
+    struct QRaw {
+        float4 x[NB][2];
+        uint32_t w[NB][2];
+        uint32_t d[NB];
+    };
+    __device__ static void fetch_q(const DecodeParams &p, uint32_t s, uint32_t h0, uint32_t G,
+                                   int gid, int tig, QRaw &r)
+    {
+        const uint64_t row = (uint64_t)s * p.hq + h0 + ((uint32_t)gid < G ? gid : 0);
+        if (p.q_f32) {
+            const float *x = static_cast<const float *>(p.q) + row * D;
+#pragma unroll
+            for (int b = 0; b < NB; ++b) {
+                r.x[b][0] = *reinterpret_cast<const float4 *>(x + 32 * b + 4 * tig);
+                r.x[b][1] = *reinterpret_cast<const float4 *>(x + 32 * b + 16 + 4 * tig);
+            }
+        } else {
+            const uint8_t *blk = static_cast<const uint8_t *>(p.q) + row * NB * 36;
+#pragma unroll
+            for (int b = 0; b < NB; ++b) {
+                r.d[b] = load_u16(blk + 36 * b);
+                r.w[b][0] = *reinterpret_cast<const uint32_t *>(blk + 36 * b + 4 + 4 * tig);
+                r.w[b][1] = *reinterpret_cast<const uint32_t *>(blk + 36 * b + 20 + 4 * tig);
+            }
+        }
+    }
+
     // Writes the fragments of query head gid of the group: qhat = f16(q * d_q
     // * scale * log2 e), in the dimension order the nibble expansion produces
-    // (see block()).  One warp per K/V head calls this.
-    __device__ static void store_q(const DecodeParams &p, uint32_t s, uint32_t h0, uint32_t G,
-                                   int gid, int tig, uint32_t qsm)
+    // (see block()).  A float32 query is first quantised to q8_1 with the
+    // pre-pass's arithmetic (the four lanes of a quad hold one block).  One
+    // warp per K/V head calls this.
+    __device__ static void store_q(const DecodeParams &p, const QRaw &r, uint32_t G, int gid,
+                                   int tig, uint32_t qsm)
     {
         const int lane = gid * 4 + tig;
         const bool live = (uint32_t)gid < G;
-        const uint8_t *row = static_cast<const uint8_t *>(p.q) +
-                             ((uint64_t)s * p.hq + h0 + (live ? gid : 0)) * NB * 36;
 #pragma unroll
         for (int b = 0; b < NB; ++b) {
-            const uint8_t *blk = row + 36 * b;
-            const float d = live ? half_bits_to_float(load_u16(blk)) * p.scale_log2 : 0.0f;
+            int code[8];
+            float d16;
+            if (p.q_f32) {
+                const float v[8] = {r.x[b][0].x, r.x[b][0].y, r.x[b][0].z, r.x[b][0].w,
+                                    r.x[b][1].x, r.x[b][1].y, r.x[b][1].z, r.x[b][1].w};
+                float amax = 0.0f;
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    amax = fmaxf(amax, fabsf(v[j]));
+                amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+                amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+                const float d = amax / 127.0f;
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    code[j] = q8_1_code(v[j], amax, d);
+                d16 = __half2float(__float2half_rn(amax == 0.0f ? 0.0f : d));
+            } else {
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    code[j] = (int)(int8_t)(uint8_t)(r.w[b][j >> 2] >> (8 * (j & 3)));
+                d16 = half_bits_to_float((uint16_t)r.d[b]);
+            }
+            const float d = live ? d16 * p.scale_log2 : 0.0f;
             __half qh[8];
             float corr = 0.0f;
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
-                const int off = j < 4 ? 4 + 4 * tig + j : 20 + 4 * tig + (j - 4);
-                qh[j] = __float2half_rn((float)(int8_t)blk[off] * d);
+                qh[j] = __float2half_rn((float)code[j] * d);
                 // low nibbles read as 1024 + n, high as 64 + n; the value is n - 8
                 corr += __half2float(qh[j]) * (j < 4 ? 1032.0f : 72.0f);
             }
@@ -292,13 +344,13 @@ struct Q40T {
             corr += __shfl_xor_sync(0xffffffffu, corr, 2);
             const float n0 = -__shfl_sync(0xffffffffu, corr, 8 * tig);
             const float n1 = -__shfl_sync(0xffffffffu, corr, 8 * tig + 4);
-            const uint32_t r = qsm + (b * 32 + lane) * QREC;
-            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(r),
+            const uint32_t rr = qsm + (b * 32 + lane) * QREC;
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(rr),
                          "r"(h2_bits(__halves2half2(qh[0], qh[2]))),
                          "r"(h2_bits(__halves2half2(qh[1], qh[3]))),
                          "r"(h2_bits(__halves2half2(qh[4], qh[6]))),
                          "r"(h2_bits(__halves2half2(qh[5], qh[7]))));
-            asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(r + QCORR), "f"(n0),
+            asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(rr + QCORR), "f"(n0),
                          "f"(n1), "f"(n0), "f"(n1));
         }
     }
@@ -431,24 +483,31 @@ struct F16T {
         uint32_t qb[KS][2];  // B fragments (query column gid) of each k-step
     };
 
-    __device__ static void store_q(const DecodeParams &, uint32_t, uint32_t, uint32_t, int, int,
-                                   uint32_t)
+    // This lane's query values (query head gid of the group), fetched before
+    // the first K/V copies are issued so that the loads do not queue behind them.
+    struct QRaw {
+        float2 x[KS][2];
+    };
+    __device__ static void fetch_q(const DecodeParams &p, uint32_t s, uint32_t h0, uint32_t G,
+                                   int gid, int tig, QRaw &r)
     {
-    }
-
-    __device__ static void load_q(const DecodeParams &p, uint32_t s, uint32_t h0, uint32_t G,
-                                  int gid, int tig, Frag &f)
-    {
-        const bool live = (uint32_t)gid < G;
         const float *row = static_cast<const float *>(p.q) +
-                           ((uint64_t)s * p.hq + h0 + (live ? gid : 0)) * D;
-        const float sc = live ? p.scale_log2 : 0.0f;
+                           ((uint64_t)s * p.hq + h0 + ((uint32_t)gid < G ? gid : 0)) * D;
 #pragma unroll
         for (int j = 0; j < KS; ++j) {
-            const float2 x = *reinterpret_cast<const float2 *>(row + 16 * j + 2 * tig);
-            const float2 y = *reinterpret_cast<const float2 *>(row + 16 * j + 8 + 2 * tig);
-            f.qb[j][0] = h2_bits(__floats2half2_rn(x.x * sc, x.y * sc));
-            f.qb[j][1] = h2_bits(__floats2half2_rn(y.x * sc, y.y * sc));
+            r.x[j][0] = *reinterpret_cast<const float2 *>(row + 16 * j + 2 * tig);
+            r.x[j][1] = *reinterpret_cast<const float2 *>(row + 16 * j + 8 + 2 * tig);
+        }
+    }
+
+    __device__ static void load_q(const DecodeParams &p, const QRaw &r, uint32_t G, int gid,
+                                  Frag &f)
+    {
+        const float sc = (uint32_t)gid < G ? p.scale_log2 : 0.0f;
+#pragma unroll
+        for (int j = 0; j < KS; ++j) {
+            f.qb[j][0] = h2_bits(__floats2half2_rn(r.x[j][0].x * sc, r.x[j][0].y * sc));
+            f.qb[j][1] = h2_bits(__floats2half2_rn(r.x[j][1].x * sc, r.x[j][1].y * sc));
         }
     }
 
@@ -533,6 +592,14 @@ __device__ __forceinline__ void combine_and_write(const DecodeParams &p, const f
                                                   uint32_t hkv, uint32_t wph, uint32_t G,
                                                   uint32_t seq, uint32_t part);
 
+// The in-launch merge, out of line so that its registers do not add to the
+// main loop's.
+__device__ __noinline__ void merge_tail(const DecodeParams &p, uint32_t seq, uint32_t part,
+                                        uint32_t warp, uint32_t nwarps)
+{
+    fused_merge(p, seq, part, warp, nwarps);
+}
+
 template <class T>
 __global__ void __launch_bounds__(T::kMaxWarps * 32, 1)
     fast_decode_kernel(const __grid_constant__ FastArgs a)
@@ -563,8 +630,11 @@ __global__ void __launch_bounds__(T::kMaxWarps * 32, 1)
     if (p.direct) {
         seq = blockIdx.x;
         part = 0;
-    } else if (!cta_work(p.seq_lens, p.n_seqs, p.part_tokens, blockIdx.x, &seq, &part)) {
+    } else if (!cta_work(p.seq_lens, p.n_seqs, p.part_tokens, p.n_parts, blockIdx.x, &seq,
+                         &part)) {
         return;  // past the last live partition: nothing was issued
+    } else if (part == 0 && tid == 0) {
+        check_len_vs_plan(p.seq_lens[seq], p.n_parts, p.part_tokens, p.status);
     }
     const int32_t L = p.seq_lens[seq] > 0 ? p.seq_lens[seq] : 0;
     const uint32_t t0 = p.direct ? 0u : part * p.part_tokens;
@@ -605,6 +675,9 @@ __global__ void __launch_bounds__(T::kMaxWarps * 32, 1)
     };
 
     int32_t ids = fetch_ids(0), ids_next = fetch_ids(32);
+    typename T::QRaw qraw;
+    if (T::QBYTES == 0 || sub == 0)
+        T::fetch_q(p, seq, g * G, G, gid, tig, qraw);
     const uint32_t pro = n_my < NSW ? n_my : NSW;
     for (uint32_t k = 0; k < pro; ++k) {
         const int32_t b = __shfl_sync(0xffffffffu, ids, k);
@@ -619,11 +692,11 @@ __global__ void __launch_bounds__(T::kMaxWarps * 32, 1)
     typename T::Frag f;
     if constexpr (T::QBYTES > 0) {
         if (sub == 0)
-            T::store_q(p, seq, g * G, G, gid, tig, qsm_base + g * T::QBYTES);
+            T::store_q(p, qraw, G, gid, tig, qsm_base + g * T::QBYTES);
         __syncthreads();
         T::load_q(qsm_base + g * T::QBYTES, lane, f);
     } else {
-        T::load_q(p, seq, g * G, G, gid, tig, f);
+        T::load_q(p, qraw, G, gid, f);
     }
     float o[T::MT][4];
 #pragma unroll
@@ -755,7 +828,7 @@ __global__ void __launch_bounds__(T::kMaxWarps * 32, 1)
     __syncthreads();
     combine_and_write<T>(p, park, hkv, wph, G, seq, part);
     if (p.counters && !p.direct)
-        fused_merge_tail(p, seq, warp, nwarps);
+        merge_tail(p, seq, part, warp, nwarps);
 }
 
 // Combine of the parked (m, l, O) of the wph warps of every head group into

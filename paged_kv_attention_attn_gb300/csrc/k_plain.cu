@@ -30,12 +30,7 @@ __global__ void __launch_bounds__(256) quantize_q8_1_kernel(const float *__restr
         const float v = x[b * 32 + lane];
         const float amax = warp_max(fabsf(v));
         float d = amax / 127.0f;
-        int q = 0;
-        if (amax != 0.0f) {
-            float r = roundf(v / d);
-            r = fminf(fmaxf(r, -127.0f), 127.0f);
-            q = (int)r;
-        }
+        const int q = q8_1_code(v, amax, d);
         const int sum = warp_sum_int(q);
         if (amax == 0.0f)
             d = 0.0f;
@@ -223,8 +218,11 @@ __global__ void __launch_bounds__(kPlainWarps * 32) plain_decode_kernel(const De
         part = 0;
         if (s >= p.n_seqs)
             return;
-    } else if (!cta_work(p.seq_lens, p.n_seqs, p.part_tokens, blockIdx.x, &s, &part)) {
+    } else if (!cta_work(p.seq_lens, p.n_seqs, p.part_tokens, p.n_parts, blockIdx.x, &s,
+                         &part)) {
         return;
+    } else if (part == 0 && threadIdx.x == 0) {
+        check_len_vs_plan(p.seq_lens[s], p.n_parts, p.part_tokens, p.status);
     }
     const int32_t L = p.seq_lens[s] > 0 ? p.seq_lens[s] : 0;
     const uint32_t t0 = p.direct ? 0u : part * p.part_tokens;
@@ -301,7 +299,7 @@ __global__ void __launch_bounds__(kPlainWarps * 32) plain_decode_kernel(const De
         __syncwarp();
     }
     if (p.counters && !p.direct)
-        fused_merge_tail(p, s, threadIdx.x >> 5, blockDim.x >> 5);
+        fused_merge(p, s, part, threadIdx.x >> 5, blockDim.x >> 5);
 }
 
 template <int KT, int VT, int D>
@@ -377,7 +375,16 @@ __global__ void __launch_bounds__(128) merge_kernel(const __half *__restrict__ p
     uint32_t n_live = L > 0 ? ((uint32_t)L + part_tokens - 1) / part_tokens : 0;
     if (n_live > n_parts)
         n_live = n_parts;
-    merge_row_warp(po + sh * n_parts * D, pml + sh * n_parts, out + sh * D, n_live, D);
+    // this warp's stage for the group results of a two-pass merge
+    __shared__ __align__(16) __half scr[4][256];
+    __shared__ float2 scr_ml[4];
+    const int w = threadIdx.x >> 5;
+    if (D == 256)
+        merge_row_two_pass_warp<8>(po + sh * n_parts * D, pml + sh * n_parts, out + sh * D,
+                                   n_live, D, scr[w], &scr_ml[w]);
+    else
+        merge_row_two_pass_warp<4>(po + sh * n_parts * D, pml + sh * n_parts, out + sh * D,
+                                   n_live, D, scr[w], &scr_ml[w]);
 }
 
 int launch_merge(const void *part_o, const float *part_ml, const int32_t *seq_lens, float *out,

@@ -95,6 +95,7 @@ int resolve(const pa_decode_args *a, const pa_plan_t *plan, const char *E, pa::D
     p->k_row_bytes = pa_row_bytes(a->k_type, a->d);
     p->v_row_bytes = pa_row_bytes(a->v_type, a->d);
     p->counters = nullptr;
+    p->q_f32 = 0;
     return PA_OK;
 }
 
@@ -216,6 +217,11 @@ extern "C" int pa_decode_step_fused(const pa_decode_args *args, const pa_plan_t 
     if (args->k_type != PA_F16) {
         if (!q8_1_scratch || (reinterpret_cast<uintptr_t>(q8_1_scratch) & 15))
             return fail(PA_ERR_INVALID, E, "quantised K needs a 16-byte aligned q8_1_scratch");
+        if (use_fast(args)) {
+            // the fast kernel quantises the query rows itself: one launch per step
+            p.q_f32 = 1;
+            return launch_decode(args, p, st, E);
+        }
         rc = pa::launch_quantize_q(static_cast<const float *>(args->q), q8_1_scratch,
                                    args->n_seqs * args->hq, args->d, st, E);
         if (rc)

@@ -4,6 +4,8 @@
 #include <cuda_fp16.h>
 #include <stdint.h>
 
+#include "pa_internal.h"
+
 namespace pa {
 
 constexpr float kLog2e = 1.4426950408889634f;
@@ -36,6 +38,21 @@ __device__ __forceinline__ uint16_t load_u16(const uint8_t *p)
     return *reinterpret_cast<const uint16_t *>(p);
 }
 
+// q8_1 code of value v in a block of 32 whose largest magnitude is amax, with
+// the block scale d = amax / 127 ("feat: add paged-attention monolithic
+// decode-only AR foundation", lucebox pull 555, Summary: Q is quantised to
+// q8_1 once per step).  float32 IEEE division, roundf (ties away from zero),
+// clamped to [-127, 127]; an all-zero block codes as 0.  The q8_1 pre-pass
+// kernel and the decode kernel that quantises its own query share this, so
+// both give the same codes.
+__device__ __forceinline__ int q8_1_code(float v, float amax, float d)
+{
+    if (amax == 0.0f)
+        return 0;
+    const float r = fminf(fmaxf(roundf(v / d), -127.0f), 127.0f);
+    return (int)r;
+}
+
 __device__ __forceinline__ float warp_max(float v)
 {
 #pragma unroll
@@ -61,19 +78,23 @@ __device__ __forceinline__ int warp_sum_int(int v)
 }
 
 // Maps a CTA of a partitioned decode grid to its (sequence, partition): CTAs
-// enumerate the live (s, p) pairs in order of s, then p, where sequence s has
-// ceil(L_s / part_tokens) live partitions.  Executed by one full warp; returns
-// false when the CTA index is past the last live pair.
+// enumerate the (s, p) pairs in order of s, then p, where sequence s has
+// min(ceil(L_s / part_tokens), n_parts) live partitions, and an empty
+// sequence (L_s <= 0) one empty partition.  Executed by one full warp; returns false when the CTA
+// index is past the last pair.
 __device__ __forceinline__ bool cta_work(const int32_t *seq_lens, uint32_t n_seqs,
-                                         uint32_t part_tokens, uint32_t cta, uint32_t *seq,
-                                         uint32_t *part)
+                                         uint32_t part_tokens, uint32_t n_parts, uint32_t cta,
+                                         uint32_t *seq, uint32_t *part)
 {
     const int lane = threadIdx.x & 31;
     uint32_t base = 0;
     for (uint32_t s0 = 0; s0 < n_seqs; s0 += 32) {
         uint32_t s = s0 + lane;
-        int32_t L = s < n_seqs ? seq_lens[s] : 0;
-        uint32_t n = L > 0 ? ((uint32_t)L + part_tokens - 1) / part_tokens : 0;
+        // an empty sequence still gets one CTA, which writes its zero output
+        // (or its empty partial, and its arrival at the completion count)
+        const int32_t L = s < n_seqs ? seq_lens[s] : 0;
+        uint32_t n = L > 0 ? ((uint32_t)L + part_tokens - 1) / part_tokens : (s < n_seqs ? 1u : 0u);
+        n = n < n_parts ? n : n_parts;  // a sequence longer than the plan is cut
         uint32_t incl = n;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -95,36 +116,81 @@ __device__ __forceinline__ bool cta_work(const int32_t *seq_lens, uint32_t n_seq
     return false;
 }
 
-// Stable split-softmax merge of the stored partials of one (sequence, query
-// head) row, NR rows at once by one warp ("feat: add paged-attention monolithic
-// decode-only AR foundation", lucebox pull 555, Summary): M = max m_p over
-// partials with l_p > 0, w_p = l_p 2^(m_p - M), out = sum_p w_p o_p / sum_p w_p;
-// partials with l_p == 0 are skipped and none gives 0.  po[r] / pml[r] point
-// at row r's partials (rows r >= nr are skipped); loads go through L2 (.cg) so
-// that partials written by other CTAs of the same launch are seen.  D is a
-// multiple of 32.
-template <int VEC, int NR>
+// ------------------------------------------------------------------ merge
+//
+// Stable split-softmax merge ("feat: add paged-attention monolithic
+// decode-only AR foundation", lucebox pull 555, Summary): for one (sequence,
+// query head) row with live partials p (normalised o_p, m_p, l_p): M = max m_p
+// over partials with l_p > 0, w_p = l_p 2^(m_p - M), out = sum_p w_p o_p /
+// sum_p w_p; partials with l_p == 0 are skipped and none gives 0.
+//
+// A row with more than 8 live partials is merged in two passes ("HRX:
+// multi-pass KV-block reduction for flash-attention decode-split", llama.cpp
+// fork pull 13, What: hierarchical KV-block reduction): the partials are cut
+// into groups of gs = merge_group_size(n) consecutive ones, each group is
+// merged into one partial of the same form (f16 o, (m, l)), then the group
+// results are merged.  The merge is associative, so this is the flat merge up
+// to rounding.  The in-launch merge and the separate merge kernel use the same
+// groups and the same arithmetic, so they give the same bits.
+
+// Merge of n partials of each of NR rows by one warp (rows r >= nr are
+// skipped); partial p of row r is at po[r] + p * stride * D and pml[r] +
+// p * stride.  kPartial: the result is written in partial form (f16 o to
+// out_o[r], (M, or -inf when no weight, and sum w) to out_ml[r]); else as
+// float32 to out_f[r].  Lane i owns dims [VEC i, VEC (i + 1)).  The weight sum
+// is lane-partial (lane i adds the weights of partials i, i + 32, ... in
+// order) and then a butterfly; every dimension is summed in partial order.
+// Loads go through L2 (.cg) so that partials written by other CTAs of the
+// same launch are seen.
+template <int VEC, int NR, bool kPartial>
 __device__ __forceinline__ void merge_rows_warp_v(const __half *const *po, const float2 *const *pml,
-                                                  float *const *out, int nr, uint32_t n_live,
-                                                  uint32_t D)
+                                                  uint32_t n, uint32_t stride, uint32_t D,
+                                                  int nr, float *const *out_f,
+                                                  __half *const *out_o, float2 *const *out_ml)
 {
     const int lane = threadIdx.x & 31;
-    // reference maximum over live partials, per row
+    // eight partials of every row in flight at once
+    uint4 raw[NR][8];
+    auto load_batch = [&](uint32_t base, uint32_t cnt) {
+#pragma unroll
+        for (int r = 0; r < NR; ++r) {
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                if (r < nr && (uint32_t)k < cnt) {
+                    const __half *src = po[r] + (uint64_t)(base + k) * stride * D + VEC * lane;
+                    if constexpr (VEC == 8) {
+                        raw[r][k] = __ldcg(reinterpret_cast<const uint4 *>(src));
+                    } else {
+                        const uint2 r2 = __ldcg(reinterpret_cast<const uint2 *>(src));
+                        raw[r][k] = make_uint4(r2.x, r2.y, 0u, 0u);
+                    }
+                }
+            }
+        }
+    };
+    // the first batch and the (m, l) of partial `lane` are loaded together:
+    // neither depends on the reference maximum
+    load_batch(0, n < 8 ? n : 8);
+    float2 ml0[NR];
     float M[NR];
 #pragma unroll
-    for (int r = 0; r < NR; ++r)
-        M[r] = -INFINITY;
-    for (uint32_t p = lane; p < n_live; p += 32) {
+    for (int r = 0; r < NR; ++r) {
+        ml0[r] = make_float2(-INFINITY, 0.0f);
+        if (r < nr && (uint32_t)lane < n)
+            ml0[r] = __ldcg(pml[r] + (uint64_t)lane * stride);
+        M[r] = ml0[r].y > 0.0f ? ml0[r].x : -INFINITY;
+    }
+    for (uint32_t p = lane + 32; p < n; p += 32) {
 #pragma unroll
         for (int r = 0; r < NR; ++r) {
             if (r < nr) {
-                const float2 ml = __ldcg(pml[r] + p);
+                const float2 ml = __ldcg(pml[r] + (uint64_t)p * stride);
                 if (ml.y > 0.0f)
                     M[r] = fmaxf(M[r], ml.x);
             }
         }
     }
-    float acc[NR][VEC], ws[NR];  // ws: lane-partial sum of the weights
+    float acc[NR][VEC], ws[NR];
 #pragma unroll
     for (int r = 0; r < NR; ++r) {
         M[r] = warp_max(M[r]);
@@ -133,38 +199,23 @@ __device__ __forceinline__ void merge_rows_warp_v(const __half *const *po, const
         for (int j = 0; j < VEC; ++j)
             acc[r][j] = 0.0f;
     }
-    for (uint32_t c = 0; c < n_live; c += 32) {
-        // lane p holds the weight of partial c + p (0 for dead or absent ones)
+    for (uint32_t c = 0; c < n; c += 32) {
+        // lane i holds the weight of partial c + i (0 for dead or absent ones)
         float w[NR];
 #pragma unroll
         for (int r = 0; r < NR; ++r) {
             w[r] = 0.0f;
-            if (r < nr && c + lane < n_live) {
-                const float2 ml = __ldcg(pml[r] + c + lane);
+            if (r < nr && c + lane < n) {
+                const float2 ml = c == 0 ? ml0[r] : __ldcg(pml[r] + (uint64_t)(c + lane) * stride);
                 if (ml.y > 0.0f)
                     w[r] = ml.y * exp2f(ml.x - M[r]);
             }
             ws[r] += w[r];
         }
-        const uint32_t cnt = min(32u, n_live - c);
+        const uint32_t cnt = min(32u, n - c);
         for (uint32_t q0 = 0; q0 < cnt; q0 += 8) {
-            // eight partial rows of every row in flight at once; VEC values each
-            uint4 raw[NR][8];
-#pragma unroll
-            for (int r = 0; r < NR; ++r) {
-#pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    if (r < nr && q0 + k < cnt) {
-                        const __half *src = po[r] + (uint64_t)(c + q0 + k) * D + VEC * lane;
-                        if constexpr (VEC == 8) {
-                            raw[r][k] = __ldcg(reinterpret_cast<const uint4 *>(src));
-                        } else {
-                            const uint2 r2 = __ldcg(reinterpret_cast<const uint2 *>(src));
-                            raw[r][k] = make_uint4(r2.x, r2.y, 0u, 0u);
-                        }
-                    }
-                }
-            }
+            if (c + q0 > 0)
+                load_batch(c + q0, cnt - q0 < 8 ? cnt - q0 : 8);
 #pragma unroll
             for (int r = 0; r < NR; ++r) {
 #pragma unroll
@@ -187,8 +238,23 @@ __device__ __forceinline__ void merge_rows_warp_v(const __half *const *po, const
     for (int r = 0; r < NR; ++r) {
         const float s = warp_sum(ws[r]);
         const float inv = s > 0.0f ? 1.0f / s : 0.0f;
-        if (r < nr) {
-            float *o = out[r] + VEC * lane;
+        if (r >= nr)
+            continue;
+        if constexpr (kPartial) {
+            uint32_t h[VEC / 2];
+#pragma unroll
+            for (int j = 0; j < VEC / 2; ++j) {
+                const __half2 v = __floats2half2_rn(acc[r][2 * j] * inv, acc[r][2 * j + 1] * inv);
+                h[j] = *reinterpret_cast<const uint32_t *>(&v);
+            }
+            if constexpr (VEC == 8)
+                *reinterpret_cast<uint4 *>(out_o[r] + VEC * lane) = make_uint4(h[0], h[1], h[2], h[3]);
+            else
+                *reinterpret_cast<uint2 *>(out_o[r] + VEC * lane) = make_uint2(h[0], h[1]);
+            if (lane == 0)
+                *out_ml[r] = make_float2(s > 0.0f ? M[r] : -INFINITY, s);
+        } else {
+            float *o = out_f[r] + VEC * lane;
 #pragma unroll
             for (int j = 0; j < VEC; ++j)
                 o[j] = acc[r][j] * inv;
@@ -196,72 +262,63 @@ __device__ __forceinline__ void merge_rows_warp_v(const __half *const *po, const
     }
 }
 
-// Stable split-softmax merge of the stored partials of one (sequence, query
-// head) row, NR rows at once by one warp ("feat: add paged-attention monolithic
-// decode-only AR foundation", lucebox pull 555, Summary): M = max m_p over
-// partials with l_p > 0, w_p = l_p 2^(m_p - M), out = sum_p w_p o_p / sum_p w_p;
-// partials with l_p == 0 are skipped and none gives 0.  po[r] / pml[r] point
-// at row r's partials (rows r >= nr are skipped); loads go through L2 (.cg) so
-// that partials written by other CTAs of the same launch are seen.  D is a
-// multiple of 32.
-template <int VEC>
-__device__ __forceinline__ void merge_row_warp_v(const __half *po, const float2 *pml, float *out,
-                                                 uint32_t n_live, uint32_t D)
+// Records a sequence longer than the plan covers (its partitions past n_parts
+// are left out).  Called by thread 0 of the CTA of partition 0.
+__device__ __forceinline__ void check_len_vs_plan(int32_t L, uint32_t n_parts,
+                                                  uint32_t part_tokens, int32_t *status)
 {
+    if (L > 0 && (uint64_t)L > (uint64_t)n_parts * part_tokens)
+        atomicOr(status, PA_STATUS_LEN_OVER_PLAN);
+}
+
+// One row merged by one warp, the flat merge or the two passes as above,
+// float32 out.  The group results are staged in scr (this warp's D halves
+// and one (m, l)) exactly as the in-launch merge stores them in part_o, so
+// the second pass sees the same bits.
+template <int VEC>
+__device__ __forceinline__ void merge_row_two_pass_warp(const __half *po, const float2 *pml,
+                                                        float *out, uint32_t n, uint32_t D,
+                                                        __half *scr, float2 *scr_ml)
+{
+    const uint32_t gs = merge_group_size(n);
+    if (gs >= n) {
+        merge_rows_warp_v<VEC, 1, false>(&po, &pml, n, 1, D, 1, &out, nullptr, nullptr);
+        return;
+    }
     const int lane = threadIdx.x & 31;
-    // reference maximum over live partials
+    const uint32_t ng = (n + gs - 1) / gs;
+    // the second pass's reference maximum: that of the groups is that of all
     float M = -INFINITY;
-    for (uint32_t p = lane; p < n_live; p += 32) {
+    for (uint32_t p = lane; p < n; p += 32) {
         const float2 ml = __ldcg(pml + p);
         if (ml.y > 0.0f)
             M = fmaxf(M, ml.x);
     }
     M = warp_max(M);
-    float acc[VEC];
+    float acc[VEC], ws = 0.0f;
 #pragma unroll
     for (int j = 0; j < VEC; ++j)
         acc[j] = 0.0f;
-    float ws = 0.0f;  // lane-partial sum of the weights
-    for (uint32_t c = 0; c < n_live; c += 32) {
-        // lane p holds the weight of partial c + p (0 for dead or absent ones)
-        float w = 0.0f;
-        if (c + lane < n_live) {
-            const float2 ml = __ldcg(pml + c + lane);
-            if (ml.y > 0.0f)
-                w = ml.y * exp2f(ml.x - M);
-        }
-        ws += w;
-        const uint32_t cnt = min(32u, n_live - c);
-        for (uint32_t q0 = 0; q0 < cnt; q0 += 8) {
-            // eight partial rows in flight at once; this lane's VEC values each
-            uint4 raw[8];
+    for (uint32_t g = 0; g < ng; ++g) {
+        const uint32_t p0 = g * gs, ng_g = min(gs, n - p0);
+        const __half *gpo = po + (uint64_t)p0 * D;
+        const float2 *gml = pml + p0;
+        merge_rows_warp_v<VEC, 1, true>(&gpo, &gml, ng_g, 1, D, 1, nullptr, &scr, &scr_ml);
+        __syncwarp();
+        const float2 ml = *scr_ml;
+        const float w = ml.y > 0.0f ? ml.y * exp2f(ml.x - M) : 0.0f;
+        if ((g & 31) == (uint32_t)lane)
+            ws += w;
+        if (w > 0.0f) {
+            const __half2 *h2 = reinterpret_cast<const __half2 *>(scr + VEC * lane);
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                const uint32_t pk = c + q0 + k;
-                if (q0 + k < cnt) {
-                    const __half *src = po + (uint64_t)pk * D + VEC * lane;
-                    if constexpr (VEC == 8) {
-                        raw[k] = __ldcg(reinterpret_cast<const uint4 *>(src));
-                    } else {
-                        const uint2 r2 = __ldcg(reinterpret_cast<const uint2 *>(src));
-                        raw[k] = make_uint4(r2.x, r2.y, 0u, 0u);
-                    }
-                }
-            }
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                const float wk = __shfl_sync(0xffffffffu, w, (q0 + k) & 31);
-                if (q0 + k < cnt && wk > 0.0f) {
-                    const __half2 *h2 = reinterpret_cast<const __half2 *>(&raw[k]);
-#pragma unroll
-                    for (int j = 0; j < VEC / 2; ++j) {
-                        const float2 f = __half22float2(h2[j]);
-                        acc[2 * j] = fmaf(wk, f.x, acc[2 * j]);
-                        acc[2 * j + 1] = fmaf(wk, f.y, acc[2 * j + 1]);
-                    }
-                }
+            for (int j = 0; j < VEC / 2; ++j) {
+                const float2 f = __half22float2(h2[j]);
+                acc[2 * j] = fmaf(w, f.x, acc[2 * j]);
+                acc[2 * j + 1] = fmaf(w, f.y, acc[2 * j + 1]);
             }
         }
+        __syncwarp();  // the group result is read before the next one lands
     }
     ws = warp_sum(ws);
     const float inv = ws > 0.0f ? 1.0f / ws : 0.0f;
@@ -271,71 +328,82 @@ __device__ __forceinline__ void merge_row_warp_v(const __half *po, const float2 
         o[j] = acc[j] * inv;
 }
 
-// Stable split-softmax merge of the stored partials of one (sequence, query
-// head) row, NR rows at once by one warp ("feat: add paged-attention monolithic
-// decode-only AR foundation", lucebox pull 555, Summary): M = max m_p over
-// partials with l_p > 0, w_p = l_p 2^(m_p - M), out = sum_p w_p o_p / sum_p w_p
-// (summed in partition order); partials with l_p == 0 are skipped and none
-// gives 0.  po / pml point at the row's partials; loads go through L2 (.cg) so
-// that partials written by other CTAs of the same launch are seen.  Lane i owns
-// dims [D/32 * i, D/32 * (i+1)); D is 128 or 256.
-__device__ __forceinline__ void merge_row_warp(const __half *po, const float2 *pml, float *out,
-                                               uint32_t n_live, uint32_t D)
-{
-    if (D == 256)
-        merge_rows_warp_v<8, 1>(&po, &pml, &out, 1, n_live, D);
-    else
-        merge_rows_warp_v<4, 1>(&po, &pml, &out, 1, n_live, D);
-}
-
-// Two rows at once, with the same arithmetic per row as merge_row_warp (the
-// loads of both rows are in flight together); row 1 is skipped when nr == 1.
-__device__ __forceinline__ void merge_row_pair_warp(const __half *const po[2],
-                                                    const float2 *const pml[2],
-                                                    float *const out[2], int nr,
-                                                    uint32_t n_live, uint32_t D)
-{
-    if (D == 256)
-        merge_rows_warp_v<8, 2>(po, pml, out, nr, n_live, D);
-    else
-        merge_rows_warp_v<4, 2>(po, pml, out, nr, n_live, D);
-}
-
-// In-launch merge ("HRX: multi-pass KV-block reduction for flash-attention
-// decode-split", llama.cpp fork pull 13, Changes: the reduction runs in the
-// same launch through an atomic completion counter, with no second dispatch and
-// no waiting).  Called by every thread of a CTA after it has written the
-// partials of (sequence seq, its partition): the CTA that completes the
-// sequence's count merges all its rows into out and resets the counter to 0.
-// Nothing ever waits on another CTA.
-template <class P>
-__device__ inline void fused_merge_tail(const P &p, uint32_t seq, uint32_t warp, uint32_t nwarps)
+// Arrival of a CTA at a completion counter of the in-launch merge ("HRX:
+// multi-pass KV-block reduction for flash-attention decode-split", llama.cpp
+// fork pull 13, Changes: the reduction runs in the same launch through an
+// atomic completion counter, no second dispatch, no waiting).  Called by every
+// thread after the CTA's writes that the count covers; true in the CTA whose
+// arrival is the target-th, which resets the counter to 0 for the next launch
+// and may then read everything the counted CTAs wrote.  Nothing waits.
+__device__ inline bool merge_arrive(int32_t *counter, uint32_t target)
 {
     __shared__ int last;
-    __threadfence();  // this thread's partial writes before the count
+    __threadfence();  // this thread's writes before the count
     __syncthreads();
-    const int32_t L = p.seq_lens[seq];
-    const uint32_t n_live = L > 0 ? ((uint32_t)L + p.part_tokens - 1) / p.part_tokens : 0;
     if (threadIdx.x == 0) {
-        const int old = atomicAdd(&p.counters[seq], 1);
-        last = (uint32_t)(old + 1) == n_live;
+        const int old = atomicAdd(counter, 1);
+        last = (uint32_t)(old + 1) == target;
         if (last)
-            p.counters[seq] = 0;  // every partition of this launch has counted
+            *counter = 0;
     }
     __syncthreads();
     if (!last)
-        return;
-    __threadfence();  // the other CTAs' partials are visible past their counts
+        return false;
+    __threadfence();  // the counted CTAs' writes are visible past their counts
+    return true;
+}
+
+// The in-launch merge, run by every thread of the CTA of (sequence seq,
+// partition part) after it has written its partials.  One pass: the CTA that
+// completes the sequence merges all its rows into out.  Two passes: the CTA
+// that completes a group merges the group's partials of every row into the
+// group's first partial slot, and the CTA that completes the last group merges
+// the group results into out.  An empty sequence has one CTA and writes 0.
+template <class P>
+__device__ inline void fused_merge(const P &p, uint32_t seq, uint32_t part, uint32_t warp,
+                                   uint32_t nwarps)
+{
+    const int32_t L = p.seq_lens[seq];
+    uint32_t n = L > 0 ? ((uint32_t)L + p.part_tokens - 1) / p.part_tokens : 0;
+    n = n < p.n_parts ? n : p.n_parts;
+    const uint32_t gs = merge_group_size(n), ng = n > gs ? (n + gs - 1) / gs : 1;
+    int32_t *cnt = p.counters + (uint64_t)seq * merge_counters_per_seq(p.n_parts);
     const __half *po = static_cast<const __half *>(p.part_o);
     const float2 *pml = reinterpret_cast<const float2 *>(p.part_ml);
-    // rows h and h + nwarps together, so that a warp has both rows' loads in flight
+    if (ng > 1) {
+        const uint32_t g = part / gs, p0 = g * gs, ng_g = min(gs, n - p0);
+        if (!merge_arrive(cnt + 1 + g, ng_g))
+            return;
+        for (uint32_t h = warp; h < p.hq; h += 2 * nwarps) {
+            const uint64_t s0 = (uint64_t)seq * p.hq + h;
+            const uint64_t s1 = h + nwarps < p.hq ? s0 + nwarps : s0;
+            const __half *rpo[2] = {po + (s0 * p.n_parts + p0) * p.d,
+                                    po + (s1 * p.n_parts + p0) * p.d};
+            const float2 *rml[2] = {pml + s0 * p.n_parts + p0, pml + s1 * p.n_parts + p0};
+            // in place: the group's first slot, read before it is written
+            __half *ro[2] = {const_cast<__half *>(rpo[0]), const_cast<__half *>(rpo[1])};
+            float2 *rm[2] = {const_cast<float2 *>(rml[0]), const_cast<float2 *>(rml[1])};
+            const int nr = h + nwarps < p.hq ? 2 : 1;
+            if (p.d == 256)
+                merge_rows_warp_v<8, 2, true>(rpo, rml, ng_g, 1, p.d, nr, nullptr, ro, rm);
+            else
+                merge_rows_warp_v<4, 2, true>(rpo, rml, ng_g, 1, p.d, nr, nullptr, ro, rm);
+        }
+    }
+    if (!merge_arrive(cnt, ng > 1 ? ng : 1))
+        return;
+    const uint32_t m = ng > 1 ? ng : n, stride = ng > 1 ? gs : 1;
     for (uint32_t h = warp; h < p.hq; h += 2 * nwarps) {
         const uint64_t s0 = (uint64_t)seq * p.hq + h;
         const uint64_t s1 = h + nwarps < p.hq ? s0 + nwarps : s0;
         const __half *rpo[2] = {po + s0 * p.n_parts * p.d, po + s1 * p.n_parts * p.d};
         const float2 *rml[2] = {pml + s0 * p.n_parts, pml + s1 * p.n_parts};
         float *rout[2] = {p.out + s0 * p.d, p.out + s1 * p.d};
-        merge_row_pair_warp(rpo, rml, rout, h + nwarps < p.hq ? 2 : 1, n_live, p.d);
+        const int nr = h + nwarps < p.hq ? 2 : 1;
+        if (p.d == 256)
+            merge_rows_warp_v<8, 2, false>(rpo, rml, m, stride, p.d, nr, rout, nullptr, nullptr);
+        else
+            merge_rows_warp_v<4, 2, false>(rpo, rml, m, stride, p.d, nr, rout, nullptr, nullptr);
     }
 }
 

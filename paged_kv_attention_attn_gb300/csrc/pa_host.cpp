@@ -222,6 +222,7 @@ extern "C" int pa_plan(const pa_plan_in *in, pa_plan_t *out)
         p.n_ctas = (uint32_t)n;
         p.part_o_bytes = (uint64_t)in->n_seqs * in->hq * n_parts * in->d * 2ull;
         p.part_ml_bytes = (uint64_t)in->n_seqs * in->hq * n_parts * 8ull;
+        p.counter_bytes = (uint64_t)in->n_seqs * pa::merge_counters_per_seq((uint32_t)n_parts) * 4ull;
     }
     *out = p;
     return PA_OK;

@@ -16,13 +16,50 @@ int cuda_check(cudaError_t e, const char *entry, const char *what);
 inline cudaStream_t stream_of(pa_stream_t s) { return reinterpret_cast<cudaStream_t>(s); }
 
 // Everything a decode kernel needs, resolved on the host.
+#ifdef __CUDACC__
+#define PA_HD __host__ __device__
+#else
+#define PA_HD
+#endif
+
+// Smallest g with g * g >= n.
+inline PA_HD uint32_t ceil_sqrt_u32(uint32_t n)
+{
+    uint32_t lo = 0, hi = 65536;
+    while (lo < hi) {
+        const uint32_t mid = (lo + hi) / 2;
+        if ((uint64_t)mid * mid >= n)
+            hi = mid;
+        else
+            lo = mid + 1;
+    }
+    return lo;
+}
+
+// Group size of the merge of n live partials: all of them (one pass) up to 8,
+// else ceil(sqrt(n)), so that both passes of the two-pass merge take about
+// sqrt(n) partials.
+inline PA_HD uint32_t merge_group_size(uint32_t n)
+{
+    return n <= 8 ? (n > 0 ? n : 1u) : ceil_sqrt_u32(n);
+}
+
+// Completion counters per sequence of the in-launch merge: one for the last
+// pass and one per group (a sequence has at most ceil(sqrt(n_parts)) groups).
+inline PA_HD uint32_t merge_counters_per_seq(uint32_t n_parts)
+{
+    return 1u + ceil_sqrt_u32(n_parts);
+}
+
 struct DecodeParams {
     const uint8_t *k_pool, *v_pool;
     uint64_t n_pool_blocks;
     const int32_t *block_table;
     uint32_t table_stride;
     const int32_t *seq_lens;
-    const void *q;          // float32 [S][hq][d] (F16 K) or q8_1 blocks
+    const void *q;          // float32 [S][hq][d] (F16 K, or q_f32) or q8_1 blocks
+    uint32_t q_f32;         // quantised K, fast kernel: q is float32 and each CTA
+                            // quantises the rows it needs to q8_1 itself
     float scale_log2;       // scale * log2(e)
     void *part_o;           // f16 [S][hq][n_parts][d]
     float *part_ml;         // float2 [S][hq][n_parts]

@@ -46,31 +46,34 @@ def with_canary(t: torch.Tensor, extra_bytes: int = 4096):
 
 
 def run(case, *, force_parts=0, flags=0, plan=None, canary=False, step=True, stream=None,
-        fused=False):
+        fused=False, out_fill=None, q=None):
     """One decode step of `case` through the C ABI.  Returns (out float32
-    tensor, workspace, plan, canary tails)."""
+    tensor, workspace, plan, canary tails).  out_fill pre-fills the output
+    buffer; q replaces the case's query."""
     sp = case.spec
     dev = case.k_pool.device
     pl = plan or pa.plan(seq_lens=sp.seq_lens, block_size=sp.block_size, hq=sp.hq, hkv=sp.hkv,
                          d=sp.d, k_type=sp.k_type, v_type=sp.v_type, force_parts=force_parts)
     ws = pa.workspace(pl, n_seqs=sp.n_seqs, hq=sp.hq, d=sp.d, device=dev)
     tails = []
+    if out_fill is not None:
+        ws.out.fill_(out_fill)
     if canary:
         ws.out, t1 = with_canary(ws.out)
         ws.part_o, t2 = with_canary(ws.part_o)
         ws.part_ml, t3 = with_canary(ws.part_ml)
         tails = [t1, t2, t3]
     args = pa.make_args(k_pool=case.k_pool, v_pool=case.v_pool, block_table=case.block_table,
-                        seq_lens=case.seq_lens, q=case.q, ws=ws, hkv=sp.hkv,
-                        block_size=sp.block_size, k_type=sp.k_type, v_type=sp.v_type,
-                        flags=flags)
+                        seq_lens=case.seq_lens, q=case.q if q is None else q, ws=ws,
+                        hkv=sp.hkv, block_size=sp.block_size, k_type=sp.k_type,
+                        v_type=sp.v_type, flags=flags)
     if fused:
         pa.decode_step_fused(args, ws, stream=stream)
     elif step:
         pa.decode_step(args, ws, stream=stream)
     else:
         if sp.k_type != synth.F16:
-            pa.quantize_q(case.q, out=ws.q8_1, stream=stream)
+            pa.quantize_q(case.q if q is None else q, out=ws.q8_1, stream=stream)
             args.q = ws.q8_1.data_ptr()
         pa.decode_partial(args, pl, stream=stream)
         if not pl.direct:

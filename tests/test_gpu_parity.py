@@ -265,3 +265,58 @@ def test_fused_merge_repeated_calls_reuse_counters(kernel):
         torch.cuda.synchronize()
         assert torch.equal(ws.out.view(torch.int32), ref.view(torch.int32))
         assert int(ws.counters.abs().sum()) == 0
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("t", [synth.F16, synth.Q4_0])
+def test_every_output_row_is_written(kernel, t):
+    """Every mode of the step writes every output row: the rows of empty
+    sequences are zero whatever the buffer held before (NaN here)."""
+    spec = synth.CaseSpec(seq_lens=[0, 900, 0, 0, 40, 0], k_type=t, v_type=t, junk=3)
+    case = synth.build_case(spec, seed=2800 + t, device=DEV)
+    ref, vmax = H.oracle_out(case), H.oracle_vmax(case)
+    for force in (0, 1, 5):
+        for fused in (False, True):
+            out, ws, pl, _ = H.run(case, force_parts=force, flags=KERNELS[kernel], fused=fused,
+                                   out_fill=float("nan"))
+            assert pa.status_read(ws.status) == 0
+            g = out.cpu()
+            for s_, L in enumerate(spec.seq_lens):
+                if L == 0:
+                    assert bool((g[s_] == 0).all()), (force, fused, s_)
+            H.assert_close(case, out, ref, vmax)
+            assert int(ws.counters.abs().sum()) == 0
+
+
+def _adversarial_query(q):
+    """Blocks that exercise the q8_1 rounding: all zero, exact ties (the
+    scale is a power of two so x / d is k + 1/2 exactly), a signed zero, tiny
+    and large magnitudes, and values at the clamp."""
+    q = q.clone()
+    q[0, 0, :32] = 0.0
+    ties = torch.tensor([15.875] + [(k + 0.5) * 0.125 for k in range(-15, 15)] + [-15.875])
+    q[0, 1, 32:64] = ties
+    q[0, 2, 64:96] = ties.flip(0) * -4.0
+    q[0, 3, :32] = -0.0
+    q[0, 3, 5] = 2.0 ** -20
+    q[1, 4, :] = q[1, 4, :] * 1e-4
+    q[1, 5, :] = q[1, 5, :] * 40.0
+    return q
+
+
+def test_in_kernel_query_quantisation_matches_the_pre_pass():
+    """The fused step of the fast kernel quantises the query itself with the
+    pre-pass's arithmetic; its output equals the three-launch step's bit for
+    bit, also on blocks built to expose rounding differences."""
+    spec = synth.CaseSpec(seq_lens=[700, 333], k_type=synth.Q4_0, v_type=synth.Q4_0, junk=2)
+    case = synth.build_case(spec, seed=2900, device=DEV)
+    q = _adversarial_query(case.q)
+    for force in (0, 1, 4):
+        a, _, _, _ = H.run(case, force_parts=force, q=q)
+        b, ws, _, _ = H.run(case, force_parts=force, q=q, fused=True, out_fill=float("nan"))
+        assert pa.status_read(ws.status) == 0
+        assert torch.equal(a.view(torch.int32), b.view(torch.int32)), force
+    # and the pre-pass itself codes these blocks as the oracle does
+    got = pa.quantize_q(q).cpu().numpy().reshape(-1, 8 * 36)
+    ref = oracle.quantize_q8_1(q.cpu().numpy().reshape(-1, 256))
+    assert np.array_equal(got, ref)
