@@ -71,8 +71,10 @@ typedef struct CUstream_st *pa_stream_t;
 /* Device status word bits (written by the kernels with atomicOr). */
 #define PA_STATUS_CORRUPT_TABLE 1 /* a block id outside [0, n_pool_blocks) */
 #define PA_STATUS_TIMEOUT 2       /* a pipeline wait exceeded its bound (2 s); output invalid */
-#define PA_STATUS_LEN_OVER_PLAN 4 /* a sequence longer than the plan's n_parts * part_tokens:
-                                     its tokens past that were left out; output invalid */
+#define PA_STATUS_LEN_OVER_PLAN 4 /* lengths the plan does not cover: a sequence longer than
+                                     n_parts * part_tokens, or more (sequence, partition) pairs
+                                     than n_ctas; the work past the plan was left out and the
+                                     output is invalid */
 
 typedef enum { PA_F16 = 0, PA_Q8_0 = 1, PA_Q4_0 = 2 } pa_type;
 
@@ -239,7 +241,8 @@ int pa_merge(const void *part_o, const float *part_ml, const int32_t *seq_lens, 
  * by the CTA that completes it.  No CTA ever waits for another.
  * counters: device int32 [plan->counter_bytes / 4], caller-owned, all zero
  * before the first call; every completed call leaves them zero.  After a call
- * that reported PA_STATUS_TIMEOUT the caller zeroes them again.  Calls that
+ * that reported PA_STATUS_TIMEOUT or PA_STATUS_LEN_OVER_PLAN the caller
+ * zeroes them again.  Calls that
  * share a counter array must not overlap on the GPU.  The partials are
  * overwritten by the group results.  Direct plans ignore counters (may be
  * NULL) and behave as pa_decode_partial.  part_o / part_ml / out are required
@@ -306,8 +309,9 @@ int pa_decode_step_fused_host(const float *q_host, float *out_host, const pa_dec
 
 /* Reads the status word into *host_out (synchronising `stream`); reset != 0
  * clears it afterwards.  Returns PA_ERR_TIMEOUT if the timeout bit is set,
- * else PA_ERR_CORRUPT_TABLE if the corrupt-table bit is set, PA_OK
- * otherwise, PA_ERR_CUDA on a runtime failure. */
+ * else PA_ERR_RANGE if the lengths-over-plan bit is set, else
+ * PA_ERR_CORRUPT_TABLE if the corrupt-table bit is set, PA_OK otherwise,
+ * PA_ERR_CUDA on a runtime failure. */
 int pa_status_read(int32_t *dev_status, pa_stream_t stream, int32_t *host_out, int reset);
 
 /* Debug ([P4] Acceptance Criteria: the offsets must be 64-bit).  Writes the

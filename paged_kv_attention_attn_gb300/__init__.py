@@ -20,7 +20,7 @@ TYPES = {"f16": F16, "q8_0": Q8_0, "q4_0": Q4_0}
 
 PA_OK, PA_ERR_INVALID, PA_ERR_NOMEM, PA_ERR_STALE = 0, -1, -2, -3
 PA_ERR_CUDA, PA_ERR_CORRUPT_TABLE, PA_ERR_RANGE, PA_ERR_TIMEOUT = -4, -5, -6, -7
-PA_STATUS_CORRUPT_TABLE, PA_STATUS_TIMEOUT = 1, 2
+PA_STATUS_CORRUPT_TABLE, PA_STATUS_TIMEOUT, PA_STATUS_LEN_OVER_PLAN = 1, 2, 4
 PA_FLAG_PLAIN = 1
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_build", "libpa.so")
@@ -342,7 +342,7 @@ def status_read(status: torch.Tensor, reset: bool = True, stream=None) -> int:
     """Returns the status word bits (synchronises the stream)."""
     v = _i32()
     rc = lib().pa_status_read(_ptr(status), _stream(stream), ctypes.byref(v), int(reset))
-    if rc not in (PA_OK, PA_ERR_CORRUPT_TABLE, PA_ERR_TIMEOUT):
+    if rc not in (PA_OK, PA_ERR_CORRUPT_TABLE, PA_ERR_TIMEOUT, PA_ERR_RANGE):
         _check(rc)
     return int(v.value)
 

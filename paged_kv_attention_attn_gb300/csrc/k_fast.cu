@@ -627,6 +627,8 @@ __global__ void __launch_bounds__(T::kMaxWarps * 32, 1)
     __syncthreads();
 
     uint32_t seq, part;
+    if (!p.direct && blockIdx.x == gridDim.x - 1 && warp == 0)
+        check_grid_vs_plan(p.seq_lens, p.n_seqs, p.part_tokens, p.n_parts, p.status);
     if (p.direct) {
         seq = blockIdx.x;
         part = 0;

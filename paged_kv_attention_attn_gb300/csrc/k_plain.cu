@@ -213,6 +213,8 @@ __global__ void __launch_bounds__(kPlainWarps * 32) plain_decode_kernel(const De
     uint8_t *qsm = smem + warp * ((QB + 15) / 16 * 16);
 
     uint32_t s, part;
+    if (!p.direct && blockIdx.x == gridDim.x - 1 && warp == 0)
+        check_grid_vs_plan(p.seq_lens, p.n_seqs, p.part_tokens, p.n_parts, p.status);
     if (p.direct) {
         s = blockIdx.x;
         part = 0;

@@ -357,6 +357,8 @@ extern "C" int pa_status_read(int32_t *dev_status, pa_stream_t stream, int32_t *
     *host_out = v;
     if (v & PA_STATUS_TIMEOUT)
         return fail(PA_ERR_TIMEOUT, E, "a kernel abandoned a bounded pipeline wait");
+    if (v & PA_STATUS_LEN_OVER_PLAN)
+        return fail(PA_ERR_RANGE, E, "sequence lengths past what the plan covers were left out");
     if (v & PA_STATUS_CORRUPT_TABLE)
         return fail(PA_ERR_CORRUPT_TABLE, E, "a block id outside the pool was skipped");
     return PA_OK;

@@ -271,6 +271,27 @@ __device__ __forceinline__ void check_len_vs_plan(int32_t L, uint32_t n_parts,
         atomicOr(status, PA_STATUS_LEN_OVER_PLAN);
 }
 
+// Records lengths that need more (sequence, partition) pairs than the grid has
+// CTAs (the pairs past the grid are left out).  Called by one full warp of the
+// grid's last CTA.
+__device__ __forceinline__ void check_grid_vs_plan(const int32_t *seq_lens, uint32_t n_seqs,
+                                                   uint32_t part_tokens, uint32_t n_parts,
+                                                   int32_t *status)
+{
+    const int lane = threadIdx.x & 31;
+    uint64_t pairs = 0;
+    for (uint32_t s = lane; s < n_seqs; s += 32) {
+        const int32_t L = seq_lens[s];
+        uint32_t n = L > 0 ? ((uint32_t)L + part_tokens - 1) / part_tokens : 1u;
+        pairs += n < n_parts ? n : n_parts;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        pairs += __shfl_xor_sync(0xffffffffu, pairs, o);
+    if (lane == 0 && pairs > gridDim.x)
+        atomicOr(status, PA_STATUS_LEN_OVER_PLAN);
+}
+
 // One row merged by one warp, the flat merge or the two passes as above,
 // float32 out.  The group results are staged in scr (this warp's D halves
 // and one (m, l)) exactly as the in-launch merge stores them in part_o, so

@@ -320,3 +320,24 @@ def test_in_kernel_query_quantisation_matches_the_pre_pass():
     got = pa.quantize_q(q).cpu().numpy().reshape(-1, 8 * 36)
     ref = oracle.quantize_q8_1(q.cpu().numpy().reshape(-1, 256))
     assert np.array_equal(got, ref)
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("fused", [False, True])
+def test_lengths_past_the_plan_are_flagged_and_stay_in_bounds(kernel, fused):
+    """Device lengths that the plan does not cover (a sequence longer than
+    n_parts * part_tokens; more partitions than the grid has CTAs) set
+    PA_STATUS_LEN_OVER_PLAN, and nothing is written past the buffers."""
+    spec = synth.CaseSpec(seq_lens=[3000, 1000], k_type=synth.Q4_0, v_type=synth.Q4_0, junk=2)
+    case = synth.build_case(spec, seed=3100, device=DEV)
+    for planned in ([1000, 1000], [1000, 100]):
+        pl = pa.plan(seq_lens=planned, block_size=16, hq=24, hkv=4, d=256, k_type=synth.Q4_0,
+                     v_type=synth.Q4_0, force_parts=4)
+        assert not pl.direct
+        out, ws, _, tails = H.run(case, plan=pl, flags=KERNELS[kernel], fused=fused,
+                                  canary=True)
+        H.check_canaries(tails)
+        assert pa.status_read(ws.status) & pa.PA_STATUS_LEN_OVER_PLAN, planned
+    # lengths inside the plan raise nothing
+    out, ws, _, _ = H.run(case, force_parts=4, flags=KERNELS[kernel], fused=fused)
+    assert pa.status_read(ws.status) == 0
