@@ -5,7 +5,10 @@ of 131,072 tokens, D=256, Hq=24, Hkv=4, 16-token blocks, Q4_0 K/V from
 N(0,1), fp32 Q from N(0,1) quantised to q8_1, block tables randomly
 interleaved in one pool ("feat: add paged-attention monolithic decode-only AR
 foundation", lucebox pull 555, Benchmark results).  A step is the whole hot
-path: the q8_1 pre-pass, the decode kernel and the merge, on one stream.
+path through the public call pa_decode_step_fused: q8_1 quantisation of the
+query, the decode and the merge.  With the fast kernel that is one launch
+(the kernel quantises the query itself and merges in-launch); otherwise the
+q8_1 pre-pass and the decode launch (--unfused: pre-pass, decode, merge).
 
 Prints ONE JSON line (rank 0).  `value` is achieved algorithmic HBM
 bandwidth in GB/s over all ranks (bytes every rank's steps must move / the
@@ -62,9 +65,11 @@ def load_peaks():
     return 6800.0, "fallback"
 
 
-def algorithmic_bytes(spec, plan, fused: bool = True) -> dict:
+def algorithmic_bytes(spec, plan, fused: bool = True, in_kernel_q: bool = False) -> dict:
     """Bytes the method must move in one step, by class.  With the fused
-    merge the decode launch also reads the partials back and writes out."""
+    merge the decode launch also reads the partials back and writes out;
+    with in-kernel quantisation it reads the float32 query and there is no
+    pre-pass."""
     S, hq, d = spec.n_seqs, spec.hq, spec.d
     krb, vrb = synth.row_bytes(spec.k_type, d), synth.row_bytes(spec.v_type, d)
     lens = spec.seq_lens
@@ -73,8 +78,8 @@ def algorithmic_bytes(spec, plan, fused: bool = True) -> dict:
     q_f32 = S * hq * d * 4
     q81 = S * hq * d // 32 * 36
     quantised = spec.k_type != synth.F16
-    prepass = (q_f32 + q81) if quantised else 0
-    q_read = q81 if quantised else q_f32
+    prepass = (q_f32 + q81) if quantised and not in_kernel_q else 0
+    q_read = q81 if quantised and not in_kernel_q else q_f32
     out = S * hq * d * 4
     if plan.direct:
         part_w = part_r = 0
@@ -282,7 +287,12 @@ def run_ours(a, world, rank, local):
                             q=ws.q8_1 if quantised else case.q, ws=ws, hkv=spec.hkv,
                             block_size=spec.block_size, k_type=spec.k_type,
                             v_type=spec.v_type, flags=flags)
-    nb = algorithmic_bytes(spec, pl, fused=not a.unfused)
+    kname = pa.decode_kernel_name(k_type=spec.k_type, v_type=spec.v_type, d=spec.d,
+                                  hq=spec.hq, hkv=spec.hkv, block_size=spec.block_size,
+                                  flags=flags)
+    # the fused step of the fast kernel quantises the query itself: one launch
+    in_kernel_q = not a.unfused and quantised and kname == "fast_decode_kernel"
+    nb = algorithmic_bytes(spec, pl, fused=not a.unfused, in_kernel_q=in_kernel_q)
     stream = torch.cuda.current_stream()
     L = pa.lib()
     import ctypes
@@ -292,7 +302,16 @@ def run_ours(a, world, rank, local):
     fused = not a.unfused
     counters = ws.counters.data_ptr()
 
+    p_step_args = ctypes.byref(args)
+
     def step(ev0=None, ev1=None):
+        if in_kernel_q:  # the public one-launch step
+            if ev0 is not None:
+                ev0.record(stream)
+            rc = L.pa_decode_step_fused(p_step_args, p_plan, ws.q8_1.data_ptr(), counters, sh)
+            if ev1 is not None:
+                ev1.record(stream)
+            return rc
         if quantised:
             L.pa_quantize_q(case.q.data_ptr(), ws.q8_1.data_ptr(), spec.n_seqs * spec.hq,
                             spec.d, sh)
@@ -373,16 +392,20 @@ def run_ours(a, world, rank, local):
     if world == 1 and not a.no_cpu_baseline:
         host = host_copy(case)
         threads = len(os.sched_getaffinity(0))
-        seqs = list(range(min(2, spec.n_seqs)))
-        dt, cb = oracle_sample(host, spec, seqs, threads)
+        # a bounded sample of about CPU_SECONDS of oracle work: whole sequences,
+        # every query head, full context, in turn until the time is spent
+        dt = cb = 0.0
+        done = []
+        while dt < a.cpu_seconds and len(done) < 64 * spec.n_seqs:
+            s = len(done) % spec.n_seqs
+            t, b = oracle_sample(host, spec, [s], threads)
+            dt, cb = dt + t, cb + b
+            done.append(s)
         cpu = {"value": cb / dt / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
-               "sample": f"sequences {seqs} of {spec.n_seqs}, all {spec.hq} query heads, "
-                         f"full context ({sum(spec.seq_lens[s] for s in seqs)} tokens), "
-                         f"{dt:.2f} s wall"}
+               "sample": f"{len(done)} whole sequences of the workload in turn (every query "
+                         f"head, full context, {sum(spec.seq_lens[s] for s in done)} tokens), "
+                         f"{dt:.1f} s wall"}
 
-    kname = pa.decode_kernel_name(k_type=spec.k_type, v_type=spec.v_type, d=spec.d,
-                                  hq=spec.hq, hkv=spec.hkv, block_size=spec.block_size,
-                                  flags=flags)
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K,
         "warmup": a.warmup, "ms_per_step": ms_per_step, "us_per_step": ms_per_step * 1e3,
@@ -394,7 +417,9 @@ def run_ours(a, world, rank, local):
                    "kv_type": synth.TYPE_LABEL[spec.k_type],
                    "l2": f"inputs larger than L2: {nb['kv'] / 1e9:.3f} GB of K/V per step",
                    "kernel": kname, "plan": pl.as_dict(),
-                   "step": ("q8_1 pre-pass + decode with in-launch merge" if fused else
+                   "step": ("one launch: in-kernel q8_1 quantisation, decode, in-launch merge"
+                            if in_kernel_q else
+                            "q8_1 pre-pass + decode with in-launch merge" if fused else
                             "q8_1 pre-pass + decode + merge kernel"),
                    "bytes_per_step": nb},
         "roofline": {"bound": "hbm", "achieved": dec_achieved, "peak": peak, "unit": "GB/s",
@@ -404,7 +429,8 @@ def run_ours(a, world, rank, local):
                      "traffic": traffic_from_profiles(kname)},
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": K * ((2 if quantised else 1) + (0 if (pl.direct or fused) else 1)),
+        "gpu_launches": K * (1 if in_kernel_q else
+                             (2 if quantised else 1) + (0 if (pl.direct or fused) else 1)),
         "clocks": clk,
     }
     if rank == 0:
@@ -423,6 +449,8 @@ def main():
     ap.add_argument("--unfused", action="store_true",
                     help="time the three-launch step (separate merge) instead of the fused one")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="oracle work timed for cpu_baseline (whole sequences in turn)")
     ap.add_argument("--ref-steps", type=int, default=None)
     ap.add_argument("--ref-warmup", type=int, default=None)
     a = ap.parse_args()
