@@ -205,19 +205,24 @@ def kernel_source_sha() -> str:
 
 # ------------------------------------------------------------------ oracle
 
-def oracle_sample(case_host, spec, seqs, threads):
-    """Times the float64 oracle on sequences `seqs` (all query heads, full
-    context) of the workload; returns (seconds, algorithmic bytes)."""
+def oracle_sample(case_host, spec, seqs, threads, group=None):
+    """Times the float64 oracle on sequences `seqs` (full context; all query
+    heads, or only those of K/V head `group`) of the workload; returns
+    (seconds, algorithmic bytes: the K/V rows those heads need, once, and
+    their outputs)."""
     import oracle
     k, v, bt, sl, q = case_host
-    units = [(s, h) for s in seqs for h in range(spec.hq)]
+    G = spec.hq // spec.hkv
+    heads = range(spec.hq) if group is None else range(group * G, (group + 1) * G)
+    units = [(s, h) for s in seqs for h in heads]
     t0 = time.perf_counter()
     oracle.decode(k, v, bt, sl, q, hkv=spec.hkv, block_size=spec.block_size,
                   k_type=spec.k_type, v_type=spec.v_type, units=units, n_threads=threads)
     dt = time.perf_counter() - t0
     krb, vrb = synth.row_bytes(spec.k_type, spec.d), synth.row_bytes(spec.v_type, spec.d)
-    nbytes = sum(spec.seq_lens[s] * spec.hkv * (krb + vrb) for s in seqs)
-    nbytes += len(seqs) * spec.hq * spec.d * 8
+    kv_heads = spec.hkv if group is None else 1
+    nbytes = sum(spec.seq_lens[s] * kv_heads * (krb + vrb) for s in seqs)
+    nbytes += len(units) * spec.d * 8
     return dt, nbytes
 
 
@@ -238,20 +243,26 @@ def run_reference(a, world, rank):
     host = host_copy(case)
     del case
     threads = len(os.sched_getaffinity(0))
-    seqs = [0]  # one sequence, every query head, full context: a bounded sample
-    for _ in range(a.ref_warmup):
-        oracle_sample(host, spec, seqs, threads)
+    # each step a bounded sample: the query heads of one K/V head of one
+    # sequence, full context, taking the sequences and heads in turn
+    def unit(i):
+        return [i % spec.n_seqs], (i // spec.n_seqs) % spec.hkv
+    for i in range(a.warmup):
+        seqs, g = unit(i)
+        oracle_sample(host, spec, seqs, threads, group=g)
     tot_t, tot_b = 0.0, 0
-    for _ in range(a.ref_steps):
-        dt, nb = oracle_sample(host, spec, seqs, threads)
+    for i in range(a.steps):
+        seqs, g = unit(i)
+        dt, nb = oracle_sample(host, spec, seqs, threads, group=g)
         tot_t += dt
         tot_b += nb
     gbs = tot_b / tot_t / 1e9
-    sample = (f"sequence 0 of {spec.n_seqs}, all {spec.hq} query heads, "
-              f"{spec.seq_lens[0]} tokens, per step")
+    G = spec.hq // spec.hkv
+    sample = (f"per step the {G} query heads of one K/V head of one sequence, full context "
+              f"({max(spec.seq_lens)} tokens at most), sequences and heads in turn")
     line = {"impl": "reference", "metric": METRIC, "value": gbs, "unit": "GB/s",
-            "n_gpus": world, "steps": a.ref_steps, "warmup": a.ref_warmup,
-            "ms_per_step": tot_t / a.ref_steps * 1e3, "higher_is_better": True,
+            "n_gpus": world, "steps": a.steps, "warmup": a.warmup,
+            "ms_per_step": tot_t / a.steps * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": a.workload, "sample": sample},
             "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": threads, "kind": "oracle",
@@ -451,12 +462,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="oracle work timed for cpu_baseline (whole sequences in turn)")
-    ap.add_argument("--ref-steps", type=int, default=None)
-    ap.add_argument("--ref-warmup", type=int, default=None)
     a = ap.parse_args()
     a.warmup = max(a.warmup, 3)
-    a.ref_steps = a.ref_steps if a.ref_steps is not None else min(a.steps, 10)
-    a.ref_warmup = a.ref_warmup if a.ref_warmup is not None else min(a.warmup, 3)
     world, rank, local = dist_setup()
     if a.impl == "reference":
         run_reference(a, world, rank)
