@@ -237,6 +237,78 @@ __device__ __forceinline__ uint32_t movmatrix_t(uint32_t x)
 //      query head), C = O[dimension][head]: columns 2tig, 2tig+1 are again this
 //      thread's heads.
 
+// --- the q8_1 query, shared by the quantised-K types ------------------------
+//
+// Lane (gid, tig) holds, for query head gid of its group, the eight values of
+// each 32-value block at dims 4tig..4tig+3 and 16+4tig..19+4tig: float32 when
+// the kernel quantises the query itself, else the q8_1 codes and scale.  They
+// are fetched before the first K/V copies are issued, so that these loads do
+// not queue behind them.
+template <int NB>
+struct Q81Query {
+    struct Raw {
+        float4 x[NB][2];
+        uint32_t w[NB][2];
+        uint32_t d[NB];
+    };
+
+    // Blocks b with b % nw == w only: the nw warps of a K/V head share the work.
+    __device__ static void fetch(const DecodeParams &p, uint32_t s, uint32_t h0, uint32_t G,
+                                 int gid, int tig, uint32_t w, uint32_t nw, Raw &r)
+    {
+        const uint64_t row = (uint64_t)s * p.hq + h0 + ((uint32_t)gid < G ? gid : 0);
+        if (p.q_f32) {
+            const float *x = static_cast<const float *>(p.q) + row * NB * 32;
+#pragma unroll
+            for (int b = 0; b < NB; ++b) {
+                if ((uint32_t)b % nw != w)
+                    continue;
+                r.x[b][0] = *reinterpret_cast<const float4 *>(x + 32 * b + 4 * tig);
+                r.x[b][1] = *reinterpret_cast<const float4 *>(x + 32 * b + 16 + 4 * tig);
+            }
+        } else {
+            const uint8_t *blk = static_cast<const uint8_t *>(p.q) + row * NB * 36;
+#pragma unroll
+            for (int b = 0; b < NB; ++b) {
+                if ((uint32_t)b % nw != w)
+                    continue;
+                r.d[b] = load_u16(blk + 36 * b);
+                r.w[b][0] = *reinterpret_cast<const uint32_t *>(blk + 36 * b + 4 + 4 * tig);
+                r.w[b][1] = *reinterpret_cast<const uint32_t *>(blk + 36 * b + 20 + 4 * tig);
+            }
+        }
+    }
+
+    // The q8_1 codes of this lane's eight values of block b and the block's
+    // f16-rounded scale.  A float32 query is quantised with the pre-pass's
+    // arithmetic (q8_1_code); the four lanes of a quad hold one block, so its
+    // maximum magnitude is two shuffles away.
+    __device__ static __forceinline__ void codes(const DecodeParams &p, const Raw &r, int b,
+                                                 int (&code)[8], float &d16)
+    {
+        if (p.q_f32) {
+            const float v[8] = {r.x[b][0].x, r.x[b][0].y, r.x[b][0].z, r.x[b][0].w,
+                                r.x[b][1].x, r.x[b][1].y, r.x[b][1].z, r.x[b][1].w};
+            float amax = 0.0f;
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                amax = fmaxf(amax, fabsf(v[j]));
+            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+            const float d = amax / 127.0f;
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                code[j] = q8_1_code(v[j], amax, d);
+            d16 = __half2float(__float2half_rn(amax == 0.0f ? 0.0f : d));
+        } else {
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                code[j] = (int)(int8_t)(uint8_t)(r.w[b][j >> 2] >> (8 * (j & 3)));
+            d16 = half_bits_to_float((uint16_t)r.d[b]);
+        }
+    }
+};
+
 // --- Q4_0, D = 256 --------------------------------------------------------
 template <uint32_t KMAXW>
 struct Q40T {
@@ -265,72 +337,29 @@ struct Q40T {
         uint32_t q;  // shared address of this lane's records (block 0)
     };
 
-    // This lane's eight query values of each block of query head gid of the
-    // group (dims 4tig..4tig+3 and 16+4tig..19+4tig): float32 when the kernel
-    // quantises the query itself, else the q8_1 codes and scale.  Fetched
-    // before the first K/V copies are issued, so that these loads do not
-    // queue behind them.
-    struct QRaw {
-        float4 x[NB][2];
-        uint32_t w[NB][2];
-        uint32_t d[NB];
-    };
+    using Consts = NibbleConsts;
+    using QRaw = typename Q81Query<NB>::Raw;
     __device__ static void fetch_q(const DecodeParams &p, uint32_t s, uint32_t h0, uint32_t G,
-                                   int gid, int tig, QRaw &r)
+                                   int gid, int tig, uint32_t w, uint32_t nw, QRaw &r)
     {
-        const uint64_t row = (uint64_t)s * p.hq + h0 + ((uint32_t)gid < G ? gid : 0);
-        if (p.q_f32) {
-            const float *x = static_cast<const float *>(p.q) + row * D;
-#pragma unroll
-            for (int b = 0; b < NB; ++b) {
-                r.x[b][0] = *reinterpret_cast<const float4 *>(x + 32 * b + 4 * tig);
-                r.x[b][1] = *reinterpret_cast<const float4 *>(x + 32 * b + 16 + 4 * tig);
-            }
-        } else {
-            const uint8_t *blk = static_cast<const uint8_t *>(p.q) + row * NB * 36;
-#pragma unroll
-            for (int b = 0; b < NB; ++b) {
-                r.d[b] = load_u16(blk + 36 * b);
-                r.w[b][0] = *reinterpret_cast<const uint32_t *>(blk + 36 * b + 4 + 4 * tig);
-                r.w[b][1] = *reinterpret_cast<const uint32_t *>(blk + 36 * b + 20 + 4 * tig);
-            }
-        }
+        Q81Query<NB>::fetch(p, s, h0, G, gid, tig, w, nw, r);
     }
 
     // Writes the fragments of query head gid of the group: qhat = f16(q * d_q
     // * scale * log2 e), in the dimension order the nibble expansion produces
-    // (see block()).  A float32 query is first quantised to q8_1 with the
-    // pre-pass's arithmetic (the four lanes of a quad hold one block).  One
-    // warp per K/V head calls this.
+    // (see block()).  One warp per K/V head calls this.
     __device__ static void store_q(const DecodeParams &p, const QRaw &r, uint32_t G, int gid,
-                                   int tig, uint32_t qsm)
+                                   int tig, uint32_t w, uint32_t nw, uint32_t qsm)
     {
         const int lane = gid * 4 + tig;
         const bool live = (uint32_t)gid < G;
 #pragma unroll
         for (int b = 0; b < NB; ++b) {
+            if ((uint32_t)b % nw != w)
+                continue;
             int code[8];
             float d16;
-            if (p.q_f32) {
-                const float v[8] = {r.x[b][0].x, r.x[b][0].y, r.x[b][0].z, r.x[b][0].w,
-                                    r.x[b][1].x, r.x[b][1].y, r.x[b][1].z, r.x[b][1].w};
-                float amax = 0.0f;
-#pragma unroll
-                for (int j = 0; j < 8; ++j)
-                    amax = fmaxf(amax, fabsf(v[j]));
-                amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-                amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-                const float d = amax / 127.0f;
-#pragma unroll
-                for (int j = 0; j < 8; ++j)
-                    code[j] = q8_1_code(v[j], amax, d);
-                d16 = __half2float(__float2half_rn(amax == 0.0f ? 0.0f : d));
-            } else {
-#pragma unroll
-                for (int j = 0; j < 8; ++j)
-                    code[j] = (int)(int8_t)(uint8_t)(r.w[b][j >> 2] >> (8 * (j & 3)));
-                d16 = half_bits_to_float((uint16_t)r.d[b]);
-            }
+            Q81Query<NB>::codes(p, r, b, code, d16);
             const float d = live ? d16 * p.scale_log2 : 0.0f;
             __half qh[8];
             float corr = 0.0f;
@@ -458,6 +487,208 @@ struct Q40T {
 
 using Q40 = Q40T<12>;
 
+// --- Q8_0, D = 256 --------------------------------------------------------
+// Slot layout per side: 16 rows of 272 bytes (eight 34-byte blocks: f16 d,
+// then 32 int8 codes), written by TMA without swizzle; the 272-byte pitch puts
+// the rows of a warp's loads in different banks.
+//  QK runs on the integer tensor path: mma m16n8k32 s8 x s8 -> s32 takes the
+//  Q8_0 codes of 16 tokens x 32 dims as A and the q8_1 codes of the query as
+//  B, so each block's dot is an exact integer (the pages' q8_1 dot), scaled by
+//  d_k * d_q * scale * log2 e in f32.
+//  PV: the code c becomes the exact f16 1024 + (c ^ 0x80) with one byte
+//  permute per two values; one extra MMA with every A entry -1152 removes the
+//  bias, and d_v is folded into P as for Q4_0.
+template <uint32_t KMAXW>
+struct Q80T {
+    static constexpr int D = 256;
+    static constexpr int NB = D / 32;
+    static constexpr int BB = 34;           // block bytes
+    static constexpr int RB = NB * BB;      // row bytes (272)
+    static constexpr int MT = D / 16;
+    static constexpr int DK = 0, DV = NB * kTile * 4;
+    static constexpr int SCRATCH = NB * kTile * 4 + NB * kTile * 2;
+    static constexpr bool kZeroInvalidV = false;
+    static constexpr uint32_t kTmaX = 1;
+    static constexpr uint32_t kMaxWarps = KMAXW;
+
+    static __host__ __device__ constexpr uint32_t side_bytes(uint32_t hkv)
+    {
+        return hkv * kTile * RB;
+    }
+
+    struct Consts {
+        uint32_t flip, f16hi;  // 0x80808080; bytes 0x64 (the high byte of f16 1024)
+        uint32_t nb[4];        // A quad of -1152 (f16 pairs)
+        __device__ __forceinline__ void init()
+        {
+            flip = opaque(0x80808080u);
+            f16hi = opaque(0x64646464u);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                nb[i] = opaque(0xE480E480u);
+        }
+    };
+
+    // Query fragments in shared memory, one 16-byte record per (block, lane)
+    // of each K/V head: the two B registers (the q8_1 codes of query head gid
+    // at dims 4tig.. and 16+4tig..), then d_q * scale * log2 e of the heads
+    // 2tig and 2tig+1 (this thread's C columns).
+    static constexpr int QREC = 16;
+    static constexpr int QBYTES = NB * 32 * QREC;
+    struct Frag {
+        uint32_t q;
+    };
+    using QRaw = typename Q81Query<NB>::Raw;
+
+    __device__ static void fetch_q(const DecodeParams &p, uint32_t s, uint32_t h0, uint32_t G,
+                                   int gid, int tig, uint32_t w, uint32_t nw, QRaw &r)
+    {
+        Q81Query<NB>::fetch(p, s, h0, G, gid, tig, w, nw, r);
+    }
+
+    __device__ static void store_q(const DecodeParams &p, const QRaw &r, uint32_t G, int gid,
+                                   int tig, uint32_t w, uint32_t nw, uint32_t qsm)
+    {
+        const int lane = gid * 4 + tig;
+        const bool live = (uint32_t)gid < G;
+#pragma unroll
+        for (int b = 0; b < NB; ++b) {
+            if ((uint32_t)b % nw != w)
+                continue;
+            int code[8];
+            float d16;
+            Q81Query<NB>::codes(p, r, b, code, d16);
+            const float dq = live ? d16 * p.scale_log2 : 0.0f;
+            uint32_t w[2];
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+                w[h] = (uint32_t)(code[4 * h] & 0xFF) | (uint32_t)(code[4 * h + 1] & 0xFF) << 8 |
+                       (uint32_t)(code[4 * h + 2] & 0xFF) << 16 |
+                       (uint32_t)(code[4 * h + 3] & 0xFF) << 24;
+            // the scales of heads 2tig and 2tig+1 live in lanes 8tig and 8tig+4
+            const float q0 = __shfl_sync(0xffffffffu, dq, 8 * tig);
+            const float q1 = __shfl_sync(0xffffffffu, dq, 8 * tig + 4);
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
+                             qsm + (b * 32 + lane) * QREC),
+                         "r"(w[0]), "r"(w[1]), "r"(__float_as_uint(q0)), "r"(__float_as_uint(q1)));
+        }
+    }
+
+    __device__ static void load_q(uint32_t qsm, int lane, Frag &f) { f.q = qsm + lane * QREC; }
+
+    // Block scales into the warp's scratch, as for Q4_0: dk as float with the
+    // pair (t, t+8) adjacent, dv as half in token order; zero for invalid tokens.
+    __device__ static void extract(uint32_t kh, uint32_t vh, uint32_t scr, int nvalid, int lane)
+    {
+        const int t = lane & 15, b0 = lane >> 4;
+        const bool v = t < nvalid;
+        const uint32_t ka = kh + t * RB + BB * b0, va = vh + t * RB + BB * b0;
+        const uint32_t sk = scr + DK + 4 * (b0 * kTile + 2 * (t & 7) + (t >> 3));
+        const uint32_t sv = scr + DV + 2 * (b0 * kTile + t);
+#pragma unroll
+        for (int k = 0; k < NB / 2; ++k) {
+            const uint32_t kd = lds_u16(ka + 2 * BB * k);
+            const uint32_t vd = lds_u16(va + 2 * BB * k);
+            sts_f32(sk + 128 * k, v ? half_bits_to_float((uint16_t)kd) : 0.0f);
+            sts_u16(sv + 64 * k, v ? vd : 0u);
+        }
+    }
+
+    __device__ static __forceinline__ void imma(int (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                                uint32_t a3, uint32_t b0, uint32_t b1)
+    {
+        asm volatile(
+            "mma.sync.aligned.m16n8k32.row.col.s32.s8.s8.s32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+            "{%8,%9}, {%0,%1,%2,%3};"
+            : "+r"(c[0]), "+r"(c[1]), "+r"(c[2]), "+r"(c[3])
+            : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+    }
+
+    // One block: a0..a3 are the code words of tokens gid / gid+8 at dims
+    // 4tig.. (a0, a1) and 16+4tig.. (a2, a3).
+    __device__ static __forceinline__ void block(uint32_t qrec, uint32_t a0, uint32_t a1,
+                                                 uint32_t a2, uint32_t a3, float2 dk,
+                                                 float (&s)[4])
+    {
+        uint32_t b0, b1, q0, q1;
+        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(b0), "=r"(b1), "=r"(q0), "=r"(q1)
+                     : "r"(qrec));
+        int c[4] = {0, 0, 0, 0};
+        imma(c, a0, a1, a2, a3, b0, b1);
+        const float dq0 = __uint_as_float(q0), dq1 = __uint_as_float(q1);
+        s[0] = fmaf((float)c[0], dk.x * dq0, s[0]);
+        s[1] = fmaf((float)c[1], dk.x * dq1, s[1]);
+        s[2] = fmaf((float)c[2], dk.y * dq0, s[2]);
+        s[3] = fmaf((float)c[3], dk.y * dq1, s[3]);
+    }
+
+    __device__ static void scores(const Consts &, const Frag &f, uint32_t kh, uint32_t scr,
+                                  int gid, int tig, float (&s)[4])
+    {
+        // blocks 2pb (codes 2 bytes past a word boundary) and 2pb+1 (aligned)
+        uint32_t r0 = kh + gid * RB + 4 * tig, r1 = r0 + 8 * RB;
+        uint32_t dk = scr + DK + 8 * gid;
+        uint32_t qr = f.q;
+        s[0] = s[1] = s[2] = s[3] = 0.0f;
+#pragma unroll
+        for (int pb = 0; pb < NB / 2; ++pb) {
+            const uint32_t x0 = lds_u32(r0), x1 = lds_u32(r0 + 4), x2 = lds_u32(r0 + 16),
+                           x3 = lds_u32(r0 + 20);
+            const uint32_t y0 = lds_u32(r1), y1 = lds_u32(r1 + 4), y2 = lds_u32(r1 + 16),
+                           y3 = lds_u32(r1 + 20);
+            const uint32_t u0 = lds_u32(r0 + 36), u2 = lds_u32(r0 + 52);
+            const uint32_t v0 = lds_u32(r1 + 36), v2 = lds_u32(r1 + 52);
+            const float2 k0 = lds_f2(dk), k1 = lds_f2(dk + 4 * kTile);
+            block(qr, __funnelshift_r(x0, x1, 16), __funnelshift_r(y0, y1, 16),
+                  __funnelshift_r(x2, x3, 16), __funnelshift_r(y2, y3, 16), k0, s);
+            block(qr + 32 * QREC, u0, v0, u2, v2, k1, s);
+            r0 += 2 * BB;
+            r1 += 2 * BB;
+            dk += 2 * 4 * kTile;
+            qr += 2 * 32 * QREC;
+        }
+    }
+
+    // O += V^T P' over the tile, P' = P * d_v per block.  m-tile 2b holds dims
+    // 32b + 2gid (row gid) and 32b + 2gid + 1 (row gid + 8); m-tile 2b+1 the
+    // same 16 dims higher.  A register pairs one dim of tokens (2tig, 2tig+1)
+    // or (2tig+8, 2tig+9).
+    __device__ static void pv(const Consts &K, float (&o)[MT][4], uint32_t vh, uint32_t scr,
+                              uint32_t p0, uint32_t p1, int gid, int tig)
+    {
+        const uint32_t ra = vh + (2 * tig) * RB + 2 + 2 * gid;
+        const uint32_t rc = ra + 8 * RB;
+#pragma unroll
+        for (int b = 0; b < NB; ++b) {
+            const uint32_t b0 = hmul2_bits(p0, lds_u32(scr + DV + 2 * (b * kTile + 2 * tig)));
+            const uint32_t b1 =
+                hmul2_bits(p1, lds_u32(scr + DV + 2 * (b * kTile + 8 + 2 * tig)));
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                const uint32_t off = BB * b + 16 * hh;
+                const uint32_t ua = lds_u16(ra + off), ub = lds_u16(ra + RB + off);
+                const uint32_t uc = lds_u16(rc + off), ud = lds_u16(rc + RB + off);
+                // [a.dim0, a.dim1, b.dim0, b.dim1], each code flipped to c + 128
+                const uint32_t xab = __byte_perm(ua, ub, 0x5410) ^ K.flip;
+                const uint32_t xcd = __byte_perm(uc, ud, 0x5410) ^ K.flip;
+                float(&acc)[4] = o[2 * b + hh];
+                mma16816(acc, __byte_perm(xab, K.f16hi, 0x4240), __byte_perm(xab, K.f16hi, 0x4341),
+                         __byte_perm(xcd, K.f16hi, 0x4240), __byte_perm(xcd, K.f16hi, 0x4341),
+                         b0, b1);
+                mma16816(acc, K.nb[0], K.nb[1], K.nb[2], K.nb[3], b0, b1);
+            }
+        }
+    }
+
+    __device__ static __forceinline__ int dim_of(int mt, int gid, int upper)
+    {
+        return 16 * mt + 2 * gid + upper;
+    }
+};
+
+using Q80 = Q80T<8>;
+
 // --- F16, D = 128 or 256 ----------------------------------------------------
 // Slot layout per side: [64-dim chunk][16 tokens][128 B], written by TMA with
 // the 128-byte swizzle (16-byte chunk c of row t stored at c ^ (t & 7)), read
@@ -482,6 +713,9 @@ struct F16T {
     struct Frag {
         uint32_t qb[KS][2];  // B fragments (query column gid) of each k-step
     };
+    struct Consts {
+        __device__ void init() {}
+    };
 
     // This lane's query values (query head gid of the group), fetched before
     // the first K/V copies are issued so that the loads do not queue behind them.
@@ -489,7 +723,7 @@ struct F16T {
         float2 x[KS][2];
     };
     __device__ static void fetch_q(const DecodeParams &p, uint32_t s, uint32_t h0, uint32_t G,
-                                   int gid, int tig, QRaw &r)
+                                   int gid, int tig, uint32_t, uint32_t, QRaw &r)
     {
         const float *row = static_cast<const float *>(p.q) +
                            ((uint64_t)s * p.hq + h0 + ((uint32_t)gid < G ? gid : 0)) * D;
@@ -527,7 +761,7 @@ struct F16T {
         }
     }
 
-    __device__ static void scores(const NibbleConsts &, const Frag &f, uint32_t kh, uint32_t,
+    __device__ static void scores(const Consts &, const Frag &f, uint32_t kh, uint32_t,
                                   int gid, int tig, float (&s)[4])
     {
         const int lane = gid * 4 + tig;
@@ -546,7 +780,7 @@ struct F16T {
         s[3] = c[3];
     }
 
-    __device__ static void pv(const NibbleConsts &, float (&o)[MT][4], uint32_t vh, uint32_t,
+    __device__ static void pv(const Consts &, float (&o)[MT][4], uint32_t vh, uint32_t,
                               uint32_t p0, uint32_t p1, int gid, int tig)
     {
         const int lane = gid * 4 + tig;
@@ -677,9 +911,9 @@ __global__ void __launch_bounds__(T::kMaxWarps * 32, 1)
     };
 
     int32_t ids = fetch_ids(0), ids_next = fetch_ids(32);
+    // quantised K: the wph warps of a head split its query blocks
     typename T::QRaw qraw;
-    if (T::QBYTES == 0 || sub == 0)
-        T::fetch_q(p, seq, g * G, G, gid, tig, qraw);
+    T::fetch_q(p, seq, g * G, G, gid, tig, sub, wph, qraw);
     const uint32_t pro = n_my < NSW ? n_my : NSW;
     for (uint32_t k = 0; k < pro; ++k) {
         const int32_t b = __shfl_sync(0xffffffffu, ids, k);
@@ -688,13 +922,11 @@ __global__ void __launch_bounds__(T::kMaxWarps * 32, 1)
     }
     __syncwarp();
 
-    NibbleConsts K;
-    if constexpr (T::kZeroInvalidV == false)
-        K.init();
+    typename T::Consts K;
+    K.init();
     typename T::Frag f;
     if constexpr (T::QBYTES > 0) {
-        if (sub == 0)
-            T::store_q(p, qraw, G, gid, tig, qsm_base + g * T::QBYTES);
+        T::store_q(p, qraw, G, gid, tig, sub, wph, qsm_base + g * T::QBYTES);
         __syncthreads();
         T::load_q(qsm_base + g * T::QBYTES, lane, f);
     } else {
@@ -1089,6 +1321,8 @@ bool fast_decode_supported(pa_type kt, pa_type vt, uint32_t d, uint32_t hq, uint
         return false;
     if (kt == PA_Q4_0)
         return d == 256 && geometry<Q40>(hkv).warps > 0;
+    if (kt == PA_Q8_0)
+        return d == 256 && geometry<Q80>(hkv).warps > 0;
     if (kt == PA_F16)
         return d == 256 ? geometry<F16T<256>>(hkv).warps > 0
                         : d == 128 && geometry<F16T<128>>(hkv).warps > 0;
@@ -1100,6 +1334,8 @@ int fast_decode_occupancy(pa_type kt, pa_type, uint32_t d, uint32_t, uint32_t hk
 {
     if (kt == PA_Q4_0)
         return occupancy_t<Q40>(hkv, ctas_per_sm);
+    if (kt == PA_Q8_0)
+        return occupancy_t<Q80>(hkv, ctas_per_sm);
     return d == 256 ? occupancy_t<F16T<256>>(hkv, ctas_per_sm)
                     : occupancy_t<F16T<128>>(hkv, ctas_per_sm);
 }
@@ -1112,6 +1348,8 @@ int launch_fast_decode(const DecodeParams &p, pa_type kt, pa_type vt, cudaStream
         return launch_plain_decode(p, kt, vt, st, entry);
     if (kt == PA_Q4_0)
         return launch_t<Q40>(p, st, entry);
+    if (kt == PA_Q8_0)
+        return launch_t<Q80>(p, st, entry);
     if (p.d == 256)
         return launch_t<F16T<256>>(p, st, entry);
     return launch_t<F16T<128>>(p, st, entry);

@@ -137,9 +137,11 @@ __device__ __forceinline__ bool cta_work(const int32_t *seq_lens, uint32_t n_seq
 // skipped); partial p of row r is at po[r] + p * stride * D and pml[r] +
 // p * stride.  kPartial: the result is written in partial form (f16 o to
 // out_o[r], (M, or -inf when no weight, and sum w) to out_ml[r]); else as
-// float32 to out_f[r].  Lane i owns dims [VEC i, VEC (i + 1)).  The weight sum
-// is lane-partial (lane i adds the weights of partials i, i + 32, ... in
-// order) and then a butterfly; every dimension is summed in partial order.
+// float32 to out_f[r].  Lane i owns the VEC/4 dimension quads
+// [128 j + 4 i, 128 j + 4 i + 4), so that every load and store of the warp is
+// one contiguous run.  The weight sum is lane-partial (lane i adds the
+// weights of partials i, i + 32, ... in order) and then a butterfly; every
+// dimension is summed in partial order.
 // Loads go through L2 (.cg) so that partials written by other CTAs of the
 // same launch are seen.
 template <int VEC, int NR, bool kPartial>
@@ -157,13 +159,12 @@ __device__ __forceinline__ void merge_rows_warp_v(const __half *const *po, const
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
                 if (r < nr && (uint32_t)k < cnt) {
-                    const __half *src = po[r] + (uint64_t)(base + k) * stride * D + VEC * lane;
-                    if constexpr (VEC == 8) {
-                        raw[r][k] = __ldcg(reinterpret_cast<const uint4 *>(src));
-                    } else {
-                        const uint2 r2 = __ldcg(reinterpret_cast<const uint2 *>(src));
-                        raw[r][k] = make_uint4(r2.x, r2.y, 0u, 0u);
-                    }
+                    const __half *src = po[r] + (uint64_t)(base + k) * stride * D + 4 * lane;
+                    const uint2 q0 = __ldcg(reinterpret_cast<const uint2 *>(src));
+                    uint2 q1 = make_uint2(0u, 0u);
+                    if constexpr (VEC == 8)
+                        q1 = __ldcg(reinterpret_cast<const uint2 *>(src + 128));
+                    raw[r][k] = make_uint4(q0.x, q0.y, q1.x, q1.y);
                 }
             }
         }
@@ -247,17 +248,18 @@ __device__ __forceinline__ void merge_rows_warp_v(const __half *const *po, const
                 const __half2 v = __floats2half2_rn(acc[r][2 * j] * inv, acc[r][2 * j + 1] * inv);
                 h[j] = *reinterpret_cast<const uint32_t *>(&v);
             }
-            if constexpr (VEC == 8)
-                *reinterpret_cast<uint4 *>(out_o[r] + VEC * lane) = make_uint4(h[0], h[1], h[2], h[3]);
-            else
-                *reinterpret_cast<uint2 *>(out_o[r] + VEC * lane) = make_uint2(h[0], h[1]);
+#pragma unroll
+            for (int i = 0; i < VEC / 4; ++i)
+                *reinterpret_cast<uint2 *>(out_o[r] + 128 * i + 4 * lane) =
+                    make_uint2(h[2 * i], h[2 * i + 1]);
             if (lane == 0)
                 *out_ml[r] = make_float2(s > 0.0f ? M[r] : -INFINITY, s);
         } else {
-            float *o = out_f[r] + VEC * lane;
 #pragma unroll
-            for (int j = 0; j < VEC; ++j)
-                o[j] = acc[r][j] * inv;
+            for (int i = 0; i < VEC / 4; ++i)
+                *reinterpret_cast<float4 *>(out_f[r] + 128 * i + 4 * lane) =
+                    make_float4(acc[r][4 * i] * inv, acc[r][4 * i + 1] * inv,
+                                acc[r][4 * i + 2] * inv, acc[r][4 * i + 3] * inv);
         }
     }
 }
@@ -331,10 +333,11 @@ __device__ __forceinline__ void merge_row_two_pass_warp(const __half *po, const 
         if ((g & 31) == (uint32_t)lane)
             ws += w;
         if (w > 0.0f) {
-            const __half2 *h2 = reinterpret_cast<const __half2 *>(scr + VEC * lane);
 #pragma unroll
             for (int j = 0; j < VEC / 2; ++j) {
-                const float2 f = __half22float2(h2[j]);
+                const __half2 *h2 =
+                    reinterpret_cast<const __half2 *>(scr + 128 * (j / 2) + 4 * lane) + (j & 1);
+                const float2 f = __half22float2(*h2);
                 acc[2 * j] = fmaf(w, f.x, acc[2 * j]);
                 acc[2 * j + 1] = fmaf(w, f.y, acc[2 * j + 1]);
             }
@@ -343,10 +346,11 @@ __device__ __forceinline__ void merge_row_two_pass_warp(const __half *po, const 
     }
     ws = warp_sum(ws);
     const float inv = ws > 0.0f ? 1.0f / ws : 0.0f;
-    float *o = out + VEC * lane;
 #pragma unroll
-    for (int j = 0; j < VEC; ++j)
-        o[j] = acc[j] * inv;
+    for (int i = 0; i < VEC / 4; ++i)
+        *reinterpret_cast<float4 *>(out + 128 * i + 4 * lane) =
+            make_float4(acc[4 * i] * inv, acc[4 * i + 1] * inv, acc[4 * i + 2] * inv,
+                        acc[4 * i + 3] * inv);
 }
 
 // Arrival of a CTA at a completion counter of the in-launch merge ("HRX:
