@@ -218,7 +218,7 @@ const char *pa_decode_kernel_name(pa_type k_type, pa_type v_type, uint32_t d, ui
  * n_live = min(ceil(L_s / part_tokens), n_parts) live partitions: M = max
  * m_p over partitions with l_p > 0, w_p = l_p 2^(m_p - M), out = sum w_p o_p
  * / sum w_p; partitions with l_p == 0 are skipped and no live partition gives
- * 0.  More than 8 live partitions are merged in two passes ([P3] What:
+ * 0.  More than 32 live partitions are merged in two passes ([P3] What:
  * hierarchical reduction): groups of gs = ceil(sqrt(n_live)) consecutive
  * partitions are merged into f16 partials of the same form, then those; the
  * same as the flat merge up to rounding.  Reads the partials only.  Layouts

@@ -321,6 +321,7 @@ struct Q40T {
     static constexpr bool kZeroInvalidV = false;
     static constexpr uint32_t kTmaX = 1;    // TMA boxes per (side, head)
     static constexpr uint32_t kMaxWarps = KMAXW;
+    static constexpr int kMergeBatch = 8;
 
     static __host__ __device__ constexpr uint32_t side_bytes(uint32_t hkv)
     {
@@ -510,6 +511,7 @@ struct Q80T {
     static constexpr bool kZeroInvalidV = false;
     static constexpr uint32_t kTmaX = 1;
     static constexpr uint32_t kMaxWarps = KMAXW;
+    static constexpr int kMergeBatch = 12;
 
     static __host__ __device__ constexpr uint32_t side_bytes(uint32_t hkv)
     {
@@ -703,6 +705,7 @@ struct F16T {
     static constexpr bool kZeroInvalidV = true;
     static constexpr uint32_t kTmaX = NC;
     static constexpr uint32_t kMaxWarps = 8;
+    static constexpr int kMergeBatch = 12;
 
     static __host__ __device__ constexpr uint32_t side_bytes(uint32_t hkv)
     {
@@ -827,11 +830,13 @@ __device__ __forceinline__ void combine_and_write(const DecodeParams &p, const f
                                                   uint32_t seq, uint32_t part);
 
 // The in-launch merge, out of line so that its registers do not add to the
-// main loop's.
+// main loop's; each warp keeps BATCH partials of each of its two rows in
+// flight, as many as the kernel's register budget holds.
+template <int BATCH>
 __device__ __noinline__ void merge_tail(const DecodeParams &p, uint32_t seq, uint32_t part,
                                         uint32_t warp, uint32_t nwarps)
 {
-    fused_merge(p, seq, part, warp, nwarps);
+    fused_merge<BATCH>(p, seq, part, warp, nwarps);
 }
 
 template <class T>
@@ -1062,7 +1067,7 @@ __global__ void __launch_bounds__(T::kMaxWarps * 32, 1)
     __syncthreads();
     combine_and_write<T>(p, park, hkv, wph, G, seq, part);
     if (p.counters && !p.direct)
-        merge_tail(p, seq, part, warp, nwarps);
+        merge_tail<T::kMergeBatch>(p, seq, part, warp, nwarps);
 }
 
 // Combine of the parked (m, l, O) of the wph warps of every head group into

@@ -124,7 +124,7 @@ __device__ __forceinline__ bool cta_work(const int32_t *seq_lens, uint32_t n_seq
 // over partials with l_p > 0, w_p = l_p 2^(m_p - M), out = sum_p w_p o_p /
 // sum_p w_p; partials with l_p == 0 are skipped and none gives 0.
 //
-// A row with more than 8 live partials is merged in two passes ("HRX:
+// A row with more than 32 live partials is merged in two passes ("HRX:
 // multi-pass KV-block reduction for flash-attention decode-split", llama.cpp
 // fork pull 13, What: hierarchical KV-block reduction): the partials are cut
 // into groups of gs = merge_group_size(n) consecutive ones, each group is
@@ -144,20 +144,21 @@ __device__ __forceinline__ bool cta_work(const int32_t *seq_lens, uint32_t n_seq
 // dimension is summed in partial order.
 // Loads go through L2 (.cg) so that partials written by other CTAs of the
 // same launch are seen.
-template <int VEC, int NR, bool kPartial>
+template <int VEC, int NR, bool kPartial, int BATCH = 8>
 __device__ __forceinline__ void merge_rows_warp_v(const __half *const *po, const float2 *const *pml,
                                                   uint32_t n, uint32_t stride, uint32_t D,
                                                   int nr, float *const *out_f,
                                                   __half *const *out_o, float2 *const *out_ml)
 {
     const int lane = threadIdx.x & 31;
-    // eight partials of every row in flight at once
-    uint4 raw[NR][8];
+    // BATCH partials of every row in flight at once (the batch size changes
+    // only how many loads are in flight, not the order of the arithmetic)
+    uint4 raw[NR][BATCH];
     auto load_batch = [&](uint32_t base, uint32_t cnt) {
 #pragma unroll
         for (int r = 0; r < NR; ++r) {
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
+            for (int k = 0; k < BATCH; ++k) {
                 if (r < nr && (uint32_t)k < cnt) {
                     const __half *src = po[r] + (uint64_t)(base + k) * stride * D + 4 * lane;
                     const uint2 q0 = __ldcg(reinterpret_cast<const uint2 *>(src));
@@ -171,7 +172,7 @@ __device__ __forceinline__ void merge_rows_warp_v(const __half *const *po, const
     };
     // the first batch and the (m, l) of partial `lane` are loaded together:
     // neither depends on the reference maximum
-    load_batch(0, n < 8 ? n : 8);
+    load_batch(0, n < BATCH ? n : BATCH);
     float2 ml0[NR];
     float M[NR];
 #pragma unroll
@@ -214,13 +215,13 @@ __device__ __forceinline__ void merge_rows_warp_v(const __half *const *po, const
             ws[r] += w[r];
         }
         const uint32_t cnt = min(32u, n - c);
-        for (uint32_t q0 = 0; q0 < cnt; q0 += 8) {
+        for (uint32_t q0 = 0; q0 < cnt; q0 += BATCH) {
             if (c + q0 > 0)
-                load_batch(c + q0, cnt - q0 < 8 ? cnt - q0 : 8);
+                load_batch(c + q0, cnt - q0 < BATCH ? cnt - q0 : BATCH);
 #pragma unroll
             for (int r = 0; r < NR; ++r) {
 #pragma unroll
-                for (int k = 0; k < 8; ++k) {
+                for (int k = 0; k < BATCH; ++k) {
                     const float wk = __shfl_sync(0xffffffffu, w[r], (q0 + k) & 31);
                     if (r < nr && q0 + k < cnt && wk > 0.0f) {
                         const __half2 *h2 = reinterpret_cast<const __half2 *>(&raw[r][k]);
@@ -384,7 +385,7 @@ __device__ inline bool merge_arrive(int32_t *counter, uint32_t target)
 // that completes a group merges the group's partials of every row into the
 // group's first partial slot, and the CTA that completes the last group merges
 // the group results into out.  An empty sequence has one CTA and writes 0.
-template <class P>
+template <int BATCH = 8, class P>
 __device__ inline void fused_merge(const P &p, uint32_t seq, uint32_t part, uint32_t warp,
                                    uint32_t nwarps)
 {
@@ -410,12 +411,14 @@ __device__ inline void fused_merge(const P &p, uint32_t seq, uint32_t part, uint
             float2 *rm[2] = {const_cast<float2 *>(rml[0]), const_cast<float2 *>(rml[1])};
             const int nr = h + nwarps < p.hq ? 2 : 1;
             if (p.d == 256)
-                merge_rows_warp_v<8, 2, true>(rpo, rml, ng_g, 1, p.d, nr, nullptr, ro, rm);
+                merge_rows_warp_v<8, 2, true, BATCH>(rpo, rml, ng_g, 1, p.d, nr, nullptr, ro, rm);
             else
-                merge_rows_warp_v<4, 2, true>(rpo, rml, ng_g, 1, p.d, nr, nullptr, ro, rm);
+                merge_rows_warp_v<4, 2, true, BATCH>(rpo, rml, ng_g, 1, p.d, nr, nullptr, ro, rm);
         }
     }
-    if (!merge_arrive(cnt, ng > 1 ? ng : 1))
+    // the last pass counts the group mergers, or every partition of the
+    // sequence (an empty sequence has one CTA)
+    if (!merge_arrive(cnt, ng > 1 ? ng : (n > 0 ? n : 1u)))
         return;
     const uint32_t m = ng > 1 ? ng : n, stride = ng > 1 ? gs : 1;
     for (uint32_t h = warp; h < p.hq; h += 2 * nwarps) {
@@ -426,9 +429,9 @@ __device__ inline void fused_merge(const P &p, uint32_t seq, uint32_t part, uint
         float *rout[2] = {p.out + s0 * p.d, p.out + s1 * p.d};
         const int nr = h + nwarps < p.hq ? 2 : 1;
         if (p.d == 256)
-            merge_rows_warp_v<8, 2, false>(rpo, rml, m, stride, p.d, nr, rout, nullptr, nullptr);
+            merge_rows_warp_v<8, 2, false, BATCH>(rpo, rml, m, stride, p.d, nr, rout, nullptr, nullptr);
         else
-            merge_rows_warp_v<4, 2, false>(rpo, rml, m, stride, p.d, nr, rout, nullptr, nullptr);
+            merge_rows_warp_v<4, 2, false, BATCH>(rpo, rml, m, stride, p.d, nr, rout, nullptr, nullptr);
     }
 }
 

@@ -36,12 +36,12 @@ inline PA_HD uint32_t ceil_sqrt_u32(uint32_t n)
     return lo;
 }
 
-// Group size of the merge of n live partials: all of them (one pass) up to 8,
+// Group size of the merge of n live partials: all of them (one pass) up to 32,
 // else ceil(sqrt(n)), so that both passes of the two-pass merge take about
 // sqrt(n) partials.
 inline PA_HD uint32_t merge_group_size(uint32_t n)
 {
-    return n <= 8 ? (n > 0 ? n : 1u) : ceil_sqrt_u32(n);
+    return n <= 32 ? (n > 0 ? n : 1u) : ceil_sqrt_u32(n);
 }
 
 // Completion counters per sequence of the in-launch merge: one for the last

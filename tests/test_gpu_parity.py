@@ -341,3 +341,26 @@ def test_lengths_past_the_plan_are_flagged_and_stay_in_bounds(kernel, fused):
     # lengths inside the plan raise nothing
     out, ws, _, _ = H.run(case, force_parts=4, flags=KERNELS[kernel], fused=fused)
     assert pa.status_read(ws.status) == 0
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("force", [8, 24, 60])
+def test_fused_merge_waits_for_every_partition(kernel, force):
+    """The in-launch merge of a sequence must start only after its last
+    partition (one pass) or last group (two passes) is written.  Many
+    sequences with many partitions each, several launches in a row: any
+    early merge shows up as a difference from the separate merge."""
+    spec = synth.CaseSpec(seq_lens=[4000 - 37 * i for i in range(24)], k_type=synth.Q4_0,
+                          v_type=synth.Q4_0, junk=5)
+    case = synth.build_case(spec, seed=3200 + force, device=DEV)
+    ref, _, pl, _ = H.run(case, force_parts=force, flags=KERNELS[kernel])
+    ws = pa.workspace(pl, n_seqs=spec.n_seqs, hq=24, d=256, device=DEV)
+    args = pa.make_args(k_pool=case.k_pool, v_pool=case.v_pool, block_table=case.block_table,
+                        seq_lens=case.seq_lens, q=case.q, ws=ws, hkv=4, block_size=16,
+                        k_type=spec.k_type, v_type=spec.v_type, flags=KERNELS[kernel])
+    for _ in range(6):
+        ws.out.fill_(float("nan"))
+        pa.decode_step_fused(args, ws)
+        torch.cuda.synchronize()
+        assert torch.equal(ws.out.view(torch.int32), ref.view(torch.int32))
+        assert int(ws.counters.abs().sum()) == 0
