@@ -982,13 +982,16 @@ __global__ void __launch_bounds__(T::kMaxWarps * 32, 1)
             sc[0] = sc[1] = -INFINITY;
         if (gid + 8 >= nvalid)
             sc[2] = sc[3] = -INFINITY;
-        float t0m = fmaxf(sc[0], sc[2]), t1m = fmaxf(sc[1], sc[3]);
+        // a score above its reference is rare: each lane checks its own four,
+        // and only then does the warp form the tile maxima of its heads
+        const bool over = fmaxf(sc[0], sc[2]) > mref0 || fmaxf(sc[1], sc[3]) > mref1;
+        if (__builtin_expect(__any_sync(0xffffffffu, over), 0)) {
+            float t0m = fmaxf(sc[0], sc[2]), t1m = fmaxf(sc[1], sc[3]);
 #pragma unroll
-        for (int off = 4; off < 32; off <<= 1) {
-            t0m = fmaxf(t0m, __shfl_xor_sync(0xffffffffu, t0m, off));
-            t1m = fmaxf(t1m, __shfl_xor_sync(0xffffffffu, t1m, off));
-        }
-        if (__builtin_expect(__any_sync(0xffffffffu, t0m > mref0 || t1m > mref1), 0)) {
+            for (int off = 4; off < 32; off <<= 1) {
+                t0m = fmaxf(t0m, __shfl_xor_sync(0xffffffffu, t0m, off));
+                t1m = fmaxf(t1m, __shfl_xor_sync(0xffffffffu, t1m, off));
+            }
             const float n0 = t0m > mref0 ? t0m + kHeadroom : mref0;
             const float n1 = t1m > mref1 ? t1m + kHeadroom : mref1;
             const float a0 = mref0 == -INFINITY ? 0.0f : exp2f(mref0 - n0);
