@@ -81,6 +81,9 @@ def lib():
             L.or_quantize_q8_1.restype = ctypes.c_int
             L.or_dequant_q8_1_row.argtypes = [ctypes.c_void_p, ctypes.c_uint32, ctypes.c_void_p]
             L.or_dequant_q8_1_row.restype = None
+            L.or_quantize_row.argtypes = [ctypes.c_int, ctypes.c_void_p, ctypes.c_uint32,
+                                          ctypes.c_void_p]
+            L.or_quantize_row.restype = ctypes.c_int
             L.or_row_offset.argtypes = [ctypes.c_int64, ctypes.c_uint32, ctypes.c_uint32,
                                         ctypes.c_uint32, ctypes.c_uint32, ctypes.c_uint64]
             L.or_row_offset.restype = ctypes.c_uint64
@@ -134,6 +137,18 @@ def quantize_q8_1(x: np.ndarray) -> np.ndarray:
     rc = lib().or_quantize_q8_1(_ptr(x), _ptr(out), n_rows, d)
     if rc != OR_OK:
         raise ValueError(f"or_quantize_q8_1 rc={rc}")
+    return out
+
+
+def quantize_row(type_: int, x: np.ndarray) -> np.ndarray:
+    """One float32 row of D values -> its pool-row bytes (F16 / Q8_0 / Q4_0),
+    the append step's quantiser."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    d = x.shape[-1]
+    out = np.empty(row_bytes(type_, d), dtype=np.uint8)
+    rc = lib().or_quantize_row(int(type_), _ptr(x), int(d), _ptr(out))
+    if rc != OR_OK:
+        raise ValueError(f"or_quantize_row rc={rc}")
     return out
 
 

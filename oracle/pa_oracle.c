@@ -191,6 +191,87 @@ int or_quantize_q8_1(const float *x, uint8_t *out, int64_t n_rows, uint32_t D)
     return OR_OK;
 }
 
+/* Pool-row quantisers of the K/V append step ("feat: add paged-attention
+ * monolithic decode-only AR foundation" (lucebox pull 555), Summary: the new
+ * token's K/V rows are written into the pool next to which the paging
+ * metadata stays resident; the block formats are those above).  The pages
+ * give the formats, not the rounding, so this takes the ggml reference
+ * convention, every step in float32 in this order:
+ *  Q8_0: amax = max|x|; d = amax / 127; id = 1 / d (0 when d is 0);
+ *        q = clamp(roundf(x * id), -127, 127); stored f16_rn(d).
+ *  Q4_0: m = the first value of largest magnitude, with its sign; d = m / -8;
+ *        id = 1 / d (0 when d is 0); nib = min(15, floor(x * id + 8.5));
+ *        stored f16_rn(d), value j < 16 in the low half of byte j, value
+ *        j + 16 in its high half.
+ *  F16:  f16_rn(x).
+ * out receives or_row_bytes(type, D) bytes. */
+int or_quantize_row(int type, const float *x, uint32_t D, uint8_t *out)
+{
+    if (D == 0 || D % 32 != 0)
+        return OR_ERR_INVALID;
+    if (type == OR_F16) {
+        for (uint32_t i = 0; i < D; ++i) {
+            uint16_t h = or_float_to_half_rn(x[i]);
+            out[2 * i] = (uint8_t)(h & 0xff);
+            out[2 * i + 1] = (uint8_t)(h >> 8);
+        }
+        return OR_OK;
+    }
+    for (uint32_t b = 0; b < D / 32; ++b) {
+        const float *xb = x + 32 * b;
+        if (type == OR_Q8_0) {
+            uint8_t *ob = out + 34 * b;
+            float amax = 0.0f;
+            for (int j = 0; j < 32; ++j) {
+                float a = fabsf(xb[j]);
+                if (a > amax)
+                    amax = a;
+            }
+            float d = amax / 127.0f;
+            float id = d > 0.0f ? 1.0f / d : 0.0f;
+            for (int j = 0; j < 32; ++j) {
+                float t = xb[j] * id;
+                float r = roundf(t);
+                if (r > 127.0f) r = 127.0f;
+                if (r < -127.0f) r = -127.0f;
+                ob[2 + j] = (uint8_t)(int8_t)(int)r;
+            }
+            uint16_t d16 = or_float_to_half_rn(d);
+            ob[0] = (uint8_t)(d16 & 0xff);
+            ob[1] = (uint8_t)(d16 >> 8);
+        } else if (type == OR_Q4_0) {
+            uint8_t *ob = out + 18 * b;
+            float m = 0.0f, amax = 0.0f;
+            for (int j = 0; j < 32; ++j) {
+                float a = fabsf(xb[j]);
+                if (a > amax) {  /* strictly greater: the first of equal magnitudes wins */
+                    amax = a;
+                    m = xb[j];
+                }
+            }
+            float d = m / -8.0f;
+            float id = d != 0.0f ? 1.0f / d : 0.0f;
+            uint8_t nib[32];
+            for (int j = 0; j < 32; ++j) {
+                float t = xb[j] * id;
+                t = t + 8.5f;
+                float f = floorf(t);
+                if (f > 15.0f) f = 15.0f;
+                if (f < 0.0f) f = 0.0f;
+                nib[j] = (uint8_t)(int)f;
+            }
+            uint16_t d16 = or_float_to_half_rn(d);
+            ob[0] = (uint8_t)(d16 & 0xff);
+            ob[1] = (uint8_t)(d16 >> 8);
+            for (int j = 0; j < 16; ++j)
+                ob[2 + j] = (uint8_t)(nib[j] | (nib[j + 16] << 4));
+        } else {
+            return OR_ERR_INVALID;
+        }
+    }
+    return OR_OK;
+}
+
 /* Dequantise one q8_1 row (D/32 blocks) into out[D]: q * d. */
 void or_dequant_q8_1_row(const uint8_t *blocks, uint32_t D, double *out)
 {
