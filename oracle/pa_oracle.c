@@ -241,10 +241,12 @@ int or_quantize_row(int type, const float *x, uint32_t D, uint8_t *out)
             ob[1] = (uint8_t)(d16 >> 8);
         } else if (type == OR_Q4_0) {
             uint8_t *ob = out + 18 * b;
-            float m = 0.0f, amax = 0.0f;
-            for (int j = 0; j < 32; ++j) {
+            /* the first of equal magnitudes wins, so an all-zero block takes
+               x[0] itself (its sign included) */
+            float m = xb[0], amax = fabsf(xb[0]);
+            for (int j = 1; j < 32; ++j) {
                 float a = fabsf(xb[j]);
-                if (a > amax) {  /* strictly greater: the first of equal magnitudes wins */
+                if (a > amax) {
                     amax = a;
                     m = xb[j];
                 }

@@ -20,6 +20,8 @@ def test_quantize_row_equals_the_independent_encoder(type_):
     g = torch.Generator().manual_seed(11)
     x = synth.source_values(g, (400, 256), "cpu", outliers=True).numpy() * 3
     x[0, :32] = 0.0                                   # zero block
+    x[0, 32:64] = 0.0
+    x[0, 32] = -0.0                                   # zero block led by -0
     x[1, :32] = np.round(x[1, :32])                   # integer values: exact ties
     x[2, 5], x[2, 9] = 4.0, -4.0                      # equal magnitudes
     x[3, :] *= 1e-3
