@@ -75,6 +75,8 @@ typedef struct CUstream_st *pa_stream_t;
                                      n_parts * part_tokens, or more (sequence, partition) pairs
                                      than n_ctas; the work past the plan was left out and the
                                      output is invalid */
+#define PA_STATUS_APPEND_RANGE 8  /* pa_append_kv: a sequence whose table has no entry left for
+                                     its new token (or a negative length); it was left untouched */
 
 typedef enum { PA_F16 = 0, PA_Q8_0 = 1, PA_Q4_0 = 2 } pa_type;
 
@@ -307,11 +309,46 @@ int pa_decode_step_fused_host(const float *q_host, float *out_host, const pa_dec
                               const pa_plan_t *plan, void *q8_1_scratch, int32_t *counters,
                               pa_stream_t stream);
 
+/* ------------------------------------------------------- K/V append
+ * The step before the decode ([P1] Summary: the paging metadata -- block
+ * table and sequence lengths -- stays resident on the device next to the
+ * pool, and a decode step uploads only the 4-byte id of each fresh 16-token
+ * block; [P1] Validation: prefill through many block boundaries).  For each
+ * sequence s, with L = seq_lens[s] read on the device: the new token's K and
+ * V rows of every K/V head are quantised to the pool's row format and
+ * written at slot L % B of block table[s][L / B], and seq_lens[s] becomes
+ * L + 1.  When L % B == 0 the token starts a block: the call takes
+ * fresh_blocks[s] (allocated by the caller, e.g. pa_pool_alloc) and writes it
+ * into table[s][L / B]; fresh_blocks is read for no other sequence.
+ * Quantisers (float32, no contracted multiply-add; the ggml convention):
+ * Q8_0 d = amax/127, q = clamp(roundf(x * (1/d)), +-127); Q4_0 m = the first
+ * value of largest magnitude, d = m / -8, nib = min(15, floor(x * (1/d) +
+ * 8.5)); F16 round to nearest even; scales stored as f16 (nearest even).
+ * A sequence whose table has no entry L / B (L / B >= table_stride) sets
+ * PA_STATUS_APPEND_RANGE, one whose block id is outside [0, n_pool_blocks)
+ * sets PA_STATUS_CORRUPT_TABLE; either is left untouched (rows, table,
+ * length).  One launch; everything device memory on `stream`.
+ * PA_ERR_INVALID for bad arguments (checked before any launch). */
+typedef struct {
+    void *k_pool, *v_pool;           /* device pools, as in pa_decode_args, 16-byte aligned */
+    uint64_t n_pool_blocks;          /* 1 .. 2^31 */
+    int32_t *block_table;            /* device int32 [n_seqs][table_stride], updated in place */
+    uint32_t table_stride;
+    int32_t *seq_lens;               /* device int32 [n_seqs], incremented in place */
+    const float *k_new, *v_new;      /* device float32 [n_seqs][hkv][d], 16-byte aligned */
+    const int32_t *fresh_blocks;     /* device int32 [n_seqs] (see above) */
+    int32_t *status;                 /* device int32 status word (required) */
+    uint32_t n_seqs, hkv, d, block_size;
+    pa_type k_type, v_type;
+} pa_append_args;
+
+int pa_append_kv(const pa_append_args *args, pa_stream_t stream);
+
 /* Reads the status word into *host_out (synchronising `stream`); reset != 0
  * clears it afterwards.  Returns PA_ERR_TIMEOUT if the timeout bit is set,
- * else PA_ERR_RANGE if the lengths-over-plan bit is set, else
- * PA_ERR_CORRUPT_TABLE if the corrupt-table bit is set, PA_OK otherwise,
- * PA_ERR_CUDA on a runtime failure. */
+ * else PA_ERR_RANGE if the lengths-over-plan or the append-range bit is set,
+ * else PA_ERR_CORRUPT_TABLE if the corrupt-table bit is set, PA_OK
+ * otherwise, PA_ERR_CUDA on a runtime failure. */
 int pa_status_read(int32_t *dev_status, pa_stream_t stream, int32_t *host_out, int reset);
 
 /* Debug ([P4] Acceptance Criteria: the offsets must be 64-bit).  Writes the

@@ -21,6 +21,7 @@ TYPES = {"f16": F16, "q8_0": Q8_0, "q4_0": Q4_0}
 PA_OK, PA_ERR_INVALID, PA_ERR_NOMEM, PA_ERR_STALE = 0, -1, -2, -3
 PA_ERR_CUDA, PA_ERR_CORRUPT_TABLE, PA_ERR_RANGE, PA_ERR_TIMEOUT = -4, -5, -6, -7
 PA_STATUS_CORRUPT_TABLE, PA_STATUS_TIMEOUT, PA_STATUS_LEN_OVER_PLAN = 1, 2, 4
+PA_STATUS_APPEND_RANGE = 8
 PA_FLAG_PLAIN = 1
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_build", "libpa.so")
@@ -69,6 +70,18 @@ _lib = None
 _lock = threading.Lock()
 _vp, _u32, _u64, _i32 = ctypes.c_void_p, ctypes.c_uint32, ctypes.c_uint64, ctypes.c_int32
 
+class AppendArgs(ctypes.Structure):
+    _fields_ = [("k_pool", ctypes.c_void_p), ("v_pool", ctypes.c_void_p),
+                ("n_pool_blocks", ctypes.c_uint64),
+                ("block_table", ctypes.c_void_p), ("table_stride", ctypes.c_uint32),
+                ("seq_lens", ctypes.c_void_p), ("k_new", ctypes.c_void_p),
+                ("v_new", ctypes.c_void_p), ("fresh_blocks", ctypes.c_void_p),
+                ("status", ctypes.c_void_p),
+                ("n_seqs", ctypes.c_uint32), ("hkv", ctypes.c_uint32), ("d", ctypes.c_uint32),
+                ("block_size", ctypes.c_uint32), ("k_type", ctypes.c_int),
+                ("v_type", ctypes.c_int)]
+
+
 _SIGNATURES = {
     "pa_strerror": ([ctypes.c_int], ctypes.c_char_p),
     "pa_last_error": ([], ctypes.c_char_p),
@@ -102,6 +115,7 @@ _SIGNATURES = {
                                ctypes.c_int),
     "pa_decode_step_fused_host": ([_vp, _vp, ctypes.POINTER(DecodeArgs), ctypes.POINTER(Plan),
                                    _vp, _vp, _vp], ctypes.c_int),
+    "pa_append_kv": ([ctypes.POINTER(AppendArgs), _vp], ctypes.c_int),
     "pa_status_read": ([_vp, _vp, ctypes.POINTER(_i32), ctypes.c_int], ctypes.c_int),
     "pa_debug_row_offsets": ([_vp, _u32, _vp, _u32, _u32, _u32, _u32, _u64, _u64, _vp,
                               _vp, _vp], ctypes.c_int),
@@ -295,6 +309,20 @@ def decode_step_fused(args: DecodeArgs, ws: Workspace, stream=None) -> None:
     the float32 query)."""
     _check(lib().pa_decode_step_fused(ctypes.byref(args), ctypes.byref(ws.plan), _ptr(ws.q8_1),
                                       _ptr(ws.counters), _stream(stream)))
+
+
+def append_kv(*, k_pool, v_pool, block_table, seq_lens, k_new, v_new, fresh_blocks, status,
+              hkv, block_size, k_type, v_type, stream=None) -> None:
+    """pa_append_kv: quantise each sequence's new K/V rows (float32
+    [S, hkv, d]) into the pool at its resident length; fresh_blocks[s] is
+    taken when the token starts a block."""
+    S, _, d = k_new.shape
+    a = AppendArgs(k_pool=_ptr(k_pool), v_pool=_ptr(v_pool), n_pool_blocks=k_pool.shape[0],
+                   block_table=_ptr(block_table), table_stride=block_table.shape[1],
+                   seq_lens=_ptr(seq_lens), k_new=_ptr(k_new), v_new=_ptr(v_new),
+                   fresh_blocks=_ptr(fresh_blocks), status=_ptr(status), n_seqs=S, hkv=hkv,
+                   d=d, block_size=block_size, k_type=k_type, v_type=v_type)
+    _check(lib().pa_append_kv(ctypes.byref(a), _stream(stream)))
 
 
 def merge(ws: Workspace, seq_lens: torch.Tensor, stream=None) -> None:

@@ -335,6 +335,36 @@ extern "C" int pa_decode_step_fused_host(const float *q_host, float *out_host,
                       "copy of out to the host");
 }
 
+extern "C" int pa_append_kv(const pa_append_args *a, pa_stream_t stream)
+{
+    static const char *E = "pa_append_kv";
+    if (!a)
+        return fail(PA_ERR_INVALID, E, "NULL args");
+    if (a->n_seqs == 0)
+        return PA_OK;
+    if (!a->k_pool || !a->v_pool || !a->block_table || !a->seq_lens || !a->k_new ||
+        !a->v_new || !a->fresh_blocks || !a->status)
+        return fail(PA_ERR_INVALID, E, "NULL device pointer");
+    if (a->k_type < PA_F16 || a->k_type > PA_Q4_0 || a->v_type < PA_F16 || a->v_type > PA_Q4_0)
+        return fail(PA_ERR_INVALID, E, "unknown K/V type");
+    if (a->d != 128 && a->d != 256)
+        return fail(PA_ERR_INVALID, E, "d %u unsupported (128 or 256)", a->d);
+    if (a->block_size != 16 && a->block_size != 32)
+        return fail(PA_ERR_INVALID, E, "block_size %u unsupported (16 or 32)", a->block_size);
+    if (a->hkv == 0 || a->hkv > 8)
+        return fail(PA_ERR_INVALID, E, "hkv %u unsupported (1..8)", a->hkv);
+    if (a->table_stride == 0)
+        return fail(PA_ERR_INVALID, E, "table_stride is 0");
+    if (a->n_pool_blocks == 0 || a->n_pool_blocks > 0x80000000ull)
+        return fail(PA_ERR_RANGE, E, "n_pool_blocks must be in [1, 2^31] (int32 table ids)");
+    if (a->n_seqs > 0x7fffffffu)
+        return fail(PA_ERR_RANGE, E, "n_seqs exceeds the grid");
+    if (!aligned16(a->k_pool) || !aligned16(a->v_pool) || !aligned16(a->k_new) ||
+        !aligned16(a->v_new))
+        return fail(PA_ERR_INVALID, E, "pools and new rows must be 16-byte aligned");
+    return pa::launch_append(a, pa::stream_of(stream), E);
+}
+
 extern "C" int pa_status_read(int32_t *dev_status, pa_stream_t stream, int32_t *host_out,
                               int reset)
 {
@@ -359,6 +389,8 @@ extern "C" int pa_status_read(int32_t *dev_status, pa_stream_t stream, int32_t *
         return fail(PA_ERR_TIMEOUT, E, "a kernel abandoned a bounded pipeline wait");
     if (v & PA_STATUS_LEN_OVER_PLAN)
         return fail(PA_ERR_RANGE, E, "sequence lengths past what the plan covers were left out");
+    if (v & PA_STATUS_APPEND_RANGE)
+        return fail(PA_ERR_RANGE, E, "an append found no table entry left for a sequence");
     if (v & PA_STATUS_CORRUPT_TABLE)
         return fail(PA_ERR_CORRUPT_TABLE, E, "a block id outside the pool was skipped");
     return PA_OK;

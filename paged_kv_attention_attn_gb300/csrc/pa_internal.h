@@ -80,6 +80,7 @@ int plain_decode_occupancy(pa_type kt, pa_type vt, uint32_t d, uint32_t hq, int 
 int launch_merge(const void *part_o, const float *part_ml, const int32_t *seq_lens, float *out,
                  uint32_t n_seqs, uint32_t hq, uint32_t d, uint32_t n_parts,
                  uint32_t part_tokens, cudaStream_t st, const char *entry);
+int launch_append(const pa_append_args *a, cudaStream_t st, const char *entry);
 int launch_debug_offsets(const int32_t *block_table, uint32_t table_stride,
                          const int32_t *seq_lens, uint32_t n_seqs, uint32_t max_tokens,
                          uint32_t block_size, uint32_t hkv, uint64_t row_bytes,

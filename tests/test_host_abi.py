@@ -166,3 +166,22 @@ def test_fused_refuses_missing_counters():
     assert pa.lib().pa_last_error().startswith(b"pa_decode_fused: ")
     assert pa.lib().pa_decode_step_fused(ctypes.byref(a), ctypes.byref(pl), 16, 2, None) == \
         pa.PA_ERR_INVALID
+
+
+def test_append_refuses_bad_arguments_before_any_launch():
+    L = pa.lib()
+    good = dict(k_pool=16, v_pool=16, n_pool_blocks=4, block_table=16, table_stride=2,
+                seq_lens=16, k_new=16, v_new=16, fresh_blocks=16, status=16, n_seqs=2, hkv=4,
+                d=256, block_size=16, k_type=pa.Q4_0, v_type=pa.Q4_0)
+    assert L.pa_append_kv(None, None) == pa.PA_ERR_INVALID
+    for key, bad, rc in [("d", 96, pa.PA_ERR_INVALID), ("block_size", 8, pa.PA_ERR_INVALID),
+                         ("hkv", 0, pa.PA_ERR_INVALID), ("k_type", 7, pa.PA_ERR_INVALID),
+                         ("status", None, pa.PA_ERR_INVALID), ("k_new", 20, pa.PA_ERR_INVALID),
+                         ("table_stride", 0, pa.PA_ERR_INVALID),
+                         ("n_pool_blocks", 2 ** 31 + 1, pa.PA_ERR_RANGE)]:
+        a = pa.AppendArgs(**dict(good, **{key: bad}))
+        assert L.pa_append_kv(ctypes.byref(a), None) == rc, key
+        assert L.pa_last_error().startswith(b"pa_append_kv: ")
+    # an empty batch is a no-op that touches nothing
+    a = pa.AppendArgs(**dict(good, n_seqs=0))
+    assert L.pa_append_kv(ctypes.byref(a), None) == pa.PA_OK
