@@ -50,6 +50,11 @@ WORKLOADS = {
     **{f"sweep-{n}-{tag}": (lambda t=t, sh=sh: synth.dtype_sweep_spec(t, short=sh))
        for n, t in (("f16", synth.F16), ("q8_0", synth.Q8_0), ("q4_0", synth.Q4_0))
        for tag, sh in (("b4x32768", False), ("short", True))},
+    # the six mixed K x V pairs of the dtype sweep (4 x 32768)
+    **{f"sweep-{kn}-{vn}-b4x32768": (lambda kt=kt, vt=vt: synth.dtype_sweep_spec(kt, v_type=vt))
+       for kn, kt in (("f16", synth.F16), ("q8_0", synth.Q8_0), ("q4_0", synth.Q4_0))
+       for vn, vt in (("f16", synth.F16), ("q8_0", synth.Q8_0), ("q4_0", synth.Q4_0))
+       if kt != vt},
     "tiny-f16-L200": synth.tiny_spec,
     "largepool-f16-b16x300000": synth.large_pool_spec,
 }

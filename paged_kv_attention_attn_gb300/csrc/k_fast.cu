@@ -1,1332 +1,17 @@
-// k_fast.cu -- the fast sm_103a paged decode kernel.
-//
-// One CTA per live (sequence, partition) covers every K/V head.  A producer
-// warp walks the partition's block-table entries and stages each 16-token
-// tile of K and V into a ring of shared-memory stages with TMA tensor copies
-// (cp.async.bulk.tensor, one tensor map per side and K/V head, so that the
-// rows of one head land contiguously in shared memory), completing on
-// mbarriers.  Eight consumer warps share the K/V heads (8 / Hkv warps per
-// head, taking alternate tiles): each computes the scores of all query heads
-// of its group with tensor-core MMAs (m16n8k16, f16 operands, f32
-// accumulators; query heads on M, padded to 16), an online softmax in the
-// log2 domain that rescales only when a running maximum changes, and PV with
-// the head dimension on M.  At the end the warps of one head combine their
-// (m, l, O) and write the normalised f16 partial with (m, l), or the output
-// itself for a direct plan.
-//
-// Q4_0 K/V stay 4-bit in HBM and in shared memory; nibbles become f16 in
-// registers with one LOP3 per two values (the nibble is OR-ed into the
-// mantissa of 1024 or 64, so the f16 value is bias + nibble exactly).  The
-// QK dot of each 32-value block is an exact integer: the q8_1 query is the A
-// operand as exact f16 integers, the biases are removed by starting the
-// accumulator at minus their (exact) contribution, and the block's scales
-// d_k * d_q multiply the result.  For PV the V nibble minus 8 is an exact f16
-// operand and the block scale d_v is folded into the probabilities.
-//
-// Sources: "feat: add paged-attention monolithic decode-only AR foundation"
-// (lucebox pull 555), Summary -- one pass over each K/V row serves all query
-// heads of its group, 32-token-class tiles, skip-if-unchanged rescale,
-// exp2 softmax, f16 normalised partials, occupancy-aware partitions;
-// "fix(paged-attention): use 64-bit pool offsets in the fused decode
-// kernels" (mlxcel issue 2153) -- pool rows are addressed by TMA from 32-bit
-// slot coordinates and 64-bit strides, never by a 32-bit product.
-#include <cuda.h>
-#include <cuda_fp16.h>
-#include <cudaTypedefs.h>
-#include <math.h>
-
-#include <cstring>
-#include <mutex>
-
-#include "pa_device.cuh"
-#include "pa_internal.h"
+// k_fast.cu -- the fast sm_103a decode kernel for K and V of one type (F16
+// with D = 128 or 256, Q8_0 and Q4_0 with D = 256), and the dispatch between
+// these, the mixed-type instances (k_fast_mix.cu) and the plain kernel.
+#include "fast_kernel.cuh"
 
 namespace pa {
-namespace {
-
-constexpr int kTile = 16;  // tokens per stage
-constexpr int kMaxHkv = 8;
-constexpr size_t kSmemBudget = 220 * 1024;
-constexpr uint64_t kWaitNs = 2000000000ull;  // bound of every mbarrier wait (2 s)
-
-struct FastArgs {
-    CUtensorMap tm[2][kMaxHkv];  // [K, V][head]
-    DecodeParams p;
-    uint32_t n_slots;            // ring slots per warp
-    uint32_t slot_bytes;         // K then V rows of one head for one tile
-    uint32_t region_bytes;       // all rings; reused at the end to park (m, l, O)
-};
-
-// ------------------------------------------------------------------- PTX
-
-__device__ __forceinline__ uint32_t smem_u32(const void *p)
-{
-    return (uint32_t)__cvta_generic_to_shared(p);
-}
-
-__device__ __forceinline__ uint64_t global_ns()
-{
-    uint64_t t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-
-__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count)
-{
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
-}
-
-__device__ __forceinline__ void mbar_arrive(uint64_t *bar)
-{
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes)
-{
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
-                 "r"(bytes)
-                 : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
-{
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred P;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 P, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, P;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int x, int y,
-                                            uint64_t *bar)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
-        : "memory");
-}
-
-__device__ __forceinline__ void fence_proxy_async()
-{
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
-__device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
-                                         uint32_t a3, uint32_t b0, uint32_t b1)
-{
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-        "{%8,%9}, {%0,%1,%2,%3};"
-        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
-__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], uint32_t addr)
-{
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-                 : "r"(addr));
-}
-
-__device__ __forceinline__ void ldsm_x4_trans(uint32_t (&r)[4], uint32_t addr)
-{
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-                 : "r"(addr));
-}
-
-__device__ __forceinline__ uint32_t h2_bits(__half2 h) { return *reinterpret_cast<uint32_t *>(&h); }
-__device__ __forceinline__ __half2 bits_h2(uint32_t u) { return *reinterpret_cast<__half2 *>(&u); }
-
-__device__ __forceinline__ uint32_t hmul2_bits(uint32_t x, uint32_t y)
-{
-    return h2_bits(__hmul2(bits_h2(x), bits_h2(y)));
-}
-
-// Shared-memory accesses by 32-bit shared-window address.
-__device__ __forceinline__ uint32_t lds_u32(uint32_t a)
-{
-    uint32_t v;
-    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(a));
-    return v;
-}
-
-__device__ __forceinline__ uint32_t lds_u16(uint32_t a)
-{
-    uint32_t v;  // zero-extended into a 32-bit register
-    asm volatile("ld.shared.u16 %0, [%1];" : "=r"(v) : "r"(a));
-    return v;
-}
-
-__device__ __forceinline__ float2 lds_f2(uint32_t a)
-{
-    float2 v;
-    asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(a));
-    return v;
-}
-
-__device__ __forceinline__ void sts_f32(uint32_t a, float v)
-{
-    asm volatile("st.shared.f32 [%0], %1;" ::"r"(a), "f"(v));
-}
-
-__device__ __forceinline__ void sts_u16(uint32_t a, uint32_t v)
-{
-    asm volatile("st.shared.u16 [%0], %1;" ::"r"(a), "r"(v));  // low 16 bits stored
-}
-
-// A 32-bit constant the compiler cannot fold back into immediates, so it is
-// materialised once and kept in a register.
-__device__ __forceinline__ uint32_t opaque(uint32_t v)
-{
-    uint32_t r;
-    asm volatile("mov.b32 %0, %1;" : "=r"(r) : "r"(v));
-    return r;
-}
-
-// (x & m) | c in one LOP3.
-__device__ __forceinline__ uint32_t and_or(uint32_t x, uint32_t m, uint32_t c)
-{
-    uint32_t r;
-    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(r) : "r"(x), "r"(m), "r"(c));
-    return r;
-}
-
-// Register constants of the Q4_0 nibble expansion: masks and f16 biases.
-struct NibbleConsts {
-    uint32_t mlo, mhi, blo, bhi;  // 0x000F000F, 0x00F000F0, f16 1024 | 1024, f16 64 | 64
-    uint32_t nlo[4], nhi[4];      // A quads of -1032 and -72 (f16 pairs)
-    __device__ __forceinline__ void init()
-    {
-        mlo = opaque(0x000F000Fu);
-        mhi = opaque(0x00F000F0u);
-        blo = opaque(0x64006400u);
-        bhi = opaque(0x54005400u);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            nlo[i] = opaque(0xE408E408u);
-            nhi[i] = opaque(0xD480D480u);
-        }
-    }
-};
-
-// Transposes an 8x8 matrix of 16-bit values held in mma fragment layout.
-__device__ __forceinline__ uint32_t movmatrix_t(uint32_t x)
-{
-    uint32_t y;
-    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
-    return y;
-}
-
-// ------------------------------------------------------------ per-type code
-//
-// Each type provides the layout of one ring slot and, for one warp, the
-// query fragments, the scores of one 16-token tile and the PV update of one
-// tile.  Thread roles follow the m16n8k16 fragment layout: gid = lane/4,
-// tig = lane%4.
-//  QK: A = keys (row = token of the tile), B = queries (column gid = query
-//      head of the group; columns >= G are zero), C = S[token][head].  Each
-//      thread ends with the scores of tokens gid, gid+8 for heads 2tig, 2tig+1
-//      in log2 units.
-//  PV: A = values (row = head dimension), B = probabilities (column gid =
-//      query head), C = O[dimension][head]: columns 2tig, 2tig+1 are again this
-//      thread's heads.
-
-// --- the q8_1 query, shared by the quantised-K types ------------------------
-//
-// Lane (gid, tig) holds, for query head gid of its group, the eight values of
-// each 32-value block at dims 4tig..4tig+3 and 16+4tig..19+4tig: float32 when
-// the kernel quantises the query itself, else the q8_1 codes and scale.  They
-// are fetched before the first K/V copies are issued, so that these loads do
-// not queue behind them.
-template <int NB>
-struct Q81Query {
-    struct Raw {
-        float4 x[NB][2];
-        uint32_t w[NB][2];
-        uint32_t d[NB];
-    };
-
-    // Blocks b with b % nw == w only: the nw warps of a K/V head share the work.
-    __device__ static void fetch(const DecodeParams &p, uint32_t s, uint32_t h0, uint32_t G,
-                                 int gid, int tig, uint32_t w, uint32_t nw, Raw &r)
-    {
-        const uint64_t row = (uint64_t)s * p.hq + h0 + ((uint32_t)gid < G ? gid : 0);
-        if (p.q_f32) {
-            const float *x = static_cast<const float *>(p.q) + row * NB * 32;
-#pragma unroll
-            for (int b = 0; b < NB; ++b) {
-                if ((uint32_t)b % nw != w)
-                    continue;
-                r.x[b][0] = *reinterpret_cast<const float4 *>(x + 32 * b + 4 * tig);
-                r.x[b][1] = *reinterpret_cast<const float4 *>(x + 32 * b + 16 + 4 * tig);
-            }
-        } else {
-            const uint8_t *blk = static_cast<const uint8_t *>(p.q) + row * NB * 36;
-#pragma unroll
-            for (int b = 0; b < NB; ++b) {
-                if ((uint32_t)b % nw != w)
-                    continue;
-                r.d[b] = load_u16(blk + 36 * b);
-                r.w[b][0] = *reinterpret_cast<const uint32_t *>(blk + 36 * b + 4 + 4 * tig);
-                r.w[b][1] = *reinterpret_cast<const uint32_t *>(blk + 36 * b + 20 + 4 * tig);
-            }
-        }
-    }
-
-    // The q8_1 codes of this lane's eight values of block b and the block's
-    // f16-rounded scale.  A float32 query is quantised with the pre-pass's
-    // arithmetic (q8_1_code); the four lanes of a quad hold one block, so its
-    // maximum magnitude is two shuffles away.
-    __device__ static __forceinline__ void codes(const DecodeParams &p, const Raw &r, int b,
-                                                 int (&code)[8], float &d16)
-    {
-        if (p.q_f32) {
-            const float v[8] = {r.x[b][0].x, r.x[b][0].y, r.x[b][0].z, r.x[b][0].w,
-                                r.x[b][1].x, r.x[b][1].y, r.x[b][1].z, r.x[b][1].w};
-            float amax = 0.0f;
-#pragma unroll
-            for (int j = 0; j < 8; ++j)
-                amax = fmaxf(amax, fabsf(v[j]));
-            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-            const float d = amax / 127.0f;
-#pragma unroll
-            for (int j = 0; j < 8; ++j)
-                code[j] = q8_1_code(v[j], amax, d);
-            d16 = __half2float(__float2half_rn(amax == 0.0f ? 0.0f : d));
-        } else {
-#pragma unroll
-            for (int j = 0; j < 8; ++j)
-                code[j] = (int)(int8_t)(uint8_t)(r.w[b][j >> 2] >> (8 * (j & 3)));
-            d16 = half_bits_to_float((uint16_t)r.d[b]);
-        }
-    }
-};
-
-// --- Q4_0, D = 256 --------------------------------------------------------
-template <uint32_t KMAXW>
-struct Q40T {
-    static constexpr int D = 256;
-    static constexpr int NB = D / 32;       // 32-value blocks per row
-    static constexpr int RB = NB * 18;      // row bytes
-    static constexpr int MT = D / 16;       // PV m-tiles
-    static constexpr int DK = 0, DV = NB * kTile * 4;  // scratch: dk f32, dv f16
-    static constexpr int SCRATCH = NB * kTile * 4 + NB * kTile * 2;
-    static constexpr bool kZeroInvalidV = false;
-    static constexpr uint32_t kTmaX = 1;    // TMA boxes per (side, head)
-    static constexpr uint32_t kMaxWarps = KMAXW;
-    static constexpr int kMergeBatch = 8;
-
-    static __host__ __device__ constexpr uint32_t side_bytes(uint32_t hkv)
-    {
-        return hkv * kTile * RB;
-    }
-
-    // Query fragments live in shared memory, one 32-byte record per (block,
-    // lane) of each K/V head: the four B registers, then the C quad that
-    // starts the accumulator at minus the bias contribution (heads 2tig, 2tig+1).
-    static constexpr int QREC = 16;                     // one uint4 per (block, lane)
-    static constexpr int QCORR = NB * 32 * QREC;         // offset of the C quads
-    static constexpr int QBYTES = 2 * NB * 32 * QREC;    // per K/V head
-    struct Frag {
-        uint32_t q;  // shared address of this lane's records (block 0)
-    };
-
-    using Consts = NibbleConsts;
-    using QRaw = typename Q81Query<NB>::Raw;
-    __device__ static void fetch_q(const DecodeParams &p, uint32_t s, uint32_t h0, uint32_t G,
-                                   int gid, int tig, uint32_t w, uint32_t nw, QRaw &r)
-    {
-        Q81Query<NB>::fetch(p, s, h0, G, gid, tig, w, nw, r);
-    }
-
-    // Writes the fragments of query head gid of the group: qhat = f16(q * d_q
-    // * scale * log2 e), in the dimension order the nibble expansion produces
-    // (see block()).  One warp per K/V head calls this.
-    __device__ static void store_q(const DecodeParams &p, const QRaw &r, uint32_t G, int gid,
-                                   int tig, uint32_t w, uint32_t nw, uint32_t qsm)
-    {
-        const int lane = gid * 4 + tig;
-        const bool live = (uint32_t)gid < G;
-#pragma unroll
-        for (int b = 0; b < NB; ++b) {
-            if ((uint32_t)b % nw != w)
-                continue;
-            int code[8];
-            float d16;
-            Q81Query<NB>::codes(p, r, b, code, d16);
-            const float d = live ? d16 * p.scale_log2 : 0.0f;
-            __half qh[8];
-            float corr = 0.0f;
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                qh[j] = __float2half_rn((float)code[j] * d);
-                // low nibbles read as 1024 + n, high as 64 + n; the value is n - 8
-                corr += __half2float(qh[j]) * (j < 4 ? 1032.0f : 72.0f);
-            }
-            corr += __shfl_xor_sync(0xffffffffu, corr, 1);
-            corr += __shfl_xor_sync(0xffffffffu, corr, 2);
-            const float n0 = -__shfl_sync(0xffffffffu, corr, 8 * tig);
-            const float n1 = -__shfl_sync(0xffffffffu, corr, 8 * tig + 4);
-            const uint32_t rr = qsm + (b * 32 + lane) * QREC;
-            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(rr),
-                         "r"(h2_bits(__halves2half2(qh[0], qh[2]))),
-                         "r"(h2_bits(__halves2half2(qh[1], qh[3]))),
-                         "r"(h2_bits(__halves2half2(qh[4], qh[6]))),
-                         "r"(h2_bits(__halves2half2(qh[5], qh[7]))));
-            asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(rr + QCORR), "f"(n0),
-                         "f"(n1), "f"(n0), "f"(n1));
-        }
-    }
-
-    __device__ static void load_q(uint32_t qsm, int lane, Frag &f) { f.q = qsm + lane * QREC; }
-
-    // Block scales of the tile into the warp's scratch: dk as float with the
-    // pair (t, t+8) adjacent, dv as half in token order; zero for invalid tokens.
-    __device__ static void extract(uint32_t kh, uint32_t vh, uint32_t scr, int nvalid, int lane)
-    {
-        // lane covers token t = lane % 16 of blocks lane / 16 + 2k, k = 0..3
-        const int t = lane & 15, b0 = lane >> 4;
-        const bool v = t < nvalid;
-        const uint32_t ka = kh + t * RB + 18 * b0, va = vh + t * RB + 18 * b0;
-        const uint32_t sk = scr + DK + 4 * (b0 * kTile + 2 * (t & 7) + (t >> 3));
-        const uint32_t sv = scr + DV + 2 * (b0 * kTile + t);
-#pragma unroll
-        for (int k = 0; k < NB / 2; ++k) {
-            const uint32_t kd = lds_u16(ka + 36 * k);
-            const uint32_t vd = lds_u16(va + 36 * k);
-            sts_f32(sk + 128 * k, v ? half_bits_to_float((uint16_t)kd) : 0.0f);
-            sts_u16(sv + 64 * k, v ? vd : 0u);
-        }
-    }
-
-    // One 32-value block: x0 / x1 are the nibble words of tokens gid / gid+8
-    // holding dims 4tig..4tig+3 (low nibbles) and 16+4tig..19+4tig (high).
-    __device__ static __forceinline__ void block(const NibbleConsts &K, uint32_t qrec, uint32_t x0,
-                                                 uint32_t x1, float2 dk, float (&s)[4])
-    {
-        uint32_t qb0, qb1, qb2, qb3;
-        float c[4];
-        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                     : "=r"(qb0), "=r"(qb1), "=r"(qb2), "=r"(qb3)
-                     : "r"(qrec));
-        asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
-                     : "=f"(c[0]), "=f"(c[1]), "=f"(c[2]), "=f"(c[3])
-                     : "r"(qrec + QCORR));
-        const uint32_t y0 = x0 >> 8, y1 = x1 >> 8;
-        mma16816(c, and_or(x0, K.mlo, K.blo), and_or(x1, K.mlo, K.blo), and_or(y0, K.mlo, K.blo),
-                 and_or(y1, K.mlo, K.blo), qb0, qb1);
-        mma16816(c, and_or(x0, K.mhi, K.bhi), and_or(x1, K.mhi, K.bhi), and_or(y0, K.mhi, K.bhi),
-                 and_or(y1, K.mhi, K.bhi), qb2, qb3);
-        s[0] = fmaf(c[0], dk.x, s[0]);
-        s[1] = fmaf(c[1], dk.x, s[1]);
-        s[2] = fmaf(c[2], dk.y, s[2]);
-        s[3] = fmaf(c[3], dk.y, s[3]);
-    }
-
-    __device__ static void scores(const NibbleConsts &K, const Frag &f, uint32_t kh, uint32_t scr,
-                                  int gid, int tig, float (&s)[4])
-    {
-        uint32_t r0 = kh + gid * RB + 4 * tig;
-        uint32_t dk = scr + DK + 8 * gid;
-        uint32_t qr = f.q;
-        s[0] = s[1] = s[2] = s[3] = 0.0f;
-#pragma unroll
-        for (int pb = 0; pb < NB / 2; ++pb) {
-            // blocks 2pb and 2pb+1 share 36 bytes = 9 aligned words
-            const uint32_t a0 = lds_u32(r0), a1 = lds_u32(r0 + 4), a2 = lds_u32(r0 + 20);
-            const uint32_t b0 = lds_u32(r0 + 8 * RB), b1 = lds_u32(r0 + 8 * RB + 4);
-            const uint32_t b2 = lds_u32(r0 + 8 * RB + 20);
-            const float2 k0 = lds_f2(dk);
-            const float2 k1 = lds_f2(dk + 4 * kTile);
-            block(K, qr, __funnelshift_r(a0, a1, 16), __funnelshift_r(b0, b1, 16), k0, s);
-            block(K, qr + 32 * QREC, a2, b2, k1, s);
-            r0 += 36;
-            dk += 2 * 4 * kTile;
-            qr += 2 * 32 * QREC;
-        }
-    }
-
-    // O += V^T P' over the tile, P' = P * d_v per block.  The V operand is the
-    // nibble read as 1024 + n (low nibbles) or 64 + n (high nibbles); a second
-    // MMA with every A entry -1032 (or -72) adds -(bias + 8) * sum_t P', so the
-    // two together contribute sum_t (n - 8) P'.
-    __device__ static void pv(const NibbleConsts &K, float (&o)[MT][4], uint32_t vh, uint32_t scr,
-                              uint32_t p0, uint32_t p1, int gid, int tig)
-    {
-        const uint32_t ra = vh + (2 * tig) * RB + 2 + 2 * gid;
-        const uint32_t rc = ra + 8 * RB;
-#pragma unroll
-        for (int b = 0; b < NB; ++b) {
-            const uint32_t ua = lds_u16(ra + 18 * b), ub = lds_u16(ra + RB + 18 * b);
-            const uint32_t uc = lds_u16(rc + 18 * b), ud = lds_u16(rc + RB + 18 * b);
-            const uint32_t xab = __byte_perm(ua, ub, 0x5410), yab = xab >> 8;
-            const uint32_t xcd = __byte_perm(uc, ud, 0x5410), ycd = xcd >> 8;
-            const uint32_t b0 = hmul2_bits(p0, lds_u32(scr + DV + 2 * (b * kTile + 2 * tig)));
-            const uint32_t b1 = hmul2_bits(p1, lds_u32(scr + DV + 2 * (b * kTile + 8 + 2 * tig)));
-            mma16816(o[2 * b], and_or(xab, K.mlo, K.blo), and_or(yab, K.mlo, K.blo),
-                     and_or(xcd, K.mlo, K.blo), and_or(ycd, K.mlo, K.blo), b0, b1);
-            mma16816(o[2 * b], K.nlo[0], K.nlo[1], K.nlo[2], K.nlo[3], b0, b1);
-            mma16816(o[2 * b + 1], and_or(xab, K.mhi, K.bhi), and_or(yab, K.mhi, K.bhi),
-                     and_or(xcd, K.mhi, K.bhi), and_or(ycd, K.mhi, K.bhi), b0, b1);
-            mma16816(o[2 * b + 1], K.nhi[0], K.nhi[1], K.nhi[2], K.nhi[3], b0, b1);
-        }
-    }
-
-    // Output dimension of PV C-fragment row (gid or gid+8) of m-tile mt.
-    __device__ static __forceinline__ int dim_of(int mt, int gid, int upper)
-    {
-        return 32 * (mt >> 1) + 16 * (mt & 1) + 2 * gid + upper;
-    }
-};
-
-using Q40 = Q40T<12>;
-
-// --- Q8_0, D = 256 --------------------------------------------------------
-// Slot layout per side: 16 rows of 272 bytes (eight 34-byte blocks: f16 d,
-// then 32 int8 codes), written by TMA without swizzle; the 272-byte pitch puts
-// the rows of a warp's loads in different banks.
-//  QK runs on the integer tensor path: mma m16n8k32 s8 x s8 -> s32 takes the
-//  Q8_0 codes of 16 tokens x 32 dims as A and the q8_1 codes of the query as
-//  B, so each block's dot is an exact integer (the pages' q8_1 dot), scaled by
-//  d_k * d_q * scale * log2 e in f32.
-//  PV: the code c becomes the exact f16 1024 + (c ^ 0x80) with one byte
-//  permute per two values; one extra MMA with every A entry -1152 removes the
-//  bias, and d_v is folded into P as for Q4_0.
-template <uint32_t KMAXW>
-struct Q80T {
-    static constexpr int D = 256;
-    static constexpr int NB = D / 32;
-    static constexpr int BB = 34;           // block bytes
-    static constexpr int RB = NB * BB;      // row bytes (272)
-    static constexpr int MT = D / 16;
-    static constexpr int DK = 0, DV = NB * kTile * 4;
-    static constexpr int SCRATCH = NB * kTile * 4 + NB * kTile * 2;
-    static constexpr bool kZeroInvalidV = false;
-    static constexpr uint32_t kTmaX = 1;
-    static constexpr uint32_t kMaxWarps = KMAXW;
-    static constexpr int kMergeBatch = 12;
-
-    static __host__ __device__ constexpr uint32_t side_bytes(uint32_t hkv)
-    {
-        return hkv * kTile * RB;
-    }
-
-    struct Consts {
-        uint32_t flip, f16hi;  // 0x80808080; bytes 0x64 (the high byte of f16 1024)
-        uint32_t nb[4];        // A quad of -1152 (f16 pairs)
-        __device__ __forceinline__ void init()
-        {
-            flip = opaque(0x80808080u);
-            f16hi = opaque(0x64646464u);
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-                nb[i] = opaque(0xE480E480u);
-        }
-    };
-
-    // Query fragments in shared memory, one 16-byte record per (block, lane)
-    // of each K/V head: the two B registers (the q8_1 codes of query head gid
-    // at dims 4tig.. and 16+4tig..), then d_q * scale * log2 e of the heads
-    // 2tig and 2tig+1 (this thread's C columns).
-    static constexpr int QREC = 16;
-    static constexpr int QBYTES = NB * 32 * QREC;
-    struct Frag {
-        uint32_t q;
-    };
-    using QRaw = typename Q81Query<NB>::Raw;
-
-    __device__ static void fetch_q(const DecodeParams &p, uint32_t s, uint32_t h0, uint32_t G,
-                                   int gid, int tig, uint32_t w, uint32_t nw, QRaw &r)
-    {
-        Q81Query<NB>::fetch(p, s, h0, G, gid, tig, w, nw, r);
-    }
-
-    __device__ static void store_q(const DecodeParams &p, const QRaw &r, uint32_t G, int gid,
-                                   int tig, uint32_t w, uint32_t nw, uint32_t qsm)
-    {
-        const int lane = gid * 4 + tig;
-        const bool live = (uint32_t)gid < G;
-#pragma unroll
-        for (int b = 0; b < NB; ++b) {
-            if ((uint32_t)b % nw != w)
-                continue;
-            int code[8];
-            float d16;
-            Q81Query<NB>::codes(p, r, b, code, d16);
-            const float dq = live ? d16 * p.scale_log2 : 0.0f;
-            uint32_t w[2];
-#pragma unroll
-            for (int h = 0; h < 2; ++h)
-                w[h] = (uint32_t)(code[4 * h] & 0xFF) | (uint32_t)(code[4 * h + 1] & 0xFF) << 8 |
-                       (uint32_t)(code[4 * h + 2] & 0xFF) << 16 |
-                       (uint32_t)(code[4 * h + 3] & 0xFF) << 24;
-            // the scales of heads 2tig and 2tig+1 live in lanes 8tig and 8tig+4
-            const float q0 = __shfl_sync(0xffffffffu, dq, 8 * tig);
-            const float q1 = __shfl_sync(0xffffffffu, dq, 8 * tig + 4);
-            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
-                             qsm + (b * 32 + lane) * QREC),
-                         "r"(w[0]), "r"(w[1]), "r"(__float_as_uint(q0)), "r"(__float_as_uint(q1)));
-        }
-    }
-
-    __device__ static void load_q(uint32_t qsm, int lane, Frag &f) { f.q = qsm + lane * QREC; }
-
-    // Block scales into the warp's scratch, as for Q4_0: dk as float with the
-    // pair (t, t+8) adjacent, dv as half in token order; zero for invalid tokens.
-    __device__ static void extract(uint32_t kh, uint32_t vh, uint32_t scr, int nvalid, int lane)
-    {
-        const int t = lane & 15, b0 = lane >> 4;
-        const bool v = t < nvalid;
-        const uint32_t ka = kh + t * RB + BB * b0, va = vh + t * RB + BB * b0;
-        const uint32_t sk = scr + DK + 4 * (b0 * kTile + 2 * (t & 7) + (t >> 3));
-        const uint32_t sv = scr + DV + 2 * (b0 * kTile + t);
-#pragma unroll
-        for (int k = 0; k < NB / 2; ++k) {
-            const uint32_t kd = lds_u16(ka + 2 * BB * k);
-            const uint32_t vd = lds_u16(va + 2 * BB * k);
-            sts_f32(sk + 128 * k, v ? half_bits_to_float((uint16_t)kd) : 0.0f);
-            sts_u16(sv + 64 * k, v ? vd : 0u);
-        }
-    }
-
-    __device__ static __forceinline__ void imma(int (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
-                                                uint32_t a3, uint32_t b0, uint32_t b1)
-    {
-        asm volatile(
-            "mma.sync.aligned.m16n8k32.row.col.s32.s8.s8.s32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-            "{%8,%9}, {%0,%1,%2,%3};"
-            : "+r"(c[0]), "+r"(c[1]), "+r"(c[2]), "+r"(c[3])
-            : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-    }
-
-    // One block: a0..a3 are the code words of tokens gid / gid+8 at dims
-    // 4tig.. (a0, a1) and 16+4tig.. (a2, a3).
-    __device__ static __forceinline__ void block(uint32_t qrec, uint32_t a0, uint32_t a1,
-                                                 uint32_t a2, uint32_t a3, float2 dk,
-                                                 float (&s)[4])
-    {
-        uint32_t b0, b1, q0, q1;
-        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                     : "=r"(b0), "=r"(b1), "=r"(q0), "=r"(q1)
-                     : "r"(qrec));
-        int c[4] = {0, 0, 0, 0};
-        imma(c, a0, a1, a2, a3, b0, b1);
-        const float dq0 = __uint_as_float(q0), dq1 = __uint_as_float(q1);
-        s[0] = fmaf((float)c[0], dk.x * dq0, s[0]);
-        s[1] = fmaf((float)c[1], dk.x * dq1, s[1]);
-        s[2] = fmaf((float)c[2], dk.y * dq0, s[2]);
-        s[3] = fmaf((float)c[3], dk.y * dq1, s[3]);
-    }
-
-    __device__ static void scores(const Consts &, const Frag &f, uint32_t kh, uint32_t scr,
-                                  int gid, int tig, float (&s)[4])
-    {
-        // blocks 2pb (codes 2 bytes past a word boundary) and 2pb+1 (aligned)
-        uint32_t r0 = kh + gid * RB + 4 * tig, r1 = r0 + 8 * RB;
-        uint32_t dk = scr + DK + 8 * gid;
-        uint32_t qr = f.q;
-        s[0] = s[1] = s[2] = s[3] = 0.0f;
-#pragma unroll
-        for (int pb = 0; pb < NB / 2; ++pb) {
-            const uint32_t x0 = lds_u32(r0), x1 = lds_u32(r0 + 4), x2 = lds_u32(r0 + 16),
-                           x3 = lds_u32(r0 + 20);
-            const uint32_t y0 = lds_u32(r1), y1 = lds_u32(r1 + 4), y2 = lds_u32(r1 + 16),
-                           y3 = lds_u32(r1 + 20);
-            const uint32_t u0 = lds_u32(r0 + 36), u2 = lds_u32(r0 + 52);
-            const uint32_t v0 = lds_u32(r1 + 36), v2 = lds_u32(r1 + 52);
-            const float2 k0 = lds_f2(dk), k1 = lds_f2(dk + 4 * kTile);
-            block(qr, __funnelshift_r(x0, x1, 16), __funnelshift_r(y0, y1, 16),
-                  __funnelshift_r(x2, x3, 16), __funnelshift_r(y2, y3, 16), k0, s);
-            block(qr + 32 * QREC, u0, v0, u2, v2, k1, s);
-            r0 += 2 * BB;
-            r1 += 2 * BB;
-            dk += 2 * 4 * kTile;
-            qr += 2 * 32 * QREC;
-        }
-    }
-
-    // O += V^T P' over the tile, P' = P * d_v per block.  m-tile 2b holds dims
-    // 32b + 2gid (row gid) and 32b + 2gid + 1 (row gid + 8); m-tile 2b+1 the
-    // same 16 dims higher.  A register pairs one dim of tokens (2tig, 2tig+1)
-    // or (2tig+8, 2tig+9).
-    __device__ static void pv(const Consts &K, float (&o)[MT][4], uint32_t vh, uint32_t scr,
-                              uint32_t p0, uint32_t p1, int gid, int tig)
-    {
-        const uint32_t ra = vh + (2 * tig) * RB + 2 + 2 * gid;
-        const uint32_t rc = ra + 8 * RB;
-#pragma unroll
-        for (int b = 0; b < NB; ++b) {
-            const uint32_t b0 = hmul2_bits(p0, lds_u32(scr + DV + 2 * (b * kTile + 2 * tig)));
-            const uint32_t b1 =
-                hmul2_bits(p1, lds_u32(scr + DV + 2 * (b * kTile + 8 + 2 * tig)));
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                const uint32_t off = BB * b + 16 * hh;
-                const uint32_t ua = lds_u16(ra + off), ub = lds_u16(ra + RB + off);
-                const uint32_t uc = lds_u16(rc + off), ud = lds_u16(rc + RB + off);
-                // [a.dim0, a.dim1, b.dim0, b.dim1], each code flipped to c + 128
-                const uint32_t xab = __byte_perm(ua, ub, 0x5410) ^ K.flip;
-                const uint32_t xcd = __byte_perm(uc, ud, 0x5410) ^ K.flip;
-                float(&acc)[4] = o[2 * b + hh];
-                mma16816(acc, __byte_perm(xab, K.f16hi, 0x4240), __byte_perm(xab, K.f16hi, 0x4341),
-                         __byte_perm(xcd, K.f16hi, 0x4240), __byte_perm(xcd, K.f16hi, 0x4341),
-                         b0, b1);
-                mma16816(acc, K.nb[0], K.nb[1], K.nb[2], K.nb[3], b0, b1);
-            }
-        }
-    }
-
-    __device__ static __forceinline__ int dim_of(int mt, int gid, int upper)
-    {
-        return 16 * mt + 2 * gid + upper;
-    }
-};
-
-using Q80 = Q80T<8>;
-
-// --- F16, D = 128 or 256 ----------------------------------------------------
-// Slot layout per side: [64-dim chunk][16 tokens][128 B], written by TMA with
-// the 128-byte swizzle (16-byte chunk c of row t stored at c ^ (t & 7)), read
-// with ldmatrix without bank conflicts.
-template <int D_>
-struct F16T {
-    static constexpr int D = D_;
-    static constexpr int NC = D / 64;   // 64-dim chunks
-    static constexpr int KS = D / 16;   // k-steps
-    static constexpr int MT = D / 16;
-    static constexpr int SCRATCH = 0;
-    static constexpr bool kZeroInvalidV = true;
-    static constexpr uint32_t kTmaX = NC;
-    static constexpr uint32_t kMaxWarps = 8;
-    static constexpr int kMergeBatch = 12;
-
-    static __host__ __device__ constexpr uint32_t side_bytes(uint32_t hkv)
-    {
-        return hkv * kTile * D * 2;
-    }
-
-    static constexpr int QBYTES = 0;
-    struct Frag {
-        uint32_t qb[KS][2];  // B fragments (query column gid) of each k-step
-    };
-    struct Consts {
-        __device__ void init() {}
-    };
-
-    // This lane's query values (query head gid of the group), fetched before
-    // the first K/V copies are issued so that the loads do not queue behind them.
-    struct QRaw {
-        float2 x[KS][2];
-    };
-    __device__ static void fetch_q(const DecodeParams &p, uint32_t s, uint32_t h0, uint32_t G,
-                                   int gid, int tig, uint32_t, uint32_t, QRaw &r)
-    {
-        const float *row = static_cast<const float *>(p.q) +
-                           ((uint64_t)s * p.hq + h0 + ((uint32_t)gid < G ? gid : 0)) * D;
-#pragma unroll
-        for (int j = 0; j < KS; ++j) {
-            r.x[j][0] = *reinterpret_cast<const float2 *>(row + 16 * j + 2 * tig);
-            r.x[j][1] = *reinterpret_cast<const float2 *>(row + 16 * j + 8 + 2 * tig);
-        }
-    }
-
-    __device__ static void load_q(const DecodeParams &p, const QRaw &r, uint32_t G, int gid,
-                                  Frag &f)
-    {
-        const float sc = (uint32_t)gid < G ? p.scale_log2 : 0.0f;
-#pragma unroll
-        for (int j = 0; j < KS; ++j) {
-            f.qb[j][0] = h2_bits(__floats2half2_rn(r.x[j][0].x * sc, r.x[j][0].y * sc));
-            f.qb[j][1] = h2_bits(__floats2half2_rn(r.x[j][1].x * sc, r.x[j][1].y * sc));
-        }
-    }
-
-    __device__ static __forceinline__ uint32_t chunk_addr(uint32_t sub, int token, int c16)
-    {
-        return sub + token * 128 + ((c16 ^ (token & 7)) << 4);
-    }
-
-    // Zero V rows of tokens >= nvalid (their bytes may be anything).
-    __device__ static void zero_invalid_v(uint8_t *vh, int nvalid, int lane)
-    {
-        const int rows = (kTile - nvalid) * NC;
-        for (int i = lane; i < rows * 8; i += 32) {
-            const int r = i >> 3, part = i & 7;
-            const int c = r / (kTile - nvalid), t = nvalid + r % (kTile - nvalid);
-            reinterpret_cast<uint4 *>(vh + (c * kTile + t) * 128)[part] = make_uint4(0, 0, 0, 0);
-        }
-    }
-
-    __device__ static void scores(const Consts &, const Frag &f, uint32_t kh, uint32_t,
-                                  int gid, int tig, float (&s)[4])
-    {
-        const int lane = gid * 4 + tig;
-        const int mi = lane >> 3, r = lane & 7;
-        const int token = (mi & 1) * 8 + r;
-        float c[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int j = 0; j < KS; ++j) {
-            uint32_t a[4];
-            ldsm_x4(a, chunk_addr(kh + (j >> 2) * kTile * 128, token, 2 * (j & 3) + (mi >> 1)));
-            mma16816(c, a[0], a[1], a[2], a[3], f.qb[j][0], f.qb[j][1]);
-        }
-        s[0] = c[0];
-        s[1] = c[1];
-        s[2] = c[2];
-        s[3] = c[3];
-    }
-
-    __device__ static void pv(const Consts &, float (&o)[MT][4], uint32_t vh, uint32_t,
-                              uint32_t p0, uint32_t p1, int gid, int tig)
-    {
-        const int lane = gid * 4 + tig;
-        const int mi = lane >> 3, r = lane & 7;
-        const int token = (mi >> 1) * 8 + r;
-#pragma unroll
-        for (int mt = 0; mt < MT; ++mt) {
-            uint32_t a[4];
-            ldsm_x4_trans(a, chunk_addr(vh + (mt >> 2) * kTile * 128, token, (mt & 3) * 2 + (mi & 1)));
-            mma16816(o[mt], a[0], a[1], a[2], a[3], p0, p1);
-        }
-    }
-
-    __device__ static __forceinline__ int dim_of(int mt, int gid, int upper)
-    {
-        return 16 * mt + gid + 8 * upper;
-    }
-};
-
-// ------------------------------------------------------------------ kernel
-//
-// Warp w serves K/V head g = w % hkv and the tiles i = sub, sub + wph, ... of
-// the partition (sub = w / hkv, wph = warps / hkv).  It owns a private ring of
-// n_slots stages, each holding the K and V rows of its head for one tile, and
-// it alone issues their TMA copies and waits on their mbarriers, so the main
-// loop needs no synchronisation between warps.  Rows of a tile for the other
-// heads are fetched by the other warps at about the same time; the whole
-// 16-token block is one contiguous range of the pool.
-
-constexpr float kHeadroom = 4.0f;  // log2 units kept between the reference and the max
-
-// Parked (m, l, O) of one warp: m of its 8 head columns, then l, then O as
-// 8 rows of D floats (row stride D + 4, so that the fragment stores of the
-// four tig lanes fall in different banks).
-template <class T>
-struct Park {
-    static constexpr int kRow = T::D + 4;
-    static constexpr int kWarp = 16 + 8 * kRow;
-};
-
-template <class T>
-__device__ __forceinline__ void combine_and_write(const DecodeParams &p, const float *park,
-                                                  uint32_t hkv, uint32_t wph, uint32_t G,
-                                                  uint32_t seq, uint32_t part);
-
-// The in-launch merge, out of line so that its registers do not add to the
-// main loop's; each warp keeps BATCH partials of each of its two rows in
-// flight, as many as the kernel's register budget holds.
-template <int BATCH>
-__device__ __noinline__ void merge_tail(const DecodeParams &p, uint32_t seq, uint32_t part,
-                                        uint32_t warp, uint32_t nwarps)
-{
-    fused_merge<BATCH>(p, seq, part, warp, nwarps);
-}
-
-template <class T>
-__global__ void __launch_bounds__(T::kMaxWarps * 32, 1)
-    fast_decode_kernel(const __grid_constant__ FastArgs a)
-{
-    const DecodeParams &p = a.p;
-    extern __shared__ __align__(16) uint8_t smem_raw[];
-    uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-    const uint32_t NSW = a.n_slots, SLOT = a.slot_bytes, nwarps = blockDim.x >> 5;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const uint32_t hkv = p.hkv, G = p.hq / p.hkv, wph = nwarps / hkv;
-    uint8_t *ring = smem + (size_t)warp * NSW * SLOT;
-    const uint32_t ring_u = smem_u32(ring);
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + a.region_bytes) + warp * NSW;
-    int *slot_ok = reinterpret_cast<int *>(reinterpret_cast<uint64_t *>(smem + a.region_bytes) +
-                                           nwarps * NSW) + warp * NSW;
-    const uint32_t scr_base = (smem_u32(slot_ok + (nwarps - warp) * NSW) + 15u) & ~15u;
-    const uint32_t scr_u = scr_base + warp * T::SCRATCH;
-    const uint32_t qsm_base = scr_base + nwarps * T::SCRATCH;  // per K/V head: T::QBYTES
-
-    if (lane == 0) {
-        for (uint32_t s = 0; s < NSW; ++s)
-            mbar_init(&full[s], 1);
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    }
-    __syncthreads();
-
-    uint32_t seq, part;
-    if (!p.direct && blockIdx.x == gridDim.x - 1 && warp == 0)
-        check_grid_vs_plan(p.seq_lens, p.n_seqs, p.part_tokens, p.n_parts, p.status);
-    if (p.direct) {
-        seq = blockIdx.x;
-        part = 0;
-    } else if (!cta_work(p.seq_lens, p.n_seqs, p.part_tokens, p.n_parts, blockIdx.x, &seq,
-                         &part)) {
-        return;  // past the last live partition: nothing was issued
-    } else if (part == 0 && tid == 0) {
-        check_len_vs_plan(p.seq_lens[seq], p.n_parts, p.part_tokens, p.status);
-    }
-    const int32_t L = p.seq_lens[seq] > 0 ? p.seq_lens[seq] : 0;
-    const uint32_t t0 = p.direct ? 0u : part * p.part_tokens;
-    const uint32_t t1 = p.direct ? (uint32_t)L : min((uint32_t)L, t0 + p.part_tokens);
-    const uint32_t n_tiles = (t1 - t0 + kTile - 1) / kTile;
-    const int gid = lane >> 2, tig = lane & 3;
-    const uint32_t g = warp % hkv, sub = warp / hkv;
-    const uint32_t n_my = n_tiles > sub ? (n_tiles - sub + wph - 1) / wph : 0;
-    const int32_t *bt = p.block_table + (uint64_t)seq * p.table_stride;
-    const CUtensorMap *tmk = &a.tm[0][g], *tmv = &a.tm[1][g];
-    const uint32_t side = SLOT / 2;
-    const uint32_t bshift = p.block_size == 32 ? 5 : 4, bmask = p.block_size - 1;
-
-    // block ids of my tiles k0 .. k0+31, one per lane
-    auto fetch_ids = [&](uint32_t k0) -> int32_t {
-        const uint32_t k = k0 + lane;
-        return k < n_my ? bt[(t0 + kTile * (sub + k * wph)) >> bshift] : 0;
-    };
-    // lane 0: start the copy of my tile k (block id blk) into slot s
-    auto issue = [&](uint32_t k, uint32_t s, int32_t blk) {
-        const uint32_t tok = t0 + kTile * (sub + k * wph);
-        const bool ok = block_in_pool(blk, p.n_pool_blocks);
-        slot_ok[s] = ok;
-        if (ok) {
-            uint8_t *dst = ring + (size_t)s * SLOT;
-            const int y = (blk << bshift) + (int)(tok & bmask);
-            fence_proxy_async();  // earlier generic reads of this slot come first
-            mbar_arrive_expect_tx(&full[s], SLOT);
-#pragma unroll
-            for (uint32_t c = 0; c < T::kTmaX; ++c) {
-                tma_load_2d(dst + c * (side / T::kTmaX), tmk, 64 * c, y, &full[s]);
-                tma_load_2d(dst + side + c * (side / T::kTmaX), tmv, 64 * c, y, &full[s]);
-            }
-        } else {
-            atomicOr(p.status, PA_STATUS_CORRUPT_TABLE);
-            mbar_arrive(&full[s]);
-        }
-    };
-
-    int32_t ids = fetch_ids(0), ids_next = fetch_ids(32);
-    // quantised K: the wph warps of a head split its query blocks
-    typename T::QRaw qraw;
-    T::fetch_q(p, seq, g * G, G, gid, tig, sub, wph, qraw);
-    const uint32_t pro = n_my < NSW ? n_my : NSW;
-    for (uint32_t k = 0; k < pro; ++k) {
-        const int32_t b = __shfl_sync(0xffffffffu, ids, k);
-        if (lane == 0)
-            issue(k, k, b);
-    }
-    __syncwarp();
-
-    typename T::Consts K;
-    K.init();
-    typename T::Frag f;
-    if constexpr (T::QBYTES > 0) {
-        T::store_q(p, qraw, G, gid, tig, sub, wph, qsm_base + g * T::QBYTES);
-        __syncthreads();
-        T::load_q(qsm_base + g * T::QBYTES, lane, f);
-    } else {
-        T::load_q(p, qraw, G, gid, f);
-    }
-    float o[T::MT][4];
-#pragma unroll
-    for (int mt = 0; mt < T::MT; ++mt)
-        o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.0f;
-    // softmax state of this thread's heads 2tig and 2tig+1: reference max
-    // (>= every score seen) and the partial sum over its tokens
-    float mref0 = -INFINITY, mref1 = -INFINITY, l0 = 0.0f, l1 = 0.0f;
-    bool aborted = false;
-    uint32_t issued = pro;
-
-    uint32_t s = 0, phase = 0;  // slot of tile k and the parity of its current use
-    for (uint32_t k = 0; k < n_my; ++k) {
-        // every lane waits (bounded) and so acquires the slot's TMA writes itself
-        bool done = mbar_try_wait(&full[s], phase);
-        if (!done) {
-            const uint64_t tw = global_ns();
-            while (!(done = mbar_try_wait(&full[s], phase)) && global_ns() - tw < kWaitNs) {
-            }
-        }
-        if (!__all_sync(0xffffffffu, done)) {
-            if (lane == 0)
-                atomicOr(p.status, PA_STATUS_TIMEOUT);
-            aborted = true;
-            break;
-        }
-        const uint32_t i = sub + k * wph;
-        const int nvalid = slot_ok[s] ? (int)min(16u, t1 - (t0 + kTile * i)) : 0;
-        const uint32_t kh = ring_u + s * SLOT, vh = kh + side;
-        if constexpr (T::kZeroInvalidV) {
-            if (nvalid < kTile) {
-                T::zero_invalid_v(ring + (size_t)s * SLOT + side, nvalid, lane);
-                __syncwarp();
-            }
-        } else {
-            T::extract(kh, vh, scr_u, nvalid, lane);
-            __syncwarp();
-        }
-        float sc[4];
-        T::scores(K, f, kh, scr_u, gid, tig, sc);
-        // online softmax over the tile (log2 domain); the reference max moves,
-        // and the accumulators are rescaled, only when a score passes it
-        if (gid >= nvalid)
-            sc[0] = sc[1] = -INFINITY;
-        if (gid + 8 >= nvalid)
-            sc[2] = sc[3] = -INFINITY;
-        // a score above its reference is rare: each lane checks its own four,
-        // and only then does the warp form the tile maxima of its heads
-        const bool over = fmaxf(sc[0], sc[2]) > mref0 || fmaxf(sc[1], sc[3]) > mref1;
-        if (__builtin_expect(__any_sync(0xffffffffu, over), 0)) {
-            float t0m = fmaxf(sc[0], sc[2]), t1m = fmaxf(sc[1], sc[3]);
-#pragma unroll
-            for (int off = 4; off < 32; off <<= 1) {
-                t0m = fmaxf(t0m, __shfl_xor_sync(0xffffffffu, t0m, off));
-                t1m = fmaxf(t1m, __shfl_xor_sync(0xffffffffu, t1m, off));
-            }
-            const float n0 = t0m > mref0 ? t0m + kHeadroom : mref0;
-            const float n1 = t1m > mref1 ? t1m + kHeadroom : mref1;
-            const float a0 = mref0 == -INFINITY ? 0.0f : exp2f(mref0 - n0);
-            const float a1 = mref1 == -INFINITY ? 0.0f : exp2f(mref1 - n1);
-#pragma unroll
-            for (int mt = 0; mt < T::MT; ++mt) {
-                o[mt][0] *= a0;
-                o[mt][1] *= a1;
-                o[mt][2] *= a0;
-                o[mt][3] *= a1;
-            }
-            l0 *= a0;
-            l1 *= a1;
-            mref0 = n0;
-            mref1 = n1;
-        }
-        const float ms0 = mref0 == -INFINITY ? 0.0f : mref0;
-        const float ms1 = mref1 == -INFINITY ? 0.0f : mref1;
-        const float q00 = exp2f(sc[0] - ms0), q01 = exp2f(sc[1] - ms1);
-        const float q10 = exp2f(sc[2] - ms0), q11 = exp2f(sc[3] - ms1);
-        l0 += q00 + q10;
-        l1 += q01 + q11;
-        // P[token][head] as two 8x8 blocks (tokens 0-7, 8-15) -> PV B operand
-        const uint32_t p0 = movmatrix_t(h2_bits(__floats2half2_rn(q00, q01)));
-        const uint32_t p1 = movmatrix_t(h2_bits(__floats2half2_rn(q10, q11)));
-        T::pv(K, o, vh, scr_u, p0, p1, gid, tig);
-        __syncwarp();  // all reads of this slot are done
-        // refill the slot with my tile k + NSW
-        const uint32_t kn = k + NSW;
-        if (kn < n_my) {
-            if ((kn & 31) == 0) {
-                ids = ids_next;
-                ids_next = fetch_ids(kn + 32);
-            }
-            const int32_t b = __shfl_sync(0xffffffffu, ids, kn & 31);
-            if (lane == 0)
-                issue(kn, s, b);
-            issued = kn + 1;
-        }
-        __syncwarp();
-        if (++s == NSW) {
-            s = 0;
-            phase ^= 1;
-        }
-    }
-    if (aborted && lane == 0) {
-        // let my copies still in flight land (bounded) before the CTA moves on
-        for (uint32_t k = issued > NSW ? issued - NSW : 0; k < issued; ++k) {
-            const uint64_t tw = global_ns();
-            while (!mbar_try_wait(&full[k % NSW], (k / NSW) & 1) && global_ns() - tw < kWaitNs) {
-            }
-        }
-    }
-#pragma unroll
-    for (int off = 4; off < 32; off <<= 1) {
-        l0 += __shfl_xor_sync(0xffffffffu, l0, off);
-        l1 += __shfl_xor_sync(0xffffffffu, l1, off);
-    }
-
-    // park (m, l, O) of every warp in the now idle rings, head-major, then
-    // all warps of the CTA combine them
-    __syncthreads();
-    float *park = reinterpret_cast<float *>(smem);
-    float *mine = park + warp * Park<T>::kWarp;
-    if (gid == 0) {
-        mine[2 * tig] = mref0;
-        mine[2 * tig + 1] = mref1;
-        mine[8 + 2 * tig] = l0;
-        mine[8 + 2 * tig + 1] = l1;
-    }
-#pragma unroll
-    for (int mt = 0; mt < T::MT; ++mt)
-#pragma unroll
-        for (int e = 0; e < 4; ++e)
-            mine[16 + (2 * tig + (e & 1)) * Park<T>::kRow + T::dim_of(mt, gid, e >> 1)] = o[mt][e];
-    __syncthreads();
-    combine_and_write<T>(p, park, hkv, wph, G, seq, part);
-    if (p.counters && !p.direct)
-        merge_tail<T::kMergeBatch>(p, seq, part, warp, nwarps);
-}
-
-// Combine of the parked (m, l, O) of the wph warps of every head group into
-// the partition's result: for each query head, M = max of the warps'
-// reference maxima, f_k = 2^(m_k - M), O = sum f_k O_k / sum f_k l_k.  Every
-// thread of the CTA takes 8-dim chunks of the output rows, so the partial
-// rows are written with coalesced 16-byte stores (f16 partials) or 32-byte
-// stores (the f32 output of a direct plan).
-template <class T>
-__device__ __forceinline__ void combine_and_write(const DecodeParams &p, const float *park,
-                                                  uint32_t hkv, uint32_t wph, uint32_t G,
-                                                  uint32_t seq, uint32_t part)
-{
-    constexpr uint32_t NQ = T::D / 8;
-    const uint32_t n_chunks = hkv * G * NQ;
-    for (uint32_t c = threadIdx.x; c < n_chunks; c += blockDim.x) {
-        const uint32_t hg = c / NQ, q = c % NQ;
-        const uint32_t g = hg / G, h = hg - g * G;
-        float M = -INFINITY;
-#pragma unroll
-        for (uint32_t k = 0; k < T::kMaxWarps; ++k)
-            if (k < wph)
-                M = fmaxf(M, park[(g + k * hkv) * Park<T>::kWarp + h]);
-        float l = 0.0f, acc[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-            acc[j] = 0.0f;
-#pragma unroll
-        for (uint32_t k = 0; k < T::kMaxWarps; ++k) {
-            if (k < wph) {
-                const float *w = park + (g + k * hkv) * Park<T>::kWarp;
-                const float mk = w[h];
-                const float f = mk == -INFINITY ? 0.0f : exp2f(mk - M);
-                l = fmaf(w[8 + h], f, l);
-                const float4 *src = reinterpret_cast<const float4 *>(w + 16 + h * Park<T>::kRow + 8 * q);
-                const float4 a = src[0], b = src[1];
-                acc[0] = fmaf(f, a.x, acc[0]);
-                acc[1] = fmaf(f, a.y, acc[1]);
-                acc[2] = fmaf(f, a.z, acc[2]);
-                acc[3] = fmaf(f, a.w, acc[3]);
-                acc[4] = fmaf(f, b.x, acc[4]);
-                acc[5] = fmaf(f, b.y, acc[5]);
-                acc[6] = fmaf(f, b.z, acc[6]);
-                acc[7] = fmaf(f, b.w, acc[7]);
-            }
-        }
-        const float inv = l > 0.0f ? 1.0f / l : 0.0f;
-        const uint64_t row = (uint64_t)seq * p.hq + hg;
-        if (p.direct) {
-            float4 *dst = reinterpret_cast<float4 *>(p.out + row * T::D + 8 * q);
-            dst[0] = make_float4(acc[0] * inv, acc[1] * inv, acc[2] * inv, acc[3] * inv);
-            dst[1] = make_float4(acc[4] * inv, acc[5] * inv, acc[6] * inv, acc[7] * inv);
-        } else {
-            uint4 v;
-            v.x = h2_bits(__floats2half2_rn(acc[0] * inv, acc[1] * inv));
-            v.y = h2_bits(__floats2half2_rn(acc[2] * inv, acc[3] * inv));
-            v.z = h2_bits(__floats2half2_rn(acc[4] * inv, acc[5] * inv));
-            v.w = h2_bits(__floats2half2_rn(acc[6] * inv, acc[7] * inv));
-            __half *po = static_cast<__half *>(p.part_o);
-            *reinterpret_cast<uint4 *>(po + (row * p.n_parts + part) * T::D + 8 * q) = v;
-            if (q == 0)
-                reinterpret_cast<float2 *>(p.part_ml)[row * p.n_parts + part] =
-                    make_float2(l > 0.0f ? M : -INFINITY, l);
-        }
-    }
-}
-
-// ------------------------------------------------------------------- host
-
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
-{
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void *ptr = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
-                                             cudaEnableDefault, &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-    });
-    return fn;
-}
-
-// Launch geometry of one kernel instance: warps per head and ring slots.
-struct Geometry {
-    uint32_t wph = 0, warps = 0, n_slots = 0, slot_bytes = 0, region = 0;
-    size_t smem = 0;
-};
-
-template <class T>
-Geometry geometry(uint32_t hkv)
-{
-    Geometry gm;
-    const size_t slot = 2 * (size_t)T::side_bytes(1);
-    const size_t park_per_warp = Park<T>::kWarp * 4;
-    for (uint32_t wph = T::kMaxWarps / hkv; wph >= 1; --wph) {
-        const uint32_t warps = wph * hkv;
-        const size_t fixed = 1024 + warps * (size_t)T::SCRATCH + warps * 16 * 12 + 64 +
-                             hkv * (size_t)T::QBYTES;
-        if (fixed >= kSmemBudget)
-            continue;
-        size_t ns = (kSmemBudget - fixed) / (warps * slot);
-        if (ns > 8)
-            ns = 8;
-        if (ns >= 2) {
-            gm.wph = wph;
-            gm.warps = warps;
-            gm.n_slots = (uint32_t)ns;
-            gm.slot_bytes = (uint32_t)slot;
-            size_t ring = warps * ns * slot, park = warps * park_per_warp;
-            gm.region = (uint32_t)(ring > park ? ring : park);
-            gm.smem = 1024 + gm.region + warps * ns * (8 + 4) + 16 + warps * (size_t)T::SCRATCH +
-                      hkv * (size_t)T::QBYTES;
-            return gm;
-        }
-        if (wph == 1)
-            break;
-    }
-    return gm;
-}
-
-template <class T>
-int encode_maps(const DecodeParams &p, FastArgs &a, const char *entry)
-{
-    auto enc = encode_fn();
-    if (!enc)
-        return fail(PA_ERR_CUDA, entry, "cuTensorMapEncodeTiled unavailable");
-    const uint64_t rb = T::side_bytes(1) / kTile;  // bytes of one row
-    const uint64_t n_slots = p.n_pool_blocks * p.block_size;
-    for (int side = 0; side < 2; ++side) {
-        const uint8_t *pool = side ? p.v_pool : p.k_pool;
-        for (uint32_t g = 0; g < p.hkv; ++g) {
-            cuuint64_t dims[2] = {rb / 2, n_slots}, strides[1] = {(cuuint64_t)p.hkv * rb};
-            cuuint32_t box[2] = {T::kTmaX > 1 ? 64u : (cuuint32_t)(rb / 2), (cuuint32_t)kTile};
-            cuuint32_t estr[2] = {1, 1};
-            // f16 rows: 64-value chunks with the 128-byte swizzle; Q4_0 rows whole
-            const CUtensorMapSwizzle sw =
-                T::kTmaX > 1 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE;
-            CUresult r = enc(&a.tm[side][g], CU_TENSOR_MAP_DATA_TYPE_UINT16, 2,
-                             const_cast<uint8_t *>(pool) + g * rb, dims, strides, box, estr,
-                             CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-            if (r != CUDA_SUCCESS)
-                return fail(PA_ERR_CUDA, entry, "cuTensorMapEncodeTiled failed (%d)", (int)r);
-        }
-    }
-    return PA_OK;
-}
-
-// Raises the kernel's dynamic shared-memory limit once per device.
-template <class T>
-cudaError_t allow_smem()
-{
-    static std::mutex mu;
-    static bool done[64] = {};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess || dev < 0 || dev >= 64)
-        return e != cudaSuccess ? e : cudaErrorInvalidDevice;
-    std::lock_guard<std::mutex> lock(mu);
-    if (!done[dev]) {
-        e = cudaFuncSetAttribute(fast_decode_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)(kSmemBudget + 4096));
-        if (e != cudaSuccess)
-            return e;
-        done[dev] = true;
-    }
-    return cudaSuccess;
-}
-
-// The tensor maps depend only on the pools, their size and the head layout;
-// a few recent encodings are kept so that repeated steps skip the encoding.
-struct MapKey {
-    const void *k, *v;
-    uint64_t n_blocks;
-    uint32_t block_size, hkv, d, type;
-    bool operator==(const MapKey &o) const
-    {
-        return k == o.k && v == o.v && n_blocks == o.n_blocks && block_size == o.block_size &&
-               hkv == o.hkv && d == o.d && type == o.type;
-    }
-};
-
-template <class T>
-int cached_maps(const DecodeParams &p, FastArgs &a, const char *entry)
-{
-    constexpr int kSlots = 8;
-    static std::mutex mu;
-    static MapKey keys[kSlots];
-    static CUtensorMap maps[kSlots][2][kMaxHkv];
-    static bool used[kSlots] = {};
-    static int next = 0;
-    const MapKey key{p.k_pool, p.v_pool, p.n_pool_blocks, p.block_size, p.hkv, (uint32_t)T::D,
-                     (uint32_t)T::kTmaX};
-    std::lock_guard<std::mutex> lock(mu);
-    for (int i = 0; i < kSlots; ++i)
-        if (used[i] && keys[i] == key) {
-            memcpy(a.tm, maps[i], sizeof a.tm);
-            return PA_OK;
-        }
-    int rc = encode_maps<T>(p, a, entry);
-    if (rc)
-        return rc;
-    keys[next] = key;
-    memcpy(maps[next], a.tm, sizeof a.tm);
-    used[next] = true;
-    next = (next + 1) % kSlots;
-    return PA_OK;
-}
-
-template <class T>
-int launch_t(const DecodeParams &p, cudaStream_t st, const char *entry)
-{
-    const Geometry gm = geometry<T>(p.hkv);
-    if (!gm.warps)
-        return fail(PA_ERR_INVALID, entry, "fast kernel: a tile does not fit shared memory");
-    FastArgs a;
-    memset(&a, 0, sizeof a);
-    int rc = cached_maps<T>(p, a, entry);
-    if (rc)
-        return rc;
-    a.p = p;
-    a.n_slots = gm.n_slots;
-    a.slot_bytes = gm.slot_bytes;
-    a.region_bytes = gm.region;
-    rc = cuda_check(allow_smem<T>(), entry, "cudaFuncSetAttribute");
-    if (rc)
-        return rc;
-    fast_decode_kernel<T><<<p.n_ctas, gm.warps * 32, gm.smem, st>>>(a);
-    return cuda_check(cudaGetLastError(), entry, "fast_decode_kernel launch");
-}
-
-template <class T>
-int occupancy_t(uint32_t hkv, int *cps)
-{
-    const Geometry gm = geometry<T>(hkv);
-    if (!gm.warps)
-        return PA_ERR_INVALID;
-    cudaError_t e = allow_smem<T>();
-    if (e == cudaSuccess)
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(cps, fast_decode_kernel<T>,
-                                                          gm.warps * 32, gm.smem);
-    return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
-}
-
-bool hkv_ok(uint32_t hkv) { return hkv == 1 || hkv == 2 || hkv == 4 || hkv == 8; }
-
-}  // namespace
 
 bool fast_decode_supported(pa_type kt, pa_type vt, uint32_t d, uint32_t hq, uint32_t hkv,
                            uint32_t block_size)
 {
-    if (kt != vt || !hkv_ok(hkv) || hq % hkv || hq / hkv > 8 ||
-        (block_size != 16 && block_size != 32))
+    if (!hkv_ok(hkv) || hq % hkv || hq / hkv > 8 || (block_size != 16 && block_size != 32))
         return false;
+    if (kt != vt)
+        return d == 256 && fast_mixed_supported(kt, vt, hkv);
     if (kt == PA_Q4_0)
         return d == 256 && geometry<Q40>(hkv).warps > 0;
     if (kt == PA_Q8_0)
@@ -1337,9 +22,11 @@ bool fast_decode_supported(pa_type kt, pa_type vt, uint32_t d, uint32_t hq, uint
     return false;
 }
 
-int fast_decode_occupancy(pa_type kt, pa_type, uint32_t d, uint32_t, uint32_t hkv, uint32_t,
+int fast_decode_occupancy(pa_type kt, pa_type vt, uint32_t d, uint32_t, uint32_t hkv, uint32_t,
                           int *ctas_per_sm)
 {
+    if (kt != vt)
+        return fast_mixed_occupancy(kt, vt, hkv, ctas_per_sm);
     if (kt == PA_Q4_0)
         return occupancy_t<Q40>(hkv, ctas_per_sm);
     if (kt == PA_Q8_0)
@@ -1354,6 +41,8 @@ int launch_fast_decode(const DecodeParams &p, pa_type kt, pa_type vt, cudaStream
     // TMA slot coordinates are int32: larger pools take the plain kernel
     if (p.n_pool_blocks * p.block_size >= (1ull << 31))
         return launch_plain_decode(p, kt, vt, st, entry);
+    if (kt != vt)
+        return launch_fast_mixed(p, kt, vt, st, entry);
     if (kt == PA_Q4_0)
         return launch_t<Q40>(p, st, entry);
     if (kt == PA_Q8_0)

@@ -95,5 +95,10 @@ int fast_decode_occupancy(pa_type kt, pa_type vt, uint32_t d, uint32_t hq, uint3
                           uint32_t block_size, int *ctas_per_sm);
 int launch_fast_decode(const DecodeParams &p, pa_type kt, pa_type vt, cudaStream_t st,
                        const char *entry);
+// The mixed K x V type instances of the fast kernel (D = 256).
+bool fast_mixed_supported(pa_type kt, pa_type vt, uint32_t hkv);
+int fast_mixed_occupancy(pa_type kt, pa_type vt, uint32_t hkv, int *ctas_per_sm);
+int launch_fast_mixed(const DecodeParams &p, pa_type kt, pa_type vt, cudaStream_t st,
+                      const char *entry);
 
 }  // namespace pa

@@ -283,13 +283,15 @@ def ragged_spec(type_: int = Q4_0) -> CaseSpec:
                     name=f"ragged-{TYPE_LABEL[type_]}-128k+7x8k")
 
 
-def dtype_sweep_spec(type_: int, short: bool = False) -> CaseSpec:
+def dtype_sweep_spec(type_: int, short: bool = False, v_type: int | None = None) -> CaseSpec:
     """Batch 4 x 32768 (or the short ragged 4096 + 7 x 256), N(0,1) values
-    with 1% outliers at x8."""
+    with 1% outliers at x8; V of type v_type when given (a mixed pair)."""
     lens = [4096] + [256] * 7 if short else [32768] * 4
     tag = "short" if short else "b4x32k"
-    return CaseSpec(seq_lens=lens, k_type=type_, v_type=type_, outliers=True,
-                    name=f"sweep-{TYPE_LABEL[type_]}-{tag}")
+    vt = type_ if v_type is None else v_type
+    pair = TYPE_LABEL[type_] if vt == type_ else f"{TYPE_LABEL[type_]}-{TYPE_LABEL[vt]}"
+    return CaseSpec(seq_lens=lens, k_type=type_, v_type=vt, outliers=True,
+                    name=f"sweep-{pair}-{tag}")
 
 
 def large_pool_spec(n_seqs: int = 16, ctx: int = 300_000) -> CaseSpec:
