@@ -58,6 +58,7 @@ class OrArgs(ctypes.Structure):
         ("n_seqs", ctypes.c_uint32), ("hq", ctypes.c_uint32), ("hkv", ctypes.c_uint32),
         ("d", ctypes.c_uint32), ("block_size", ctypes.c_uint32),
         ("k_type", ctypes.c_int32), ("v_type", ctypes.c_int32),
+        ("q_tokens", ctypes.c_uint32),
     ]
 
 
@@ -173,8 +174,13 @@ class OracleError(RuntimeError):
 
 
 def _args(k_pool, v_pool, block_table, seq_lens, q, hkv, block_size, k_type, v_type, scale):
+    """q: float32 [S][hq][d], or [S][T][hq][d] for T query tokens per
+    sequence (query row u = s * T + i)."""
     q = np.ascontiguousarray(q, dtype=np.float32)
-    S, hq, d = q.shape
+    T = q.shape[1] if q.ndim == 4 else 1
+    q = q.reshape(-1, q.shape[-2], q.shape[-1])
+    S = q.shape[0] // T
+    _, hq, d = q.shape
     k_pool = np.ascontiguousarray(k_pool).view(np.uint8)
     v_pool = np.ascontiguousarray(v_pool).view(np.uint8)
     bt = np.ascontiguousarray(block_table, dtype=np.int32)
@@ -187,7 +193,7 @@ def _args(k_pool, v_pool, block_table, seq_lens, q, hkv, block_size, k_type, v_t
                seq_lens=_ptr(sl), q=_ptr(q),
                scale=float(1.0 / np.sqrt(d)) if scale is None else float(scale),
                n_seqs=S, hq=hq, hkv=hkv, d=d, block_size=block_size,
-               k_type=int(k_type), v_type=int(v_type))
+               k_type=int(k_type), v_type=int(v_type), q_tokens=T)
     keep = (q, k_pool, v_pool, bt, sl)  # arrays the struct points into
     return a, keep
 
@@ -216,10 +222,12 @@ def decode(k_pool, v_pool, block_table, seq_lens, q, *, hkv: int, block_size: in
 
     k_pool / v_pool: uint8 arrays whose bytes are the token-major pools
     [n_blocks][block_size][hkv][row_bytes].  block_table int32 [S][stride],
-    seq_lens int32 [S], q float32 [S][Hq][D].  units: optional list of
-    (seq, head) pairs; default every pair.  Returns float64 [n_units][D]
-    (or [S][Hq][D] when units is None).  part_tokens > 0 selects the
-    partitioned-with-merge form of the same definition."""
+    seq_lens int32 [S], q float32 [S][Hq][D], or [S][T][Hq][D] for T query
+    tokens per sequence (token i at position L - T + i attends causally to
+    keys 0 .. L - T + i).  units: optional list of (query row, head) pairs,
+    query row u = s * T + i; default every pair.  Returns float64
+    [n_units][D] (or q's shape when units is None).  part_tokens > 0 selects
+    the partitioned-with-merge form of the same definition."""
     a, keep = _args(k_pool, v_pool, block_table, seq_lens, q, hkv, block_size, k_type, v_type,
                     scale)
     S, hq, d = keep[0].shape
@@ -234,7 +242,7 @@ def decode(k_pool, v_pool, block_table, seq_lens, q, *, hkv: int, block_size: in
                                _ptr(out), int(n_threads))
     if rc != OR_OK:
         raise OracleError(rc)
-    return out.reshape(S, hq, d) if full else out
+    return out.reshape(np.shape(q)) if full else out
 
 
 def merge(o_bits: np.ndarray, ml: np.ndarray, n_live: np.ndarray) -> np.ndarray:

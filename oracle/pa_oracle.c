@@ -303,11 +303,27 @@ typedef struct {
     const int32_t *block_table; /* [n_seqs][table_stride] */
     uint32_t table_stride;
     const int32_t *seq_lens;    /* [n_seqs] */
-    const float *q;             /* [n_seqs][hq][d] float32 */
+    const float *q;             /* [n_seqs][q_tokens][hq][d] float32 */
     double scale;
     uint32_t n_seqs, hq, hkv, d, block_size;
     int32_t k_type, v_type;
+    uint32_t q_tokens;          /* query tokens per sequence (0 is read as 1) */
 } or_args;
+
+/* Query rows.  With T query tokens per sequence ("TensorFold pull 1418",
+ * What: several query rows of a sequence -- a prompt chunk or a verify window
+ * -- attend over the same paged cache), query row u is token i = u % T of
+ * sequence s = u / T, at position L_s - T + i, and attends causally to the
+ * keys 0 .. L_s - T + i: its length is L_s - T + 1 + i (none when that is not
+ * positive).  T = 1 is the one-token decode step. */
+static uint32_t n_tokens(const or_args *a) { return a->q_tokens > 1 ? a->q_tokens : 1; }
+
+static uint32_t row_len(const or_args *a, uint32_t u)
+{
+    uint32_t T = n_tokens(a);
+    int64_t L = (int64_t)a->seq_lens[u / T] - (int64_t)(T - 1 - u % T);
+    return L > 0 ? (uint32_t)L : 0;
+}
 
 static int check_args(const or_args *a)
 {
@@ -323,9 +339,9 @@ static int check_args(const or_args *a)
 
 /* The query row that the dot products use: fp32 Q for F16 K, otherwise the
  * dequantised q8_1 quantisation of Q (quantised here by the oracle itself). */
-static void query_row(const or_args *a, uint32_t s, uint32_t h, double *qhat)
+static void query_row(const or_args *a, uint32_t u, uint32_t h, double *qhat)
 {
-    const float *qr = a->q + ((uint64_t)s * a->hq + h) * a->d;
+    const float *qr = a->q + ((uint64_t)u * a->hq + h) * a->d;
     if (a->k_type == OR_F16) {
         for (uint32_t i = 0; i < a->d; ++i)
             qhat[i] = (double)qr[i];
@@ -337,11 +353,12 @@ static void query_row(const or_args *a, uint32_t s, uint32_t h, double *qhat)
     }
 }
 
-/* Resolve token t of sequence s to the byte offset of its kv_head row; -1 on
- * a table entry outside the pool. */
-static int token_row(const or_args *a, uint32_t s, uint32_t t, uint32_t g,
+/* Resolve token t of the sequence of query row u to the byte offset of its
+ * kv_head row; -1 on a table entry outside the pool. */
+static int token_row(const or_args *a, uint32_t u, uint32_t t, uint32_t g,
                      uint64_t row_bytes, uint64_t *off)
 {
+    uint32_t s = u / n_tokens(a);
     int32_t blk = a->block_table[(uint64_t)s * a->table_stride + t / a->block_size];
     if (blk < 0 || (uint64_t)blk >= a->n_pool_blocks)
         return -1;
@@ -368,14 +385,14 @@ static int scores(const or_args *a, uint32_t s, uint32_t h, const double *qhat,
     return OR_OK;
 }
 
-/* One (sequence, query head) unit: out[d] = sum_t softmax(s)_t * vhat_t. */
+/* One (query row, query head) unit: out[d] = sum_t softmax(s)_t * vhat_t. */
 static int decode_unit(const or_args *a, uint32_t s, uint32_t h, double *out)
 {
-    uint32_t L = (uint32_t)a->seq_lens[s];
+    uint32_t L = row_len(a, s);
     uint32_t D = a->d;
     for (uint32_t i = 0; i < D; ++i)
         out[i] = 0.0;
-    if (a->seq_lens[s] <= 0)
+    if (L == 0)
         return OR_OK; /* empty sequence: zero output */
     double *qhat = (double *)malloc(sizeof(double) * D);
     double *row = (double *)malloc(sizeof(double) * D);
@@ -416,7 +433,7 @@ static int decode_unit(const or_args *a, uint32_t s, uint32_t h, double *out)
 static int decode_unit_partitioned(const or_args *a, uint32_t s, uint32_t h,
                                    uint32_t part_tokens, double *out)
 {
-    uint32_t L = (uint32_t)(a->seq_lens[s] > 0 ? a->seq_lens[s] : 0);
+    uint32_t L = row_len(a, s);
     uint32_t D = a->d;
     for (uint32_t i = 0; i < D; ++i)
         out[i] = 0.0;
@@ -484,7 +501,7 @@ done:
 
 typedef struct {
     const or_args *a;
-    const int32_t *units; /* pairs (seq, head) */
+    const int32_t *units; /* pairs (query row, head) */
     int64_t n_units;
     uint32_t part_tokens; /* 0 = single pass */
     double *out;          /* [n_units][d] */
@@ -506,7 +523,7 @@ static void *worker(void *arg)
         uint32_t h = (uint32_t)j->units[2 * u + 1];
         double *o = j->out + (size_t)u * j->a->d;
         int rc;
-        if (s >= j->a->n_seqs || h >= j->a->hq)
+        if (s >= j->a->n_seqs * n_tokens(j->a) || h >= j->a->hq)
             rc = OR_ERR_INVALID;
         else if (j->part_tokens)
             rc = decode_unit_partitioned(j->a, s, h, j->part_tokens, o);
@@ -521,7 +538,8 @@ static void *worker(void *arg)
     return NULL;
 }
 
-/* Decode the listed (seq, head) units; part_tokens = 0 for the single-pass
+/* Decode the listed (query row, head) units (the query row is the sequence
+ * when there is one query token); part_tokens = 0 for the single-pass
  * definition, otherwise the partitioned form with that partition length. */
 int or_decode_units(const or_args *a, const int32_t *units, int64_t n_units,
                     uint32_t part_tokens, double *out, int n_threads)
@@ -610,8 +628,12 @@ int or_vmax_units(const or_args *a, const int32_t *units, int64_t n_units, doubl
     double mx = 0.0;
     for (int64_t u = 0; u < n_units; ++u) {
         uint32_t s = (uint32_t)units[2 * u], h = (uint32_t)units[2 * u + 1];
+        if (s >= a->n_seqs * n_tokens(a) || h >= a->hq) {
+            free(row);
+            return OR_ERR_INVALID;
+        }
         uint32_t g = h / (a->hq / a->hkv);
-        int32_t L = a->seq_lens[s];
+        int32_t L = (int32_t)row_len(a, s);
         for (int32_t t = 0; t < L; ++t) {
             uint64_t off;
             if (token_row(a, s, (uint32_t)t, g, vrb, &off)) {

@@ -258,3 +258,86 @@ def test_merge_dead_and_single_partials():
     assert np.array_equal(got[0], row.astype(np.float64))
     assert np.all(got[1] == 0.0)
     assert np.all(got[2] == 2.0)
+
+
+# ------------------------------------------------- several query tokens
+
+def _query_rows_of(case, q_hd):
+    """float64 [hq, D] query rows as the oracle uses them (q8_1 for a
+    quantised K)."""
+    sp = case.spec
+    if sp.k_type == synth.F16:
+        return q_hd.astype(np.float64)
+    blocks = oracle.quantize_q8_1(q_hd)
+    return np.stack([oracle.dequant_q8_1_row(blocks[h], sp.d) for h in range(sp.hq)])
+
+
+def causal_sdpa_reference(case, q4):
+    """torch SDPA in float64 for T query tokens per sequence: token i sits at
+    position L - T + i and sees the keys 0 .. L - T + i (a boolean mask); a
+    token with no key gives 0."""
+    sp = case.spec
+    G, T = sp.hq // sp.hkv, q4.shape[1]
+    out = np.zeros((sp.n_seqs, T, sp.hq, sp.d))
+    for s in range(sp.n_seqs):
+        L = sp.seq_lens[s]
+        if L == 0:
+            continue
+        k = torch.from_numpy(dequant_seq(case, s, "k")).permute(1, 0, 2).repeat_interleave(G, 0)
+        v = torch.from_numpy(dequant_seq(case, s, "v")).permute(1, 0, 2).repeat_interleave(G, 0)
+        q = torch.from_numpy(np.stack([_query_rows_of(case, q4[s, i]) for i in range(T)], 1))
+        mask = torch.tensor([[t <= L - T + i for t in range(L)] for i in range(T)])
+        o = torch.nn.functional.scaled_dot_product_attention(
+            q.unsqueeze(0), k.unsqueeze(0), v.unsqueeze(0), attn_mask=mask,
+            scale=1.0 / np.sqrt(sp.d))[0].permute(1, 0, 2).numpy()   # [T, hq, D]
+        for i in range(T):
+            if L - T + i >= 0:
+                out[s, i] = o[i]
+    return out
+
+
+MULTI = [
+    (dict(seq_lens=[40, 2, 0, 17], k_type=synth.F16, v_type=synth.F16, junk=3, d=64, hq=4,
+          hkv=2), 3),
+    (dict(seq_lens=[50, 5], k_type=synth.Q8_0, v_type=synth.Q4_0, junk=2, d=64, hq=6, hkv=3,
+          block_size=32), 4),
+    (dict(seq_lens=[33], k_type=synth.Q4_0, v_type=synth.F16, d=32, hq=2, hkv=1), 7),
+]
+
+
+@pytest.mark.parametrize("kw,T", MULTI)
+def test_oracle_several_query_tokens_match_causal_sdpa(kw, T):
+    case = synth.build_case(synth.CaseSpec(**kw), seed=21)
+    q4 = np.random.default_rng(4).standard_normal((case.spec.n_seqs, T, case.spec.hq,
+                                                   case.spec.d)).astype(np.float32)
+    k, v, bt, sl, _ = _np(case)
+    sp = case.spec
+    got = oracle.decode(k, v, bt, sl, q4, hkv=sp.hkv, block_size=sp.block_size,
+                        k_type=sp.k_type, v_type=sp.v_type)
+    assert got.shape == q4.shape
+    np.testing.assert_allclose(got, causal_sdpa_reference(case, q4), rtol=1e-12, atol=1e-12)
+    # partitioned form of the same rows
+    got_p = oracle.decode(k, v, bt, sl, q4, hkv=sp.hkv, block_size=sp.block_size,
+                          k_type=sp.k_type, v_type=sp.v_type, part_tokens=16)
+    np.testing.assert_allclose(got_p, got, rtol=1e-12, atol=1e-12)
+
+
+def test_query_token_i_is_the_one_token_step_on_the_prefix():
+    kw, T = MULTI[0]
+    case = synth.build_case(synth.CaseSpec(**kw), seed=22)
+    sp = case.spec
+    q4 = np.random.default_rng(5).standard_normal((sp.n_seqs, T, sp.hq, sp.d)).astype(np.float32)
+    k, v, bt, sl, _ = _np(case)
+    got = oracle.decode(k, v, bt, sl, q4, hkv=sp.hkv, block_size=sp.block_size,
+                        k_type=sp.k_type, v_type=sp.v_type)
+    for i in range(T):
+        li = np.maximum(sl - (T - 1 - i), 0).astype(np.int32)
+        one = oracle.decode(k, v, bt, li, q4[:, i], hkv=sp.hkv, block_size=sp.block_size,
+                            k_type=sp.k_type, v_type=sp.v_type)
+        assert np.array_equal(got[:, i], one)
+    # one token in the 4-D form is the plain step
+    one = oracle.decode(k, v, bt, sl, q4[:, :1], hkv=sp.hkv, block_size=sp.block_size,
+                        k_type=sp.k_type, v_type=sp.v_type)
+    ref = oracle.decode(k, v, bt, sl, q4[:, 0], hkv=sp.hkv, block_size=sp.block_size,
+                        k_type=sp.k_type, v_type=sp.v_type)
+    assert np.array_equal(one[:, 0], ref)
