@@ -144,6 +144,13 @@ int pa_quantize_q(const float *q, void *q8_1, uint32_t n_rows, uint32_t d, pa_st
  *    float32 [n_seqs][hq][n_parts][2] (0 bytes when direct);
  *  - counter_bytes = 4 * n_seqs * (1 + ceil(sqrt(n_parts))), the int32
  *    completion counters of the fused merge (0 when direct).
+ * Several query tokens ([P2] What: a prompt chunk or a verify window of
+ * several query rows per sequence over one paged cache): with q_tokens = T,
+ * query token i of sequence s sits at position L_s - T + i and attends to the
+ * keys 0 .. L_s - T + i.  The rule then runs over the n_seqs * T query rows
+ * (row u = s * T + i, of length L_s - T + 1 + i) with T * total_len tokens of
+ * work: every n_seqs above reads n_seqs * T and total_len reads T * total_len;
+ * max_len and n_parts are per row.
  * Limits: block_size 16 or 32, d 128 or 256, hq a multiple of hkv with
  * hq / hkv <= 8, total_len <= n_seqs * max_len.  PA_ERR_INVALID otherwise. */
 typedef struct {
@@ -153,12 +160,14 @@ typedef struct {
     pa_type k_type, v_type;
     int32_t sm_count, ctas_per_sm;
     int32_t force_parts;         /* 0 = automatic */
+    uint32_t q_tokens;           /* query tokens per sequence (0 or 1: one; see below) */
 } pa_plan_in;
 
 typedef struct {
     uint32_t part_tokens, n_parts, direct, n_ctas;
     uint64_t part_o_bytes, part_ml_bytes;
     uint64_t counter_bytes;      /* completion counters of pa_decode_fused (0 when direct) */
+    uint32_t q_tokens;           /* query tokens per sequence (>= 1) */
 } pa_plan_t;
 
 int pa_plan(const pa_plan_in *in, pa_plan_t *out);
@@ -183,19 +192,24 @@ int pa_query_occupancy(const pa_plan_in *in, int32_t *sm_count, int32_t *ctas_pe
  * A block id outside [0, n_pool_blocks) is never dereferenced: the kernel
  * sets PA_STATUS_CORRUPT_TABLE in *status and treats that block's tokens as
  * absent (pa_status_read reports it).  Pool offsets are 64-bit throughout:
- * pools past 2^32 elements are supported. */
+ * pools past 2^32 elements are supported.
+ * With plan->q_tokens = T > 1 ([P2] What) every sequence has T query tokens:
+ * q, out and the partials hold n_seqs * T query rows (row s * T + i, token i
+ * of sequence s, at position L_s - T + i, attending to the keys 0 .. L_s - T
+ * + i); the block table and lengths stay per sequence.  A row with no key
+ * gives O = 0. */
 typedef struct {
     const void *k_pool, *v_pool;     /* device, token-major pools, 16-byte aligned */
     uint64_t n_pool_blocks;          /* 1 .. 2^31 */
     const int32_t *block_table;      /* device int32 [n_seqs][table_stride] */
     uint32_t table_stride;
     const int32_t *seq_lens;         /* device int32 [n_seqs], 0 <= L <= table_stride*block_size */
-    const void *q;                   /* device: float32 [n_seqs][hq][d] for F16 K,
-                                        q8_1 [n_seqs][hq][d/32] otherwise */
+    const void *q;                   /* device: float32 [n_seqs][T][hq][d] for F16 K,
+                                        q8_1 [n_seqs][T][hq][d/32] otherwise (T = q_tokens) */
     float scale;                     /* softmax scale; callers pass 1/sqrt(d) */
-    void *part_o;                    /* device f16 [n_seqs][hq][n_parts][d] (unused if direct) */
-    float *part_ml;                  /* device float32 [n_seqs][hq][n_parts][2] */
-    float *out;                      /* device float32 [n_seqs][hq][d], 16-byte aligned
+    void *part_o;                    /* device f16 [n_seqs*T][hq][n_parts][d] (unused if direct) */
+    float *part_ml;                  /* device float32 [n_seqs*T][hq][n_parts][2] */
+    float *out;                      /* device float32 [n_seqs][T][hq][d], 16-byte aligned
                                         (written if direct or fused) */
     int32_t *status;                 /* device int32 status word (required) */
     uint32_t n_seqs, hq, hkv, d, block_size;

@@ -24,7 +24,11 @@ frozen here so that the C++ planner can be compared with it exactly:
 - an empty batch (max_len == 0) is direct with part_tokens = 32;
 - the fused merge keeps 1 + ceil(sqrt(n_parts)) int32 completion counters
   per sequence (one for the last pass, one per group of the two-pass merge):
-  counter_bytes = 4 * S * (1 + ceil(sqrt(n_parts))), 0 when direct.
+  counter_bytes = 4 * S * (1 + ceil(sqrt(n_parts))), 0 when direct;
+- with q_tokens = T > 1 (several query tokens per sequence, each a query
+  row of its own that attends causally) the rule runs over the S * T query
+  rows with T * total_len tokens of work: every S above reads S * T and
+  total_len reads T * total_len.
 """
 import math
 
@@ -43,7 +47,7 @@ def _roundup(a: int, b: int) -> int:
 
 
 def plan(*, n_seqs, max_len, total_len, block_size, hq, hkv, d, k_type, v_type,
-         sm_count, ctas_per_sm, force_parts=0):
+         sm_count, ctas_per_sm, force_parts=0, q_tokens=1):
     """Returns (rc, dict).  dict keys: part_tokens, n_parts, direct, n_ctas,
     part_o_bytes, part_ml_bytes, counter_bytes."""
     if (n_seqs < 1 or block_size not in (16, 32) or hkv < 1 or hq < hkv or hq % hkv
@@ -52,6 +56,10 @@ def plan(*, n_seqs, max_len, total_len, block_size, hq, hkv, d, k_type, v_type,
             or force_parts < 0 or max_len < 0 or total_len < max_len
             or total_len > n_seqs * max_len):
         return INVALID, None
+    T = max(1, q_tokens)
+    if T > 4096:
+        return INVALID, None
+    rows, work = n_seqs * T, T * total_len   # query rows and their work at most
     if max_len == 0:
         part, n_parts = TILE, 1
     elif force_parts > 0:
@@ -59,17 +67,17 @@ def plan(*, n_seqs, max_len, total_len, block_size, hq, hkv, d, k_type, v_type,
         n_parts = _cdiv(max_len, part)
     else:
         slots = sm_count * ctas_per_sm
-        part = max(MIN_PART, _roundup(_cdiv(total_len, slots), TILE))
+        part = max(MIN_PART, _roundup(_cdiv(work, slots), TILE))
         part = min(part, _roundup(max_len, TILE))
         n_parts = _cdiv(max_len, part)
     direct = 1 if n_parts == 1 else 0
     if direct:
-        n_ctas = n_seqs
+        n_ctas = rows
         po = pm = cb = 0
     else:
-        n_ctas = min(n_seqs * n_parts, _cdiv(total_len, part) + n_seqs)
-        po = n_seqs * hq * n_parts * d * 2
-        pm = n_seqs * hq * n_parts * 8
-        cb = 4 * n_seqs * (1 + math.isqrt(n_parts - 1) + 1)
+        n_ctas = min(rows * n_parts, _cdiv(work, part) + rows)
+        po = rows * hq * n_parts * d * 2
+        pm = rows * hq * n_parts * 8
+        cb = 4 * rows * (1 + math.isqrt(n_parts - 1) + 1)
     return OK, dict(part_tokens=part, n_parts=n_parts, direct=direct, n_ctas=n_ctas,
-                    part_o_bytes=po, part_ml_bytes=pm, counter_bytes=cb)
+                    part_o_bytes=po, part_ml_bytes=pm, counter_bytes=cb, q_tokens=T)

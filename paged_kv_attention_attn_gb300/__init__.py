@@ -39,14 +39,14 @@ class PlanIn(ctypes.Structure):
                 ("hq", ctypes.c_uint32), ("hkv", ctypes.c_uint32), ("d", ctypes.c_uint32),
                 ("k_type", ctypes.c_int), ("v_type", ctypes.c_int),
                 ("sm_count", ctypes.c_int32), ("ctas_per_sm", ctypes.c_int32),
-                ("force_parts", ctypes.c_int32)]
+                ("force_parts", ctypes.c_int32), ("q_tokens", ctypes.c_uint32)]
 
 
 class Plan(ctypes.Structure):
     _fields_ = [("part_tokens", ctypes.c_uint32), ("n_parts", ctypes.c_uint32),
                 ("direct", ctypes.c_uint32), ("n_ctas", ctypes.c_uint32),
                 ("part_o_bytes", ctypes.c_uint64), ("part_ml_bytes", ctypes.c_uint64),
-                ("counter_bytes", ctypes.c_uint64)]
+                ("counter_bytes", ctypes.c_uint64), ("q_tokens", ctypes.c_uint32)]
 
     def as_dict(self):
         return {k: int(getattr(self, k)) for k, _ in self._fields_}
@@ -223,7 +223,8 @@ def query_occupancy(*, hq, hkv, d, block_size, k_type, v_type) -> tuple[int, int
 
 
 def plan(*, seq_lens, block_size, hq, hkv, d, k_type, v_type, sm_count=None,
-         ctas_per_sm=None, force_parts=0) -> Plan:
+         ctas_per_sm=None, force_parts=0, q_tokens=1) -> Plan:
+    """pa_plan for these lengths; q_tokens query tokens per sequence."""
     lens = [int(x) for x in seq_lens]
     if sm_count is None or ctas_per_sm is None:
         sm, cps = query_occupancy(hq=hq, hkv=hkv, d=d, block_size=block_size, k_type=k_type,
@@ -232,6 +233,7 @@ def plan(*, seq_lens, block_size, hq, hkv, d, k_type, v_type, sm_count=None,
         ctas_per_sm = cps if ctas_per_sm is None else ctas_per_sm
     pin = _plan_in(len(lens), max(lens) if lens else 0, sum(lens), block_size, hq, hkv, d,
                    k_type, v_type, sm_count, ctas_per_sm, force_parts)
+    pin.q_tokens = int(q_tokens)
     out = Plan()
     _check(lib().pa_plan(ctypes.byref(pin), ctypes.byref(out)))
     return out
@@ -263,21 +265,26 @@ class Workspace:
 
 
 def workspace(pl: Plan, *, n_seqs, hq, d, device) -> Workspace:
+    """Buffers of one step: out float32 [S, hq, d], or [S, T, hq, d] for a
+    plan with T > 1 query tokens per sequence; partials per query row."""
     P = 0 if pl.direct else int(pl.n_parts)
+    T = max(1, int(pl.q_tokens))
+    rows = n_seqs * T
+    lead = (n_seqs,) if T == 1 else (n_seqs, T)
     return Workspace(
         plan=pl,
-        out=torch.zeros((n_seqs, hq, d), dtype=torch.float32, device=device),
-        part_o=torch.empty((n_seqs, hq, P, d), dtype=torch.float16, device=device),
-        part_ml=torch.empty((n_seqs, hq, P, 2), dtype=torch.float32, device=device),
+        out=torch.zeros(lead + (hq, d), dtype=torch.float32, device=device),
+        part_o=torch.empty((rows, hq, P, d), dtype=torch.float16, device=device),
+        part_ml=torch.empty((rows, hq, P, 2), dtype=torch.float32, device=device),
         status=torch.zeros(1, dtype=torch.int32, device=device),
-        q8_1=torch.empty((n_seqs, hq, d // 32 * 36), dtype=torch.uint8, device=device),
+        q8_1=torch.empty(lead + (hq, d // 32 * 36), dtype=torch.uint8, device=device),
         counters=torch.zeros(max(1, int(pl.counter_bytes) // 4), dtype=torch.int32,
                              device=device))
 
 
 def make_args(*, k_pool, v_pool, block_table, seq_lens, q, ws: Workspace, hkv, block_size,
               k_type, v_type, scale=None, flags=0) -> DecodeArgs:
-    S, hq, d = ws.out.shape
+    S, hq, d = ws.out.shape[0], ws.out.shape[-2], ws.out.shape[-1]
     return DecodeArgs(k_pool=_ptr(k_pool), v_pool=_ptr(v_pool), n_pool_blocks=k_pool.shape[0],
                       block_table=_ptr(block_table), table_stride=block_table.shape[1],
                       seq_lens=_ptr(seq_lens), q=_ptr(q),

@@ -1017,24 +1017,27 @@ __global__ void __launch_bounds__(T::kMaxWarps * 32, 1)
 
     uint32_t seq, part;
     if (!p.direct && blockIdx.x == gridDim.x - 1 && warp == 0)
-        check_grid_vs_plan(p.seq_lens, p.n_seqs, p.part_tokens, p.n_parts, p.status);
+        check_grid_vs_plan(p.seq_lens, p.q_tokens, p.n_seqs, p.part_tokens, p.n_parts,
+                           p.status);
     if (p.direct) {
         seq = blockIdx.x;
         part = 0;
-    } else if (!cta_work(p.seq_lens, p.n_seqs, p.part_tokens, p.n_parts, blockIdx.x, &seq,
-                         &part)) {
+    } else if (!cta_work(p.seq_lens, p.q_tokens, p.n_seqs, p.part_tokens, p.n_parts,
+                         blockIdx.x, &seq, &part)) {
         return;  // past the last live partition: nothing was issued
     } else if (part == 0 && tid == 0) {
-        check_len_vs_plan(p.seq_lens[seq], p.n_parts, p.part_tokens, p.status);
+        check_len_vs_plan(row_len(p.seq_lens, p.q_tokens, seq), p.n_parts, p.part_tokens,
+                          p.status);
     }
-    const int32_t L = p.seq_lens[seq] > 0 ? p.seq_lens[seq] : 0;
+    const int32_t Lrow = row_len(p.seq_lens, p.q_tokens, seq);
+    const int32_t L = Lrow > 0 ? Lrow : 0;
     const uint32_t t0 = p.direct ? 0u : part * p.part_tokens;
     const uint32_t t1 = p.direct ? (uint32_t)L : min((uint32_t)L, t0 + p.part_tokens);
     const uint32_t n_tiles = (t1 - t0 + kTile - 1) / kTile;
     const int gid = lane >> 2, tig = lane & 3;
     const uint32_t g = warp % hkv, sub = warp / hkv;
     const uint32_t n_my = n_tiles > sub ? (n_tiles - sub + wph - 1) / wph : 0;
-    const int32_t *bt = p.block_table + (uint64_t)seq * p.table_stride;
+    const int32_t *bt = p.block_table + (uint64_t)table_row(p.q_tokens, seq) * p.table_stride;
     const CUtensorMap *tmk = &a.tm[0][g], *tmv = &a.tm[1][g];
     // V rows of a slot start here: the slot's middle for one type on both
     // sides, the padded K size for a mixed pair

@@ -214,22 +214,25 @@ __global__ void __launch_bounds__(kPlainWarps * 32) plain_decode_kernel(const De
 
     uint32_t s, part;
     if (!p.direct && blockIdx.x == gridDim.x - 1 && warp == 0)
-        check_grid_vs_plan(p.seq_lens, p.n_seqs, p.part_tokens, p.n_parts, p.status);
+        check_grid_vs_plan(p.seq_lens, p.q_tokens, p.n_seqs, p.part_tokens, p.n_parts,
+                           p.status);
     if (p.direct) {
         s = blockIdx.x;
         part = 0;
         if (s >= p.n_seqs)
             return;
-    } else if (!cta_work(p.seq_lens, p.n_seqs, p.part_tokens, p.n_parts, blockIdx.x, &s,
-                         &part)) {
+    } else if (!cta_work(p.seq_lens, p.q_tokens, p.n_seqs, p.part_tokens, p.n_parts,
+                         blockIdx.x, &s, &part)) {
         return;
     } else if (part == 0 && threadIdx.x == 0) {
-        check_len_vs_plan(p.seq_lens[s], p.n_parts, p.part_tokens, p.status);
+        check_len_vs_plan(row_len(p.seq_lens, p.q_tokens, s), p.n_parts, p.part_tokens,
+                          p.status);
     }
-    const int32_t L = p.seq_lens[s] > 0 ? p.seq_lens[s] : 0;
+    const int32_t Lrow = row_len(p.seq_lens, p.q_tokens, s);
+    const int32_t L = Lrow > 0 ? Lrow : 0;
     const uint32_t t0 = p.direct ? 0u : part * p.part_tokens;
     const uint32_t t1 = p.direct ? (uint32_t)L : min((uint32_t)L, t0 + p.part_tokens);
-    const int32_t *bt = p.block_table + (uint64_t)s * p.table_stride;
+    const int32_t *bt = p.block_table + (uint64_t)table_row(p.q_tokens, s) * p.table_stride;
     const uint32_t G = p.hq / p.hkv;
 
     for (uint32_t h = warp; h < p.hq; h += nwarps) {
@@ -366,14 +369,14 @@ int launch_plain_decode(const DecodeParams &p, pa_type kt, pa_type vt, cudaStrea
 __global__ void __launch_bounds__(128) merge_kernel(const __half *__restrict__ po,
                                                     const float2 *__restrict__ pml,
                                                     const int32_t *__restrict__ seq_lens,
-                                                    float *__restrict__ out, uint32_t hq,
-                                                    uint32_t D, uint32_t n_parts,
+                                                    float *__restrict__ out, uint32_t T,
+                                                    uint32_t hq, uint32_t D, uint32_t n_parts,
                                                     uint32_t part_tokens, uint64_t units)
 {
     const uint64_t sh = (uint64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     if (sh >= units)
         return;
-    const int32_t L = seq_lens[sh / hq];
+    const int32_t L = row_len(seq_lens, T, (uint32_t)(sh / hq));
     uint32_t n_live = L > 0 ? ((uint32_t)L + part_tokens - 1) / part_tokens : 0;
     if (n_live > n_parts)
         n_live = n_parts;
@@ -390,10 +393,11 @@ __global__ void __launch_bounds__(128) merge_kernel(const __half *__restrict__ p
 }
 
 int launch_merge(const void *part_o, const float *part_ml, const int32_t *seq_lens, float *out,
-                 uint32_t n_seqs, uint32_t hq, uint32_t d, uint32_t n_parts,
+                 uint32_t n_seqs, uint32_t q_tokens, uint32_t hq, uint32_t d, uint32_t n_parts,
                  uint32_t part_tokens, cudaStream_t st, const char *entry)
 {
-    uint64_t units = (uint64_t)n_seqs * hq;
+    const uint32_t T = q_tokens > 1 ? q_tokens : 1;
+    uint64_t units = (uint64_t)n_seqs * T * hq;
     if (units == 0)
         return PA_OK;
     if ((units + 3) / 4 > 0x7fffffffull)
@@ -402,7 +406,7 @@ int launch_merge(const void *part_o, const float *part_ml, const int32_t *seq_le
         return fail(PA_ERR_INVALID, entry, "d %u unsupported by the merge (128 or 256)", d);
     merge_kernel<<<(unsigned)((units + 3) / 4), 128, 0, st>>>(
         static_cast<const __half *>(part_o), reinterpret_cast<const float2 *>(part_ml), seq_lens,
-        out, hq, d, n_parts, part_tokens, units);
+        out, T, hq, d, n_parts, part_tokens, units);
     return cuda_check(cudaGetLastError(), entry, "merge_kernel launch");
 }
 

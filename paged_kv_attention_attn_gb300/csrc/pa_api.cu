@@ -63,8 +63,11 @@ int resolve(const pa_decode_args *a, const pa_plan_t *plan, const char *E, pa::D
         return fail(PA_ERR_INVALID, E, "part_o must be 16-byte and part_ml 8-byte aligned");
     if (a->out && (reinterpret_cast<uintptr_t>(a->out) & 15))
         return fail(PA_ERR_INVALID, E, "out must be 16-byte aligned");
-    if (plan->direct && plan->n_ctas != a->n_seqs)
-        return fail(PA_ERR_INVALID, E, "direct plan must have n_ctas == n_seqs");
+    const uint32_t T = plan->q_tokens > 1 ? plan->q_tokens : 1;
+    if ((uint64_t)a->n_seqs * T > 0x7fffffffull)
+        return fail(PA_ERR_RANGE, E, "n_seqs * q_tokens exceeds 2^31 - 1");
+    if (plan->direct && plan->n_ctas != a->n_seqs * T)
+        return fail(PA_ERR_INVALID, E, "direct plan must have n_ctas == n_seqs * q_tokens");
     if (a->table_stride == 0)
         return fail(PA_ERR_INVALID, E, "table_stride is 0");
     if (a->n_pool_blocks == 0 || a->n_pool_blocks > 0x80000000ull)
@@ -83,7 +86,8 @@ int resolve(const pa_decode_args *a, const pa_plan_t *plan, const char *E, pa::D
     p->part_ml = a->part_ml;
     p->out = a->out;
     p->status = a->status;
-    p->n_seqs = a->n_seqs;
+    p->n_seqs = a->n_seqs * T;  // query rows
+    p->q_tokens = T;
     p->hq = a->hq;
     p->hkv = a->hkv;
     p->d = a->d;
@@ -223,7 +227,7 @@ extern "C" int pa_decode_step_fused(const pa_decode_args *args, const pa_plan_t 
             return launch_decode(args, p, st, E);
         }
         rc = pa::launch_quantize_q(static_cast<const float *>(args->q), q8_1_scratch,
-                                   args->n_seqs * args->hq, args->d, st, E);
+                                   p.n_seqs * args->hq, args->d, st, E);
         if (rc)
             return rc;
         p.q = q8_1_scratch;
@@ -248,12 +252,13 @@ extern "C" int pa_merge(const void *part_o, const float *part_ml, const int32_t 
         return fail(PA_ERR_INVALID, E, "part_o and out must be 16-byte, part_ml 8-byte aligned");
     if (n_seqs == 0 || hq == 0 || (d != 128 && d != 256))
         return fail(PA_ERR_INVALID, E, "bad shape (n_seqs %u, hq %u, d %u)", n_seqs, hq, d);
-    const uint64_t elems = (uint64_t)n_seqs * hq * plan->n_parts * d;
+    const uint64_t T = plan->q_tokens > 1 ? plan->q_tokens : 1;
+    const uint64_t elems = (uint64_t)n_seqs * T * hq * plan->n_parts * d;
     if (elems > (1ull << 40))
         return fail(PA_ERR_RANGE, E, "partial buffer of %llu elements exceeds 2^40",
                     (unsigned long long)elems);
-    return pa::launch_merge(part_o, part_ml, seq_lens, out, n_seqs, hq, d, plan->n_parts,
-                            plan->part_tokens, pa::stream_of(stream), E);
+    return pa::launch_merge(part_o, part_ml, seq_lens, out, n_seqs, plan->q_tokens, hq, d,
+                            plan->n_parts, plan->part_tokens, pa::stream_of(stream), E);
 }
 
 extern "C" int pa_decode_step(const pa_decode_args *args, const pa_plan_t *plan,
@@ -269,7 +274,7 @@ extern "C" int pa_decode_step(const pa_decode_args *args, const pa_plan_t *plan,
         if (!q8_1_scratch || (reinterpret_cast<uintptr_t>(q8_1_scratch) & 15))
             return fail(PA_ERR_INVALID, E, "quantised K needs a 16-byte aligned q8_1_scratch");
         rc = pa::launch_quantize_q(static_cast<const float *>(args->q), q8_1_scratch,
-                                   args->n_seqs * args->hq, args->d, st, E);
+                                   p.n_seqs * args->hq, args->d, st, E);
         if (rc)
             return rc;
         p.q = q8_1_scratch;
@@ -278,8 +283,8 @@ extern "C" int pa_decode_step(const pa_decode_args *args, const pa_plan_t *plan,
     if (rc || plan->direct)
         return rc;
     return pa::launch_merge(args->part_o, args->part_ml, args->seq_lens, args->out,
-                            args->n_seqs, args->hq, args->d, plan->n_parts, plan->part_tokens,
-                            st, E);
+                            args->n_seqs, plan->q_tokens, args->hq, args->d, plan->n_parts,
+                            plan->part_tokens, st, E);
 }
 
 extern "C" int pa_decode_step_host(const float *q_host, float *out_host,
@@ -293,7 +298,7 @@ extern "C" int pa_decode_step_host(const float *q_host, float *out_host,
     int rc = resolve(args, plan, E, &p);  // refuse before copying anything
     if (rc)
         return rc;
-    const size_t bytes = (size_t)args->n_seqs * args->hq * args->d * sizeof(float);
+    const size_t bytes = (size_t)p.n_seqs * args->hq * args->d * sizeof(float);
     cudaStream_t st = pa::stream_of(stream);
     rc = cuda_check(cudaMemcpyAsync(const_cast<void *>(args->q), q_host, bytes,
                                     cudaMemcpyHostToDevice, st),
@@ -321,7 +326,7 @@ extern "C" int pa_decode_step_fused_host(const float *q_host, float *out_host,
         return rc;
     if (!plan->direct && !counters)
         return fail(PA_ERR_INVALID, E, "a partitioned plan needs counters");
-    const size_t bytes = (size_t)args->n_seqs * args->hq * args->d * sizeof(float);
+    const size_t bytes = (size_t)p.n_seqs * args->hq * args->d * sizeof(float);
     cudaStream_t st = pa::stream_of(stream);
     rc = cuda_check(cudaMemcpyAsync(const_cast<void *>(args->q), q_host, bytes,
                                     cudaMemcpyHostToDevice, st),

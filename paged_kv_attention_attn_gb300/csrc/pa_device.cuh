@@ -77,12 +77,29 @@ __device__ __forceinline__ int warp_sum_int(int v)
     return v;
 }
 
+// Query rows.  A plan with T query tokens per sequence decodes n_seqs * T
+// rows; row v is token i = v % T of sequence v / T, at position L - T + i,
+// and attends to the keys 0 .. L - T + i ("TensorFold pull 1418", What:
+// several query rows of a sequence -- a prompt chunk or a verify window --
+// over one paged cache).  With one token the row is the sequence.
+__device__ __forceinline__ int32_t row_len(const int32_t *seq_lens, uint32_t T, uint32_t v)
+{
+    if (T <= 1)
+        return seq_lens[v];
+    const int32_t L = seq_lens[v / T] - (int32_t)(T - 1 - v % T);
+    return L > 0 ? L : 0;
+}
+__device__ __forceinline__ uint32_t table_row(uint32_t T, uint32_t v)
+{
+    return T <= 1 ? v : v / T;
+}
+
 // Maps a CTA of a partitioned decode grid to its (sequence, partition): CTAs
 // enumerate the (s, p) pairs in order of s, then p, where sequence s has
 // min(ceil(L_s / part_tokens), n_parts) live partitions, and an empty
 // sequence (L_s <= 0) one empty partition.  Executed by one full warp; returns false when the CTA
 // index is past the last pair.
-__device__ __forceinline__ bool cta_work(const int32_t *seq_lens, uint32_t n_seqs,
+__device__ __forceinline__ bool cta_work(const int32_t *seq_lens, uint32_t T, uint32_t n_seqs,
                                          uint32_t part_tokens, uint32_t n_parts, uint32_t cta,
                                          uint32_t *seq, uint32_t *part)
 {
@@ -92,7 +109,7 @@ __device__ __forceinline__ bool cta_work(const int32_t *seq_lens, uint32_t n_seq
         uint32_t s = s0 + lane;
         // an empty sequence still gets one CTA, which writes its zero output
         // (or its empty partial, and its arrival at the completion count)
-        const int32_t L = s < n_seqs ? seq_lens[s] : 0;
+        const int32_t L = s < n_seqs ? row_len(seq_lens, T, s) : 0;
         uint32_t n = L > 0 ? ((uint32_t)L + part_tokens - 1) / part_tokens : (s < n_seqs ? 1u : 0u);
         n = n < n_parts ? n : n_parts;  // a sequence longer than the plan is cut
         uint32_t incl = n;
@@ -277,14 +294,14 @@ __device__ __forceinline__ void check_len_vs_plan(int32_t L, uint32_t n_parts,
 // Records lengths that need more (sequence, partition) pairs than the grid has
 // CTAs (the pairs past the grid are left out).  Called by one full warp of the
 // grid's last CTA.
-__device__ __forceinline__ void check_grid_vs_plan(const int32_t *seq_lens, uint32_t n_seqs,
-                                                   uint32_t part_tokens, uint32_t n_parts,
-                                                   int32_t *status)
+__device__ __forceinline__ void check_grid_vs_plan(const int32_t *seq_lens, uint32_t T,
+                                                   uint32_t n_seqs, uint32_t part_tokens,
+                                                   uint32_t n_parts, int32_t *status)
 {
     const int lane = threadIdx.x & 31;
     uint64_t pairs = 0;
     for (uint32_t s = lane; s < n_seqs; s += 32) {
-        const int32_t L = seq_lens[s];
+        const int32_t L = row_len(seq_lens, T, s);
         uint32_t n = L > 0 ? ((uint32_t)L + part_tokens - 1) / part_tokens : 1u;
         pairs += n < n_parts ? n : n_parts;
     }
@@ -389,7 +406,7 @@ template <int BATCH = 8, class P>
 __device__ inline void fused_merge(const P &p, uint32_t seq, uint32_t part, uint32_t warp,
                                    uint32_t nwarps)
 {
-    const int32_t L = p.seq_lens[seq];
+    const int32_t L = row_len(p.seq_lens, p.q_tokens, seq);
     uint32_t n = L > 0 ? ((uint32_t)L + p.part_tokens - 1) / p.part_tokens : 0;
     n = n < p.n_parts ? n : p.n_parts;
     const uint32_t gs = merge_group_size(n), ng = n > gs ? (n + gs - 1) / gs : 1;

@@ -191,6 +191,14 @@ extern "C" int pa_plan(const pa_plan_in *in, pa_plan_t *out)
         return fail(PA_ERR_INVALID, E, "sm_count / ctas_per_sm / force_parts out of range");
     if (in->total_len < in->max_len || in->total_len > (uint64_t)in->n_seqs * in->max_len)
         return fail(PA_ERR_INVALID, E, "total_len inconsistent with max_len and n_seqs");
+    // T query tokens per sequence: n_seqs * T query rows, each at most max_len
+    // long, T * total_len tokens of work at most
+    const uint64_t T = in->q_tokens > 1 ? in->q_tokens : 1;
+    if (T > 4096)
+        return fail(PA_ERR_INVALID, E, "q_tokens %u exceeds 4096", in->q_tokens);
+    const uint64_t rows = (uint64_t)in->n_seqs * T, work = T * in->total_len;
+    if (rows > 0x7fffffffull)
+        return fail(PA_ERR_RANGE, E, "n_seqs * q_tokens exceeds 2^31 - 1");
     uint64_t part, n_parts;
     if (in->max_len == 0) {
         part = TILE;
@@ -200,7 +208,7 @@ extern "C" int pa_plan(const pa_plan_in *in, pa_plan_t *out)
         n_parts = cdiv(in->max_len, part);
     } else {
         uint64_t slots = (uint64_t)in->sm_count * (uint64_t)in->ctas_per_sm;
-        part = roundup(cdiv(in->total_len, slots), TILE);
+        part = roundup(cdiv(work, slots), TILE);
         if (part < MIN_PART) part = MIN_PART;
         uint64_t cap = roundup(in->max_len, TILE);
         if (part > cap) part = cap;
@@ -211,18 +219,19 @@ extern "C" int pa_plan(const pa_plan_in *in, pa_plan_t *out)
     p.part_tokens = (uint32_t)part;
     p.n_parts = (uint32_t)n_parts;
     p.direct = n_parts == 1;
+    p.q_tokens = (uint32_t)T;
     if (p.direct) {
-        p.n_ctas = in->n_seqs;
+        p.n_ctas = (uint32_t)rows;
     } else {
-        uint64_t a = (uint64_t)in->n_seqs * n_parts;
-        uint64_t b = cdiv(in->total_len, part) + in->n_seqs;
+        uint64_t a = rows * n_parts;
+        uint64_t b = cdiv(work, part) + rows;
         uint64_t n = a < b ? a : b;
         if (n > 0x7fffffffull)
             return fail(PA_ERR_RANGE, E, "grid of %llu CTAs exceeds 2^31-1", (unsigned long long)n);
         p.n_ctas = (uint32_t)n;
-        p.part_o_bytes = (uint64_t)in->n_seqs * in->hq * n_parts * in->d * 2ull;
-        p.part_ml_bytes = (uint64_t)in->n_seqs * in->hq * n_parts * 8ull;
-        p.counter_bytes = (uint64_t)in->n_seqs * pa::merge_counters_per_seq((uint32_t)n_parts) * 4ull;
+        p.part_o_bytes = rows * in->hq * n_parts * in->d * 2ull;
+        p.part_ml_bytes = rows * in->hq * n_parts * 8ull;
+        p.counter_bytes = rows * pa::merge_counters_per_seq((uint32_t)n_parts) * 4ull;
     }
     *out = p;
     return PA_OK;

@@ -64,7 +64,8 @@ extern "C" int pa_decode_step_noalloc(const pa_decode_args *args, const pa_plan_
     if (plan->n_parts == 0 || plan->direct != (plan->n_parts == 1u))
         return pa::fail(PA_ERR_INVALID, E, "inconsistent plan");
     const bool quantised = args->k_type != PA_F16;
-    const uint64_t rows = (uint64_t)args->n_seqs * args->hq;
+    const uint64_t rows = (uint64_t)args->n_seqs * (plan->q_tokens > 1 ? plan->q_tokens : 1) *
+                          args->hq;
     const uint64_t q81_bytes = quantised ? round256(rows * (args->d / 32) * 36ull) : 0;
     const uint64_t po_bytes = plan->direct ? 0 : round256(rows * plan->n_parts * args->d * 2ull);
     const uint64_t pm_bytes = plan->direct ? 0 : round256(rows * plan->n_parts * 8ull);
@@ -88,8 +89,8 @@ extern "C" int pa_decode_step_noalloc(const pa_decode_args *args, const pa_plan_
     // q8_1 block, and the merge reads only partitions the decode kernel wrote
     // in this same step.
     if (quantised) {
-        rc = pa_quantize_q(static_cast<const float *>(args->q), s, args->n_seqs * args->hq,
-                           args->d, stream);
+        rc = pa_quantize_q(static_cast<const float *>(args->q), s, (uint32_t)rows, args->d,
+                           stream);
         if (rc)
             return rc;
         a.q = s;

@@ -1,0 +1,81 @@
+"""Several query tokens per sequence (a verify window or prompt chunk over the
+paged cache, TensorFold pull 1418, What): token i of sequence s sits at
+position L - T + i and attends causally to the keys 0 .. L - T + i.  The CUDA
+path is checked against the oracle's causal form for both kernels, every
+mode, plain and mixed K/V types, and the paged layout against a contiguous
+layout of the same cache bit for bit."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_attention_attn_gb300 as pa
+import synth
+from tests import helpers as H
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+KERNELS = {"fast": 0, "plain": pa.PA_FLAG_PLAIN}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from paged_kv_attention_attn_gb300 import build
+    build.build()
+    oracle.build()
+
+
+def _q4(spec, T, seed):
+    g = torch.Generator().manual_seed(seed)
+    return torch.randn(spec.n_seqs, T, spec.hq, spec.d, generator=g).to(DEV)
+
+
+def _plan(spec, T, force):
+    return pa.plan(seq_lens=spec.seq_lens, block_size=spec.block_size, hq=spec.hq,
+                   hkv=spec.hkv, d=spec.d, k_type=spec.k_type, v_type=spec.v_type,
+                   force_parts=force, q_tokens=T)
+
+
+def _oracle(case, q4):
+    k, v, bt, sl, _ = H.host_inputs(case)
+    return oracle.decode(k, v, bt, sl, q4.cpu().numpy(), **H.oracle_kw(case.spec))
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("kt,vt", [(synth.F16, synth.F16), (synth.Q4_0, synth.Q4_0),
+                                   (synth.Q8_0, synth.Q4_0)])
+@pytest.mark.parametrize("T", [2, 5])
+def test_several_query_tokens_match_the_oracle(kernel, kt, vt, T):
+    spec = synth.CaseSpec(seq_lens=[700, 3, 0, 130, 16], k_type=kt, v_type=vt, junk=3)
+    case = synth.build_case(spec, seed=3300 + 10 * kt + vt, device=DEV)
+    q4 = _q4(spec, T, 3400 + T)
+    ref = _oracle(case, q4)
+    vmax = H.oracle_vmax(case)
+    outs = []
+    for force in (0, 1, 4):
+        pl = _plan(spec, T, force)
+        assert pl.q_tokens == T
+        for fused in (False, True):
+            out, ws, _, _ = H.run(case, plan=pl, q=q4, flags=KERNELS[kernel], fused=fused,
+                                  out_fill=float("nan"))
+            assert pa.status_read(ws.status) == 0
+            assert tuple(out.shape) == (spec.n_seqs, T, spec.hq, spec.d)
+            H.assert_close(case, out, ref, vmax)
+            outs.append(out.clone())
+            assert int(ws.counters.abs().sum()) == 0
+    # the fused and separate merges agree bit for bit in each plan
+    for a, b in zip(outs[0::2], outs[1::2]):
+        assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_several_query_tokens_paged_equals_contiguous(kernel):
+    spec = synth.CaseSpec(seq_lens=[1000, 257, 64], k_type=synth.Q4_0, v_type=synth.Q4_0,
+                          junk=6)
+    case = synth.build_case(spec, seed=3500, device=DEV)
+    twin = synth.contiguous_twin(case)
+    q4 = _q4(spec, 4, 3501)
+    pl = _plan(spec, 4, 3)
+    a, _, _, _ = H.run(case, plan=pl, q=q4, flags=KERNELS[kernel], fused=True)
+    b, _, _, _ = H.run(twin, plan=pl, q=q4, flags=KERNELS[kernel], fused=True)
+    assert torch.equal(a.view(torch.int32), b.view(torch.int32))

@@ -108,7 +108,7 @@ def test_plan_matches_model():
                   hkv=rng.choice([4, 8, 1]), d=rng.choice([128, 256, 64]),
                   k_type=rng.choice([0, 1, 2]), v_type=rng.choice([0, 1, 2]),
                   sm_count=rng.choice([152, 148, 1]), ctas_per_sm=rng.choice([1, 2]),
-                  force_parts=rng.choice([0, 0, 3, 64]))
+                  force_parts=rng.choice([0, 0, 3, 64]), q_tokens=rng.choice([1, 1, 2, 5]))
         mrc, mp = plan_model.plan(**kw)
         pin = pa.PlanIn(**kw)
         out = pa.Plan()

@@ -96,24 +96,26 @@ def test_plan_covers_every_token_and_bounds_the_grid():
         lens = [rng.choice([0, 1, 15, 16, 17, 200, rng.randint(0, 300000)]) for _ in range(S)]
         mx, tot = max(lens), sum(lens)
         force = rng.choice([0, 0, 1, 2, 7, 1000])
+        T = rng.choice([1, 1, 2, 6])
         rc, p = _plan(n_seqs=S, max_len=mx, total_len=tot, force_parts=force,
                       block_size=rng.choice([16, 32]), sm_count=rng.choice([1, 152, 160]),
-                      ctas_per_sm=rng.choice([1, 2, 3]))
+                      ctas_per_sm=rng.choice([1, 2, 3]), q_tokens=T)
         assert rc == plan_model.OK
         P, n = p["part_tokens"], p["n_parts"]
         assert P % 32 == 0 and P > 0
         assert n * P >= mx and (n - 1) * P < max(mx, 1)
         assert p["direct"] == (n == 1)
-        # the grid has a CTA for every live partition and one for every empty
-        # sequence (which writes that sequence's zero output)
-        live = sum(max(1, math.ceil(L / P)) for L in lens)
-        assert p["n_ctas"] >= (S if p["direct"] else live)
-        assert p["n_ctas"] <= S * n
+        # the grid has a CTA for every live partition of every query row and
+        # one for every empty row (which writes its zero output)
+        rows = [max(0, L - (T - 1 - i)) for L in lens for i in range(T)]
+        live = sum(max(1, math.ceil(L / P)) for L in rows)
+        assert p["n_ctas"] >= (S * T if p["direct"] else live)
+        assert p["n_ctas"] <= S * T * n
         if force:
             assert n <= force
         if not p["direct"]:
-            assert p["part_o_bytes"] == S * 24 * n * 256 * 2
-            assert p["part_ml_bytes"] == S * 24 * n * 8
+            assert p["part_o_bytes"] == S * T * 24 * n * 256 * 2
+            assert p["part_ml_bytes"] == S * T * 24 * n * 8
 
 
 def test_plan_worked_examples():
