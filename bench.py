@@ -55,6 +55,7 @@ WORKLOADS = {
        for kn, kt in (("f16", synth.F16), ("q8_0", synth.Q8_0), ("q4_0", synth.Q4_0))
        for vn, vt in (("f16", synth.F16), ("q8_0", synth.Q8_0), ("q4_0", synth.Q4_0))
        if kt != vt},
+    "verify-q4_0-b8x32768-T4": synth.verify_spec,
     "tiny-f16-L200": synth.tiny_spec,
     "largepool-f16-b16x300000": synth.large_pool_spec,
 }
@@ -76,21 +77,23 @@ def algorithmic_bytes(spec, plan, fused: bool = True, in_kernel_q: bool = False)
     with in-kernel quantisation it reads the float32 query and there is no
     pre-pass."""
     S, hq, d = spec.n_seqs, spec.hq, spec.d
+    T = int(spec.extra.get("q_tokens", 1))
     krb, vrb = synth.row_bytes(spec.k_type, d), synth.row_bytes(spec.v_type, d)
     lens = spec.seq_lens
-    kv = sum(lens) * spec.hkv * (krb + vrb)
+    kv = sum(lens) * spec.hkv * (krb + vrb)   # once: a sequence's query rows share them
     table = sum(math.ceil(L / spec.block_size) for L in lens) * 4
-    q_f32 = S * hq * d * 4
-    q81 = S * hq * d // 32 * 36
+    rows = [max(0, L - (T - 1 - i)) for L in lens for i in range(T)]
+    q_f32 = S * T * hq * d * 4
+    q81 = S * T * hq * d // 32 * 36
     quantised = spec.k_type != synth.F16
     prepass = (q_f32 + q81) if quantised and not in_kernel_q else 0
     q_read = q81 if quantised and not in_kernel_q else q_f32
-    out = S * hq * d * 4
+    out = S * T * hq * d * 4
     if plan.direct:
         part_w = part_r = 0
         dec_out = out
     else:
-        live = sum(math.ceil(L / plan.part_tokens) for L in lens)
+        live = sum(math.ceil(L / plan.part_tokens) for L in rows)
         part_w = part_r = live * hq * (2 * d + 8)
         dec_out = part_w
     merge = 0 if plan.direct else part_r + out + S * 4
@@ -218,8 +221,9 @@ def oracle_sample(case_host, spec, seqs, threads, group=None):
     import oracle
     k, v, bt, sl, q = case_host
     G = spec.hq // spec.hkv
+    T = int(spec.extra.get("q_tokens", 1))
     heads = range(spec.hq) if group is None else range(group * G, (group + 1) * G)
-    units = [(s, h) for s in seqs for h in heads]
+    units = [(s * T + i, h) for s in seqs for i in range(T) for h in heads]
     t0 = time.perf_counter()
     oracle.decode(k, v, bt, sl, q, hkv=spec.hkv, block_size=spec.block_size,
                   k_type=spec.k_type, v_type=spec.v_type, units=units, n_threads=threads)
@@ -290,7 +294,8 @@ def run_ours(a, world, rank, local):
     if a.workload.endswith("-contiguous"):
         case = synth.contiguous_twin(case)
     flags = pa.PA_FLAG_PLAIN if a.plain else 0
-    pl = pa.plan(seq_lens=spec.seq_lens, block_size=spec.block_size, hq=spec.hq, hkv=spec.hkv,
+    pl = pa.plan(q_tokens=int(spec.extra.get("q_tokens", 1)),
+                 seq_lens=spec.seq_lens, block_size=spec.block_size, hq=spec.hq, hkv=spec.hkv,
                  d=spec.d, k_type=spec.k_type, v_type=spec.v_type)
     ws = pa.workspace(pl, n_seqs=spec.n_seqs, hq=spec.hq, d=spec.d, device=dev)
     args = pa.make_args(k_pool=case.k_pool, v_pool=case.v_pool, block_table=case.block_table,
@@ -329,7 +334,7 @@ def run_ours(a, world, rank, local):
                 ev1.record(stream)
             return rc
         if quantised:
-            L.pa_quantize_q(case.q.data_ptr(), ws.q8_1.data_ptr(), spec.n_seqs * spec.hq,
+            L.pa_quantize_q(case.q.data_ptr(), ws.q8_1.data_ptr(), case.q.numel() // spec.d,
                             spec.d, sh)
         if ev0 is not None:
             ev0.record(stream)

@@ -135,7 +135,11 @@ int pa_quantize_q(const float *q, void *q8_1, uint32_t n_rows, uint32_t d, pa_st
  *  - partitions are multiples of 32 tokens;
  *  - force_parts > 0: part_tokens = roundup(ceil(max_len / force_parts), 32);
  *  - else part_tokens = roundup(ceil(total_len / (sm_count * ctas_per_sm)),
- *    32), clamped to [128, roundup(max_len, 32)];
+ *    32), clamped to [128, roundup(max_len, 32)]; a nearly uniform batch
+ *    (10 * total_len >= 9 * n_seqs * max_len) with n_seqs <= slots whose
+ *    n_seqs * ceil(max_len / part_tokens) would exceed the slots takes
+ *    roundup(ceil(max_len / floor(slots / n_seqs)), 32) instead, within the
+ *    same bounds (one wave of CTAs);
  *  - n_parts = ceil(max_len / part_tokens); direct = (n_parts == 1): no
  *    partials, the decode kernel writes the output;
  *  - n_ctas = n_seqs when direct, else min(n_seqs * n_parts,

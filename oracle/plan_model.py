@@ -12,7 +12,11 @@ frozen here so that the C++ planner can be compared with it exactly:
 - forced: part_tokens = roundup(ceil(max_len / force_parts), 32);
 - otherwise the total live work is spread over the resident CTA slots:
   part_tokens = roundup(ceil(total_len / (sm_count * ctas_per_sm)), 32),
-  at least MIN_PART = 128 tokens and at most roundup(max_len, 32);
+  at least MIN_PART = 128 tokens and at most roundup(max_len, 32); when the
+  batch is nearly uniform (10 * total_len >= 9 * S * max_len), S <= slots,
+  and S * ceil(max_len / part_tokens) would exceed the slots, it is instead
+  roundup(ceil(max_len / floor(slots / S)), 32) within the same bounds, so
+  that the CTAs fit one wave;
 - n_parts = ceil(max_len / part_tokens) (partition slots per sequence, the
   partial buffers' second dimension); a sequence of length L has
   ceil(L / part_tokens) live partitions;
@@ -69,6 +73,10 @@ def plan(*, n_seqs, max_len, total_len, block_size, hq, hkv, d, k_type, v_type,
         slots = sm_count * ctas_per_sm
         part = max(MIN_PART, _roundup(_cdiv(work, slots), TILE))
         part = min(part, _roundup(max_len, TILE))
+        if (rows * _cdiv(max_len, part) > slots and rows <= slots
+                and 10 * work >= 9 * rows * max_len):
+            part = max(MIN_PART, _roundup(_cdiv(max_len, slots // rows), TILE))
+            part = min(part, _roundup(max_len, TILE))
         n_parts = _cdiv(max_len, part)
     direct = 1 if n_parts == 1 else 0
     if direct:

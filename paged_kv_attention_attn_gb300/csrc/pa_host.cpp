@@ -212,6 +212,14 @@ extern "C" int pa_plan(const pa_plan_in *in, pa_plan_t *out)
         if (part < MIN_PART) part = MIN_PART;
         uint64_t cap = roundup(in->max_len, TILE);
         if (part > cap) part = cap;
+        // a nearly uniform batch whose rows would round up to more CTAs than
+        // slots takes partitions that fit every row's share into one wave
+        if (rows * cdiv(in->max_len, part) > slots && rows <= slots &&
+            10 * work >= 9 * rows * (uint64_t)in->max_len) {
+            part = roundup(cdiv(in->max_len, slots / rows), TILE);
+            if (part < MIN_PART) part = MIN_PART;
+            if (part > cap) part = cap;
+        }
         n_parts = cdiv(in->max_len, part);
     }
     pa_plan_t p;

@@ -202,7 +202,10 @@ def build_case(spec: CaseSpec, seed: int, device="cpu", chunk_blocks: int = 2048
             last = int(table[s, nbs[s] - 1])
             k_pool[last, L % B:] = POISON
             v_pool[last, L % B:] = POISON
-    q = source_values(gen, (S, spec.hq, spec.d), device, False)
+    # T query tokens per sequence (spec.extra["q_tokens"]): q is [S, T, hq, d]
+    T = int(spec.extra.get("q_tokens", 1))
+    q = source_values(gen, (S, spec.hq, spec.d) if T == 1 else (S, T, spec.hq, spec.d), device,
+                      False)
     lens = torch.tensor(spec.seq_lens, dtype=torch.int32)
     return Case(spec=spec, k_pool=k_pool, v_pool=v_pool, block_table=table.to(device),
                 seq_lens=lens.to(device), q=q, seed=seed)
@@ -292,6 +295,14 @@ def dtype_sweep_spec(type_: int, short: bool = False, v_type: int | None = None)
     pair = TYPE_LABEL[type_] if vt == type_ else f"{TYPE_LABEL[type_]}-{TYPE_LABEL[vt]}"
     return CaseSpec(seq_lens=lens, k_type=type_, v_type=vt, outliers=True,
                     name=f"sweep-{pair}-{tag}")
+
+
+def verify_spec(n_seqs: int = 8, ctx: int = 32768, T: int = 4, type_: int = Q4_0) -> CaseSpec:
+    """A verify window: T query tokens per sequence (token i at position
+    ctx - T + i attends to the keys up to its own position) over uniform
+    contexts, Q4_0 K/V at the Qwen attention dims."""
+    return CaseSpec(seq_lens=[ctx] * n_seqs, k_type=type_, v_type=type_,
+                    name=f"verify-{TYPE_LABEL[type_]}-b{n_seqs}x{ctx}-T{T}", extra={"q_tokens": T})
 
 
 def large_pool_spec(n_seqs: int = 16, ctx: int = 300_000) -> CaseSpec:

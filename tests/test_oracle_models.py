@@ -126,6 +126,13 @@ def test_plan_worked_examples():
     rc, p = _plan(n_seqs=8, max_len=131072, total_len=131072 + 7 * 8192)
     assert p["part_tokens"] == 1248 and p["n_parts"] == 106
     assert sum(math.ceil(L / 1248) for L in [131072] + [8192] * 7) <= p["n_ctas"] == 159
+    # a nearly uniform batch that would spill past one wave fits it instead:
+    # 3 x 100000 rounds to 51 partitions each (153 CTAs), one wave takes 50
+    rc, p = _plan(n_seqs=3, max_len=100000, total_len=300000)
+    assert (p["part_tokens"], p["n_parts"], p["n_ctas"]) == (2016, 50, 150)
+    # a verify window of 4 tokens on 8 x 32768: 32 query rows in one wave
+    rc, p = _plan(n_seqs=8, max_len=32768, total_len=8 * 32768, q_tokens=4)
+    assert (p["part_tokens"], p["n_parts"], p["n_ctas"]) == (8192, 4, 128)
     # a batch at least as wide as the machine runs direct
     rc, p = _plan(n_seqs=512, max_len=4096, total_len=512 * 4096)
     assert p["direct"] == 1 and p["n_ctas"] == 512
