@@ -145,6 +145,11 @@ __device__ __forceinline__ void ldsm_x4_trans(uint32_t (&r)[4], uint32_t addr)
 __device__ __forceinline__ uint32_t h2_bits(__half2 h) { return *reinterpret_cast<uint32_t *>(&h); }
 __device__ __forceinline__ __half2 bits_h2(uint32_t u) { return *reinterpret_cast<__half2 *>(&u); }
 
+__device__ __forceinline__ uint32_t hadd2_bits(uint32_t x, uint32_t y)
+{
+    return h2_bits(__hadd2(bits_h2(x), bits_h2(y)));
+}
+
 __device__ __forceinline__ uint32_t hmul2_bits(uint32_t x, uint32_t y)
 {
     return h2_bits(__hmul2(bits_h2(x), bits_h2(y)));
@@ -503,12 +508,15 @@ struct Q40T {
             const uint32_t xcd = __byte_perm(uc, ud, 0x5410), ycd = xcd >> 8;
             const uint32_t b0 = hmul2_bits(p0, lds_u32(scr + DV + 2 * (b * kTile + 2 * tig)));
             const uint32_t b1 = hmul2_bits(p1, lds_u32(scr + DV + 2 * (b * kTile + 8 + 2 * tig)));
-            mma16816(o[2 * b], and_or(xab, K.mlo, K.blo), and_or(yab, K.mlo, K.blo),
-                     and_or(xcd, K.mlo, K.blo), and_or(ycd, K.mlo, K.blo), b0, b1);
-            mma16816(o[2 * b], K.nlo[0], K.nlo[1], K.nlo[2], K.nlo[3], b0, b1);
-            mma16816(o[2 * b + 1], and_or(xab, K.mhi, K.bhi), and_or(yab, K.mhi, K.bhi),
-                     and_or(xcd, K.mhi, K.bhi), and_or(ycd, K.mhi, K.bhi), b0, b1);
-            mma16816(o[2 * b + 1], K.nhi[0], K.nhi[1], K.nhi[2], K.nhi[3], b0, b1);
+            // (1024 + n) - 1032 and (64 + n) - 72 are n - 8 exactly
+            mma16816(o[2 * b], hadd2_bits(and_or(xab, K.mlo, K.blo), K.nlo[0]),
+                     hadd2_bits(and_or(yab, K.mlo, K.blo), K.nlo[1]),
+                     hadd2_bits(and_or(xcd, K.mlo, K.blo), K.nlo[2]),
+                     hadd2_bits(and_or(ycd, K.mlo, K.blo), K.nlo[3]), b0, b1);
+            mma16816(o[2 * b + 1], hadd2_bits(and_or(xab, K.mhi, K.bhi), K.nhi[0]),
+                     hadd2_bits(and_or(yab, K.mhi, K.bhi), K.nhi[1]),
+                     hadd2_bits(and_or(xcd, K.mhi, K.bhi), K.nhi[2]),
+                     hadd2_bits(and_or(ycd, K.mhi, K.bhi), K.nhi[3]), b0, b1);
         }
     }
 
