@@ -20,8 +20,9 @@
 // in registers: Q4_0 nibbles with one LOP3 per two values (OR-ed into the
 // mantissa of 1024 or 64: bias + nibble exactly), Q8_0 codes straight into
 // the integer tensor path for scores and into biased f16 for PV.  The biases
-// are removed by the accumulator's start value (scores) or one constant-A MMA
-// (PV), and block scales multiply the block dots (K) or the probabilities (V).
+// are removed by the accumulator's start value (scores), by an exact f16
+// subtraction from the operands (Q4_0 PV) or by a constant-A MMA (Q8_0 PV),
+// and block scales multiply the block dots (K) or the probabilities (V).
 //
 // Sources: "feat: add paged-attention monolithic decode-only AR foundation"
 // (lucebox pull 555), Summary -- one pass over each K/V row serves all query
@@ -207,7 +208,7 @@ __device__ __forceinline__ uint32_t and_or(uint32_t x, uint32_t m, uint32_t c)
 // Register constants of the Q4_0 nibble expansion: masks and f16 biases.
 struct NibbleConsts {
     uint32_t mlo, mhi, blo, bhi;  // 0x000F000F, 0x00F000F0, f16 1024 | 1024, f16 64 | 64
-    uint32_t nlo[4], nhi[4];      // A quads of -1032 and -72 (f16 pairs)
+    uint32_t nlo[4], nhi[4];      // -1032 and -72 (f16 pairs): 1024 + n or 64 + n to n - 8
     __device__ __forceinline__ void init()
     {
         mlo = opaque(0x000F000Fu);
@@ -492,9 +493,8 @@ struct Q40T {
     }
 
     // O += V^T P' over the tile, P' = P * d_v per block.  The V operand is the
-    // nibble read as 1024 + n (low nibbles) or 64 + n (high nibbles); a second
-    // MMA with every A entry -1032 (or -72) adds -(bias + 8) * sum_t P', so the
-    // two together contribute sum_t (n - 8) P'.
+    // nibble read as 1024 + n (low nibbles) or 64 + n (high nibbles) minus
+    // 1032 (or 72): n - 8 exactly, one HADD2 per two values.
     __device__ static void pv(const NibbleConsts &K, float (&o)[MT][4], uint32_t vh, uint32_t scr,
                               uint32_t p0, uint32_t p1, int gid, int tig)
     {
@@ -745,6 +745,9 @@ struct Q80T {
                 // [a.dim0, a.dim1, b.dim0, b.dim1], each code flipped to c + 128
                 const uint32_t xab = __byte_perm(ua, ub, 0x5410) ^ K.flip;
                 const uint32_t xcd = __byte_perm(uc, ud, 0x5410) ^ K.flip;
+                // the bias 1152 comes off in a second MMA with a constant A
+                // (for Q8_0 this keeps more time than the operand subtraction
+                // that Q4_0 uses)
                 float(&acc)[4] = o[2 * b + hh];
                 mma16816(acc, __byte_perm(xab, K.f16hi, 0x4240), __byte_perm(xab, K.f16hi, 0x4341),
                          __byte_perm(xcd, K.f16hi, 0x4240), __byte_perm(xcd, K.f16hi, 0x4341),
