@@ -364,3 +364,30 @@ def test_fused_merge_waits_for_every_partition(kernel, force):
         torch.cuda.synchronize()
         assert torch.equal(ws.out.view(torch.int32), ref.view(torch.int32))
         assert int(ws.counters.abs().sum()) == 0
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("t", TYPES)
+def test_sharp_softmax(kernel, t):
+    """Query norms six times the unit draws: scores spread over tens of log2
+    units, so nearly every probability, and its product with a V block scale,
+    lies deep below the maximum, many in the f16 subnormal range."""
+    spec = synth.CaseSpec(seq_lens=[3000, 517, 16], k_type=t, v_type=t, outliers=True,
+                          name=f"sharp-{t}")
+    case = synth.build_case(spec, seed=1400 + t, device=DEV)
+    case.q.mul_(6.0)
+    out, ws, pl, _ = H.run(case, flags=KERNELS[kernel])
+    assert pa.status_read(ws.status) == 0
+    H.assert_close(case, out, H.oracle_out(case), H.oracle_vmax(case))
+
+
+@pytest.mark.parametrize("t", TYPES)
+def test_long_single_partition(t):
+    """One partition of 40000 tokens: every warp of the fast kernel folds
+    more than 800 tiles into one accumulator."""
+    spec = synth.CaseSpec(seq_lens=[40000], k_type=t, v_type=t, outliers=True,
+                          name=f"long-{t}")
+    case = synth.build_case(spec, seed=1500 + t, device=DEV)
+    out, ws, pl, _ = H.run(case, force_parts=1)
+    assert pa.status_read(ws.status) == 0
+    H.assert_close(case, out, H.oracle_out(case), H.oracle_vmax(case))
