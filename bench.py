@@ -60,6 +60,8 @@ WORKLOADS = {
     "largepool-f16-b16x300000": synth.large_pool_spec,
 }
 DEFAULT_WORKLOAD = "uniform-q4_0-b8x131072"
+L2_BYTES = 129 * 10**6        # GB300 L2
+FLUSH_BYTES = 512 * 2**20     # the write that evicts it between timed steps
 L2_BYTES = 129 * 2**20
 
 
@@ -359,8 +361,24 @@ def run_ours(a, world, rank, local):
     torch.cuda.synchronize()
 
     K = a.steps
+    # K/V smaller than twice the L2: a write of FLUSH_BYTES between steps
+    # evicts it, and a read of the same buffer then writes the dirty lines
+    # back, so that the step starts on a clean L2 holding none of its inputs;
+    # only the steps themselves are timed (events around each)
+    flush = a.flush == "on" or (a.flush == "auto" and nb["kv"] < 2 * L2_BYTES)
+    flush_buf = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev) if flush else None
+
+    def flush_l2(k):
+        flush_buf.fill_(k & 0xFF)
+        flush_buf.view(torch.int32).sum()
+    # one launch per step and nothing between steps: the launches run back to
+    # back and the decode time is the timed region over K; otherwise events
+    # bracket the decode launch of every step
+    per_launch = flush or not in_kernel_q
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(K)]
+           for _ in range(K)] if per_launch else None
+    sevs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            for _ in range(K)] if flush else None
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(local)
     clocks.start()
@@ -369,17 +387,26 @@ def run_ours(a, world, rank, local):
     torch.cuda.synchronize()
     start.record(stream)
     for k in range(K):
-        step(*evs[k])
+        if flush:
+            flush_l2(k)
+            sevs[k][0].record(stream)
+        if per_launch:
+            step(*evs[k])
+        else:
+            step()
+        if flush:
+            sevs[k][1].record(stream)
     end.record(stream)
     torch.cuda.synchronize()
     barrier(world)
     clk = clocks.stop()
     total_ms = start.elapsed_time(end)
-    dec_ms = [e0.elapsed_time(e1) for e0, e1 in evs]
-    max_s = reduce_max(total_ms / 1e3, world, dev)
+    step_ms = sum(e0.elapsed_time(e1) for e0, e1 in sevs) if flush else total_ms
+    max_s = reduce_max(step_ms / 1e3, world, dev)
     value = aggregate(nb["step"], K, world, max_s)
     ms_per_step = max_s * 1e3 / K
-    dec_avg_ms = sum(dec_ms) / K
+    dec_avg_ms = (sum(e0.elapsed_time(e1) for e0, e1 in evs) / K if per_launch
+                  else total_ms / K)
     peak, peak_kind = load_peaks()
     dec_achieved = nb["decode"] / (dec_avg_ms / 1e3) / 1e9
 
@@ -396,14 +423,22 @@ def run_ours(a, world, rank, local):
         e2e_call(q_host, out_host, e2e_args, ws)
     torch.cuda.synchronize()
     barrier(world)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(K):
-        e2e_call(q_host, out_host, e2e_args, ws)
-    e1.record(stream)
+    e2e_evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(K if flush else 1)]
+    if flush:  # every call timed alone, after the L2 flush
+        for k in range(K):
+            flush_l2(k)
+            e2e_evs[k][0].record(stream)
+            e2e_call(q_host, out_host, e2e_args, ws)
+            e2e_evs[k][1].record(stream)
+    else:
+        e2e_evs[0][0].record(stream)
+        for _ in range(K):
+            e2e_call(q_host, out_host, e2e_args, ws)
+        e2e_evs[0][1].record(stream)
     torch.cuda.synchronize()
     barrier(world)
-    e2e_s = reduce_max(e0.elapsed_time(e1) / 1e3, world, dev)
+    e2e_s = reduce_max(sum(e0.elapsed_time(e1) for e0, e1 in e2e_evs) / 1e3, world, dev)
     h2d = q_host.numel() * 4
     d2h = out_host.numel() * 4
     e2e = {"value": aggregate(nb["step"], K, world, e2e_s), "unit": "GB/s",
@@ -436,7 +471,13 @@ def run_ours(a, world, rank, local):
                    "context": max(spec.seq_lens), "d": spec.d, "hq": spec.hq,
                    "hkv": spec.hkv, "block_size": spec.block_size,
                    "kv_type": synth.TYPE_LABEL[spec.k_type],
-                   "l2": f"inputs larger than L2: {nb['kv'] / 1e9:.3f} GB of K/V per step",
+                   "l2": (f"L2 flushed between steps by a {FLUSH_BYTES >> 20} MiB write and read; "
+                          f"{nb['kv'] / 1e9:.3f} GB of K/V per step" if flush else
+                          f"inputs larger than L2: {nb['kv'] / 1e9:.3f} GB of K/V per step"
+                          if nb["kv"] >= L2_BYTES else
+                          f"L2 not flushed: {nb['kv'] / 1e9:.3f} GB of K/V per step"),
+                   "timing": ("events around each step" if per_launch else
+                              "back-to-back launches, events around the timed region"),
                    "kernel": kname, "plan": pl.as_dict(),
                    "step": ("one launch: in-kernel q8_1 quantisation, decode, in-launch merge"
                             if in_kernel_q else
@@ -470,6 +511,8 @@ def main():
     ap.add_argument("--unfused", action="store_true",
                     help="time the three-launch step (separate merge) instead of the fused one")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--flush", choices=["auto", "on", "off"], default="auto",
+                    help="L2 flush between timed steps (auto: when K/V < 2 x L2)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="oracle work timed for cpu_baseline (whole sequences in turn)")
     a = ap.parse_args()
