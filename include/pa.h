@@ -139,7 +139,11 @@ int pa_quantize_q(const float *q, void *q8_1, uint32_t n_rows, uint32_t d, pa_st
  *    (10 * total_len >= 9 * n_seqs * max_len) with n_seqs <= slots whose
  *    n_seqs * ceil(max_len / part_tokens) would exceed the slots takes
  *    roundup(ceil(max_len / floor(slots / n_seqs)), 32) instead, within the
- *    same bounds (one wave of CTAs);
+ *    same bounds (one wave of CTAs); then any plan of more than one
+ *    partition per sequence with n_seqs < slots whose grid bound (n_ctas
+ *    below) would exceed the slots takes part_tokens =
+ *    roundup(ceil(total_len / (slots - n_seqs)), 32) if that is larger (at
+ *    most roundup(max_len, 32)), so that the grid fits one wave;
  *  - n_parts = ceil(max_len / part_tokens); direct = (n_parts == 1): no
  *    partials, the decode kernel writes the output;
  *  - n_ctas = n_seqs when direct, else min(n_seqs * n_parts,

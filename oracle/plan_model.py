@@ -17,6 +17,11 @@ frozen here so that the C++ planner can be compared with it exactly:
   and S * ceil(max_len / part_tokens) would exceed the slots, it is instead
   roundup(ceil(max_len / floor(slots / S)), 32) within the same bounds, so
   that the CTAs fit one wave;
+- then, if the partitions are still more than one per sequence, S < slots,
+  and the grid bound min(S * n_parts, ceil(total_len / part_tokens) + S)
+  (below) would exceed the slots, part_tokens grows to
+  roundup(ceil(total_len / (slots - S)), 32) (at most roundup(max_len, 32)),
+  so that the bound, and so the grid, fits one wave;
 - n_parts = ceil(max_len / part_tokens) (partition slots per sequence, the
   partial buffers' second dimension); a sequence of length L has
   ceil(L / part_tokens) live partitions;
@@ -77,6 +82,10 @@ def plan(*, n_seqs, max_len, total_len, block_size, hq, hkv, d, k_type, v_type,
                 and 10 * work >= 9 * rows * max_len):
             part = max(MIN_PART, _roundup(_cdiv(max_len, slots // rows), TILE))
             part = min(part, _roundup(max_len, TILE))
+        np_ = _cdiv(max_len, part)
+        if np_ > 1 and min(rows * np_, _cdiv(work, part) + rows) > slots and rows < slots:
+            part = max(part, min(_roundup(_cdiv(work, slots - rows), TILE),
+                                 _roundup(max_len, TILE)))
         n_parts = _cdiv(max_len, part)
     direct = 1 if n_parts == 1 else 0
     if direct:

@@ -220,6 +220,15 @@ extern "C" int pa_plan(const pa_plan_in *in, pa_plan_t *out)
             if (part < MIN_PART) part = MIN_PART;
             if (part > cap) part = cap;
         }
+        // any other batch whose grid bound would pass the slots: partitions
+        // long enough that ceil(work / part) + rows CTAs fit one wave
+        const uint64_t np = cdiv(in->max_len, part);
+        const uint64_t bound = rows * np < cdiv(work, part) + rows ? rows * np
+                                                                   : cdiv(work, part) + rows;
+        if (np > 1 && bound > slots && rows < slots) {
+            const uint64_t wide = roundup(cdiv(work, slots - rows), TILE);
+            if (wide > part) part = wide < cap ? wide : cap;
+        }
         n_parts = cdiv(in->max_len, part);
     }
     pa_plan_t p;

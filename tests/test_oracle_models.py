@@ -97,9 +97,10 @@ def test_plan_covers_every_token_and_bounds_the_grid():
         mx, tot = max(lens), sum(lens)
         force = rng.choice([0, 0, 1, 2, 7, 1000])
         T = rng.choice([1, 1, 2, 6])
+        sm, cps = rng.choice([1, 152, 160]), rng.choice([1, 2, 3])
         rc, p = _plan(n_seqs=S, max_len=mx, total_len=tot, force_parts=force,
-                      block_size=rng.choice([16, 32]), sm_count=rng.choice([1, 152, 160]),
-                      ctas_per_sm=rng.choice([1, 2, 3]), q_tokens=T)
+                      block_size=rng.choice([16, 32]), sm_count=sm, ctas_per_sm=cps,
+                      q_tokens=T)
         assert rc == plan_model.OK
         P, n = p["part_tokens"], p["n_parts"]
         assert P % 32 == 0 and P > 0
@@ -113,6 +114,9 @@ def test_plan_covers_every_token_and_bounds_the_grid():
         assert p["n_ctas"] <= S * T * n
         if force:
             assert n <= force
+        elif not p["direct"] and S * T < sm * cps:
+            # fewer query rows than slots: the grid fits one wave
+            assert p["n_ctas"] <= sm * cps
         if not p["direct"]:
             assert p["part_o_bytes"] == S * T * 24 * n * 256 * 2
             assert p["part_ml_bytes"] == S * T * 24 * n * 8
@@ -122,10 +126,13 @@ def test_plan_worked_examples():
     # uniform 8 x 128K on 152 SMs: the live work spread over one wave
     rc, p = _plan(n_seqs=8, max_len=131072, total_len=8 * 131072)
     assert (p["part_tokens"], p["n_parts"], p["n_ctas"]) == (6912, 19, 152)
-    # ragged 128K + 7 x 8K: partitions sized by total work, not by the longest sequence
+    # ragged 128K + 7 x 8K: partitions sized by total work, not by the longest
+    # sequence; 1248 tokens (the work over 152 slots) would bound the grid at
+    # 151 + 8 = 159 CTAs, a second wave, so they grow to ceil(188416 / 144)
+    # rounded to 1312: at most 144 + 8 = 152 CTAs (149 live)
     rc, p = _plan(n_seqs=8, max_len=131072, total_len=131072 + 7 * 8192)
-    assert p["part_tokens"] == 1248 and p["n_parts"] == 106
-    assert sum(math.ceil(L / 1248) for L in [131072] + [8192] * 7) <= p["n_ctas"] == 159
+    assert p["part_tokens"] == 1312 and p["n_parts"] == 100
+    assert sum(math.ceil(L / 1312) for L in [131072] + [8192] * 7) == 149 <= p["n_ctas"] == 152
     # a nearly uniform batch that would spill past one wave fits it instead:
     # 3 x 100000 rounds to 51 partitions each (153 CTAs), one wave takes 50
     rc, p = _plan(n_seqs=3, max_len=100000, total_len=300000)
