@@ -114,6 +114,24 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, i
         : "memory");
 }
 
+// One contiguous global range into shared memory (both 16-byte aligned, bytes
+// a multiple of 16), completing on the mbarrier.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes,
+                                          uint64_t *bar)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// Generic-proxy writes to global memory (other CTAs' partials, seen through
+// an acquire) before this thread's later bulk copies read them.
+__device__ __forceinline__ void fence_proxy_async_global()
+{
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 __device__ __forceinline__ void fence_proxy_async()
 {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -330,6 +348,7 @@ struct Q40T {
     static constexpr uint32_t kTmaX = 1;    // TMA boxes per (side, head)
     static constexpr uint32_t kMaxWarps = KMAXW;
     static constexpr int kMergeBatch = 8;
+    static constexpr bool kStagedMerge = true;
 
     static __host__ __device__ constexpr uint32_t side_bytes(uint32_t hkv)
     {
@@ -553,6 +572,7 @@ struct Q80T {
     static constexpr uint32_t kTmaX = 1;
     static constexpr uint32_t kMaxWarps = KMAXW;
     static constexpr int kMergeBatch = 12;
+    static constexpr bool kStagedMerge = true;
 
     static __host__ __device__ constexpr uint32_t side_bytes(uint32_t hkv)
     {
@@ -780,6 +800,7 @@ struct F16T {
     static constexpr uint32_t kTmaX = NC;
     static constexpr uint32_t kMaxWarps = 8;
     static constexpr int kMergeBatch = 12;
+    static constexpr bool kStagedMerge = true;
 
     static __host__ __device__ constexpr uint32_t side_bytes(uint32_t hkv)
     {
@@ -901,6 +922,7 @@ struct Mix {
         KT::kMaxWarps < VT::kMaxWarps ? KT::kMaxWarps : VT::kMaxWarps;
     static constexpr int kMergeBatch =
         KT::kMergeBatch < VT::kMergeBatch ? KT::kMergeBatch : VT::kMergeBatch;
+    static constexpr bool kStagedMerge = false;  // one instance per mixed pair
     static constexpr uint32_t kSideK = KT::kSideK, kSideV = VT::kSideV;
     static constexpr uint32_t kTmaXK = KT::kTmaXK, kTmaXV = VT::kTmaXV;
     static constexpr uint32_t kRowK = KT::kRowK, kRowV = VT::kRowV;
@@ -990,9 +1012,102 @@ __device__ __forceinline__ void combine_and_write(const DecodeParams &p, const f
                                                   uint32_t hkv, uint32_t wph, uint32_t G,
                                                   uint32_t seq, uint32_t part);
 
+// One row of the in-launch merge by one warp from partials staged in shared
+// memory: m partials of D halves at po (global; partial k at po + k * stride
+// * D) and their (m, l) at pml (stride likewise).  Lane 0 copies the m rows
+// into this warp's stage with bulk copies on the warp's mbarrier (parity
+// `phase`, flipped here), the lanes fetch the (m, l) meanwhile, and then the
+// weighted sum runs from shared memory.  The arithmetic is that of
+// merge_rows_warp_v for m <= 32 (weight of partial k in lane k, warp sums,
+// partials added in order), so the results are the same bits.  False if a
+// copy did not land in time (status flagged; nothing written).
+template <bool kPartial>
+__device__ bool merge_row_staged(const DecodeParams &p, const __half *po, const float2 *pml,
+                                 uint32_t m, uint32_t stride, uint32_t stage, uint64_t *bar,
+                                 uint32_t &phase, float *out_f, __half *out_o, float2 *out_ml)
+{
+    const int lane = threadIdx.x & 31;
+    const uint32_t D = p.d, rb = D * 2;
+    if (lane == 0) {
+        fence_proxy_async();  // this warp's earlier reads of the stage come first
+        mbar_arrive_expect_tx(bar, m * rb);
+        if (stride == 1)
+            bulk_load(stage, po, m * rb, bar);
+        else
+            for (uint32_t k = 0; k < m; ++k)
+                bulk_load(stage + k * rb, po + (uint64_t)k * stride * D, rb, bar);
+    }
+    float2 ml = make_float2(-INFINITY, 0.0f);
+    if ((uint32_t)lane < m)
+        ml = __ldcg(pml + (uint64_t)lane * stride);
+    const float M = warp_max(ml.y > 0.0f ? ml.x : -INFINITY);
+    const float w = ml.y > 0.0f ? ml.y * exp2f(ml.x - M) : 0.0f;
+    const float s = warp_sum(w);
+    bool done = mbar_try_wait(bar, phase);
+    if (!done) {
+        const uint64_t tw = global_ns();
+        while (!(done = mbar_try_wait(bar, phase)) && global_ns() - tw < kWaitNs) {
+        }
+    }
+    phase ^= 1;
+    if (!__all_sync(0xffffffffu, done)) {
+        if (lane == 0) {
+            atomicOr(p.status, PA_STATUS_TIMEOUT);
+            // let the copies land (bounded) before the stage is given up
+            const uint64_t tw = global_ns();
+            while (!mbar_try_wait(bar, phase ^ 1) && global_ns() - tw < kWaitNs) {
+            }
+        }
+        __syncwarp();
+        return false;
+    }
+    // lane l owns the dimension quads 4l.. and 128 + 4l.. (D = 256) or 4l.. (D = 128)
+    float acc[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+        acc[j] = 0.0f;
+    const uint32_t base = stage + 8 * lane;
+    for (uint32_t k = 0; k < m; ++k) {
+        const float wk = __shfl_sync(0xffffffffu, w, k);
+        if (wk > 0.0f) {
+            const uint32_t a = base + k * rb;
+            uint32_t h[4];
+            asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(h[0]), "=r"(h[1]) : "r"(a));
+            if (D == 256)
+                asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];"
+                             : "=r"(h[2]), "=r"(h[3])
+                             : "r"(a + 256));
+            else
+                h[2] = h[3] = 0u;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float2 f = __half22float2(bits_h2(h[j]));
+                acc[2 * j] = fmaf(wk, f.x, acc[2 * j]);
+                acc[2 * j + 1] = fmaf(wk, f.y, acc[2 * j + 1]);
+            }
+        }
+    }
+    __syncwarp();  // the stage is read before the next row lands
+    const float inv = s > 0.0f ? 1.0f / s : 0.0f;
+    for (int q = 0; q < (D == 256 ? 2 : 1); ++q) {
+        if constexpr (kPartial) {
+            *reinterpret_cast<uint2 *>(out_o + 128 * q + 4 * lane) =
+                make_uint2(h2_bits(__floats2half2_rn(acc[4 * q] * inv, acc[4 * q + 1] * inv)),
+                           h2_bits(__floats2half2_rn(acc[4 * q + 2] * inv, acc[4 * q + 3] * inv)));
+        } else {
+            *reinterpret_cast<float4 *>(out_f + 128 * q + 4 * lane) =
+                make_float4(acc[4 * q] * inv, acc[4 * q + 1] * inv, acc[4 * q + 2] * inv,
+                            acc[4 * q + 3] * inv);
+        }
+    }
+    if (kPartial && lane == 0)
+        *out_ml = make_float2(s > 0.0f ? M : -INFINITY, s);
+    return true;
+}
+
 // The in-launch merge, out of line so that its registers do not add to the
-// main loop's; each warp keeps BATCH partials of each of its two rows in
-// flight, as many as the kernel's register budget holds.
+// main loop's: fused_merge, with BATCH partials of each of two rows in flight
+// per warp.
 template <int BATCH>
 __device__ __noinline__ void merge_tail(const DecodeParams &p, uint32_t seq, uint32_t part,
                                         uint32_t warp, uint32_t nwarps)
@@ -1000,7 +1115,64 @@ __device__ __noinline__ void merge_tail(const DecodeParams &p, uint32_t seq, uin
     fused_merge<BATCH>(p, seq, part, warp, nwarps);
 }
 
-template <class T>
+// The in-launch merge of a plan of more than 32 partitions (two passes), out
+// of line as above.  When the passes of this sequence merge at most
+// min(32, cap) partials per row (cap: the rows a warp's share of the idle
+// rings holds) and the partials are 16-byte aligned, each warp copies its
+// rows into shared memory one at a time (merge_row_staged): one bulk copy per
+// row instead of rounds of loads, with the same groups, order and arithmetic
+// as fused_merge.  Otherwise fused_merge.
+template <int BATCH>
+__device__ __noinline__ void merge_tail_staged(const DecodeParams &p, uint32_t seq,
+                                               uint32_t part, uint32_t warp, uint32_t nwarps,
+                                               uint32_t stage, uint32_t cap, uint64_t *bar,
+                                               uint32_t phase)
+{
+    const int32_t L = row_len(p.seq_lens, p.q_tokens, seq);
+    uint32_t n = L > 0 ? ((uint32_t)L + p.part_tokens - 1) / p.part_tokens : 0;
+    n = n < p.n_parts ? n : p.n_parts;
+    const uint32_t gs = merge_group_size(n), ng = n > gs ? (n + gs - 1) / gs : 1;
+    const uint32_t widest = gs > ng ? gs : ng;
+    if (bar == nullptr || ng == 1 || widest > 32 || widest > cap ||
+        (reinterpret_cast<uintptr_t>(p.part_o) & 15u) != 0) {
+        fused_merge<BATCH>(p, seq, part, warp, nwarps);
+        return;
+    }
+    fence_proxy_async();  // every thread's generic accesses to the rings come first
+    int32_t *cnt = p.counters + (uint64_t)seq * merge_counters_per_seq(p.n_parts);
+    const __half *po = static_cast<const __half *>(p.part_o);
+    const float2 *pml = reinterpret_cast<const float2 *>(p.part_ml);
+    const int lane = threadIdx.x & 31;
+    bool ok = true;  // a copy that timed out ends this warp's merging, not its arrivals
+    const uint32_t g = part / gs, p0 = g * gs, ng_g = min(gs, n - p0);
+    if (!merge_arrive(cnt + 1 + g, ng_g))
+        return;
+    if (lane == 0)
+        fence_proxy_async_global();
+    __syncwarp();
+    for (uint32_t h = warp; h < p.hq && ok; h += nwarps) {
+        const uint64_t r = (uint64_t)seq * p.hq + h;
+        // in place: the group's first slot, read before it is written
+        __half *ro = const_cast<__half *>(po) + (r * p.n_parts + p0) * p.d;
+        float2 *rm = const_cast<float2 *>(pml) + r * p.n_parts + p0;
+        ok = merge_row_staged<true>(p, ro, rm, ng_g, 1, stage, bar, phase, nullptr, ro, rm);
+    }
+    if (!merge_arrive(cnt, ng))
+        return;
+    if (lane == 0)
+        fence_proxy_async_global();
+    __syncwarp();
+    for (uint32_t h = warp; h < p.hq && ok; h += nwarps) {
+        const uint64_t r = (uint64_t)seq * p.hq + h;
+        ok = merge_row_staged<false>(p, po + r * p.n_parts * p.d, pml + r * p.n_parts, ng, gs,
+                                     stage, bar, phase, p.out + r * p.d, nullptr, nullptr);
+    }
+}
+
+// kStaged: the instance for plans of more than 32 partitions, whose merges
+// run in two passes (merge_tail_staged); the other plans take the instance
+// without it, whose code stays as it was tuned.
+template <class T, bool kStaged = false>
 __global__ void __launch_bounds__(T::kMaxWarps * 32, 1)
     fast_decode_kernel(const __grid_constant__ FastArgs a)
 {
@@ -1210,7 +1382,6 @@ __global__ void __launch_bounds__(T::kMaxWarps * 32, 1)
                 issue(kn, s, b);
             issued = kn + 1;
         }
-        __syncwarp();
         if (++s == NSW) {
             s = 0;
             phase ^= 1;
@@ -1232,7 +1403,11 @@ __global__ void __launch_bounds__(T::kMaxWarps * 32, 1)
 
     // park (m, l, O) of every warp in the now idle rings, head-major, then
     // all warps of the CTA combine them
-    __syncthreads();
+    bool any_abort = false;
+    if constexpr (kStaged)
+        any_abort = __syncthreads_or(aborted);
+    else
+        __syncthreads();
     float *park = reinterpret_cast<float *>(smem);
     float *mine = park + warp * Park<T>::kWarp;
     if (gid == 0) {
@@ -1248,8 +1423,20 @@ __global__ void __launch_bounds__(T::kMaxWarps * 32, 1)
             mine[16 + (2 * tig + (e & 1)) * Park<T>::kRow + T::dim_of(mt, gid, e >> 1)] = o[mt][e];
     __syncthreads();
     combine_and_write<T>(p, park, hkv, wph, G, seq, part);
-    if (p.counters && !p.direct)
-        merge_tail<T::kMergeBatch>(p, seq, part, warp, nwarps);
+    if (p.counters && !p.direct) {
+        if constexpr (kStaged) {
+            // each warp stages its merge rows in its share of the idle rings
+            // and waits on its slot-0 mbarrier, whose next parity follows the
+            // loop's uses of slot 0 (all landed unless the loop aborted)
+            const uint32_t share = (a.region_bytes / nwarps) & ~15u;
+            const uint32_t phase0 = ((n_my + NSW - 1) / NSW) & 1u;
+            merge_tail_staged<T::kMergeBatch>(p, seq, part, warp, nwarps,
+                                              smem_u32(smem) + warp * share, share / (p.d * 2),
+                                              any_abort ? nullptr : full, phase0);
+        } else {
+            merge_tail<T::kMergeBatch>(p, seq, part, warp, nwarps);
+        }
+    }
 }
 
 // Combine of the parked (m, l, O) of the wph warps of every head group into
@@ -1413,8 +1600,13 @@ cudaError_t allow_smem()
         return e != cudaSuccess ? e : cudaErrorInvalidDevice;
     std::lock_guard<std::mutex> lock(mu);
     if (!done[dev]) {
-        e = cudaFuncSetAttribute(fast_decode_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        e = cudaFuncSetAttribute(fast_decode_kernel<T, false>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)(kSmemBudget + 4096));
+        if (e == cudaSuccess && T::kStagedMerge)
+            e = cudaFuncSetAttribute(fast_decode_kernel<T, T::kStagedMerge>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)(kSmemBudget + 4096));
         if (e != cudaSuccess)
             return e;
         done[dev] = true;
@@ -1480,7 +1672,13 @@ int launch_t(const DecodeParams &p, cudaStream_t st, const char *entry)
     rc = cuda_check(allow_smem<T>(), entry, "cudaFuncSetAttribute");
     if (rc)
         return rc;
-    fast_decode_kernel<T><<<p.n_ctas, gm.warps * 32, gm.smem, st>>>(a);
+    // two-pass merges (more than 32 partitions) on CTAs of 8 warps or more
+    // take the instance with the staged merge
+    if (T::kStagedMerge && p.counters && !p.direct && merge_group_size(p.n_parts) < p.n_parts &&
+        gm.warps >= 8)
+        fast_decode_kernel<T, T::kStagedMerge><<<p.n_ctas, gm.warps * 32, gm.smem, st>>>(a);
+    else
+        fast_decode_kernel<T, false><<<p.n_ctas, gm.warps * 32, gm.smem, st>>>(a);
     return cuda_check(cudaGetLastError(), entry, "fast_decode_kernel launch");
 }
 
@@ -1492,7 +1690,7 @@ int occupancy_t(uint32_t hkv, int *cps)
         return PA_ERR_INVALID;
     cudaError_t e = allow_smem<T>();
     if (e == cudaSuccess)
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(cps, fast_decode_kernel<T>,
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(cps, fast_decode_kernel<T, false>,
                                                           gm.warps * 32, gm.smem);
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
