@@ -192,24 +192,29 @@ def aggregate(bytes_per_step_per_rank: float, steps: int, world: int, max_second
     return bytes_per_step_per_rank * steps * world / max_seconds / 1e9
 
 
-def traffic_from_profiles(kernel_name: str):
+def traffic_from_profiles(kernel_name: str, workload: str, plan: dict):
     """dram bytes per launch from a committed ncu summary, if it was taken on
-    the current kernel source; else None."""
+    the current kernel source, for this workload and plan; else None."""
     p = os.path.join(ROOT, "profiles", "decode_traffic.json")
     if not os.path.exists(p):
         return None
     d = json.load(open(p))
-    if d.get("kernel") != kernel_name or d.get("source_sha") != kernel_source_sha():
+    if (d.get("kernel") != kernel_name or d.get("source_sha") != kernel_source_sha()
+            or d.get("workload_name") != workload or d.get("plan") != plan):
         return None
     return d.get("dram_bytes_per_launch")
+
+
+# the sources the fast decode kernel is compiled from (the planner, the API
+# and the other kernels do not change its launches' traffic for a given plan)
+KERNEL_SOURCES = ("fast_kernel.cuh", "pa_device.cuh", "pa_internal.h", "k_fast.cu")
 
 
 def kernel_source_sha() -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "paged_kv_attention_attn_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".cuh", ".h", ".cpp")):
-            h.update(open(os.path.join(csrc, f), "rb").read())
+    for f in KERNEL_SOURCES:
+        h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()[:16]
 
 
@@ -488,7 +493,7 @@ def run_ours(a, world, rank, local):
                      "frac": dec_achieved / peak, "peak_kind": peak_kind,
                      "kernel": kname, "kernel_us": dec_avg_ms * 1e3,
                      "bytes_per_launch": nb["decode"],
-                     "traffic": traffic_from_profiles(kname)},
+                     "traffic": traffic_from_profiles(kname, a.workload, pl.as_dict())},
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": K * (1 if in_kernel_q else
