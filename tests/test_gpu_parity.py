@@ -232,10 +232,13 @@ def test_host_buffer_step_equals_device_step(kernel):
 
 @pytest.mark.parametrize("kernel", KERNELS)
 @pytest.mark.parametrize("t", TYPES)
-@pytest.mark.parametrize("force", [0, 1, 6])
+@pytest.mark.parametrize("force", [0, 1, 6, 60])
 def test_fused_merge_equals_separate_merge(kernel, t, force):
-    """The in-launch merge runs the same merge routine as pa_merge, so the
-    two paths give the same bits; the counters are left at zero."""
+    """The in-launch merge runs the same merge arithmetic as pa_merge, so the
+    two paths give the same bits; the counters are left at zero.  force=60
+    makes 47 partitions of the longest sequence: a two-pass plan, which on the
+    fast kernel stages its merge rows in shared memory (the short sequences
+    of the same plan merge in one pass)."""
     spec = synth.CaseSpec(seq_lens=[1500, 33, 0, 700, 16], k_type=t, v_type=t, junk=7,
                           outliers=True)
     case = synth.build_case(spec, seed=2600 + t, device=DEV)
