@@ -61,7 +61,8 @@ WORKLOADS = {
 }
 DEFAULT_WORKLOAD = "uniform-q4_0-b8x131072"
 L2_BYTES = 129 * 10**6        # GB300 L2
-FLUSH_BYTES = 512 * 2**20     # the write that evicts it between timed steps
+FLUSH_BYTES = 512 * 2**20     # the write that evicts it between timed steps (--flush on)
+MAX_LAYERS = 1024             # pool copies cycled through when K/V is under twice the L2
 L2_BYTES = 129 * 2**20
 
 
@@ -206,15 +207,20 @@ def traffic_from_profiles(kernel_name: str, workload: str, plan: dict):
 
 
 # the sources the fast decode kernel is compiled from (the planner, the API
-# and the other kernels do not change its launches' traffic for a given plan)
+# and the other kernels do not change its launches' traffic for a given plan);
+# of fast_kernel.cuh only the device part, above its host section
 KERNEL_SOURCES = ("fast_kernel.cuh", "pa_device.cuh", "pa_internal.h", "k_fast.cu")
+HOST_SECTION = b"\n// ------------------------------------------------------------------- host\n"
 
 
 def kernel_source_sha() -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "paged_kv_attention_attn_gb300", "csrc")
     for f in KERNEL_SOURCES:
-        h.update(open(os.path.join(csrc, f), "rb").read())
+        text = open(os.path.join(csrc, f), "rb").read()
+        if f == "fast_kernel.cuh" and HOST_SECTION in text:
+            text = text[:text.index(HOST_SECTION)]
+        h.update(text)
     return h.hexdigest()[:16]
 
 
@@ -305,16 +311,25 @@ def run_ours(a, world, rank, local):
                  seq_lens=spec.seq_lens, block_size=spec.block_size, hq=spec.hq, hkv=spec.hkv,
                  d=spec.d, k_type=spec.k_type, v_type=spec.v_type)
     ws = pa.workspace(pl, n_seqs=spec.n_seqs, hq=spec.hq, d=spec.d, device=dev)
-    args = pa.make_args(k_pool=case.k_pool, v_pool=case.v_pool, block_table=case.block_table,
-                        seq_lens=case.seq_lens, q=case.q, ws=ws, hkv=spec.hkv,
-                        block_size=spec.block_size, k_type=spec.k_type, v_type=spec.v_type,
-                        flags=flags)
     quantised = spec.k_type != synth.F16
-    dec_args = pa.make_args(k_pool=case.k_pool, v_pool=case.v_pool,
-                            block_table=case.block_table, seq_lens=case.seq_lens,
-                            q=ws.q8_1 if quantised else case.q, ws=ws, hkv=spec.hkv,
+    kv_bytes = (case.k_pool.numel() + case.v_pool.numel())
+    # K/V under twice the L2: the steps take copies of the pools in turn, like
+    # the layers of a model that share one block table and one query buffer,
+    # so every step reads K/V that the L2 no longer holds (unless --flush on)
+    n_layers = 1
+    if a.flush == "auto" and kv_bytes < 2 * L2_BYTES:
+        n_layers = min(MAX_LAYERS, -(-2 * L2_BYTES // kv_bytes) + 1)
+    pools = [(case.k_pool, case.v_pool)] + [(case.k_pool.clone(), case.v_pool.clone())
+                                            for _ in range(n_layers - 1)]
+
+    def args_for(kp, vp, q):
+        return pa.make_args(k_pool=kp, v_pool=vp, block_table=case.block_table,
+                            seq_lens=case.seq_lens, q=q, ws=ws, hkv=spec.hkv,
                             block_size=spec.block_size, k_type=spec.k_type,
                             v_type=spec.v_type, flags=flags)
+    layer_args = [args_for(kp, vp, case.q) for kp, vp in pools]
+    layer_dec_args = [args_for(kp, vp, ws.q8_1 if quantised else case.q) for kp, vp in pools]
+    args, dec_args = layer_args[0], layer_dec_args[0]
     kname = pa.decode_kernel_name(k_type=spec.k_type, v_type=spec.v_type, d=spec.d,
                                   hq=spec.hq, hkv=spec.hkv, block_size=spec.block_size,
                                   flags=flags)
@@ -324,15 +339,19 @@ def run_ours(a, world, rank, local):
     stream = torch.cuda.current_stream()
     L = pa.lib()
     import ctypes
-    p_args, p_plan = ctypes.byref(dec_args), ctypes.byref(pl)
+    p_plan = ctypes.byref(pl)
     sh = stream.cuda_stream
 
     fused = not a.unfused
     counters = ws.counters.data_ptr()
-
-    p_step_args = ctypes.byref(args)
+    p_layer_args = [ctypes.byref(x) for x in layer_args]
+    p_layer_dec_args = [ctypes.byref(x) for x in layer_dec_args]
+    layer = [0]  # the pool copy of the next step
 
     def step(ev0=None, ev1=None):
+        p_step_args = p_layer_args[layer[0]]
+        p_args = p_layer_dec_args[layer[0]]
+        layer[0] = (layer[0] + 1) % n_layers
         if in_kernel_q:  # the public one-launch step
             if ev0 is not None:
                 ev0.record(stream)
@@ -356,11 +375,15 @@ def run_ours(a, world, rank, local):
                        ws.out.data_ptr(), spec.n_seqs, spec.hq, spec.d, p_plan, sh)
         return rc
 
-    # correctness of the configuration before timing
+    # correctness of the configuration before timing, then one step on every
+    # pool copy (each copy's tensor maps are encoded once, as a model's layers
+    # would have them after its first token), then the warm-up
     if step() != 0:
         raise RuntimeError(L.pa_last_error().decode())
     torch.cuda.synchronize()
     assert pa.status_read(ws.status) == 0
+    for _ in range(n_layers - 1):
+        step()
     for _ in range(a.warmup):
         step()
     torch.cuda.synchronize()
@@ -370,7 +393,7 @@ def run_ours(a, world, rank, local):
     # evicts it, and a read of the same buffer then writes the dirty lines
     # back, so that the step starts on a clean L2 holding none of its inputs;
     # only the steps themselves are timed (events around each)
-    flush = a.flush == "on" or (a.flush == "auto" and nb["kv"] < 2 * L2_BYTES)
+    flush = a.flush == "on"
     flush_buf = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev) if flush else None
 
     def flush_l2(k):
@@ -420,12 +443,9 @@ def run_ours(a, world, rank, local):
     out_host = torch.empty(ws.out.shape, dtype=torch.float32).pin_memory()
     qdev = torch.empty_like(case.q)
     e2e_call = pa.decode_step_host if a.unfused else pa.decode_step_fused_host
-    e2e_args = pa.make_args(k_pool=case.k_pool, v_pool=case.v_pool,
-                            block_table=case.block_table, seq_lens=case.seq_lens, q=qdev,
-                            ws=ws, hkv=spec.hkv, block_size=spec.block_size,
-                            k_type=spec.k_type, v_type=spec.v_type, flags=flags)
-    for _ in range(a.warmup):
-        e2e_call(q_host, out_host, e2e_args, ws)
+    e2e_layer_args = [args_for(kp, vp, qdev) for kp, vp in pools]
+    for k in range(a.warmup):
+        e2e_call(q_host, out_host, e2e_layer_args[k % n_layers], ws)
     torch.cuda.synchronize()
     barrier(world)
     e2e_evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
@@ -434,12 +454,12 @@ def run_ours(a, world, rank, local):
         for k in range(K):
             flush_l2(k)
             e2e_evs[k][0].record(stream)
-            e2e_call(q_host, out_host, e2e_args, ws)
+            e2e_call(q_host, out_host, e2e_layer_args[0], ws)
             e2e_evs[k][1].record(stream)
     else:
         e2e_evs[0][0].record(stream)
-        for _ in range(K):
-            e2e_call(q_host, out_host, e2e_args, ws)
+        for k in range(K):
+            e2e_call(q_host, out_host, e2e_layer_args[k % n_layers], ws)
         e2e_evs[0][1].record(stream)
     torch.cuda.synchronize()
     barrier(world)
@@ -478,8 +498,12 @@ def run_ours(a, world, rank, local):
                    "kv_type": synth.TYPE_LABEL[spec.k_type],
                    "l2": (f"L2 flushed between steps by a {FLUSH_BYTES >> 20} MiB write and read; "
                           f"{nb['kv'] / 1e9:.3f} GB of K/V per step" if flush else
+                          f"inputs larger than L2: {n_layers} copies of the K/V pools "
+                          f"({n_layers * kv_bytes / 1e6:.0f} MB), one per step in turn, like the "
+                          f"layers of a model sharing one block table; {nb['kv'] / 1e9:.4f} GB of "
+                          f"K/V read per step" if n_layers > 1 else
                           f"inputs larger than L2: {nb['kv'] / 1e9:.3f} GB of K/V per step"
-                          if nb["kv"] >= L2_BYTES else
+                          if kv_bytes >= L2_BYTES else
                           f"L2 not flushed: {nb['kv'] / 1e9:.3f} GB of K/V per step"),
                    "timing": ("events around each step" if per_launch else
                               "back-to-back launches, events around the timed region"),
@@ -517,7 +541,8 @@ def main():
                     help="time the three-launch step (separate merge) instead of the fused one")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--flush", choices=["auto", "on", "off"], default="auto",
-                    help="L2 flush between timed steps (auto: when K/V < 2 x L2)")
+                    help="auto: K/V under 2 x L2 cycles through pool copies (one per step); "
+                         "on: flush the L2 before every step instead; off: neither")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="oracle work timed for cpu_baseline (whole sequences in turn)")
     a = ap.parse_args()

@@ -40,6 +40,7 @@
 
 #include <cstring>
 #include <mutex>
+#include <unordered_map>
 
 #include "pa_device.cuh"
 #include "pa_internal.h"
@@ -1614,8 +1615,10 @@ cudaError_t allow_smem()
     return cudaSuccess;
 }
 
-// The tensor maps depend only on the pools, their size and the head layout;
-// a few recent encodings are kept so that repeated steps skip the encoding.
+// The tensor maps depend only on the pools, their size and the head layout.
+// Encodings are kept per pool pair, so that the steps of every layer of a
+// model (one pool pair each) skip the encoding; the table is emptied when it
+// passes kMaxMaps entries.
 struct MapKey {
     const void *k, *v;
     uint64_t n_blocks;
@@ -1627,30 +1630,47 @@ struct MapKey {
     }
 };
 
+struct MapKeyHash {
+    size_t operator()(const MapKey &m) const
+    {
+        uint64_t h = reinterpret_cast<uintptr_t>(m.k) * 0x9E3779B97F4A7C15ull;
+        h ^= reinterpret_cast<uintptr_t>(m.v) + 0x632BE59BD9B4E019ull + (h << 6) + (h >> 2);
+        h ^= m.n_blocks + ((uint64_t)m.block_size << 40) + ((uint64_t)m.hkv << 48) +
+             ((uint64_t)m.d << 20) + m.type + (h << 6) + (h >> 2);
+        return (size_t)h;
+    }
+};
+
+struct Maps {
+    CUtensorMap tm[2][kMaxHkv];
+};
+
 template <class T>
 int cached_maps(const DecodeParams &p, FastArgs &a, const char *entry)
 {
-    constexpr int kSlots = 8;
+    constexpr size_t kMaxMaps = 4096;
     static std::mutex mu;
-    static MapKey keys[kSlots];
-    static CUtensorMap maps[kSlots][2][kMaxHkv];
-    static bool used[kSlots] = {};
-    static int next = 0;
+    static std::unordered_map<MapKey, Maps, MapKeyHash> table;
     const MapKey key{p.k_pool, p.v_pool, p.n_pool_blocks, p.block_size, p.hkv, (uint32_t)T::D,
                      T::kTypeKey};
     std::lock_guard<std::mutex> lock(mu);
-    for (int i = 0; i < kSlots; ++i)
-        if (used[i] && keys[i] == key) {
-            memcpy(a.tm, maps[i], sizeof a.tm);
-            return PA_OK;
-        }
+    const auto it = table.find(key);
+    if (it != table.end()) {
+        memcpy(a.tm, it->second.tm, sizeof a.tm);
+        return PA_OK;
+    }
     int rc = encode_maps<T>(p, a, entry);
     if (rc)
         return rc;
-    keys[next] = key;
-    memcpy(maps[next], a.tm, sizeof a.tm);
-    used[next] = true;
-    next = (next + 1) % kSlots;
+    try {
+        if (table.size() >= kMaxMaps)
+            table.clear();
+        Maps m;
+        memcpy(m.tm, a.tm, sizeof a.tm);
+        table.emplace(key, m);
+    } catch (...) {
+        // out of host memory: this launch still has its maps
+    }
     return PA_OK;
 }
 
