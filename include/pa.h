@@ -292,9 +292,13 @@ int pa_decode_step(const pa_decode_args *args, const pa_plan_t *plan, void *q8_1
 
 /* The same step with the query taken from and the output returned to HOST
  * memory: copies q_host (float32 [n_seqs][hq][d]) into args->q (device),
- * runs pa_decode_step, and copies args->out back into out_host, all on
- * `stream` (page-locked host buffers make the copies asynchronous).  The
- * caller synchronises before reading out_host. */
+ * runs pa_decode_step, and returns the output in out_host, all on `stream`.
+ * When out_host is page-locked memory mapped into the device's address space
+ * (cudaHostAlloc / cudaMallocHost under unified addressing, 16-byte aligned),
+ * the kernels store the output into it directly and args->out is left
+ * untouched; otherwise args->out is copied back into out_host.  Page-locked
+ * q_host makes the query copy asynchronous.  The caller synchronises before
+ * reading out_host. */
 int pa_decode_step_host(const float *q_host, float *out_host, const pa_decode_args *args,
                         const pa_plan_t *plan, void *q8_1_scratch, pa_stream_t stream);
 

@@ -287,6 +287,22 @@ extern "C" int pa_decode_step(const pa_decode_args *args, const pa_plan_t *plan,
                             plan->part_tokens, st, E);
 }
 
+// The device address of page-locked host memory that the kernels may store
+// to directly (16-byte aligned for their vector stores), or nullptr for any
+// other pointer: pageable memory is never handed to a kernel.
+static float *mapped_host_out(float *h)
+{
+    cudaPointerAttributes at;
+    if (cudaPointerGetAttributes(&at, h) != cudaSuccess) {
+        cudaGetLastError();  // clear the (non-sticky) error of an unknown pointer
+        return nullptr;
+    }
+    if (at.type != cudaMemoryTypeHost || at.devicePointer == nullptr ||
+        (reinterpret_cast<uintptr_t>(at.devicePointer) & 15u) != 0)
+        return nullptr;
+    return static_cast<float *>(at.devicePointer);
+}
+
 extern "C" int pa_decode_step_host(const float *q_host, float *out_host,
                                    const pa_decode_args *args, const pa_plan_t *plan,
                                    void *q8_1_scratch, pa_stream_t stream)
@@ -305,8 +321,13 @@ extern "C" int pa_decode_step_host(const float *q_host, float *out_host,
                     E, "copy of q to the device");
     if (rc)
         return rc;
-    rc = pa_decode_step(args, plan, q8_1_scratch, stream);
-    if (rc)
+    // page-locked out_host: the kernels write it directly, no copy back
+    pa_decode_args a = *args;
+    float *out_mapped = mapped_host_out(out_host);
+    if (out_mapped)
+        a.out = out_mapped;
+    rc = pa_decode_step(&a, plan, q8_1_scratch, stream);
+    if (rc || out_mapped)
         return rc;
     return cuda_check(cudaMemcpyAsync(out_host, args->out, bytes, cudaMemcpyDeviceToHost, st), E,
                       "copy of out to the host");
@@ -333,8 +354,13 @@ extern "C" int pa_decode_step_fused_host(const float *q_host, float *out_host,
                     E, "copy of q to the device");
     if (rc)
         return rc;
-    rc = pa_decode_step_fused(args, plan, q8_1_scratch, counters, stream);
-    if (rc)
+    // page-locked out_host: the kernels write it directly, no copy back
+    pa_decode_args a = *args;
+    float *out_mapped = mapped_host_out(out_host);
+    if (out_mapped)
+        a.out = out_mapped;
+    rc = pa_decode_step_fused(&a, plan, q8_1_scratch, counters, stream);
+    if (rc || out_mapped)
         return rc;
     return cuda_check(cudaMemcpyAsync(out_host, args->out, bytes, cudaMemcpyDeviceToHost, st), E,
                       "copy of out to the host");

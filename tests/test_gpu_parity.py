@@ -207,25 +207,32 @@ def test_merge_kernel_against_oracle_merge():
 
 @pytest.mark.parametrize("kernel", KERNELS)
 def test_host_buffer_step_equals_device_step(kernel):
+    """The host-buffer steps give the device step's bits, for a partitioned
+    and a direct plan.  Page-locked out_host: the kernels store into it and
+    the device out buffer is left as it was; pageable out_host: the device
+    out buffer is copied back."""
     spec = synth.CaseSpec(seq_lens=[700, 90], k_type=synth.Q4_0, v_type=synth.Q4_0, junk=3)
     case = synth.build_case(spec, seed=1900, device=DEV)
-    dev_out, _, _, _ = H.run(case, flags=KERNELS[kernel])
-    pl = pa.plan(seq_lens=spec.seq_lens, block_size=16, hq=24, hkv=4, d=256,
-                 k_type=spec.k_type, v_type=spec.v_type)
-    ws = pa.workspace(pl, n_seqs=2, hq=24, d=256, device=DEV)
-    qdev = torch.empty_like(case.q)
-    args = pa.make_args(k_pool=case.k_pool, v_pool=case.v_pool, block_table=case.block_table,
-                        seq_lens=case.seq_lens, q=qdev, ws=ws, hkv=4, block_size=16,
-                        k_type=spec.k_type, v_type=spec.v_type, flags=KERNELS[kernel])
     q_host = case.q.cpu().pin_memory()
-    out_host = torch.empty(2, 24, 256, dtype=torch.float32).pin_memory()
-    pa.decode_step_host(q_host, out_host, args, ws)
-    torch.cuda.synchronize()
-    assert torch.equal(out_host.view(torch.int32), dev_out.cpu().view(torch.int32))
-    out_host.zero_()
-    pa.decode_step_fused_host(q_host, out_host, args, ws)
-    torch.cuda.synchronize()
-    assert torch.equal(out_host.view(torch.int32), dev_out.cpu().view(torch.int32))
+    for force in (0, 1):
+        dev_out, _, _, _ = H.run(case, force_parts=force, flags=KERNELS[kernel])
+        pl = pa.plan(seq_lens=spec.seq_lens, block_size=16, hq=24, hkv=4, d=256,
+                     k_type=spec.k_type, v_type=spec.v_type, force_parts=force)
+        ws = pa.workspace(pl, n_seqs=2, hq=24, d=256, device=DEV)
+        qdev = torch.empty_like(case.q)
+        args = pa.make_args(k_pool=case.k_pool, v_pool=case.v_pool,
+                            block_table=case.block_table, seq_lens=case.seq_lens, q=qdev,
+                            ws=ws, hkv=4, block_size=16, k_type=spec.k_type,
+                            v_type=spec.v_type, flags=KERNELS[kernel])
+        for out_host, direct_store in ((torch.empty(2, 24, 256).pin_memory(), True),
+                                       (torch.empty(2, 24, 256), False)):
+            for call in (pa.decode_step_host, pa.decode_step_fused_host):
+                out_host.fill_(float("nan"))
+                ws.out.fill_(float("nan"))
+                call(q_host, out_host, args, ws)
+                torch.cuda.synchronize()
+                assert torch.equal(out_host.view(torch.int32), dev_out.cpu().view(torch.int32))
+                assert bool(ws.out.isnan().all()) == direct_store
 
 
 # ------------------------------------------------------------- fused merge
