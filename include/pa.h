@@ -178,6 +178,9 @@ typedef struct {
     uint32_t q_tokens;           /* query tokens per sequence (>= 1) */
 } pa_plan_t;
 
+/* With the environment variable PA_LOG_PLAN set (to anything but "" or
+ * "0"), every successful pa_plan also writes one line with its inputs and
+ * the chosen plan to stderr. */
 int pa_plan(const pa_plan_in *in, pa_plan_t *out);
 /* Fills sm_count and ctas_per_sm of the current device for the decode
  * kernel that pa_decode_partial would choose for these shapes.

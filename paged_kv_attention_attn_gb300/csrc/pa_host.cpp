@@ -3,6 +3,7 @@
 // device memory here.
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <new>
 #include <vector>
@@ -251,5 +252,14 @@ extern "C" int pa_plan(const pa_plan_in *in, pa_plan_t *out)
         p.counter_bytes = rows * pa::merge_counters_per_seq((uint32_t)n_parts) * 4ull;
     }
     *out = p;
+    // PA_LOG_PLAN (set, not "0"): one line per plan on stderr
+    const char *log = getenv("PA_LOG_PLAN");
+    if (log && *log && strcmp(log, "0") != 0)
+        fprintf(stderr,
+                "pa_plan: n_seqs=%u q_tokens=%u max_len=%u total_len=%llu slots=%lld "
+                "force_parts=%d -> part_tokens=%u n_parts=%u direct=%u n_ctas=%u\n",
+                in->n_seqs, p.q_tokens, in->max_len, (unsigned long long)in->total_len,
+                (long long)in->sm_count * in->ctas_per_sm, in->force_parts, p.part_tokens,
+                p.n_parts, p.direct, p.n_ctas);
     return PA_OK;
 }

@@ -5,6 +5,8 @@ import ctypes
 import os
 import random
 import re
+import subprocess
+import sys
 
 import pytest
 
@@ -185,3 +187,27 @@ def test_append_refuses_bad_arguments_before_any_launch():
     # an empty batch is a no-op that touches nothing
     a = pa.AppendArgs(**dict(good, n_seqs=0))
     assert L.pa_append_kv(ctypes.byref(a), None) == pa.PA_OK
+
+
+def test_plan_log_line_when_asked():
+    """PA_LOG_PLAN=1 makes pa_plan write one line with its inputs and the plan
+    to stderr; without it nothing is written."""
+    code = ("import paged_kv_attention_attn_gb300 as pa; "
+            "pa.plan(seq_lens=[131072] * 8, block_size=16, hq=24, hkv=4, d=256, k_type=2, "
+            "v_type=2, sm_count=152, ctas_per_sm=1)")
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    for value, expect in (("1", True), ("0", False), (None, False)):
+        env = dict(os.environ)
+        env.pop("PA_LOG_PLAN", None)
+        if value is not None:
+            env["PA_LOG_PLAN"] = value
+        r = subprocess.run([sys.executable, "-c", code], cwd=root, env=env, capture_output=True,
+                           text=True, timeout=300)
+        assert r.returncode == 0, r.stderr[-2000:]
+        lines = [l for l in r.stderr.splitlines() if l.startswith("pa_plan:")]
+        if expect:
+            assert lines == ["pa_plan: n_seqs=8 q_tokens=1 max_len=131072 total_len=1048576 "
+                             "slots=152 force_parts=0 -> part_tokens=6912 n_parts=19 direct=0 "
+                             "n_ctas=152"]
+        else:
+            assert lines == []
