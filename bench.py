@@ -438,6 +438,23 @@ def run_ours(a, world, rank, local):
     peak, peak_kind = load_peaks()
     dec_achieved = nb["decode"] / (dec_avg_ms / 1e3) / 1e9
 
+    # the spread of single steps: after the timed region, up to 200 more steps
+    # each between two events (this pass feeds no other figure)
+    n_dist = min(K, 200)
+    dist_evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                for _ in range(n_dist)]
+    for k in range(n_dist):
+        if flush:
+            flush_l2(k)
+        dist_evs[k][0].record(stream)
+        step()
+        dist_evs[k][1].record(stream)
+    torch.cuda.synchronize()
+    dist = sorted(e0.elapsed_time(e1) * 1e3 for e0, e1 in dist_evs)
+    step_dist = {"p10": dist[n_dist // 10], "median": dist[n_dist // 2],
+                 "p90": dist[(9 * n_dist) // 10], "n": n_dist,
+                 "how": "events around each step, after the timed region"}
+
     # end to end through the public C call with host buffers
     q_host = case.q.cpu().pin_memory()
     out_host = torch.empty(ws.out.shape, dtype=torch.float32).pin_memory()
@@ -490,6 +507,7 @@ def run_ours(a, world, rank, local):
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K,
         "warmup": a.warmup, "ms_per_step": ms_per_step, "us_per_step": ms_per_step * 1e3,
+        "step_us_dist": step_dist,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic (seeded N(0,1), see synth/)",
         "config": {"workload": a.workload, "batch": spec.n_seqs,
