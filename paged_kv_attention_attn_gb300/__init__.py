@@ -312,8 +312,9 @@ def decode_fused(args: DecodeArgs, ws: Workspace, stream=None) -> None:
 
 
 def decode_step_fused(args: DecodeArgs, ws: Workspace, stream=None) -> None:
-    """pa_decode_step_fused: q8_1 pre-pass and the fused decode (args.q is
-    the float32 query)."""
+    """pa_decode_step_fused: the step with the in-launch merge (args.q is the
+    float32 query).  On the fast kernel one launch that also quantises the
+    query; otherwise the q8_1 pre-pass first."""
     _check(lib().pa_decode_step_fused(ctypes.byref(args), ctypes.byref(ws.plan), _ptr(ws.q8_1),
                                       _ptr(ws.counters), _stream(stream)))
 
