@@ -56,6 +56,10 @@ WORKLOADS = {
        for vn, vt in (("f16", synth.F16), ("q8_0", synth.Q8_0), ("q4_0", synth.Q4_0))
        if kt != vt},
     "verify-q4_0-b8x32768-T4": synth.verify_spec,
+    # batches wider than the machine (152 SMs): a short last wave filled by
+    # splitting its sequences, and whole waves
+    **{f"wide-q4_0-b{b}x{c}": (lambda b=b, c=c: synth.uniform_spec(b, c, synth.Q4_0))
+       for b, c in ((160, 6912), (512, 4096), (304, 4096), (1024, 1024))},
     "tiny-f16-L200": synth.tiny_spec,
     "largepool-f16-b16x300000": synth.large_pool_spec,
 }
@@ -96,9 +100,13 @@ def algorithmic_bytes(spec, plan, fused: bool = True, in_kernel_q: bool = False)
         part_w = part_r = 0
         dec_out = out
     else:
-        live = sum(math.ceil(L / plan.part_tokens) for L in rows)
+        # the leading n_direct rows of a wave-filling plan write out directly
+        nd = int(plan.n_direct)
+        live = sum(math.ceil(L / plan.part_tokens) for L in rows[nd:])
         part_w = part_r = live * hq * (2 * d + 8)
-        dec_out = part_w
+        out_direct = nd * hq * d * 4
+        dec_out = part_w + out_direct
+        out -= out_direct  # what the merge writes
     merge = 0 if plan.direct else part_r + out + S * 4
     decode = kv + table + q_read + dec_out + S * 4
     if fused and not plan.direct:

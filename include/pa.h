@@ -146,11 +146,21 @@ int pa_quantize_q(const float *q, void *q8_1, uint32_t n_rows, uint32_t d, pa_st
  *    most roundup(max_len, 32)), so that the grid fits one wave;
  *  - n_parts = ceil(max_len / part_tokens); direct = (n_parts == 1): no
  *    partials, the decode kernel writes the output;
- *  - n_ctas = n_seqs when direct, else min(n_seqs * n_parts,
- *    ceil(total_len / part_tokens) + n_seqs) (>= the live partitions);
- *  - partial buffers: part_o f16 [n_seqs][hq][n_parts][d] and part_ml
- *    float32 [n_seqs][hq][n_parts][2] (0 bytes when direct);
- *  - counter_bytes = 4 * n_seqs * (1 + ceil(sqrt(n_parts))), the int32
+ *  - a batch wider than the machine (n_seqs > slots) that this makes direct,
+ *    with n_seqs = k * slots + r, 0 < r and floor(slots / r) >= 2, fills its
+ *    last wave instead: the first n_direct = k * slots sequences stay direct
+ *    (one CTA each, output written by the decode kernel) and the last r are
+ *    split into partitions of part_tokens = roundup(ceil(max_len /
+ *    floor(slots / r)), 32) (at least 128), n_parts = ceil(max_len /
+ *    part_tokens) >= 2 of them; direct = 0.  Every other plan has
+ *    n_direct = 0;
+ *  - n_ctas = n_seqs when direct, else n_direct + min(m * n_parts,
+ *    ceil(total_len / part_tokens) + m) with m = n_seqs - n_direct (>= the
+ *    live partitions; a wave-filling plan counts m * n_parts);
+ *  - partial buffers, for the m partitioned sequences only (sequence s at
+ *    index s - n_direct): part_o f16 [m][hq][n_parts][d] and part_ml
+ *    float32 [m][hq][n_parts][2] (0 bytes when direct);
+ *  - counter_bytes = 4 * m * (1 + ceil(sqrt(n_parts))), the int32
  *    completion counters of the fused merge (0 when direct).
  * Several query tokens ([P2] What: a prompt chunk or a verify window of
  * several query rows per sequence over one paged cache): with q_tokens = T,
@@ -176,6 +186,7 @@ typedef struct {
     uint64_t part_o_bytes, part_ml_bytes;
     uint64_t counter_bytes;      /* completion counters of pa_decode_fused (0 when direct) */
     uint32_t q_tokens;           /* query tokens per sequence (>= 1) */
+    uint32_t n_direct;           /* leading query rows decoded directly in a partitioned plan */
 } pa_plan_t;
 
 /* With the environment variable PA_LOG_PLAN set (to anything but "" or

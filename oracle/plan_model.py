@@ -25,15 +25,25 @@ frozen here so that the C++ planner can be compared with it exactly:
 - n_parts = ceil(max_len / part_tokens) (partition slots per sequence, the
   partial buffers' second dimension); a sequence of length L has
   ceil(L / part_tokens) live partitions;
+- a batch wider than the machine (S > slots) left direct by the above, with
+  S = k * slots + r, r > 0 and floor(slots / r) >= 2, fills its last wave:
+  the first n_direct = k * slots sequences stay direct (one CTA each) and the
+  last r take part_tokens = max(128, roundup(ceil(max_len / floor(slots /
+  r)), 32)), n_parts = ceil(max_len / part_tokens) (only when that is >= 2);
+  every other plan has n_direct = 0;
 - n_parts == 1 selects direct mode: no partials, the decode kernel writes
   the output itself;
-- the decode grid has n_ctas = S in direct mode, otherwise
-  min(S * n_parts, ceil(total_len / part_tokens) + S) CTAs, an upper bound
+- the decode grid has n_ctas = S in direct mode, otherwise n_direct +
+  min(m * n_parts, ceil(total_len / part_tokens) + m) CTAs with m = S -
+  n_direct (n_direct + m * n_parts for a wave-filling plan), an upper bound
   on the live (sequence, partition) pairs;
 - an empty batch (max_len == 0) is direct with part_tokens = 32;
-- the fused merge keeps 1 + ceil(sqrt(n_parts)) int32 completion counters
-  per sequence (one for the last pass, one per group of the two-pass merge):
-  counter_bytes = 4 * S * (1 + ceil(sqrt(n_parts))), 0 when direct;
+- partial buffers and counters cover the m partitioned sequences only:
+  part_o_bytes = m * hq * n_parts * d * 2, part_ml_bytes = m * hq * n_parts
+  * 8, and the fused merge keeps 1 + ceil(sqrt(n_parts)) int32 completion
+  counters per such sequence (one for the last pass, one per group of the
+  two-pass merge): counter_bytes = 4 * m * (1 + ceil(sqrt(n_parts))); all 0
+  when direct;
 - with q_tokens = T > 1 (several query tokens per sequence, each a query
   row of its own that attends causally) the rule runs over the S * T query
   rows with T * total_len tokens of work: every S above reads S * T and
@@ -58,7 +68,7 @@ def _roundup(a: int, b: int) -> int:
 def plan(*, n_seqs, max_len, total_len, block_size, hq, hkv, d, k_type, v_type,
          sm_count, ctas_per_sm, force_parts=0, q_tokens=1):
     """Returns (rc, dict).  dict keys: part_tokens, n_parts, direct, n_ctas,
-    part_o_bytes, part_ml_bytes, counter_bytes."""
+    part_o_bytes, part_ml_bytes, counter_bytes, q_tokens, n_direct."""
     if (n_seqs < 1 or block_size not in (16, 32) or hkv < 1 or hq < hkv or hq % hkv
             or hq // hkv > 8 or d not in (128, 256) or k_type not in (0, 1, 2)
             or v_type not in (0, 1, 2) or sm_count < 1 or ctas_per_sm < 1
@@ -69,6 +79,7 @@ def plan(*, n_seqs, max_len, total_len, block_size, hq, hkv, d, k_type, v_type,
     if T > 4096:
         return INVALID, None
     rows, work = n_seqs * T, T * total_len   # query rows and their work at most
+    n_direct = 0
     if max_len == 0:
         part, n_parts = TILE, 1
     elif force_parts > 0:
@@ -87,14 +98,22 @@ def plan(*, n_seqs, max_len, total_len, block_size, hq, hkv, d, k_type, v_type,
             part = max(part, min(_roundup(_cdiv(work, slots - rows), TILE),
                                  _roundup(max_len, TILE)))
         n_parts = _cdiv(max_len, part)
+        r = rows % slots
+        if n_parts == 1 and rows > slots and r > 0 and slots // r >= 2:
+            pr = max(MIN_PART, _roundup(_cdiv(max_len, slots // r), TILE))
+            if _cdiv(max_len, pr) >= 2:
+                part, n_parts, n_direct = pr, _cdiv(max_len, pr), rows - r
     direct = 1 if n_parts == 1 else 0
     if direct:
         n_ctas = rows
         po = pm = cb = 0
     else:
-        n_ctas = min(rows * n_parts, _cdiv(work, part) + rows)
-        po = rows * hq * n_parts * d * 2
-        pm = rows * hq * n_parts * 8
-        cb = 4 * rows * (1 + math.isqrt(n_parts - 1) + 1)
+        m = rows - n_direct
+        n_ctas = n_direct + (m * n_parts if n_direct else
+                             min(m * n_parts, _cdiv(work, part) + m))
+        po = m * hq * n_parts * d * 2
+        pm = m * hq * n_parts * 8
+        cb = 4 * m * (1 + math.isqrt(n_parts - 1) + 1)
     return OK, dict(part_tokens=part, n_parts=n_parts, direct=direct, n_ctas=n_ctas,
-                    part_o_bytes=po, part_ml_bytes=pm, counter_bytes=cb, q_tokens=T)
+                    part_o_bytes=po, part_ml_bytes=pm, counter_bytes=cb, q_tokens=T,
+                    n_direct=n_direct)

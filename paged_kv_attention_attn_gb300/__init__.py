@@ -46,7 +46,8 @@ class Plan(ctypes.Structure):
     _fields_ = [("part_tokens", ctypes.c_uint32), ("n_parts", ctypes.c_uint32),
                 ("direct", ctypes.c_uint32), ("n_ctas", ctypes.c_uint32),
                 ("part_o_bytes", ctypes.c_uint64), ("part_ml_bytes", ctypes.c_uint64),
-                ("counter_bytes", ctypes.c_uint64), ("q_tokens", ctypes.c_uint32)]
+                ("counter_bytes", ctypes.c_uint64), ("q_tokens", ctypes.c_uint32),
+                ("n_direct", ctypes.c_uint32)]
 
     def as_dict(self):
         return {k: int(getattr(self, k)) for k, _ in self._fields_}
@@ -266,10 +267,11 @@ class Workspace:
 
 def workspace(pl: Plan, *, n_seqs, hq, d, device) -> Workspace:
     """Buffers of one step: out float32 [S, hq, d], or [S, T, hq, d] for a
-    plan with T > 1 query tokens per sequence; partials per query row."""
+    plan with T > 1 query tokens per sequence; partials per partitioned query
+    row (the rows after the plan's n_direct leading direct ones)."""
     P = 0 if pl.direct else int(pl.n_parts)
     T = max(1, int(pl.q_tokens))
-    rows = n_seqs * T
+    rows = n_seqs * T - (0 if pl.direct else int(pl.n_direct))
     lead = (n_seqs,) if T == 1 else (n_seqs, T)
     return Workspace(
         plan=pl,

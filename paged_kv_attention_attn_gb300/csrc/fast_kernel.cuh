@@ -1011,7 +1011,7 @@ struct Park {
 template <class T>
 __device__ __forceinline__ void combine_and_write(const DecodeParams &p, const float *park,
                                                   uint32_t hkv, uint32_t wph, uint32_t G,
-                                                  uint32_t seq, uint32_t part);
+                                                  uint32_t seq, uint32_t part, bool dir);
 
 // One row of the in-launch merge by one warp from partials staged in shared
 // memory: m partials of D halves at po (global; partial k at po + k * stride
@@ -1140,7 +1140,8 @@ __device__ __noinline__ void merge_tail_staged(const DecodeParams &p, uint32_t s
         return;
     }
     fence_proxy_async();  // every thread's generic accesses to the rings come first
-    int32_t *cnt = p.counters + (uint64_t)seq * merge_counters_per_seq(p.n_parts);
+    const uint64_t pseq = seq - p.n_direct;  // index of the row's partials and counters
+    int32_t *cnt = p.counters + pseq * merge_counters_per_seq(p.n_parts);
     const __half *po = static_cast<const __half *>(p.part_o);
     const float2 *pml = reinterpret_cast<const float2 *>(p.part_ml);
     const int lane = threadIdx.x & 31;
@@ -1152,7 +1153,7 @@ __device__ __noinline__ void merge_tail_staged(const DecodeParams &p, uint32_t s
         fence_proxy_async_global();
     __syncwarp();
     for (uint32_t h = warp; h < p.hq && ok; h += nwarps) {
-        const uint64_t r = (uint64_t)seq * p.hq + h;
+        const uint64_t r = pseq * p.hq + h;
         // in place: the group's first slot, read before it is written
         __half *ro = const_cast<__half *>(po) + (r * p.n_parts + p0) * p.d;
         float2 *rm = const_cast<float2 *>(pml) + r * p.n_parts + p0;
@@ -1164,9 +1165,10 @@ __device__ __noinline__ void merge_tail_staged(const DecodeParams &p, uint32_t s
         fence_proxy_async_global();
     __syncwarp();
     for (uint32_t h = warp; h < p.hq && ok; h += nwarps) {
-        const uint64_t r = (uint64_t)seq * p.hq + h;
+        const uint64_t r = pseq * p.hq + h;
         ok = merge_row_staged<false>(p, po + r * p.n_parts * p.d, pml + r * p.n_parts, ng, gs,
-                                     stage, bar, phase, p.out + r * p.d, nullptr, nullptr);
+                                     stage, bar, phase, p.out + ((uint64_t)seq * p.hq + h) * p.d,
+                                     nullptr, nullptr);
     }
 }
 
@@ -1202,21 +1204,24 @@ __global__ void __launch_bounds__(T::kMaxWarps * 32, 1)
     uint32_t seq, part;
     if (!p.direct && blockIdx.x == gridDim.x - 1 && warp == 0)
         check_grid_vs_plan(p.seq_lens, p.q_tokens, p.n_seqs, p.part_tokens, p.n_parts,
-                           p.status);
+                           p.n_direct, p.status);
     if (p.direct) {
         seq = blockIdx.x;
         part = 0;
     } else if (!cta_work(p.seq_lens, p.q_tokens, p.n_seqs, p.part_tokens, p.n_parts,
-                         blockIdx.x, &seq, &part)) {
+                         p.n_direct, blockIdx.x, &seq, &part)) {
         return;  // past the last live partition: nothing was issued
-    } else if (part == 0 && tid == 0) {
+    } else if (seq >= p.n_direct && part == 0 && tid == 0) {
         check_len_vs_plan(row_len(p.seq_lens, p.q_tokens, seq), p.n_parts, p.part_tokens,
                           p.status);
     }
+    // a direct CTA: the whole row, output written here (every CTA of a direct
+    // plan, and the leading rows of a wave-filling plan)
+    const bool dir = p.direct || seq < p.n_direct;
     const int32_t Lrow = row_len(p.seq_lens, p.q_tokens, seq);
     const int32_t L = Lrow > 0 ? Lrow : 0;
-    const uint32_t t0 = p.direct ? 0u : part * p.part_tokens;
-    const uint32_t t1 = p.direct ? (uint32_t)L : min((uint32_t)L, t0 + p.part_tokens);
+    const uint32_t t0 = dir ? 0u : part * p.part_tokens;
+    const uint32_t t1 = dir ? (uint32_t)L : min((uint32_t)L, t0 + p.part_tokens);
     const uint32_t n_tiles = (t1 - t0 + kTile - 1) / kTile;
     const int gid = lane >> 2, tig = lane & 3;
     const uint32_t g = warp % hkv, sub = warp / hkv;
@@ -1423,8 +1428,8 @@ __global__ void __launch_bounds__(T::kMaxWarps * 32, 1)
         for (int e = 0; e < 4; ++e)
             mine[16 + (2 * tig + (e & 1)) * Park<T>::kRow + T::dim_of(mt, gid, e >> 1)] = o[mt][e];
     __syncthreads();
-    combine_and_write<T>(p, park, hkv, wph, G, seq, part);
-    if (p.counters && !p.direct) {
+    combine_and_write<T>(p, park, hkv, wph, G, seq, part, dir);
+    if (p.counters && !dir) {
         if constexpr (kStaged) {
             // each warp stages its merge rows in its share of the idle rings
             // and waits on its slot-0 mbarrier, whose next parity follows the
@@ -1445,11 +1450,11 @@ __global__ void __launch_bounds__(T::kMaxWarps * 32, 1)
 // reference maxima, f_k = 2^(m_k - M), O = sum f_k O_k / sum f_k l_k.  Every
 // thread of the CTA takes 8-dim chunks of the output rows, so the partial
 // rows are written with coalesced 16-byte stores (f16 partials) or 32-byte
-// stores (the f32 output of a direct plan).
+// stores (the f32 output of a direct CTA, `dir`).
 template <class T>
 __device__ __forceinline__ void combine_and_write(const DecodeParams &p, const float *park,
                                                   uint32_t hkv, uint32_t wph, uint32_t G,
-                                                  uint32_t seq, uint32_t part)
+                                                  uint32_t seq, uint32_t part, bool dir)
 {
     constexpr uint32_t NQ = T::D / 8;
     const uint32_t n_chunks = hkv * G * NQ;
@@ -1485,8 +1490,8 @@ __device__ __forceinline__ void combine_and_write(const DecodeParams &p, const f
             }
         }
         const float inv = l > 0.0f ? 1.0f / l : 0.0f;
-        const uint64_t row = (uint64_t)seq * p.hq + hg;
-        if (p.direct) {
+        if (dir) {
+            const uint64_t row = (uint64_t)seq * p.hq + hg;
             float4 *dst = reinterpret_cast<float4 *>(p.out + row * T::D + 8 * q);
             dst[0] = make_float4(acc[0] * inv, acc[1] * inv, acc[2] * inv, acc[3] * inv);
             dst[1] = make_float4(acc[4] * inv, acc[5] * inv, acc[6] * inv, acc[7] * inv);
@@ -1496,6 +1501,8 @@ __device__ __forceinline__ void combine_and_write(const DecodeParams &p, const f
             v.y = h2_bits(__floats2half2_rn(acc[2] * inv, acc[3] * inv));
             v.z = h2_bits(__floats2half2_rn(acc[4] * inv, acc[5] * inv));
             v.w = h2_bits(__floats2half2_rn(acc[6] * inv, acc[7] * inv));
+            // partials of partitioned row seq sit at index seq - n_direct
+            const uint64_t row = (uint64_t)(seq - p.n_direct) * p.hq + hg;
             __half *po = static_cast<__half *>(p.part_o);
             *reinterpret_cast<uint4 *>(po + (row * p.n_parts + part) * T::D + 8 * q) = v;
             if (q == 0)

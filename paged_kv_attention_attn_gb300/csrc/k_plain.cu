@@ -215,23 +215,25 @@ __global__ void __launch_bounds__(kPlainWarps * 32) plain_decode_kernel(const De
     uint32_t s, part;
     if (!p.direct && blockIdx.x == gridDim.x - 1 && warp == 0)
         check_grid_vs_plan(p.seq_lens, p.q_tokens, p.n_seqs, p.part_tokens, p.n_parts,
-                           p.status);
+                           p.n_direct, p.status);
     if (p.direct) {
         s = blockIdx.x;
         part = 0;
         if (s >= p.n_seqs)
             return;
     } else if (!cta_work(p.seq_lens, p.q_tokens, p.n_seqs, p.part_tokens, p.n_parts,
-                         blockIdx.x, &s, &part)) {
+                         p.n_direct, blockIdx.x, &s, &part)) {
         return;
-    } else if (part == 0 && threadIdx.x == 0) {
+    } else if (s >= p.n_direct && part == 0 && threadIdx.x == 0) {
         check_len_vs_plan(row_len(p.seq_lens, p.q_tokens, s), p.n_parts, p.part_tokens,
                           p.status);
     }
+    // a direct CTA: the whole row, output written here
+    const bool dir = p.direct || s < p.n_direct;
     const int32_t Lrow = row_len(p.seq_lens, p.q_tokens, s);
     const int32_t L = Lrow > 0 ? Lrow : 0;
-    const uint32_t t0 = p.direct ? 0u : part * p.part_tokens;
-    const uint32_t t1 = p.direct ? (uint32_t)L : min((uint32_t)L, t0 + p.part_tokens);
+    const uint32_t t0 = dir ? 0u : part * p.part_tokens;
+    const uint32_t t1 = dir ? (uint32_t)L : min((uint32_t)L, t0 + p.part_tokens);
     const int32_t *bt = p.block_table + (uint64_t)table_row(p.q_tokens, s) * p.table_stride;
     const uint32_t G = p.hq / p.hkv;
 
@@ -287,13 +289,14 @@ __global__ void __launch_bounds__(kPlainWarps * 32) plain_decode_kernel(const De
         }
         const float inv = l > 0.0f ? 1.0f / l : 0.0f;
         const uint64_t sh = (uint64_t)s * p.hq + h;
-        if (p.direct) {
+        if (dir) {
             float *o = p.out + sh * D + lane * DPL;
 #pragma unroll
             for (int k = 0; k < DPL; ++k)
                 o[k] = acc[k] * inv;
         } else {
-            const uint64_t slot = sh * p.n_parts + part;
+            // partials of partitioned row s sit at index s - n_direct
+            const uint64_t slot = ((uint64_t)(s - p.n_direct) * p.hq + h) * p.n_parts + part;
             __half *o = static_cast<__half *>(p.part_o) + slot * D + lane * DPL;
 #pragma unroll
             for (int k = 0; k < DPL; ++k)
@@ -303,7 +306,7 @@ __global__ void __launch_bounds__(kPlainWarps * 32) plain_decode_kernel(const De
         }
         __syncwarp();
     }
-    if (p.counters && !p.direct)
+    if (p.counters && !dir)
         fused_merge(p, s, part, threadIdx.x >> 5, blockDim.x >> 5);
 }
 
@@ -371,12 +374,16 @@ __global__ void __launch_bounds__(128) merge_kernel(const __half *__restrict__ p
                                                     const int32_t *__restrict__ seq_lens,
                                                     float *__restrict__ out, uint32_t T,
                                                     uint32_t hq, uint32_t D, uint32_t n_parts,
-                                                    uint32_t part_tokens, uint64_t units)
+                                                    uint32_t part_tokens, uint32_t n_direct,
+                                                    uint64_t units)
 {
+    // unit sh: (partitioned row, head) at partial index sh; its row is
+    // n_direct + sh / hq (the leading direct rows have no partials)
     const uint64_t sh = (uint64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     if (sh >= units)
         return;
-    const int32_t L = row_len(seq_lens, T, (uint32_t)(sh / hq));
+    const uint64_t osh = sh + (uint64_t)n_direct * hq;  // its output row
+    const int32_t L = row_len(seq_lens, T, (uint32_t)(osh / hq));
     uint32_t n_live = L > 0 ? ((uint32_t)L + part_tokens - 1) / part_tokens : 0;
     if (n_live > n_parts)
         n_live = n_parts;
@@ -385,19 +392,23 @@ __global__ void __launch_bounds__(128) merge_kernel(const __half *__restrict__ p
     __shared__ float2 scr_ml[4];
     const int w = threadIdx.x >> 5;
     if (D == 256)
-        merge_row_two_pass_warp<8>(po + sh * n_parts * D, pml + sh * n_parts, out + sh * D,
+        merge_row_two_pass_warp<8>(po + sh * n_parts * D, pml + sh * n_parts, out + osh * D,
                                    n_live, D, scr[w], &scr_ml[w]);
     else
-        merge_row_two_pass_warp<4>(po + sh * n_parts * D, pml + sh * n_parts, out + sh * D,
+        merge_row_two_pass_warp<4>(po + sh * n_parts * D, pml + sh * n_parts, out + osh * D,
                                    n_live, D, scr[w], &scr_ml[w]);
 }
 
 int launch_merge(const void *part_o, const float *part_ml, const int32_t *seq_lens, float *out,
                  uint32_t n_seqs, uint32_t q_tokens, uint32_t hq, uint32_t d, uint32_t n_parts,
-                 uint32_t part_tokens, cudaStream_t st, const char *entry)
+                 uint32_t part_tokens, uint32_t n_direct, cudaStream_t st, const char *entry)
 {
     const uint32_t T = q_tokens > 1 ? q_tokens : 1;
-    uint64_t units = (uint64_t)n_seqs * T * hq;
+    const uint64_t rows = (uint64_t)n_seqs * T;
+    if (n_direct > rows)
+        return fail(PA_ERR_INVALID, entry, "n_direct %u exceeds the %llu query rows", n_direct,
+                    (unsigned long long)rows);
+    uint64_t units = (rows - n_direct) * hq;
     if (units == 0)
         return PA_OK;
     if ((units + 3) / 4 > 0x7fffffffull)
@@ -406,7 +417,7 @@ int launch_merge(const void *part_o, const float *part_ml, const int32_t *seq_le
         return fail(PA_ERR_INVALID, entry, "d %u unsupported by the merge (128 or 256)", d);
     merge_kernel<<<(unsigned)((units + 3) / 4), 128, 0, st>>>(
         static_cast<const __half *>(part_o), reinterpret_cast<const float2 *>(part_ml), seq_lens,
-        out, T, hq, d, n_parts, part_tokens, units);
+        out, T, hq, d, n_parts, part_tokens, n_direct, units);
     return cuda_check(cudaGetLastError(), entry, "merge_kernel launch");
 }
 

@@ -68,6 +68,10 @@ int resolve(const pa_decode_args *a, const pa_plan_t *plan, const char *E, pa::D
         return fail(PA_ERR_RANGE, E, "n_seqs * q_tokens exceeds 2^31 - 1");
     if (plan->direct && plan->n_ctas != a->n_seqs * T)
         return fail(PA_ERR_INVALID, E, "direct plan must have n_ctas == n_seqs * q_tokens");
+    if (plan->direct ? plan->n_direct != 0
+                     : (plan->n_direct >= a->n_seqs * T || plan->n_ctas <= plan->n_direct))
+        return fail(PA_ERR_INVALID, E, "inconsistent n_direct %u for %u query rows",
+                    plan->n_direct, a->n_seqs * T);
     if (a->table_stride == 0)
         return fail(PA_ERR_INVALID, E, "table_stride is 0");
     if (a->n_pool_blocks == 0 || a->n_pool_blocks > 0x80000000ull)
@@ -100,6 +104,7 @@ int resolve(const pa_decode_args *a, const pa_plan_t *plan, const char *E, pa::D
     p->v_row_bytes = pa_row_bytes(a->v_type, a->d);
     p->counters = nullptr;
     p->q_f32 = 0;
+    p->n_direct = plan->direct ? 0 : plan->n_direct;
     return PA_OK;
 }
 
@@ -253,12 +258,16 @@ extern "C" int pa_merge(const void *part_o, const float *part_ml, const int32_t 
     if (n_seqs == 0 || hq == 0 || (d != 128 && d != 256))
         return fail(PA_ERR_INVALID, E, "bad shape (n_seqs %u, hq %u, d %u)", n_seqs, hq, d);
     const uint64_t T = plan->q_tokens > 1 ? plan->q_tokens : 1;
-    const uint64_t elems = (uint64_t)n_seqs * T * hq * plan->n_parts * d;
+    if (plan->n_direct >= (uint64_t)n_seqs * T)
+        return fail(PA_ERR_INVALID, E, "n_direct %u leaves no partitioned row of %llu",
+                    plan->n_direct, (unsigned long long)((uint64_t)n_seqs * T));
+    const uint64_t elems = ((uint64_t)n_seqs * T - plan->n_direct) * hq * plan->n_parts * d;
     if (elems > (1ull << 40))
         return fail(PA_ERR_RANGE, E, "partial buffer of %llu elements exceeds 2^40",
                     (unsigned long long)elems);
     return pa::launch_merge(part_o, part_ml, seq_lens, out, n_seqs, plan->q_tokens, hq, d,
-                            plan->n_parts, plan->part_tokens, pa::stream_of(stream), E);
+                            plan->n_parts, plan->part_tokens, plan->n_direct,
+                            pa::stream_of(stream), E);
 }
 
 extern "C" int pa_decode_step(const pa_decode_args *args, const pa_plan_t *plan,
@@ -284,7 +293,7 @@ extern "C" int pa_decode_step(const pa_decode_args *args, const pa_plan_t *plan,
         return rc;
     return pa::launch_merge(args->part_o, args->part_ml, args->seq_lens, args->out,
                             args->n_seqs, plan->q_tokens, args->hq, args->d, plan->n_parts,
-                            plan->part_tokens, st, E);
+                            plan->part_tokens, plan->n_direct, st, E);
 }
 
 // The device address of page-locked host memory that the kernels may store

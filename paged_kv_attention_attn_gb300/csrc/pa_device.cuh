@@ -100,12 +100,20 @@ __device__ __forceinline__ uint32_t table_row(uint32_t T, uint32_t v)
 // sequence (L_s <= 0) one empty partition.  Executed by one full warp; returns false when the CTA
 // index is past the last pair.
 __device__ __forceinline__ bool cta_work(const int32_t *seq_lens, uint32_t T, uint32_t n_seqs,
-                                         uint32_t part_tokens, uint32_t n_parts, uint32_t cta,
-                                         uint32_t *seq, uint32_t *part)
+                                         uint32_t part_tokens, uint32_t n_parts,
+                                         uint32_t n_direct, uint32_t cta, uint32_t *seq,
+                                         uint32_t *part)
 {
+    // the leading n_direct rows of a wave-filling plan: one CTA each, in order
+    if (cta < n_direct) {
+        *seq = cta;
+        *part = 0;
+        return true;
+    }
+    cta -= n_direct;
     const int lane = threadIdx.x & 31;
     uint32_t base = 0;
-    for (uint32_t s0 = 0; s0 < n_seqs; s0 += 32) {
+    for (uint32_t s0 = n_direct; s0 < n_seqs; s0 += 32) {
         uint32_t s = s0 + lane;
         // an empty sequence still gets one CTA, which writes its zero output
         // (or its empty partial, and its arrival at the completion count)
@@ -296,11 +304,12 @@ __device__ __forceinline__ void check_len_vs_plan(int32_t L, uint32_t n_parts,
 // grid's last CTA.
 __device__ __forceinline__ void check_grid_vs_plan(const int32_t *seq_lens, uint32_t T,
                                                    uint32_t n_seqs, uint32_t part_tokens,
-                                                   uint32_t n_parts, int32_t *status)
+                                                   uint32_t n_parts, uint32_t n_direct,
+                                                   int32_t *status)
 {
     const int lane = threadIdx.x & 31;
-    uint64_t pairs = 0;
-    for (uint32_t s = lane; s < n_seqs; s += 32) {
+    uint64_t pairs = lane == 0 ? n_direct : 0;  // the direct rows: one CTA each
+    for (uint32_t s = n_direct + lane; s < n_seqs; s += 32) {
         const int32_t L = row_len(seq_lens, T, s);
         uint32_t n = L > 0 ? ((uint32_t)L + part_tokens - 1) / part_tokens : 1u;
         pairs += n < n_parts ? n : n_parts;
@@ -410,7 +419,9 @@ __device__ inline void fused_merge(const P &p, uint32_t seq, uint32_t part, uint
     uint32_t n = L > 0 ? ((uint32_t)L + p.part_tokens - 1) / p.part_tokens : 0;
     n = n < p.n_parts ? n : p.n_parts;
     const uint32_t gs = merge_group_size(n), ng = n > gs ? (n + gs - 1) / gs : 1;
-    int32_t *cnt = p.counters + (uint64_t)seq * merge_counters_per_seq(p.n_parts);
+    // partials and counters of partitioned row seq sit at index seq - n_direct
+    const uint64_t pseq = seq - p.n_direct;
+    int32_t *cnt = p.counters + pseq * merge_counters_per_seq(p.n_parts);
     const __half *po = static_cast<const __half *>(p.part_o);
     const float2 *pml = reinterpret_cast<const float2 *>(p.part_ml);
     if (ng > 1) {
@@ -418,7 +429,7 @@ __device__ inline void fused_merge(const P &p, uint32_t seq, uint32_t part, uint
         if (!merge_arrive(cnt + 1 + g, ng_g))
             return;
         for (uint32_t h = warp; h < p.hq; h += 2 * nwarps) {
-            const uint64_t s0 = (uint64_t)seq * p.hq + h;
+            const uint64_t s0 = pseq * p.hq + h;
             const uint64_t s1 = h + nwarps < p.hq ? s0 + nwarps : s0;
             const __half *rpo[2] = {po + (s0 * p.n_parts + p0) * p.d,
                                     po + (s1 * p.n_parts + p0) * p.d};
@@ -439,11 +450,13 @@ __device__ inline void fused_merge(const P &p, uint32_t seq, uint32_t part, uint
         return;
     const uint32_t m = ng > 1 ? ng : n, stride = ng > 1 ? gs : 1;
     for (uint32_t h = warp; h < p.hq; h += 2 * nwarps) {
-        const uint64_t s0 = (uint64_t)seq * p.hq + h;
+        const uint64_t s0 = pseq * p.hq + h;
         const uint64_t s1 = h + nwarps < p.hq ? s0 + nwarps : s0;
+        const uint64_t o0 = (uint64_t)seq * p.hq + h;
+        const uint64_t o1 = h + nwarps < p.hq ? o0 + nwarps : o0;
         const __half *rpo[2] = {po + s0 * p.n_parts * p.d, po + s1 * p.n_parts * p.d};
         const float2 *rml[2] = {pml + s0 * p.n_parts, pml + s1 * p.n_parts};
-        float *rout[2] = {p.out + s0 * p.d, p.out + s1 * p.d};
+        float *rout[2] = {p.out + o0 * p.d, p.out + o1 * p.d};
         const int nr = h + nwarps < p.hq ? 2 : 1;
         if (p.d == 256)
             merge_rows_warp_v<8, 2, false, BATCH>(rpo, rml, m, stride, p.d, nr, rout, nullptr, nullptr);

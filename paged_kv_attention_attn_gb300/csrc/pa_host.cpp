@@ -200,7 +200,7 @@ extern "C" int pa_plan(const pa_plan_in *in, pa_plan_t *out)
     const uint64_t rows = (uint64_t)in->n_seqs * T, work = T * in->total_len;
     if (rows > 0x7fffffffull)
         return fail(PA_ERR_RANGE, E, "n_seqs * q_tokens exceeds 2^31 - 1");
-    uint64_t part, n_parts;
+    uint64_t part, n_parts, n_direct = 0;
     if (in->max_len == 0) {
         part = TILE;
         n_parts = 1;
@@ -231,6 +231,19 @@ extern "C" int pa_plan(const pa_plan_in *in, pa_plan_t *out)
             if (wide > part) part = wide < cap ? wide : cap;
         }
         n_parts = cdiv(in->max_len, part);
+        // a direct batch wider than the machine with a short last wave: the
+        // full waves stay direct, the r rows of the last one are split so
+        // that their partitions fill it
+        const uint64_t r = rows % slots;
+        if (n_parts == 1 && rows > slots && r > 0 && slots / r >= 2) {
+            uint64_t pr = roundup(cdiv(in->max_len, slots / r), TILE);
+            if (pr < MIN_PART) pr = MIN_PART;
+            if (cdiv(in->max_len, pr) >= 2) {
+                part = pr;
+                n_parts = cdiv(in->max_len, pr);
+                n_direct = rows - r;
+            }
+        }
     }
     pa_plan_t p;
     memset(&p, 0, sizeof p);
@@ -238,18 +251,20 @@ extern "C" int pa_plan(const pa_plan_in *in, pa_plan_t *out)
     p.n_parts = (uint32_t)n_parts;
     p.direct = n_parts == 1;
     p.q_tokens = (uint32_t)T;
+    p.n_direct = (uint32_t)n_direct;
     if (p.direct) {
         p.n_ctas = (uint32_t)rows;
     } else {
-        uint64_t a = rows * n_parts;
-        uint64_t b = cdiv(work, part) + rows;
-        uint64_t n = a < b ? a : b;
+        const uint64_t m = rows - n_direct;  // partitioned rows
+        uint64_t a = m * n_parts;
+        uint64_t b = cdiv(work, part) + m;
+        uint64_t n = n_direct + (n_direct || a < b ? a : b);
         if (n > 0x7fffffffull)
             return fail(PA_ERR_RANGE, E, "grid of %llu CTAs exceeds 2^31-1", (unsigned long long)n);
         p.n_ctas = (uint32_t)n;
-        p.part_o_bytes = rows * in->hq * n_parts * in->d * 2ull;
-        p.part_ml_bytes = rows * in->hq * n_parts * 8ull;
-        p.counter_bytes = rows * pa::merge_counters_per_seq((uint32_t)n_parts) * 4ull;
+        p.part_o_bytes = m * in->hq * n_parts * in->d * 2ull;
+        p.part_ml_bytes = m * in->hq * n_parts * 8ull;
+        p.counter_bytes = m * pa::merge_counters_per_seq((uint32_t)n_parts) * 4ull;
     }
     *out = p;
     // PA_LOG_PLAN (set, not "0"): one line per plan on stderr
@@ -257,9 +272,9 @@ extern "C" int pa_plan(const pa_plan_in *in, pa_plan_t *out)
     if (log && *log && strcmp(log, "0") != 0)
         fprintf(stderr,
                 "pa_plan: n_seqs=%u q_tokens=%u max_len=%u total_len=%llu slots=%lld "
-                "force_parts=%d -> part_tokens=%u n_parts=%u direct=%u n_ctas=%u\n",
+                "force_parts=%d -> part_tokens=%u n_parts=%u direct=%u n_direct=%u n_ctas=%u\n",
                 in->n_seqs, p.q_tokens, in->max_len, (unsigned long long)in->total_len,
                 (long long)in->sm_count * in->ctas_per_sm, in->force_parts, p.part_tokens,
-                p.n_parts, p.direct, p.n_ctas);
+                p.n_parts, p.direct, p.n_direct, p.n_ctas);
     return PA_OK;
 }

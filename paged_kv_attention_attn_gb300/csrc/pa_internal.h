@@ -70,6 +70,8 @@ struct DecodeParams {
     uint64_t k_row_bytes, v_row_bytes;
     int32_t *counters;      // fused merge: per-sequence completion counters, or null
     uint32_t q_tokens;      // query tokens per sequence; n_seqs counts query rows
+    uint32_t n_direct;      // leading rows decoded directly in a partitioned plan; the
+                            // partials, counters and merges index row r at r - n_direct
 };
 
 // Launchers (each returns PA_OK or an error already recorded for `entry`).
@@ -80,7 +82,7 @@ int launch_plain_decode(const DecodeParams &p, pa_type kt, pa_type vt, cudaStrea
 int plain_decode_occupancy(pa_type kt, pa_type vt, uint32_t d, uint32_t hq, int *ctas_per_sm);
 int launch_merge(const void *part_o, const float *part_ml, const int32_t *seq_lens, float *out,
                  uint32_t n_seqs, uint32_t q_tokens, uint32_t hq, uint32_t d, uint32_t n_parts,
-                 uint32_t part_tokens, cudaStream_t st, const char *entry);
+                 uint32_t part_tokens, uint32_t n_direct, cudaStream_t st, const char *entry);
 int launch_append(const pa_append_args *a, cudaStream_t st, const char *entry);
 int launch_debug_offsets(const int32_t *block_table, uint32_t table_stride,
                          const int32_t *seq_lens, uint32_t n_seqs, uint32_t max_tokens,

@@ -67,8 +67,12 @@ extern "C" int pa_decode_step_noalloc(const pa_decode_args *args, const pa_plan_
     const uint64_t rows = (uint64_t)args->n_seqs * (plan->q_tokens > 1 ? plan->q_tokens : 1) *
                           args->hq;
     const uint64_t q81_bytes = quantised ? round256(rows * (args->d / 32) * 36ull) : 0;
-    const uint64_t po_bytes = plan->direct ? 0 : round256(rows * plan->n_parts * args->d * 2ull);
-    const uint64_t pm_bytes = plan->direct ? 0 : round256(rows * plan->n_parts * 8ull);
+    // partials of the partitioned rows only (those after the n_direct leading ones)
+    const uint64_t prows = plan->direct || plan->n_direct * (uint64_t)args->hq > rows
+                               ? 0
+                               : rows - (uint64_t)plan->n_direct * args->hq;
+    const uint64_t po_bytes = plan->direct ? 0 : round256(prows * plan->n_parts * args->d * 2ull);
+    const uint64_t pm_bytes = plan->direct ? 0 : round256(prows * plan->n_parts * 8ull);
     const uint64_t need = q81_bytes + po_bytes + pm_bytes;
     if (need > PA_NOALLOC_SCRATCH_BYTES)
         return pa::fail(PA_ERR_RANGE, E,

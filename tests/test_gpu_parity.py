@@ -401,3 +401,67 @@ def test_long_single_partition(t):
     out, ws, pl, _ = H.run(case, force_parts=1)
     assert pa.status_read(ws.status) == 0
     H.assert_close(case, out, H.oracle_out(case), H.oracle_vmax(case))
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("t", TYPES)
+def test_wave_filling_plan(kernel, t):
+    """A batch wider than the machine (here 4 slots, so that a few rows make
+    it wide) and about even, so that it would run direct: 10 rows = 2 waves +
+    2, so the first 8 rows run direct and the last 2 are split in halves to
+    fill the third wave.  Empty rows sit on both sides of the cut.  Fused and
+    separate merges, against the oracle; the fused merge gives the separate
+    merge's bits and leaves the counters at zero."""
+    lens = [700, 650, 0, 700, 16, 690, 700, 680, 0, 700]
+    spec = synth.CaseSpec(seq_lens=lens, k_type=t, v_type=t, junk=5, outliers=True,
+                          name=f"wavefill-{t}")
+    case = synth.build_case(spec, seed=3400 + t, device=DEV)
+    pl = pa.plan(seq_lens=lens, block_size=16, hq=24, hkv=4, d=256, k_type=t, v_type=t,
+                 sm_count=4, ctas_per_sm=1)
+    assert pl.n_direct == 8 and not pl.direct and pl.n_parts >= 2
+    ref, vmax = H.oracle_out(case), H.oracle_vmax(case)
+    a, ws_a, _, _ = H.run(case, plan=pl, flags=KERNELS[kernel], canary=True)
+    b, ws_b, _, tails = H.run(case, plan=pl, flags=KERNELS[kernel], fused=True, canary=True)
+    H.check_canaries(tails)
+    assert pa.status_read(ws_a.status) == 0 and pa.status_read(ws_b.status) == 0
+    assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+    assert int(ws_b.counters.abs().sum()) == 0
+    H.assert_close(case, b, ref, vmax)
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_wave_filling_plan_two_pass(kernel):
+    """41 rows of 5000 tokens on 40 slots: 40 direct rows, and the last row in
+    40 partitions of 128 tokens, merged in two passes (the staged merge on
+    the fast kernel)."""
+    lens = [5000] * 41
+    spec = synth.CaseSpec(seq_lens=lens, k_type=synth.Q4_0, v_type=synth.Q4_0, junk=3,
+                          name="wavefill-2pass")
+    case = synth.build_case(spec, seed=3450, device=DEV)
+    pl = pa.plan(seq_lens=lens, block_size=16, hq=24, hkv=4, d=256, k_type=2, v_type=2,
+                 sm_count=40, ctas_per_sm=1)
+    assert (pl.n_direct, pl.n_parts, pl.part_tokens) == (40, 40, 128)
+    a, _, _, _ = H.run(case, plan=pl, flags=KERNELS[kernel])
+    b, ws, _, _ = H.run(case, plan=pl, flags=KERNELS[kernel], fused=True)
+    assert pa.status_read(ws.status) == 0
+    assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+    assert int(ws.counters.abs().sum()) == 0
+    units = [(s, h) for s in (0, 17, 39, 40) for h in (0, 5, 23)]
+    H.assert_close(case, b, H.oracle_out(case, units=units), H.oracle_vmax(case, units=units),
+                   units=units)
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_wave_filling_plan_multitoken(kernel):
+    """The same cut over query rows: 5 sequences x 2 query tokens = 10 rows on
+    4 slots, 8 direct rows and 2 split ones (the last sequence's tokens)."""
+    lens = [300, 41, 0, 520, 777]
+    spec = synth.CaseSpec(seq_lens=lens, k_type=synth.Q4_0, v_type=synth.Q4_0, junk=3,
+                          extra={"q_tokens": 2}, name="wavefill-T2")
+    case = synth.build_case(spec, seed=3500, device=DEV)
+    pl = pa.plan(seq_lens=lens, block_size=16, hq=24, hkv=4, d=256, k_type=2, v_type=2,
+                 sm_count=4, ctas_per_sm=1, q_tokens=2)
+    assert pl.n_direct == 8 and not pl.direct
+    out, ws, _, _ = H.run(case, plan=pl, flags=KERNELS[kernel], fused=True)
+    assert pa.status_read(ws.status) == 0
+    H.assert_close(case, out, H.oracle_out(case), H.oracle_vmax(case))

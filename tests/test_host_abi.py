@@ -208,6 +208,6 @@ def test_plan_log_line_when_asked():
         if expect:
             assert lines == ["pa_plan: n_seqs=8 q_tokens=1 max_len=131072 total_len=1048576 "
                              "slots=152 force_parts=0 -> part_tokens=6912 n_parts=19 direct=0 "
-                             "n_ctas=152"]
+                             "n_direct=0 n_ctas=152"]
         else:
             assert lines == []

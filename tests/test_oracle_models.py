@@ -107,19 +107,26 @@ def test_plan_covers_every_token_and_bounds_the_grid():
         assert n * P >= mx and (n - 1) * P < max(mx, 1)
         assert p["direct"] == (n == 1)
         # the grid has a CTA for every live partition of every query row and
-        # one for every empty row (which writes its zero output)
+        # one for every empty row (which writes its zero output); the leading
+        # n_direct rows of a wave-filling plan have one CTA each
         rows = [max(0, L - (T - 1 - i)) for L in lens for i in range(T)]
-        live = sum(max(1, math.ceil(L / P)) for L in rows)
+        nd = p["n_direct"]
+        live = nd + sum(max(1, math.ceil(L / P)) for L in rows[nd:])
         assert p["n_ctas"] >= (S * T if p["direct"] else live)
         assert p["n_ctas"] <= S * T * n
+        if nd:
+            # only a direct-sized batch wider than the machine fills its last wave
+            slots = sm * cps
+            assert not force and not p["direct"] and n >= 2 and S * T > slots
+            assert nd == S * T - (S * T) % slots and p["n_ctas"] == nd + (S * T - nd) * n
         if force:
             assert n <= force
         elif not p["direct"] and S * T < sm * cps:
             # fewer query rows than slots: the grid fits one wave
             assert p["n_ctas"] <= sm * cps
         if not p["direct"]:
-            assert p["part_o_bytes"] == S * T * 24 * n * 256 * 2
-            assert p["part_ml_bytes"] == S * T * 24 * n * 8
+            assert p["part_o_bytes"] == (S * T - nd) * 24 * n * 256 * 2
+            assert p["part_ml_bytes"] == (S * T - nd) * 24 * n * 8
 
 
 def test_plan_worked_examples():
@@ -140,9 +147,21 @@ def test_plan_worked_examples():
     # a verify window of 4 tokens on 8 x 32768: 32 query rows in one wave
     rc, p = _plan(n_seqs=8, max_len=32768, total_len=8 * 32768, q_tokens=4)
     assert (p["part_tokens"], p["n_parts"], p["n_ctas"]) == (8192, 4, 128)
-    # a batch at least as wide as the machine runs direct
+    # a batch of whole waves runs direct
+    rc, p = _plan(n_seqs=304, max_len=4096, total_len=304 * 4096)
+    assert p["direct"] == 1 and p["n_ctas"] == 304 and p["n_direct"] == 0
+    # wider batches fill their last wave: 160 x 6912 keeps 152 direct rows and
+    # splits the other 8 into ceil(6912 / 19) -> 384-token partitions (18 each),
+    # 152 + 144 CTAs instead of a second wave of 8 full-length ones
+    rc, p = _plan(n_seqs=160, max_len=6912, total_len=160 * 6912)
+    assert (p["part_tokens"], p["n_parts"], p["n_direct"], p["n_ctas"]) == (384, 18, 152, 296)
+    assert p["part_o_bytes"] == 8 * 24 * 18 * 256 * 2 and p["direct"] == 0
+    # 512 x 4096: three direct waves (456 rows) and 56 rows in halves
     rc, p = _plan(n_seqs=512, max_len=4096, total_len=512 * 4096)
-    assert p["direct"] == 1 and p["n_ctas"] == 512
+    assert (p["part_tokens"], p["n_parts"], p["n_direct"], p["n_ctas"]) == (2048, 2, 456, 568)
+    # a last wave more than half full stays direct (no split fits it)
+    rc, p = _plan(n_seqs=256, max_len=4096, total_len=256 * 4096)
+    assert p["direct"] == 1 and p["n_ctas"] == 256
     # forcing one partition is direct; empty batch is direct
     assert _plan(n_seqs=4, max_len=32768, total_len=4 * 32768, force_parts=1)[1]["direct"] == 1
     assert _plan(n_seqs=3, max_len=0, total_len=0)[1]["direct"] == 1
