@@ -210,7 +210,9 @@ int pa_query_occupancy(const pa_plan_in *in, int32_t *sm_count, int32_t *ctas_pe
  * part_o[s][h][p][:] = (sum over the partition of 2^(s2_t - m) V_t) / l in
  * f16 and part_ml[s][h][p] = (m, l), where s2_t = s_t * log2(e), m is the
  * partition maximum of s2_t and l = sum 2^(s2_t - m); pa_merge then forms
- * O.  Direct plans write out directly and touch no partial.
+ * O.  Direct plans write out directly and touch no partial.  A wave-filling
+ * plan (plan->n_direct > 0) writes out directly for its first n_direct
+ * query rows and partials for the others, at row index s - n_direct.
  * A block id outside [0, n_pool_blocks) is never dereferenced: the kernel
  * sets PA_STATUS_CORRUPT_TABLE in *status and treats that block's tokens as
  * absent (pa_status_read reports it).  Pool offsets are 64-bit throughout:
@@ -229,8 +231,9 @@ typedef struct {
     const void *q;                   /* device: float32 [n_seqs][T][hq][d] for F16 K,
                                         q8_1 [n_seqs][T][hq][d/32] otherwise (T = q_tokens) */
     float scale;                     /* softmax scale; callers pass 1/sqrt(d) */
-    void *part_o;                    /* device f16 [n_seqs*T][hq][n_parts][d] (unused if direct) */
-    float *part_ml;                  /* device float32 [n_seqs*T][hq][n_parts][2] */
+    void *part_o;                    /* device f16 [n_seqs*T - n_direct][hq][n_parts][d]
+                                        (unused if direct) */
+    float *part_ml;                  /* device float32 [n_seqs*T - n_direct][hq][n_parts][2] */
     float *out;                      /* device float32 [n_seqs][T][hq][d], 16-byte aligned
                                         (written if direct or fused) */
     int32_t *status;                 /* device int32 status word (required) */
@@ -260,8 +263,9 @@ const char *pa_decode_kernel_name(pa_type k_type, pa_type v_type, uint32_t d, ui
  * hierarchical reduction): groups of gs = ceil(sqrt(n_live)) consecutive
  * partitions are merged into f16 partials of the same form, then those; the
  * same as the flat merge up to rounding.  Reads the partials only.  Layouts
- * as in pa_decode_args.  PA_ERR_INVALID for a direct plan (nothing to
- * merge).  Indexing is 64-bit; PA_ERR_RANGE if the partial buffer exceeds
+ * as in pa_decode_args; the first plan->n_direct query rows have no
+ * partials and their out rows are left as they are.  PA_ERR_INVALID for a
+ * direct plan (nothing to merge).  Indexing is 64-bit; PA_ERR_RANGE if the partial buffer exceeds
  * 2^40 elements. */
 int pa_merge(const void *part_o, const float *part_ml, const int32_t *seq_lens, float *out,
              uint32_t n_seqs, uint32_t hq, uint32_t d, const pa_plan_t *plan,
