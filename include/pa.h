@@ -147,13 +147,14 @@ int pa_quantize_q(const float *q, void *q8_1, uint32_t n_rows, uint32_t d, pa_st
  *  - n_parts = ceil(max_len / part_tokens); direct = (n_parts == 1): no
  *    partials, the decode kernel writes the output;
  *  - a batch wider than the machine (n_seqs > slots) that this makes direct,
- *    with n_seqs = k * slots + r, 0 < r and floor(slots / r) >= 2, fills its
- *    last wave instead: the first n_direct = k * slots sequences stay direct
- *    (one CTA each, output written by the decode kernel) and the last r are
- *    split into partitions of part_tokens = roundup(ceil(max_len /
- *    floor(slots / r)), 32) (at least 128), n_parts = ceil(max_len /
- *    part_tokens) >= 2 of them; direct = 0.  Every other plan has
- *    n_direct = 0;
+ *    with n_seqs = k * slots + r and 0 < r, may fill its last wave instead:
+ *    the first n_direct = k * slots sequences stay direct (one CTA each,
+ *    output written by the decode kernel) and the last r are split into
+ *    n_parts >= 2 partitions of part_tokens = max(128, roundup(ceil(max_len
+ *    / np), 32)), where np in 2..64 minimises ceil(r * n_parts / slots) *
+ *    (part_tokens + 512), the estimated time of those waves (512 tokens
+ *    stand for a CTA's fixed work), if that is below max_len + 512 (the
+ *    first minimum wins); direct = 0.  Every other plan has n_direct = 0;
  *  - n_ctas = n_seqs when direct, else n_direct + min(m * n_parts,
  *    ceil(total_len / part_tokens) + m) with m = n_seqs - n_direct (>= the
  *    live partitions; a wave-filling plan counts m * n_parts);

@@ -26,11 +26,15 @@ frozen here so that the C++ planner can be compared with it exactly:
   partial buffers' second dimension); a sequence of length L has
   ceil(L / part_tokens) live partitions;
 - a batch wider than the machine (S > slots) left direct by the above, with
-  S = k * slots + r, r > 0 and floor(slots / r) >= 2, fills its last wave:
-  the first n_direct = k * slots sequences stay direct (one CTA each) and the
-  last r take part_tokens = max(128, roundup(ceil(max_len / floor(slots /
-  r)), 32)), n_parts = ceil(max_len / part_tokens) (only when that is >= 2);
-  every other plan has n_direct = 0;
+  S = k * slots + r and r > 0, may split the r rows of its last wave: for
+  np = 2 .. 64 (stopping where fewer than 2 partitions remain), part =
+  max(128, roundup(ceil(max_len / np), 32)), nparts = ceil(max_len / part),
+  the estimated time ceil(r * nparts / slots) * (part + CTA_COST) with
+  CTA_COST = 512 tokens; the first strict minimum below max_len + CTA_COST
+  (the time of leaving them whole) wins, and then the first n_direct =
+  k * slots sequences stay direct (one CTA each) and the last r take
+  part_tokens = part, n_parts = nparts; otherwise the plan stays direct.
+  Every other plan has n_direct = 0;
 - n_parts == 1 selects direct mode: no partials, the decode kernel writes
   the output itself;
 - the decode grid has n_ctas = S in direct mode, otherwise n_direct +
@@ -53,6 +57,7 @@ import math
 
 TILE = 32
 MIN_PART = 128
+CTA_COST = 512  # a CTA's fixed work in tokens of streaming (wave-filling plans)
 
 OK, INVALID = 0, -1
 
@@ -99,10 +104,18 @@ def plan(*, n_seqs, max_len, total_len, block_size, hq, hkv, d, k_type, v_type,
                                  _roundup(max_len, TILE)))
         n_parts = _cdiv(max_len, part)
         r = rows % slots
-        if n_parts == 1 and rows > slots and r > 0 and slots // r >= 2:
-            pr = max(MIN_PART, _roundup(_cdiv(max_len, slots // r), TILE))
-            if _cdiv(max_len, pr) >= 2:
-                part, n_parts, n_direct = pr, _cdiv(max_len, pr), rows - r
+        if n_parts == 1 and rows > slots and r > 0:
+            best_t, best_part = max_len + CTA_COST, 0
+            for np_ in range(2, 65):
+                pr = max(MIN_PART, _roundup(_cdiv(max_len, np_), TILE))
+                nparts = _cdiv(max_len, pr)
+                if nparts < 2:
+                    break
+                t = _cdiv(r * nparts, slots) * (pr + CTA_COST)
+                if t < best_t:
+                    best_t, best_part = t, pr
+            if best_part:
+                part, n_parts, n_direct = best_part, _cdiv(max_len, best_part), rows - r
     direct = 1 if n_parts == 1 else 0
     if direct:
         n_ctas = rows

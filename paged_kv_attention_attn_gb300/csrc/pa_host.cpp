@@ -231,16 +231,33 @@ extern "C" int pa_plan(const pa_plan_in *in, pa_plan_t *out)
             if (wide > part) part = wide < cap ? wide : cap;
         }
         n_parts = cdiv(in->max_len, part);
-        // a direct batch wider than the machine with a short last wave: the
-        // full waves stay direct, the r rows of the last one are split so
-        // that their partitions fill it
+        // a direct batch wider than the machine with a partial last wave:
+        // the full waves stay direct, and the r rows of the last one are
+        // split into the partition count np (2..64) that minimises the
+        // estimated time of what follows the full waves,
+        //   ceil(r * np / slots) waves * (partition tokens + CTA_COST),
+        // against max_len + CTA_COST for leaving them whole.  CTA_COST is
+        // the fixed work of a CTA (prologue, combine, merge arrival, about
+        // 15 us) in tokens streamed at one SM's share of HBM (about 26 ns).
+        const uint64_t CTA_COST = 512;
         const uint64_t r = rows % slots;
-        if (n_parts == 1 && rows > slots && r > 0 && slots / r >= 2) {
-            uint64_t pr = roundup(cdiv(in->max_len, slots / r), TILE);
-            if (pr < MIN_PART) pr = MIN_PART;
-            if (cdiv(in->max_len, pr) >= 2) {
-                part = pr;
-                n_parts = cdiv(in->max_len, pr);
+        if (n_parts == 1 && rows > slots && r > 0) {
+            uint64_t best_t = in->max_len + CTA_COST, best_part = 0;
+            for (uint64_t np = 2; np <= 64; ++np) {
+                uint64_t pr = roundup(cdiv(in->max_len, np), TILE);
+                if (pr < MIN_PART) pr = MIN_PART;
+                const uint64_t nparts = cdiv(in->max_len, pr);
+                if (nparts < 2)
+                    break;
+                const uint64_t t = cdiv(r * nparts, slots) * (pr + CTA_COST);
+                if (t < best_t) {
+                    best_t = t;
+                    best_part = pr;
+                }
+            }
+            if (best_part) {
+                part = best_part;
+                n_parts = cdiv(in->max_len, best_part);
                 n_direct = rows - r;
             }
         }

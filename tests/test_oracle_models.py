@@ -159,7 +159,11 @@ def test_plan_worked_examples():
     # 512 x 4096: three direct waves (456 rows) and 56 rows in halves
     rc, p = _plan(n_seqs=512, max_len=4096, total_len=512 * 4096)
     assert (p["part_tokens"], p["n_parts"], p["n_direct"], p["n_ctas"]) == (2048, 2, 456, 568)
-    # a last wave more than half full stays direct (no split fits it)
+    # 230 x 4096: a last wave of 78 rows in thirds, two waves of 1376-token
+    # partitions (2 x (1376 + 512) < 4096 + 512 in the planner's estimate)
+    rc, p = _plan(n_seqs=230, max_len=4096, total_len=230 * 4096)
+    assert (p["part_tokens"], p["n_parts"], p["n_direct"], p["n_ctas"]) == (1376, 3, 152, 386)
+    # 256 x 4096: no split of the last 104 rows beats leaving them whole
     rc, p = _plan(n_seqs=256, max_len=4096, total_len=256 * 4096)
     assert p["direct"] == 1 and p["n_ctas"] == 256
     # forcing one partition is direct; empty batch is direct
