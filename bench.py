@@ -304,6 +304,52 @@ def run_reference(a, world, rank):
 
 # ------------------------------------------------------------------- ours
 
+def time_append(spec, dev, stream, K, warmup):
+    """The step before the decode: pa_append_kv of one new token per
+    sequence of the workload (its types, heads and head size), K calls back
+    to back between two events.  Separate one-block-per-sequence buffers;
+    every call starts from its own copy of the lengths (mid-block, so no
+    fresh block), so that each writes the same slot and the workload's own
+    pools are left alone."""
+    import ctypes
+    import paged_kv_attention_attn_gb300 as pa
+    S, B, hkv, d = spec.n_seqs, spec.block_size, spec.hkv, spec.d
+    krb, vrb = synth.row_bytes(spec.k_type, d), synth.row_bytes(spec.v_type, d)
+    kp = torch.zeros((S, B, hkv, krb), dtype=torch.uint8, device=dev)
+    vp = torch.zeros((S, B, hkv, vrb), dtype=torch.uint8, device=dev)
+    table = torch.arange(S, dtype=torch.int32, device=dev).view(S, 1)
+    lens = torch.full((warmup + K, S), B // 2, dtype=torch.int32, device=dev)
+    g = torch.Generator(device=dev).manual_seed(7)
+    k_new = torch.randn((S, hkv, d), generator=g, device=dev)
+    v_new = torch.randn((S, hkv, d), generator=g, device=dev)
+    fresh = torch.zeros(S, dtype=torch.int32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    calls = [pa.AppendArgs(k_pool=kp.data_ptr(), v_pool=vp.data_ptr(), n_pool_blocks=S,
+                           block_table=table.data_ptr(), table_stride=1,
+                           seq_lens=lens[i].data_ptr(), k_new=k_new.data_ptr(),
+                           v_new=v_new.data_ptr(), fresh_blocks=fresh.data_ptr(),
+                           status=status.data_ptr(), n_seqs=S, hkv=hkv, d=d, block_size=B,
+                           k_type=spec.k_type, v_type=spec.v_type) for i in range(warmup + K)]
+    refs = [ctypes.byref(c) for c in calls]
+    L, sh = pa.lib(), stream.cuda_stream
+    for i in range(warmup):
+        if L.pa_append_kv(refs[i], sh) != 0:
+            raise RuntimeError(L.pa_last_error().decode())
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(warmup, warmup + K):
+        L.pa_append_kv(refs[i], sh)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    assert pa.status_read(status) == 0
+    us = e0.elapsed_time(e1) * 1e3 / K
+    nbytes = S * hkv * d * 4 * 2 + S * hkv * (krb + vrb) + S * 4 * 3
+    return {"us_per_call": us, "GB/s": nbytes / us / 1e3, "bytes_per_call": nbytes,
+            "n_seqs": S, "calls": K,
+            "how": "pa_append_kv of one token per sequence, back to back between two events"}
+
+
 def run_ours(a, world, rank, local):
     import paged_kv_attention_attn_gb300 as pa
     from paged_kv_attention_attn_gb300 import build as pa_build
@@ -494,6 +540,8 @@ def run_ours(a, world, rank, local):
     e2e = {"value": aggregate(nb["step"], K, world, e2e_s), "unit": "GB/s",
            "us_per_step": e2e_s * 1e6 / K, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
+    append = time_append(spec, dev, stream, min(K, 500), a.warmup)
+
     cpu = None
     if world == 1 and not a.no_cpu_baseline:
         host = host_copy(case)
@@ -545,6 +593,7 @@ def run_ours(a, world, rank, local):
                      "bytes_per_launch": nb["decode"],
                      "traffic": traffic_from_profiles(kname, a.workload, pl.as_dict())},
         "cpu_baseline": cpu,
+        "append": append,
         "e2e": e2e,
         "gpu_launches": K * (1 if in_kernel_q else
                              (2 if quantised else 1) + (0 if (pl.direct or fused) else 1)),
