@@ -341,3 +341,83 @@ def test_query_token_i_is_the_one_token_step_on_the_prefix():
     ref = oracle.decode(k, v, bt, sl, q4[:, 0], hkv=sp.hkv, block_size=sp.block_size,
                         k_type=sp.k_type, v_type=sp.v_type)
     assert np.array_equal(one[:, 0], ref)
+
+
+# ------------------------------------------------------- the gate's scale
+
+def _vmax_case():
+    """A case built by hand for the pin of oracle.vmax: K rows Q8_0, V rows
+    F16 (so the expected value comes from numpy's own half decoding), D=32,
+    Hq=4, Hkv=2 (heads 0, 1 read K/V head 0; heads 2, 3 head 1), 16-token
+    blocks.  Sequences of 20, 0 and 33 tokens.  The live V rows of head 0
+    stay below 1 except two planted values (2.5 at token 19 of sequence 0,
+    3.5 at token 32 of sequence 2); every row that a plausible mistake would
+    read instead holds a larger magnitude: K (100), the other K/V head's V
+    (40), junk blocks (70), slots past L in a last block (60) and the block
+    that the empty sequence's table row names (80)."""
+    d, hq, hkv, B = 32, 4, 2, 16
+    lens = [20, 0, 33]
+    table = np.array([[5, 2, -1], [7, -1, -1], [0, 3, 6]], dtype=np.int32)
+    n_blocks = 8                      # 1 and 4 are junk; 7 is named only by the empty row
+    rng = np.random.default_rng(31)
+    v = np.clip(rng.standard_normal((n_blocks, B, hkv, d)), -0.99, 0.99).astype(np.float16)
+    v[:, :, 1, :] = 40.0              # K/V head 1 everywhere
+    v[[1, 4]] = 70.0                  # junk blocks
+    v[7] = 80.0                       # the block of the empty sequence's table row
+    v[2, 4:] = 60.0                   # sequence 0: slots 4..15 of its last block (L = 20)
+    v[6, 1:] = 60.0                   # sequence 2: slots 1..15 of its last block (L = 33)
+    v[2, 3, 0, 5] = -2.5              # sequence 0, token 19, head 0
+    v[6, 0, 0, 7] = 3.5               # sequence 2, token 32, head 0
+    v_pool = v.view(np.uint8).reshape(n_blocks, B, hkv, 2 * d)
+    # Q8_0 K rows: scale 100 (f16) and every code 1, so |K| = 100 everywhere
+    k_row = np.zeros(34, dtype=np.uint8)
+    k_row[0:2] = np.array([100.0], dtype=np.float16).view(np.uint8)
+    k_row[2:] = 1
+    k_pool = np.broadcast_to(k_row, (n_blocks, B, hkv, 34)).copy()
+    q = rng.standard_normal((3, hq, d)).astype(np.float32)
+    return dict(k_pool=k_pool, v_pool=v_pool, table=table, lens=np.array(lens, np.int32), q=q,
+                hkv=hkv, B=B)
+
+
+def _numpy_vmax(c, units, T=1):
+    """max |V| over the rows the units read, walked in numpy from the
+    definition (row u of a T-token plan is token u % T of sequence u // T
+    and sees L - T + 1 + u % T keys)."""
+    G = c["q"].shape[-2] // c["hkv"]
+    v = c["v_pool"].view(np.float16).reshape(c["v_pool"].shape[:3] + (-1,))
+    m = 0.0
+    for u, h in units:
+        s, i = divmod(u, T)
+        L = max(int(c["lens"][s]) - (T - 1 - i), 0)
+        for t in range(L):
+            blk = int(c["table"][s, t // c["B"]])
+            m = max(m, float(np.abs(v[blk, t % c["B"], h // G].astype(np.float64)).max()))
+    return m
+
+
+@pytest.mark.parametrize("units,expect", [
+    ([(0, 0), (2, 1)], 3.5),   # both planted values of head 0; 3.5 is the larger
+    ([(0, 1)], 2.5),           # sequence 0 alone: its planted value
+    ([(1, 0)], 0.0),           # the empty sequence reads no row
+    ([(1, 0), (0, 2)], 40.0),  # K/V head 1 of sequence 0
+])
+def test_oracle_vmax_reads_exactly_the_units_live_v_rows(units, expect):
+    c = _vmax_case()
+    got = oracle.vmax(c["k_pool"], c["v_pool"], c["table"], c["lens"], c["q"], hkv=c["hkv"],
+                      block_size=c["B"], k_type=synth.Q8_0, v_type=synth.F16, units=units)
+    assert got == expect
+    assert got == _numpy_vmax(c, units)
+
+
+def test_oracle_vmax_of_query_rows_sees_only_their_causal_prefix():
+    """With two query tokens per sequence, row 0 (token 0 of sequence 0)
+    sees 19 keys and misses the planted 2.5 at token 19; row 1 sees it."""
+    c = _vmax_case()
+    q2 = np.stack([c["q"], c["q"]], axis=1)  # [S, T=2, hq, d]
+    kw = dict(hkv=c["hkv"], block_size=c["B"], k_type=synth.Q8_0, v_type=synth.F16)
+    first = oracle.vmax(c["k_pool"], c["v_pool"], c["table"], c["lens"], q2, units=[(0, 0)],
+                        **kw)
+    second = oracle.vmax(c["k_pool"], c["v_pool"], c["table"], c["lens"], q2, units=[(1, 0)],
+                         **kw)
+    assert 0.0 < first < 1.0 and first == _numpy_vmax(c, [(0, 0)], T=2)
+    assert second == 2.5
