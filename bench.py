@@ -64,10 +64,9 @@ WORKLOADS = {
     "largepool-f16-b16x300000": synth.large_pool_spec,
 }
 DEFAULT_WORKLOAD = "uniform-q4_0-b8x131072"
-L2_BYTES = 129 * 10**6        # GB300 L2
+L2_BYTES = 129 * 2**20        # GB300 L2
 FLUSH_BYTES = 512 * 2**20     # the write that evicts it between timed steps (--flush on)
 MAX_LAYERS = 1024             # pool copies cycled through when K/V is under twice the L2
-L2_BYTES = 129 * 2**20
 
 
 def load_peaks():
@@ -350,6 +349,15 @@ def time_append(spec, dev, stream, K, warmup):
             "how": "pa_append_kv of one token per sequence, back to back between two events"}
 
 
+def check_status(pa, status, what: str):
+    """The kernels' status word must still be clear after `what`: a corrupt
+    table, a length past the plan or an abandoned pipeline wait during the
+    timed steps makes the whole line invalid."""
+    bits = pa.status_read(status)
+    if bits:
+        raise RuntimeError(f"status word 0x{bits:x} raised during {what}")
+
+
 def run_ours(a, world, rank, local):
     import paged_kv_attention_attn_gb300 as pa
     from paged_kv_attention_attn_gb300 import build as pa_build
@@ -482,6 +490,7 @@ def run_ours(a, world, rank, local):
     torch.cuda.synchronize()
     barrier(world)
     clk = clocks.stop()
+    check_status(pa, ws.status, "the timed steps")
     total_ms = start.elapsed_time(end)
     step_ms = sum(e0.elapsed_time(e1) for e0, e1 in sevs) if flush else total_ms
     max_s = reduce_max(step_ms / 1e3, world, dev)
@@ -504,6 +513,7 @@ def run_ours(a, world, rank, local):
         step()
         dist_evs[k][1].record(stream)
     torch.cuda.synchronize()
+    check_status(pa, ws.status, "the single-step timing pass")
     dist = sorted(e0.elapsed_time(e1) * 1e3 for e0, e1 in dist_evs)
     step_dist = {"p10": dist[n_dist // 10], "median": dist[n_dist // 2],
                  "p90": dist[(9 * n_dist) // 10], "n": n_dist,
@@ -534,6 +544,7 @@ def run_ours(a, world, rank, local):
         e2e_evs[0][1].record(stream)
     torch.cuda.synchronize()
     barrier(world)
+    check_status(pa, ws.status, "the end-to-end steps")
     e2e_s = reduce_max(sum(e0.elapsed_time(e1) for e0, e1 in e2e_evs) / 1e3, world, dev)
     h2d = q_host.numel() * 4
     d2h = out_host.numel() * 4
