@@ -333,8 +333,12 @@ int pa_decode_step_host(const float *q_host, float *out_host, const pa_decode_ar
  * output in *args (pools, table, lengths, the float32 query in args->q, out
  * and the status word); args->part_o and args->part_ml are ignored.
  *  - The first call on a device looks up the array's device address with
- *    that device current (cudaGetSymbolAddress), once per device; make that
- *    first call before any stream capture.
+ *    that device current (cudaGetSymbolAddress); later calls reuse it while
+ *    the device keeps the same context (a context made again, after
+ *    cudaDeviceReset say, is looked up afresh).  Make the first call on a
+ *    device before any stream capture.
+ *  - Every argument is checked before anything is launched, as for
+ *    pa_decode_step.
  *  - A step whose scratch (q8_1 rows plus partials, each rounded up to 256
  *    bytes) exceeds PA_NOALLOC_SCRATCH_BYTES is refused with PA_ERR_RANGE
  *    and the size it would need; nothing is launched.

@@ -123,6 +123,12 @@ int launch_decode(const pa_decode_args *a, const pa::DecodeParams &p, cudaStream
 
 }  // namespace
 
+int pa::check_decode(const pa_decode_args *a, const pa_plan_t *plan, const char *entry)
+{
+    pa::DecodeParams p;
+    return resolve(a, plan, entry, &p);
+}
+
 extern "C" int pa_quantize_q(const float *q, void *q8_1, uint32_t n_rows, uint32_t d,
                              pa_stream_t stream)
 {

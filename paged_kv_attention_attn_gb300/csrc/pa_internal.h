@@ -74,6 +74,10 @@ struct DecodeParams {
                             // partials, counters and merges index row r at r - n_direct
 };
 
+// The argument checks of pa_decode_partial alone: PA_OK, or the error
+// already recorded for `entry`.  Launches nothing.
+int check_decode(const pa_decode_args *a, const pa_plan_t *plan, const char *entry);
+
 // Launchers (each returns PA_OK or an error already recorded for `entry`).
 int launch_quantize_q(const float *q, void *q8_1, uint32_t n_rows, uint32_t d,
                       cudaStream_t st, const char *entry);

@@ -14,6 +14,9 @@
 // The step itself is the existing one: this file calls pa_quantize_q,
 // pa_decode_partial and pa_merge with pointers into the array and changes
 // nothing in them.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include <mutex>
 
 #include "pa_internal.h"
@@ -26,10 +29,46 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[PA_NOALLOC_SCRA
 
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
-void *g_addr[kMaxDevices] = {};
+// Per device: the address looked up, and the unique id of the context it
+// was looked up in.  A context that is destroyed and made again (after
+// cudaDeviceReset, say) has a new id, so the look-up runs again there.
+struct Entry {
+    void *addr = nullptr;
+    unsigned long long ctx_id = 0;
+    bool valid = false;
+};
+Entry g_entry[kMaxDevices];
 
-// Device address of the scratch on the current device, looked up once per
-// device (the first call on a device does it, with that device current).
+// The driver's cuCtxGetCurrent and cuCtxGetId, through the runtime's entry
+// point query (the library links only the runtime).
+struct CtxFns {
+    PFN_cuCtxGetCurrent_v4000 current = nullptr;
+    PFN_cuCtxGetId_v12000 id = nullptr;
+};
+
+const CtxFns &ctx_fns()
+{
+    static CtxFns f;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            f.current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            f.id = reinterpret_cast<PFN_cuCtxGetId_v12000>(p);
+    });
+    return f;
+}
+
+// Device address of the scratch in the current device's context.  The
+// look-up (cudaGetSymbolAddress, with that device current) runs on the first
+// call on a device and again only when the device's context has changed
+// since; it allocates nothing.
 int scratch_address(void **out, const char *E)
 {
     int dev = -1;
@@ -38,16 +77,30 @@ int scratch_address(void **out, const char *E)
         return rc;
     if (dev < 0 || dev >= kMaxDevices)
         return pa::fail(PA_ERR_RANGE, E, "device ordinal %d beyond %d", dev, kMaxDevices);
+    // make the device's primary context current on this thread (the
+    // runtime initialises it here if no earlier call did)
+    rc = pa::cuda_check(cudaSetDevice(dev), E, "cudaSetDevice");
+    if (rc)
+        return rc;
+    const CtxFns &f = ctx_fns();
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    // a context that cannot be identified is looked up afresh every call
+    const bool known = f.current && f.id && f.current(&ctx) == CUDA_SUCCESS && ctx &&
+                       f.id(ctx, &id) == CUDA_SUCCESS;
     std::lock_guard<std::mutex> lock(g_mu);
-    if (!g_addr[dev]) {
+    Entry &e = g_entry[dev];
+    if (!known || !e.valid || e.ctx_id != id) {
         void *p = nullptr;
         rc = pa::cuda_check(cudaGetSymbolAddress(&p, g_noalloc_scratch), E,
                             "cudaGetSymbolAddress of the static scratch");
         if (rc)
             return rc;
-        g_addr[dev] = p;
+        e.addr = p;
+        e.ctx_id = id;
+        e.valid = known;
     }
-    *out = g_addr[dev];
+    *out = e.addr;
     return PA_OK;
 }
 
@@ -89,6 +142,11 @@ extern "C" int pa_decode_step_noalloc(const pa_decode_args *args, const pa_plan_
         a.part_o = s + q81_bytes;
         a.part_ml = reinterpret_cast<float *>(s + q81_bytes + po_bytes);
     }
+    // every check of the decode call runs before the pre-pass is launched,
+    // so a refused call launches nothing
+    rc = pa::check_decode(&a, plan, E);
+    if (rc)
+        return rc;
     // Nothing in the scratch has to start at zero: the pre-pass writes every
     // q8_1 block, and the merge reads only partitions the decode kernel wrote
     // in this same step.
