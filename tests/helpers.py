@@ -87,12 +87,26 @@ def check_canaries(tails):
         assert bool((t == CANARY).all()), "a kernel wrote past the end of a buffer"
 
 
-def assert_close(case, got: torch.Tensor, ref: np.ndarray, vmax: float, units=None):
+# worst max|err| / max|V| seen per workload label, printed at the end of the
+# run (the margin of each gate: the gate is tol_for(spec))
+MARGINS: dict = {}
+
+
+def record_margin(label: str, err: float, vmax: float, tol: float):
+    r = err / vmax if vmax > 0 else 0.0
+    if r >= MARGINS.get(label, (-1.0, tol))[0]:
+        MARGINS[label] = (r, tol)
+
+
+def assert_close(case, got: torch.Tensor, ref: np.ndarray, vmax: float, units=None,
+                 label: str | None = None):
     g = got.cpu().double().numpy()
     if units is not None:
         g = np.stack([g[s, h] for s, h in units])
     assert np.isfinite(g).all(), "non-finite output"
     err = float(np.abs(g - ref).max()) if g.size else 0.0
     bound = tol_for(case.spec) * vmax
+    if label is not None:
+        record_margin(label, err, vmax, tol_for(case.spec))
     assert err <= bound, f"{case.spec.name}: max|err| {err:.3e} > {bound:.3e}"
     return err
