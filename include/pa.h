@@ -247,6 +247,10 @@ typedef struct {
  * the shapes, else the plain kernel; PA_FLAG_PLAIN forces the plain kernel
  * (one warp per query head, CUDA cores), kept as a second implementation. */
 #define PA_FLAG_PLAIN 1u
+/* For tests: the cooperative in-launch merge (see pa_decode_fused) gives up
+ * waiting at once, so the CTA that completes each count merges the rows of
+ * every CTA that stopped waiting.  The output is the same bit for bit. */
+#define PA_FLAG_MERGE_NO_WAIT 2u
 
 int pa_decode_partial(const pa_decode_args *args, const pa_plan_t *plan, pa_stream_t stream);
 
@@ -281,7 +285,16 @@ int pa_merge(const void *part_o, const float *part_ml, const int32_t *seq_lens, 
  * two-pass one (see pa_merge) its group's partials into the group's first
  * partial slot, and the CTA that completes the last group the group results
  * into out.  The result is pa_merge's bit for bit.  Every count is reset to 0
- * by the CTA that completes it.  No CTA ever waits for another.
+ * by the CTA that completes it, and no CTA waits for another -- except on the
+ * fast kernel, for one-pass plans (n_parts <= 32, n_direct == 0) whose whole
+ * grid fits the device at once: there the CTAs of a sequence wait for each
+ * other (at most 100 us; an environment variable PA_COOP_MERGE=0 turns this
+ * off) and each merges its share of the rows, same bits again; a CTA whose
+ * wait runs out leaves its rows to the CTA that completes the count.  The
+ * fast kernel is launched with programmatic stream serialisation (off with
+ * PA_PDL=0): it may be scheduled while the previous kernel on the stream
+ * finishes, and waits for that kernel's completion before it reads any
+ * input.
  * counters: device int32 [plan->counter_bytes / 4], caller-owned, all zero
  * before the first call; every completed call leaves them zero.  After a call
  * that reported PA_STATUS_TIMEOUT or PA_STATUS_LEN_OVER_PLAN the caller

@@ -23,6 +23,7 @@ PA_ERR_CUDA, PA_ERR_CORRUPT_TABLE, PA_ERR_RANGE, PA_ERR_TIMEOUT = -4, -5, -6, -7
 PA_STATUS_CORRUPT_TABLE, PA_STATUS_TIMEOUT, PA_STATUS_LEN_OVER_PLAN = 1, 2, 4
 PA_STATUS_APPEND_RANGE = 8
 PA_FLAG_PLAIN = 1
+PA_FLAG_MERGE_NO_WAIT = 2
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_build", "libpa.so")
 

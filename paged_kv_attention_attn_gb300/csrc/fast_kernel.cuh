@@ -38,6 +38,7 @@
 #include <cudaTypedefs.h>
 #include <math.h>
 
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 #include <unordered_map>
@@ -59,7 +60,13 @@ struct FastArgs {
     uint32_t n_slots;            // ring slots per warp
     uint32_t slot_bytes;         // K then V rows of one head for one tile
     uint32_t region_bytes;       // all rings; reused at the end to park (m, l, O)
+    uint32_t coop;               // in-launch merge shared by the CTAs of a sequence
+    uint32_t coop_wait_ns;       // bound of a CTA's wait for the others of its sequence
 };
+
+// Bound of the wait of the cooperative merge: far above the spread of the
+// finishing times of one sequence's CTAs in a grid that is resident at once.
+constexpr uint32_t kCoopWaitNs = 100000;
 
 // ------------------------------------------------------------------- PTX
 
@@ -105,14 +112,26 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
     return ok != 0;
 }
 
-__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int x, int y,
-                                            uint64_t *bar)
+// A 2-D tensor copy of box (x, y) into shared memory, completing on the
+// mbarrier, with an L2 eviction-priority hint (a createpolicy value).
+__device__ __forceinline__ void tma_load_2d_hint(void *dst, const CUtensorMap *map, int x, int y,
+                                                 uint64_t *bar, uint64_t policy)
 {
     asm volatile(
         "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+        ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(policy)
         : "memory");
+}
+
+// L2 policy for data read once: evicted before anything else, so that a
+// stream of K/V rows does not push the kernel's code, the block table, the
+// lengths and the partials out of the L2.
+__device__ __forceinline__ uint64_t l2_evict_first_policy()
+{
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
 }
 
 // One contiguous global range into shared memory (both 16-byte aligned, bytes
@@ -151,15 +170,17 @@ __device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1
 __device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], uint32_t addr)
 {
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-                 : "r"(addr));
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+        : "r"(addr)
+        : "memory");
 }
 
 __device__ __forceinline__ void ldsm_x4_trans(uint32_t (&r)[4], uint32_t addr)
 {
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-                 : "r"(addr));
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+        : "r"(addr)
+        : "memory");
 }
 
 __device__ __forceinline__ uint32_t h2_bits(__half2 h) { return *reinterpret_cast<uint32_t *>(&h); }
@@ -179,21 +200,21 @@ __device__ __forceinline__ uint32_t hmul2_bits(uint32_t x, uint32_t y)
 __device__ __forceinline__ uint32_t lds_u32(uint32_t a)
 {
     uint32_t v;
-    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(a));
+    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(a) : "memory");
     return v;
 }
 
 __device__ __forceinline__ uint32_t lds_u16(uint32_t a)
 {
     uint32_t v;  // zero-extended into a 32-bit register
-    asm volatile("ld.shared.u16 %0, [%1];" : "=r"(v) : "r"(a));
+    asm volatile("ld.shared.u16 %0, [%1];" : "=r"(v) : "r"(a) : "memory");
     return v;
 }
 
 __device__ __forceinline__ float2 lds_f2(uint32_t a)
 {
     float2 v;
-    asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(a));
+    asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(a) : "memory");
     return v;
 }
 
@@ -214,6 +235,25 @@ __device__ __forceinline__ uint32_t opaque(uint32_t v)
     uint32_t r;
     asm volatile("mov.b32 %0, %1;" : "=r"(r) : "r"(v));
     return r;
+}
+
+__device__ __forceinline__ uint32_t ld_acquire_u32(const int32_t *p)
+{
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Programmatic dependent launch: the wait for the grids this one depends on
+// (their writes visible), and the signal that the grids depending on this
+// one may be scheduled.
+__device__ __forceinline__ void grid_dependency_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 // (x & m) | c in one LOP3.
@@ -322,10 +362,10 @@ struct Q81Query {
                 amax = fmaxf(amax, fabsf(v[j]));
             amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
             amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-            const float d = amax / 127.0f;
+            const float d = amax / 127.0f, inv_d = 1.0f / d;
 #pragma unroll
             for (int j = 0; j < 8; ++j)
-                code[j] = q8_1_code(v[j], amax, d);
+                code[j] = q8_1_code(v[j], amax, d, inv_d);
             d16 = __half2float(__float2half_rn(amax == 0.0f ? 0.0f : d));
         } else {
 #pragma unroll
@@ -473,11 +513,13 @@ struct Q40T {
         uint32_t qb0, qb1, qb2, qb3;
         float c[4];
         asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                     : "=r"(qb0), "=r"(qb1), "=r"(qb2), "=r"(qb3)
-                     : "r"(qrec));
+            : "=r"(qb0), "=r"(qb1), "=r"(qb2), "=r"(qb3)
+            : "r"(qrec)
+            : "memory");
         asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
-                     : "=f"(c[0]), "=f"(c[1]), "=f"(c[2]), "=f"(c[3])
-                     : "r"(qrec + QCORR));
+            : "=f"(c[0]), "=f"(c[1]), "=f"(c[2]), "=f"(c[3])
+            : "r"(qrec + QCORR)
+            : "memory");
         const uint32_t y0 = x0 >> 8, y1 = x1 >> 8;
         mma16816(c, and_or(x0, K.mlo, K.blo), and_or(x1, K.mlo, K.blo), and_or(y0, K.mlo, K.blo),
                  and_or(y1, K.mlo, K.blo), qb0, qb1);
@@ -545,6 +587,7 @@ struct Q40T {
     {
         return 32 * (mt >> 1) + 16 * (mt & 1) + 2 * gid + upper;
     }
+    static constexpr bool kDimPairs = true;  // dim_of(mt, gid, 1) == dim_of(mt, gid, 0) + 1
 };
 
 using Q40 = Q40T<12>;
@@ -706,8 +749,9 @@ struct Q80T {
     {
         uint32_t b0, b1, q0, q1;
         asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                     : "=r"(b0), "=r"(b1), "=r"(q0), "=r"(q1)
-                     : "r"(qrec));
+            : "=r"(b0), "=r"(b1), "=r"(q0), "=r"(q1)
+            : "r"(qrec)
+            : "memory");
         int c[4] = {0, 0, 0, 0};
         imma(c, a0, a1, a2, a3, b0, b1);
         const float dq0 = __uint_as_float(q0), dq1 = __uint_as_float(q1);
@@ -782,6 +826,7 @@ struct Q80T {
     {
         return 16 * mt + 2 * gid + upper;
     }
+    static constexpr bool kDimPairs = true;
 };
 
 using Q80 = Q80T<8>;
@@ -905,6 +950,7 @@ struct F16T {
     {
         return 16 * mt + gid + 8 * upper;
     }
+    static constexpr bool kDimPairs = false;
 };
 
 // --- mixed K x V types, D = 256 -------------------------------------------
@@ -985,6 +1031,7 @@ struct Mix {
     {
         return VT::dim_of(mt, gid, upper);
     }
+    static constexpr bool kDimPairs = VT::kDimPairs;
 };
 
 // ------------------------------------------------------------------ kernel
@@ -1002,16 +1049,21 @@ constexpr float kHeadroom = 4.0f;  // log2 units kept between the reference and 
 // Parked (m, l, O) of one warp: m of its 8 head columns, then l, then O as
 // 8 rows of D floats (row stride D + 4, so that the fragment stores of the
 // four tig lanes fall in different banks).
+// After the warps' records: per query head, the combine's factors f_k of
+// the head's warps, then 1 / l, M and l (kFac floats per head).
 template <class T>
 struct Park {
     static constexpr int kRow = T::D + 4;
     static constexpr int kWarp = 16 + 8 * kRow;
+    static constexpr int kFac = T::kMaxWarps + 3;
+    static constexpr int kFacBytes = 64 * kFac * 4;  // 64 query heads at most
 };
 
 template <class T>
 __device__ __forceinline__ void combine_and_write(const DecodeParams &p, const float *park,
-                                                  uint32_t hkv, uint32_t wph, uint32_t G,
-                                                  uint32_t seq, uint32_t part, bool dir);
+                                                  float *fac, uint32_t hkv, uint32_t wph,
+                                                  uint32_t G, uint32_t seq, uint32_t part,
+                                                  bool dir);
 
 // One row of the in-launch merge by one warp from partials staged in shared
 // memory: m partials of D halves at po (global; partial k at po + k * stride
@@ -1068,16 +1120,18 @@ __device__ bool merge_row_staged(const DecodeParams &p, const __half *po, const 
     for (int j = 0; j < 8; ++j)
         acc[j] = 0.0f;
     const uint32_t base = stage + 8 * lane;
+#pragma unroll 4
     for (uint32_t k = 0; k < m; ++k) {
         const float wk = __shfl_sync(0xffffffffu, w, k);
         if (wk > 0.0f) {
             const uint32_t a = base + k * rb;
             uint32_t h[4];
-            asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(h[0]), "=r"(h[1]) : "r"(a));
+            asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(h[0]), "=r"(h[1]) : "r"(a) : "memory");
             if (D == 256)
                 asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];"
-                             : "=r"(h[2]), "=r"(h[3])
-                             : "r"(a + 256));
+                    : "=r"(h[2]), "=r"(h[3])
+                    : "r"(a + 256)
+                    : "memory");
             else
                 h[2] = h[3] = 0u;
 #pragma unroll
@@ -1172,6 +1226,123 @@ __device__ __noinline__ void merge_tail_staged(const DecodeParams &p, uint32_t s
     }
 }
 
+// The in-launch merge shared by the CTAs of a sequence, for one-pass plans
+// whose grid is resident at once (every CTA of the launch holds an SM slot
+// from the start, so the CTAs of a sequence finish within microseconds of one
+// another).  Each CTA counts its partial (word 0 of the sequence's counters),
+// waits until the count is complete, then merges the rows r with r % na ==
+// its partition (na = the sequence's live partitions), each row with the same
+// arithmetic, in the same order, as every other merge here.  The wait is
+// bounded (wait_ns): a CTA whose wait runs out sets its bit in word 1 and
+// merges nothing unless the count completed meanwhile; the CTA that completes
+// the count merges the rows of every partition whose bit it sees.  The two
+// sides order their write and read of words 0 and 1 with sequentially
+// consistent fences, so at least one of them merges each such row (both may:
+// they write the same bits).  Word 2 counts the CTAs that are done; the last
+// one resets the three words to 0.
+// A row's partials are contiguous, so a merging warp copies them into its
+// share of the idle rings with one bulk copy and sums them from shared
+// memory (merge_row_staged): one round trip, and a short loop -- this code
+// runs once per launch, when the instruction caches do not hold it.
+template <class T>
+__device__ __noinline__ void merge_coop(const DecodeParams &p, uint32_t seq, uint32_t part,
+                                        int32_t L, uint32_t warp, uint32_t nwarps,
+                                        uint32_t wait_ns, uint32_t region, uint32_t region_bytes)
+{
+    __shared__ uint32_t s_set;
+    const int lane = threadIdx.x & 31;
+    uint32_t n = L > 0 ? ((uint32_t)L + p.part_tokens - 1) / p.part_tokens : 0;
+    n = n < p.n_parts ? n : p.n_parts;
+    const uint32_t na = n > 0 ? n : 1u;  // arrivals: an empty sequence has one CTA
+    const uint64_t pseq = seq - p.n_direct;
+    int32_t *cnt = p.counters + pseq * merge_counters_per_seq(p.n_parts);
+    __syncthreads();  // every thread's partial stores come before the count
+    if (threadIdx.x == 0) {
+        __threadfence();
+        const uint32_t old = atomicAdd(reinterpret_cast<unsigned *>(cnt), 1u);
+        uint32_t set = 0;
+        if (old + 1 == na) {
+            __threadfence();  // the count before the read of the stop bits
+            set = (1u << part) | *reinterpret_cast<volatile uint32_t *>(cnt + 1);
+        } else {
+            const uint64_t t0 = global_ns();
+            while (true) {
+                if (ld_acquire_u32(cnt) >= na) {
+                    set = 1u << part;
+                    break;
+                }
+                if (global_ns() - t0 >= wait_ns) {
+                    atomicOr(reinterpret_cast<unsigned *>(cnt + 1), 1u << part);
+                    __threadfence();  // the stop bit before the read of the count
+                    if (*reinterpret_cast<volatile uint32_t *>(cnt) >= na)
+                        set = 1u << part;
+                    break;
+                }
+                __nanosleep(128);
+            }
+        }
+        __threadfence();  // the counted CTAs' partials before this CTA's reads
+        s_set = set;
+    }
+    __syncthreads();
+    const uint32_t set = s_set;
+    if (set) {
+        const __half *po = static_cast<const __half *>(p.part_o);
+        const float2 *pml = reinterpret_cast<const float2 *>(p.part_ml);
+        // k consecutive warp shares of the rings hold one row's n partials
+        // and the worker's mbarrier (its last 16 bytes)
+        const uint32_t share = (region_bytes / nwarps) & ~15u;
+        const uint32_t need = n * p.d * 2 + 16;
+        const uint32_t k = share ? (need + share - 1) / share : 0;
+        const bool staged = n > 0 && k >= 1 && k <= nwarps &&
+                            (reinterpret_cast<uintptr_t>(p.part_o) & 15u) == 0;
+        const uint32_t workers = staged ? nwarps / k : nwarps;
+        const bool worker = staged ? warp % k == 0 : true;
+        const uint32_t wid = staged ? warp / k : warp;
+        uint32_t stage = 0, phase = 0;
+        uint64_t *bar = nullptr;
+        if (staged && worker) {
+            stage = region + warp * share;
+            bar = reinterpret_cast<uint64_t *>(__cvta_shared_to_generic(stage + k * share - 16));
+            if (lane == 0) {
+                mbar_init(bar, 1);
+                asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+            }
+            __syncwarp();
+        }
+        uint32_t u = 0;  // rows of this CTA, in order; row u goes to worker u % workers
+        for (uint32_t r = 0; r < p.hq; ++r) {
+            if (!((set >> (r % na)) & 1u))
+                continue;
+            if (worker && wid < workers && u % workers == wid) {
+                const uint64_t row = pseq * p.hq + r;
+                const __half *rpo = po + row * p.n_parts * p.d;
+                const float2 *rml = pml + row * p.n_parts;
+                float *rout = p.out + ((uint64_t)seq * p.hq + r) * p.d;
+                if (staged)
+                    merge_row_staged<false>(p, rpo, rml, n, 1, stage, bar, phase, rout, nullptr,
+                                            nullptr);
+                else if (p.d == 256)
+                    merge_rows_warp_v<8, 1, false, 8>(&rpo, &rml, n, 1, p.d, 1, &rout, nullptr,
+                                                      nullptr);
+                else
+                    merge_rows_warp_v<4, 1, false, 8>(&rpo, &rml, n, 1, p.d, 1, &rout, nullptr,
+                                                      nullptr);
+            }
+            ++u;
+        }
+    }
+    __syncthreads();  // this CTA's reads of the words and the partials are done
+    if (threadIdx.x == 0) {
+        __threadfence();
+        if (atomicAdd(reinterpret_cast<unsigned *>(cnt + 2), 1u) + 1 == na) {
+            cnt[0] = 0;
+            cnt[1] = 0;
+            cnt[2] = 0;
+        }
+    }
+}
+
 // kStaged: the instance for plans of more than 32 partitions, whose merges
 // run in two passes (merge_tail_staged); the other plans take the instance
 // without it, whose code stays as it was tuned.
@@ -1200,6 +1371,8 @@ __global__ void __launch_bounds__(T::kMaxWarps * 32, 1)
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
+    // everything below reads inputs that an earlier grid may have written
+    grid_dependency_wait();
 
     uint32_t seq, part;
     if (!p.direct && blockIdx.x == gridDim.x - 1 && warp == 0)
@@ -1248,22 +1421,26 @@ __global__ void __launch_bounds__(T::kMaxWarps * 32, 1)
             uint8_t *dst = ring + (size_t)s * SLOT;
             const int y = (blk << bshift) + (int)(tok & bmask);
             fence_proxy_async();  // earlier generic reads of this slot come first
+            // K/V rows are read once: evict-first in the L2
+            const uint64_t pol = l2_evict_first_policy();
             if constexpr (kSym) {
                 mbar_arrive_expect_tx(&full[s], SLOT);
 #pragma unroll
                 for (uint32_t c = 0; c < T::kTmaXK; ++c) {
-                    tma_load_2d(dst + c * (voff / T::kTmaXK), tmk, 64 * c, y, &full[s]);
-                    tma_load_2d(dst + voff + c * (voff / T::kTmaXK), tmv, 64 * c, y, &full[s]);
+                    tma_load_2d_hint(dst + c * (voff / T::kTmaXK), tmk, 64 * c, y, &full[s], pol);
+                    tma_load_2d_hint(dst + voff + c * (voff / T::kTmaXK), tmv, 64 * c, y,
+                                     &full[s], pol);
                 }
             } else {
                 mbar_arrive_expect_tx(&full[s], T::kSideK + T::kSideV);
 #pragma unroll
                 for (uint32_t c = 0; c < T::kTmaXK; ++c)
-                    tma_load_2d(dst + c * (T::kSideK / T::kTmaXK), tmk, 64 * c, y, &full[s]);
+                    tma_load_2d_hint(dst + c * (T::kSideK / T::kTmaXK), tmk, 64 * c, y, &full[s],
+                                     pol);
 #pragma unroll
                 for (uint32_t c = 0; c < T::kTmaXV; ++c)
-                    tma_load_2d(dst + voff + c * (T::kSideV / T::kTmaXV), tmv, 64 * c, y,
-                                &full[s]);
+                    tma_load_2d_hint(dst + voff + c * (T::kSideV / T::kTmaXV), tmv, 64 * c, y,
+                                     &full[s], pol);
             }
         } else {
             atomicOr(p.status, PA_STATUS_CORRUPT_TABLE);
@@ -1393,6 +1570,10 @@ __global__ void __launch_bounds__(T::kMaxWarps * 32, 1)
             phase ^= 1;
         }
     }
+    // the next grid on this stream may be scheduled once every CTA is here
+    // (its CTAs take the SMs that this grid's CTAs leave, and wait for this
+    // grid's completion before they read anything)
+    launch_dependents();
     if (aborted && lane == 0) {
         // let my copies still in flight land (bounded) before the CTA moves on
         for (uint32_t k = issued > NSW ? issued - NSW : 0; k < issued; ++k) {
@@ -1422,15 +1603,34 @@ __global__ void __launch_bounds__(T::kMaxWarps * 32, 1)
         mine[8 + 2 * tig] = l0;
         mine[8 + 2 * tig + 1] = l1;
     }
+    // the columns of query heads past the group (2 tig + e % 2 >= G) are not read
+    if (2u * tig < G) {
 #pragma unroll
-    for (int mt = 0; mt < T::MT; ++mt)
+        for (int mt = 0; mt < T::MT; ++mt) {
+            if constexpr (T::kDimPairs) {
+                // the two rows of a column are adjacent dimensions: one 8-byte store
 #pragma unroll
-        for (int e = 0; e < 4; ++e)
-            mine[16 + (2 * tig + (e & 1)) * Park<T>::kRow + T::dim_of(mt, gid, e >> 1)] = o[mt][e];
+                for (int c = 0; c < 2; ++c)
+                    if (c == 0 || 2u * tig + 1 < G)
+                        *reinterpret_cast<float2 *>(
+                            mine + 16 + (2 * tig + c) * Park<T>::kRow + T::dim_of(mt, gid, 0)) =
+                            make_float2(o[mt][c], o[mt][c + 2]);
+            } else {
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    if ((e & 1) == 0 || 2u * tig + 1 < G)
+                        mine[16 + (2 * tig + (e & 1)) * Park<T>::kRow +
+                             T::dim_of(mt, gid, e >> 1)] = o[mt][e];
+            }
+        }
+    }
     __syncthreads();
-    combine_and_write<T>(p, park, hkv, wph, G, seq, part, dir);
+    combine_and_write<T>(p, park, park + nwarps * Park<T>::kWarp, hkv, wph, G, seq, part, dir);
     if (p.counters && !dir) {
-        if constexpr (kStaged) {
+        if (a.coop) {
+            merge_coop<T>(p, seq, part, Lrow, warp, nwarps, a.coop_wait_ns, smem_u32(smem),
+                          a.region_bytes);
+        } else if constexpr (kStaged) {
             // each warp stages its merge rows in its share of the idle rings
             // and waits on its slot-0 mbarrier, whose next parity follows the
             // loop's uses of slot 0 (all landed unless the loop aborted)
@@ -1447,49 +1647,66 @@ __global__ void __launch_bounds__(T::kMaxWarps * 32, 1)
 
 // Combine of the parked (m, l, O) of the wph warps of every head group into
 // the partition's result: for each query head, M = max of the warps'
-// reference maxima, f_k = 2^(m_k - M), O = sum f_k O_k / sum f_k l_k.  Every
-// thread of the CTA takes 8-dim chunks of the output rows, so the partial
-// rows are written with coalesced 16-byte stores (f16 partials) or 32-byte
-// stores (the f32 output of a direct CTA, `dir`).
+// reference maxima, f_k = 2^(m_k - M), O = sum f_k O_k / sum f_k l_k.  First
+// one thread per query head forms M, the f_k and 1 / sum f_k l_k into `fac`;
+// then every thread of the CTA takes 8-dim chunks of the output rows, so the
+// partial rows are written with coalesced 16-byte stores (f16 partials) or
+// 32-byte stores (the f32 output of a direct CTA, `dir`).  The loops stay
+// rolled: this runs once per launch, from cold instruction caches.
 template <class T>
 __device__ __forceinline__ void combine_and_write(const DecodeParams &p, const float *park,
-                                                  uint32_t hkv, uint32_t wph, uint32_t G,
-                                                  uint32_t seq, uint32_t part, bool dir)
+                                                  float *fac, uint32_t hkv, uint32_t wph,
+                                                  uint32_t G, uint32_t seq, uint32_t part,
+                                                  bool dir)
 {
     constexpr uint32_t NQ = T::D / 8;
-    const uint32_t n_chunks = hkv * G * NQ;
+    constexpr uint32_t FS = Park<T>::kFac;
+    const uint32_t nh = hkv * G;
+    for (uint32_t hg = threadIdx.x; hg < nh; hg += blockDim.x) {
+        const uint32_t g = hg / G, h = hg - g * G;
+        float M = -INFINITY;
+#pragma unroll 1
+        for (uint32_t k = 0; k < wph; ++k)
+            M = fmaxf(M, park[(g + k * hkv) * Park<T>::kWarp + h]);
+        float l = 0.0f;
+#pragma unroll 1
+        for (uint32_t k = 0; k < wph; ++k) {
+            const float *w = park + (g + k * hkv) * Park<T>::kWarp;
+            const float mk = w[h];
+            const float f = mk == -INFINITY ? 0.0f : exp2f(mk - M);
+            l = fmaf(w[8 + h], f, l);
+            fac[hg * FS + k] = f;
+        }
+        fac[hg * FS + T::kMaxWarps] = l > 0.0f ? 1.0f / l : 0.0f;
+        fac[hg * FS + T::kMaxWarps + 1] = l > 0.0f ? M : -INFINITY;
+        fac[hg * FS + T::kMaxWarps + 2] = l;
+    }
+    __syncthreads();
+    const uint32_t n_chunks = nh * NQ;
+#pragma unroll 1
     for (uint32_t c = threadIdx.x; c < n_chunks; c += blockDim.x) {
         const uint32_t hg = c / NQ, q = c % NQ;
         const uint32_t g = hg / G, h = hg - g * G;
-        float M = -INFINITY;
-#pragma unroll
-        for (uint32_t k = 0; k < T::kMaxWarps; ++k)
-            if (k < wph)
-                M = fmaxf(M, park[(g + k * hkv) * Park<T>::kWarp + h]);
-        float l = 0.0f, acc[8];
+        float acc[8];
 #pragma unroll
         for (int j = 0; j < 8; ++j)
             acc[j] = 0.0f;
-#pragma unroll
-        for (uint32_t k = 0; k < T::kMaxWarps; ++k) {
-            if (k < wph) {
-                const float *w = park + (g + k * hkv) * Park<T>::kWarp;
-                const float mk = w[h];
-                const float f = mk == -INFINITY ? 0.0f : exp2f(mk - M);
-                l = fmaf(w[8 + h], f, l);
-                const float4 *src = reinterpret_cast<const float4 *>(w + 16 + h * Park<T>::kRow + 8 * q);
-                const float4 a = src[0], b = src[1];
-                acc[0] = fmaf(f, a.x, acc[0]);
-                acc[1] = fmaf(f, a.y, acc[1]);
-                acc[2] = fmaf(f, a.z, acc[2]);
-                acc[3] = fmaf(f, a.w, acc[3]);
-                acc[4] = fmaf(f, b.x, acc[4]);
-                acc[5] = fmaf(f, b.y, acc[5]);
-                acc[6] = fmaf(f, b.z, acc[6]);
-                acc[7] = fmaf(f, b.w, acc[7]);
-            }
+#pragma unroll 4
+        for (uint32_t k = 0; k < wph; ++k) {
+            const float f = fac[hg * FS + k];
+            const float4 *src = reinterpret_cast<const float4 *>(
+                park + (g + k * hkv) * Park<T>::kWarp + 16 + h * Park<T>::kRow + 8 * q);
+            const float4 a = src[0], b = src[1];
+            acc[0] = fmaf(f, a.x, acc[0]);
+            acc[1] = fmaf(f, a.y, acc[1]);
+            acc[2] = fmaf(f, a.z, acc[2]);
+            acc[3] = fmaf(f, a.w, acc[3]);
+            acc[4] = fmaf(f, b.x, acc[4]);
+            acc[5] = fmaf(f, b.y, acc[5]);
+            acc[6] = fmaf(f, b.z, acc[6]);
+            acc[7] = fmaf(f, b.w, acc[7]);
         }
-        const float inv = l > 0.0f ? 1.0f / l : 0.0f;
+        const float inv = fac[hg * FS + T::kMaxWarps];
         if (dir) {
             const uint64_t row = (uint64_t)seq * p.hq + hg;
             float4 *dst = reinterpret_cast<float4 *>(p.out + row * T::D + 8 * q);
@@ -1506,8 +1723,8 @@ __device__ __forceinline__ void combine_and_write(const DecodeParams &p, const f
             __half *po = static_cast<__half *>(p.part_o);
             *reinterpret_cast<uint4 *>(po + (row * p.n_parts + part) * T::D + 8 * q) = v;
             if (q == 0)
-                reinterpret_cast<float2 *>(p.part_ml)[row * p.n_parts + part] =
-                    make_float2(l > 0.0f ? M : -INFINITY, l);
+                reinterpret_cast<float2 *>(p.part_ml)[row * p.n_parts + part] = make_float2(
+                    fac[hg * FS + T::kMaxWarps + 1], fac[hg * FS + T::kMaxWarps + 2]);
         }
     }
 }
@@ -1540,7 +1757,7 @@ Geometry geometry(uint32_t hkv)
 {
     Geometry gm;
     const size_t slot = T::kSlot;
-    const size_t park_per_warp = Park<T>::kWarp * 4;
+    const size_t park_per_warp = Park<T>::kWarp * 4, fac_bytes = Park<T>::kFacBytes;
     for (uint32_t wph = T::kMaxWarps / hkv; wph >= 1; --wph) {
         const uint32_t warps = wph * hkv;
         const size_t fixed = 1024 + warps * (size_t)T::SCRATCH + warps * 16 * 12 + 64 +
@@ -1555,7 +1772,7 @@ Geometry geometry(uint32_t hkv)
             gm.warps = warps;
             gm.n_slots = (uint32_t)ns;
             gm.slot_bytes = (uint32_t)slot;
-            size_t ring = warps * ns * slot, park = warps * park_per_warp;
+            size_t ring = warps * ns * slot, park = warps * park_per_warp + fac_bytes;
             gm.region = (uint32_t)(ring > park ? ring : park);
             gm.smem = 1024 + gm.region + warps * ns * (8 + 4) + 16 + warps * (size_t)T::SCRATCH +
                       hkv * (size_t)T::QBYTES;
@@ -1681,6 +1898,38 @@ int cached_maps(const DecodeParams &p, FastArgs &a, const char *entry)
     return PA_OK;
 }
 
+// A boolean setting from the environment, read once: unset, "" or anything
+// but "0" keeps the default `on`.
+bool env_on(const char *name)
+{
+    const char *v = getenv(name);
+    return !(v && v[0] == '0' && v[1] == '\0');
+}
+
+// CTA slots of the current device for this instance (SMs x CTAs per SM), once
+// per device; 0 if unknown.
+template <class T>
+uint32_t resident_slots(const Geometry &gm)
+{
+    static std::mutex mu;
+    static uint32_t slots[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+        return 0;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!slots[dev]) {
+        int sms = 0, cps = 0;
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&cps, fast_decode_kernel<T, false>,
+                                                          gm.warps * 32, gm.smem) != cudaSuccess) {
+            cudaGetLastError();
+            return 0;
+        }
+        slots[dev] = (uint32_t)(sms * cps);
+    }
+    return slots[dev];
+}
+
 template <class T>
 int launch_t(const DecodeParams &p, cudaStream_t st, const char *entry)
 {
@@ -1699,13 +1948,34 @@ int launch_t(const DecodeParams &p, cudaStream_t st, const char *entry)
     rc = cuda_check(allow_smem<T>(), entry, "cudaFuncSetAttribute");
     if (rc)
         return rc;
+    // the cooperative in-launch merge: one-pass plans (at most 32 partitions)
+    // without direct rows whose whole grid is resident at once
+    static const bool coop_on = env_on("PA_COOP_MERGE");
+    a.coop = coop_on && p.counters && !p.direct && p.n_direct == 0 &&
+             merge_group_size(p.n_parts) >= p.n_parts && p.n_ctas <= resident_slots<T>(gm);
+    a.coop_wait_ns = p.merge_no_wait ? 0u : kCoopWaitNs;
     // two-pass merges (more than 32 partitions) on CTAs of 8 warps or more
     // take the instance with the staged merge
-    if (T::kStagedMerge && p.counters && !p.direct && merge_group_size(p.n_parts) < p.n_parts &&
-        gm.warps >= 8)
-        fast_decode_kernel<T, T::kStagedMerge><<<p.n_ctas, gm.warps * 32, gm.smem, st>>>(a);
-    else
-        fast_decode_kernel<T, false><<<p.n_ctas, gm.warps * 32, gm.smem, st>>>(a);
+    const bool staged = T::kStagedMerge && p.counters && !p.direct &&
+                        merge_group_size(p.n_parts) < p.n_parts && gm.warps >= 8;
+    // programmatic dependent launch: this grid may be scheduled while the
+    // previous grid on the stream finishes; the kernel waits for that grid
+    // (griddepcontrol.wait) before it reads any input
+    static const bool pdl_on = env_on("PA_PDL");
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.n_ctas);
+    cfg.blockDim = dim3(gm.warps * 32);
+    cfg.dynamicSmemBytes = gm.smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl_on ? 1 : 0;
+    cudaError_t e = staged ? cudaLaunchKernelEx(&cfg, fast_decode_kernel<T, T::kStagedMerge>, a)
+                           : cudaLaunchKernelEx(&cfg, fast_decode_kernel<T, false>, a);
+    if (e != cudaSuccess)
+        return cuda_check(e, entry, "fast_decode_kernel launch");
     return cuda_check(cudaGetLastError(), entry, "fast_decode_kernel launch");
 }
 

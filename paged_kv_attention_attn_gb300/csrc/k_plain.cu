@@ -30,7 +30,7 @@ __global__ void __launch_bounds__(256) quantize_q8_1_kernel(const float *__restr
         const float v = x[b * 32 + lane];
         const float amax = warp_max(fabsf(v));
         float d = amax / 127.0f;
-        const int q = q8_1_code(v, amax, d);
+        const int q = q8_1_code(v, amax, d, 1.0f / d);
         const int sum = warp_sum_int(q);
         if (amax == 0.0f)
             d = 0.0f;

@@ -105,6 +105,7 @@ int resolve(const pa_decode_args *a, const pa_plan_t *plan, const char *E, pa::D
     p->counters = nullptr;
     p->q_f32 = 0;
     p->n_direct = plan->direct ? 0 : plan->n_direct;
+    p->merge_no_wait = (a->flags & PA_FLAG_MERGE_NO_WAIT) ? 1u : 0u;
     return PA_OK;
 }
 

@@ -45,12 +45,20 @@ __device__ __forceinline__ uint16_t load_u16(const uint8_t *p)
 // clamped to [-127, 127]; an all-zero block codes as 0.  The q8_1 pre-pass
 // kernel and the decode kernel that quantises its own query share this, so
 // both give the same codes.
-__device__ __forceinline__ int q8_1_code(float v, float amax, float d)
+// The product v * inv_d (inv_d = 1 / d rounded) is within about 1.5e-5 of the
+// exact quotient v / d, and so is the rounded quotient (|v / d| <= 127 + a
+// rounding step); both round to the same integer unless a half-integer lies
+// within that distance.  So the quotient is divided out exactly only when the
+// product is within 3e-5 of a half-integer, and the codes are those of the
+// IEEE division either way.
+__device__ __forceinline__ int q8_1_code(float v, float amax, float d, float inv_d)
 {
     if (amax == 0.0f)
         return 0;
-    const float r = fminf(fmaxf(roundf(v / d), -127.0f), 127.0f);
-    return (int)r;
+    const float r = v * inv_d;
+    const float a = fabsf(r);
+    const float q = fabsf(a - truncf(a) - 0.5f) > 3.0e-5f ? roundf(r) : roundf(v / d);
+    return (int)fminf(fmaxf(q, -127.0f), 127.0f);
 }
 
 __device__ __forceinline__ float warp_max(float v)

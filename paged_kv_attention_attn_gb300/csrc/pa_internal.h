@@ -72,6 +72,7 @@ struct DecodeParams {
     uint32_t q_tokens;      // query tokens per sequence; n_seqs counts query rows
     uint32_t n_direct;      // leading rows decoded directly in a partitioned plan; the
                             // partials, counters and merges index row r at r - n_direct
+    uint32_t merge_no_wait; // PA_FLAG_MERGE_NO_WAIT: cooperative merges give up waiting
 };
 
 // The argument checks of pa_decode_partial alone: PA_OK, or the error

@@ -354,20 +354,26 @@ def test_lengths_past_the_plan_are_flagged_and_stay_in_bounds(kernel, fused):
 
 
 @pytest.mark.parametrize("kernel", KERNELS)
-@pytest.mark.parametrize("force", [8, 24, 60])
-def test_fused_merge_waits_for_every_partition(kernel, force):
+@pytest.mark.parametrize("force", [6, 8, 24, 60])
+@pytest.mark.parametrize("no_wait", [False, True])
+def test_fused_merge_waits_for_every_partition(kernel, force, no_wait):
     """The in-launch merge of a sequence must start only after its last
     partition (one pass) or last group (two passes) is written.  Many
     sequences with many partitions each, several launches in a row: any
-    early merge shows up as a difference from the separate merge."""
+    early merge shows up as a difference from the separate merge.  On the
+    fast kernel the one-pass plans whose grid is resident at once merge
+    cooperatively (every CTA of a sequence waits for the others and merges
+    its share of the rows); no_wait makes every such wait give up at once, so
+    the CTA that completes each count merges the rows of the others."""
     spec = synth.CaseSpec(seq_lens=[4000 - 37 * i for i in range(24)], k_type=synth.Q4_0,
                           v_type=synth.Q4_0, junk=5)
     case = synth.build_case(spec, seed=3200 + force, device=DEV)
     ref, _, pl, _ = H.run(case, force_parts=force, flags=KERNELS[kernel])
     ws = pa.workspace(pl, n_seqs=spec.n_seqs, hq=24, d=256, device=DEV)
+    flags = KERNELS[kernel] | (pa.PA_FLAG_MERGE_NO_WAIT if no_wait else 0)
     args = pa.make_args(k_pool=case.k_pool, v_pool=case.v_pool, block_table=case.block_table,
                         seq_lens=case.seq_lens, q=case.q, ws=ws, hkv=4, block_size=16,
-                        k_type=spec.k_type, v_type=spec.v_type, flags=KERNELS[kernel])
+                        k_type=spec.k_type, v_type=spec.v_type, flags=flags)
     for _ in range(6):
         ws.out.fill_(float("nan"))
         pa.decode_step_fused(args, ws)
