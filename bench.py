@@ -98,6 +98,23 @@ def algorithmic_bytes(spec, plan, fused: bool = True, in_kernel_q: bool = False)
     if plan.direct:
         part_w = part_r = 0
         dec_out = out
+    elif getattr(plan, "stream", 0):
+        # a stream plan: rows cut by the CTAs' tile ranges get one partial per
+        # CTA that covers them; the others are written directly
+        chunk = plan.part_tokens // 16
+        pre, live, out_direct = 0, 0, 0
+        for L in rows:
+            tiles = -(-L // 16)
+            if tiles:
+                nr = (pre + tiles - 1) // chunk - pre // chunk + 1
+                if nr > 1:
+                    live += nr
+                else:
+                    out_direct += hq * d * 4
+            pre += tiles
+        part_w = part_r = live * hq * (2 * d + 8)
+        dec_out = part_w + out_direct
+        out -= out_direct  # what the merges write
     else:
         # the leading n_direct rows of a wave-filling plan write out directly
         nd = int(plan.n_direct)
@@ -371,7 +388,8 @@ def run_ours(a, world, rank, local):
     flags = pa.PA_FLAG_PLAIN if a.plain else 0
     pl = pa.plan(q_tokens=int(spec.extra.get("q_tokens", 1)),
                  seq_lens=spec.seq_lens, block_size=spec.block_size, hq=spec.hq, hkv=spec.hkv,
-                 d=spec.d, k_type=spec.k_type, v_type=spec.v_type)
+                 d=spec.d, k_type=spec.k_type, v_type=spec.v_type,
+                 stream_ok=not a.unfused and not a.plain and a.stream == "on")
     ws = pa.workspace(pl, n_seqs=spec.n_seqs, hq=spec.hq, d=spec.d, device=dev)
     quantised = spec.k_type != synth.F16
     kv_bytes = (case.k_pool.numel() + case.v_pool.numel())
@@ -396,7 +414,8 @@ def run_ours(a, world, rank, local):
                                   hq=spec.hq, hkv=spec.hkv, block_size=spec.block_size,
                                   flags=flags)
     # the fused step of the fast kernel quantises the query itself: one launch
-    in_kernel_q = not a.unfused and quantised and kname == "fast_decode_kernel"
+    in_kernel_q = (not a.unfused and quantised and kname == "fast_decode_kernel"
+                   and not pl.stream)
     nb = algorithmic_bytes(spec, pl, fused=not a.unfused, in_kernel_q=in_kernel_q)
     stream = torch.cuda.current_stream()
     L = pa.lib()
@@ -414,7 +433,7 @@ def run_ours(a, world, rank, local):
         p_step_args = p_layer_args[layer[0]]
         p_args = p_layer_dec_args[layer[0]]
         layer[0] = (layer[0] + 1) % n_layers
-        if in_kernel_q:  # the public one-launch step
+        if in_kernel_q or (pl.stream and fused):  # the public fused step
             if ev0 is not None:
                 ev0.record(stream)
             rc = L.pa_decode_step_fused(p_step_args, p_plan, ws.q8_1.data_ptr(), counters, sh)
@@ -595,6 +614,8 @@ def run_ours(a, world, rank, local):
                    "kernel": kname, "plan": pl.as_dict(),
                    "step": ("one launch: in-kernel q8_1 quantisation, decode, in-launch merge"
                             if in_kernel_q else
+                            "stream plan: q8_1 pre-pass + stream-K decode with in-launch merges"
+                            if pl.stream else
                             "q8_1 pre-pass + decode with in-launch merge" if fused else
                             "q8_1 pre-pass + decode + merge kernel"),
                    "bytes_per_step": nb},
@@ -607,7 +628,8 @@ def run_ours(a, world, rank, local):
         "append": append,
         "e2e": e2e,
         "gpu_launches": K * (1 if in_kernel_q else
-                             (2 if quantised else 1) + (0 if (pl.direct or fused) else 1)),
+                             (2 if quantised else 1) + (0 if (pl.direct or fused or pl.stream)
+                                                        else 1)),
         "clocks": clk,
     }
     if rank == 0:
@@ -629,6 +651,8 @@ def main():
     ap.add_argument("--flush", choices=["auto", "on", "off"], default="auto",
                     help="auto: K/V under 2 x L2 cycles through pool copies (one per step); "
                          "on: flush the L2 before every step instead; off: neither")
+    ap.add_argument("--stream", choices=["on", "off"], default="off",
+                    help="let the planner return stream plans (batches wider than the grid)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="oracle work timed for cpu_baseline (whole sequences in turn)")
     a = ap.parse_args()

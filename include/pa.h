@@ -170,6 +170,17 @@ int pa_quantize_q(const float *q, void *q8_1, uint32_t n_rows, uint32_t d, pa_st
  * (row u = s * T + i, of length L_s - T + 1 + i) with T * total_len tokens of
  * work: every n_seqs above reads n_seqs * T and total_len reads T * total_len;
  * max_len and n_parts are per row.
+ * Stream plans ("feat: add paged-attention monolithic decode-only AR
+ * foundation", lucebox pull 555, Roadmap: stream-K decode): with
+ * PA_PLAN_STREAM_OK in flags, force_parts = 0, more query rows than slots,
+ * k_type == v_type, hkv in {1, 2, 4, 8} and d = 256 (or F16 K/V), the grid
+ * takes equal ranges of the rows' 16-token tiles instead of whole rows or
+ * partitions: with B = ceil((T * total_len + 15 * rows) / 16) (a bound on
+ * the tiles), chunk = roundup(ceil(B / slots), 2) tiles, part_tokens =
+ * 16 * chunk, n_ctas = min(slots, ceil(B / chunk)), n_parts = ceil(ceil(
+ * max_len / 16) / chunk) + 1 (the most CTAs one row can span), stream = 1,
+ * direct = 0, n_direct = 0, partial buffers and counters for every row
+ * (m = rows below), if n_parts <= 32 and rows <= 16384; else the rules above.
  * Limits: block_size 16 or 32, d 128 or 256, hq a multiple of hkv with
  * hq / hkv <= 8, total_len <= n_seqs * max_len.  PA_ERR_INVALID otherwise. */
 typedef struct {
@@ -180,7 +191,12 @@ typedef struct {
     int32_t sm_count, ctas_per_sm;
     int32_t force_parts;         /* 0 = automatic */
     uint32_t q_tokens;           /* query tokens per sequence (0 or 1: one; see below) */
+    uint32_t flags;              /* PA_PLAN_* */
 } pa_plan_in;
+
+/* pa_plan_in.flags: the plan may be a stream plan (see below); only
+ * pa_decode_fused and pa_decode_step_fused on the fast kernel run those. */
+#define PA_PLAN_STREAM_OK 1u
 
 typedef struct {
     uint32_t part_tokens, n_parts, direct, n_ctas;
@@ -188,6 +204,7 @@ typedef struct {
     uint64_t counter_bytes;      /* completion counters of pa_decode_fused (0 when direct) */
     uint32_t q_tokens;           /* query tokens per sequence (>= 1) */
     uint32_t n_direct;           /* leading query rows decoded directly in a partitioned plan */
+    uint32_t stream;             /* 1: a stream plan (equal tile ranges per CTA) */
 } pa_plan_t;
 
 /* With the environment variable PA_LOG_PLAN set (to anything but "" or
@@ -214,6 +231,8 @@ int pa_query_occupancy(const pa_plan_in *in, int32_t *sm_count, int32_t *ctas_pe
  * O.  Direct plans write out directly and touch no partial.  A wave-filling
  * plan (plan->n_direct > 0) writes out directly for its first n_direct
  * query rows and partials for the others, at row index s - n_direct.
+ * Stream plans run only through pa_decode_fused and pa_decode_step_fused on
+ * the fast kernel (PA_ERR_INVALID here and in pa_merge and pa_decode_step).
  * A block id outside [0, n_pool_blocks) is never dereferenced: the kernel
  * sets PA_STATUS_CORRUPT_TABLE in *status and treats that block's tokens as
  * absent (pa_status_read reports it).  Pool offsets are 64-bit throughout:

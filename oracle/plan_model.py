@@ -48,6 +48,13 @@ frozen here so that the C++ planner can be compared with it exactly:
   counters per such sequence (one for the last pass, one per group of the
   two-pass merge): counter_bytes = 4 * m * (1 + ceil(sqrt(n_parts))); all 0
   when direct;
+- a stream plan (flags & STREAM_OK, no force_parts, max_len > 0, rows >
+  sm_count * ctas_per_sm = slots, rows <= 16384, k_type == v_type, hkv in
+  {1, 2, 4, 8}, d = 256 or F16): B = ceil((T * total_len + 15 * rows) / 16)
+  tiles at most, chunk = roundup(ceil(B / slots), 2), part_tokens = 16 *
+  chunk, n_parts = ceil(ceil(max_len / 16) / chunk) + 1 when that is <= 32
+  (else the rules above), n_ctas = min(slots, ceil(B / chunk)), direct = 0,
+  n_direct = 0, stream = 1, partials and counters for every row;
 - with q_tokens = T > 1 (several query tokens per sequence, each a query
   row of its own that attends causally) the rule runs over the S * T query
   rows with T * total_len tokens of work: every S above reads S * T and
@@ -58,6 +65,7 @@ import math
 TILE = 32
 MIN_PART = 128
 CTA_COST = 512  # a CTA's fixed work in tokens of streaming (wave-filling plans)
+STREAM_OK = 1   # flags: the plan may be a stream plan
 
 OK, INVALID = 0, -1
 
@@ -71,9 +79,9 @@ def _roundup(a: int, b: int) -> int:
 
 
 def plan(*, n_seqs, max_len, total_len, block_size, hq, hkv, d, k_type, v_type,
-         sm_count, ctas_per_sm, force_parts=0, q_tokens=1):
+         sm_count, ctas_per_sm, force_parts=0, q_tokens=1, flags=0):
     """Returns (rc, dict).  dict keys: part_tokens, n_parts, direct, n_ctas,
-    part_o_bytes, part_ml_bytes, counter_bytes, q_tokens, n_direct."""
+    part_o_bytes, part_ml_bytes, counter_bytes, q_tokens, n_direct, stream."""
     if (n_seqs < 1 or block_size not in (16, 32) or hkv < 1 or hq < hkv or hq % hkv
             or hq // hkv > 8 or d not in (128, 256) or k_type not in (0, 1, 2)
             or v_type not in (0, 1, 2) or sm_count < 1 or ctas_per_sm < 1
@@ -116,6 +124,21 @@ def plan(*, n_seqs, max_len, total_len, block_size, hq, hkv, d, k_type, v_type,
                     best_t, best_part = t, pr
             if best_part:
                 part, n_parts, n_direct = best_part, _cdiv(max_len, best_part), rows - r
+    # a stream plan: equal ranges of the rows' 16-token tiles per CTA
+    slots = sm_count * ctas_per_sm
+    shapes = k_type == v_type and hkv in (1, 2, 4, 8) and (d == 256 or k_type == 0)
+    if ((flags & STREAM_OK) and force_parts == 0 and max_len > 0 and rows > slots
+            and rows <= 16384 and shapes):
+        bound = _cdiv(work + 15 * rows, 16)
+        chunk = _roundup(_cdiv(bound, slots), 2)
+        np_ = _cdiv(_cdiv(max_len, 16), chunk) + 1
+        if np_ <= 32:
+            return OK, dict(part_tokens=16 * chunk, n_parts=np_, direct=0,
+                            n_ctas=min(slots, _cdiv(bound, chunk)),
+                            part_o_bytes=rows * hq * np_ * d * 2,
+                            part_ml_bytes=rows * hq * np_ * 8,
+                            counter_bytes=4 * rows * (1 + math.isqrt(np_ - 1) + 1),
+                            q_tokens=T, n_direct=0, stream=1)
     direct = 1 if n_parts == 1 else 0
     if direct:
         n_ctas = rows
@@ -129,4 +152,4 @@ def plan(*, n_seqs, max_len, total_len, block_size, hq, hkv, d, k_type, v_type,
         cb = 4 * m * (1 + math.isqrt(n_parts - 1) + 1)
     return OK, dict(part_tokens=part, n_parts=n_parts, direct=direct, n_ctas=n_ctas,
                     part_o_bytes=po, part_ml_bytes=pm, counter_bytes=cb, q_tokens=T,
-                    n_direct=n_direct)
+                    n_direct=n_direct, stream=0)

@@ -390,6 +390,7 @@ struct Q40T {
     static constexpr uint32_t kMaxWarps = KMAXW;
     static constexpr int kMergeBatch = 8;
     static constexpr bool kStagedMerge = true;
+    static constexpr bool kStream = true;
 
     static __host__ __device__ constexpr uint32_t side_bytes(uint32_t hkv)
     {
@@ -617,6 +618,7 @@ struct Q80T {
     static constexpr uint32_t kMaxWarps = KMAXW;
     static constexpr int kMergeBatch = 12;
     static constexpr bool kStagedMerge = true;
+    static constexpr bool kStream = true;
 
     static __host__ __device__ constexpr uint32_t side_bytes(uint32_t hkv)
     {
@@ -847,6 +849,7 @@ struct F16T {
     static constexpr uint32_t kMaxWarps = 8;
     static constexpr int kMergeBatch = 12;
     static constexpr bool kStagedMerge = true;
+    static constexpr bool kStream = true;
 
     static __host__ __device__ constexpr uint32_t side_bytes(uint32_t hkv)
     {
@@ -970,6 +973,7 @@ struct Mix {
     static constexpr int kMergeBatch =
         KT::kMergeBatch < VT::kMergeBatch ? KT::kMergeBatch : VT::kMergeBatch;
     static constexpr bool kStagedMerge = false;  // one instance per mixed pair
+    static constexpr bool kStream = false;       // stream plans take one K/V type
     static constexpr uint32_t kSideK = KT::kSideK, kSideV = VT::kSideV;
     static constexpr uint32_t kTmaXK = KT::kTmaXK, kTmaXV = VT::kTmaXV;
     static constexpr uint32_t kRowK = KT::kRowK, kRowV = VT::kRowV;
@@ -1120,26 +1124,28 @@ __device__ bool merge_row_staged(const DecodeParams &p, const __half *po, const 
     for (int j = 0; j < 8; ++j)
         acc[j] = 0.0f;
     const uint32_t base = stage + 8 * lane;
+    // every partial sits in the stage, so it is loaded whatever its weight
+    // and added only for a positive weight: the sums of a skip, without a
+    // branch between each weight and its loads
 #pragma unroll 4
     for (uint32_t k = 0; k < m; ++k) {
         const float wk = __shfl_sync(0xffffffffu, w, k);
-        if (wk > 0.0f) {
-            const uint32_t a = base + k * rb;
-            uint32_t h[4];
-            asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(h[0]), "=r"(h[1]) : "r"(a) : "memory");
-            if (D == 256)
-                asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];"
-                    : "=r"(h[2]), "=r"(h[3])
-                    : "r"(a + 256)
-                    : "memory");
-            else
-                h[2] = h[3] = 0u;
+        const uint32_t a = base + k * rb;
+        uint32_t h[4];
+        asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(h[0]), "=r"(h[1]) : "r"(a) : "memory");
+        if (D == 256)
+            asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];"
+                         : "=r"(h[2]), "=r"(h[3])
+                         : "r"(a + 256)
+                         : "memory");
+        else
+            h[2] = h[3] = 0u;
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const float2 f = __half22float2(bits_h2(h[j]));
-                acc[2 * j] = fmaf(wk, f.x, acc[2 * j]);
-                acc[2 * j + 1] = fmaf(wk, f.y, acc[2 * j + 1]);
-            }
+        for (int j = 0; j < 4; ++j) {
+            const float2 f = __half22float2(bits_h2(h[j]));
+            const float x = fmaf(wk, f.x, acc[2 * j]), y = fmaf(wk, f.y, acc[2 * j + 1]);
+            acc[2 * j] = wk > 0.0f ? x : acc[2 * j];
+            acc[2 * j + 1] = wk > 0.0f ? y : acc[2 * j + 1];
         }
     }
     __syncwarp();  // the stage is read before the next row lands
@@ -1343,16 +1349,23 @@ __device__ __noinline__ void merge_coop(const DecodeParams &p, uint32_t seq, uin
     }
 }
 
-// kStaged: the instance for plans of more than 32 partitions, whose merges
-// run in two passes (merge_tail_staged); the other plans take the instance
-// without it, whose code stays as it was tuned.
-template <class T, bool kStaged = false>
-__global__ void __launch_bounds__(T::kMaxWarps * 32, 1)
-    fast_decode_kernel(const __grid_constant__ FastArgs a)
+// The decode of one token range [t0, t1) of one query row (`seq`), by the whole
+// CTA: the table walk, the per-warp TMA rings, the tile loop, and the combine
+// of the warps' results into the range's partial (index `part`), or into the
+// output row when `dir`.  The rings continue from slot s / parity phase (the
+// next use of each warp's ring: use u of a ring takes slot u % NSW with
+// parity (u / NSW) % 2) and are left drained, at the slot and parity after
+// the range's last tile.  any_abort: a bounded wait of some warp ran out
+// (status flagged; the rings may then hold copies of this range), reported
+// only by the kReportAbort instances.
+template <class T, bool kReportAbort>
+__device__ __forceinline__ void range_body(const FastArgs &a, uint8_t *smem, uint32_t seq,
+                                           uint32_t part, int32_t Lrow, uint32_t t0in,
+                                           bool dir, uint32_t t1in, uint32_t &s,
+                                           uint32_t &phase, uint32_t &n_my_out,
+                                           bool &any_abort)
 {
     const DecodeParams &p = a.p;
-    extern __shared__ __align__(16) uint8_t smem_raw[];
-    uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const uint32_t NSW = a.n_slots, SLOT = a.slot_bytes, nwarps = blockDim.x >> 5;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t hkv = p.hkv, G = p.hq / p.hkv, wph = nwarps / hkv;
@@ -1364,37 +1377,10 @@ __global__ void __launch_bounds__(T::kMaxWarps * 32, 1)
     const uint32_t scr_base = (smem_u32(slot_ok + (nwarps - warp) * NSW) + 15u) & ~15u;
     const uint32_t scr_u = scr_base + warp * T::SCRATCH;
     const uint32_t qsm_base = scr_base + nwarps * T::SCRATCH;  // per K/V head: T::QBYTES
-
-    if (lane == 0) {
-        for (uint32_t s = 0; s < NSW; ++s)
-            mbar_init(&full[s], 1);
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    }
-    __syncthreads();
-    // everything below reads inputs that an earlier grid may have written
-    grid_dependency_wait();
-
-    uint32_t seq, part;
-    if (!p.direct && blockIdx.x == gridDim.x - 1 && warp == 0)
-        check_grid_vs_plan(p.seq_lens, p.q_tokens, p.n_seqs, p.part_tokens, p.n_parts,
-                           p.n_direct, p.status);
-    if (p.direct) {
-        seq = blockIdx.x;
-        part = 0;
-    } else if (!cta_work(p.seq_lens, p.q_tokens, p.n_seqs, p.part_tokens, p.n_parts,
-                         p.n_direct, blockIdx.x, &seq, &part)) {
-        return;  // past the last live partition: nothing was issued
-    } else if (seq >= p.n_direct && part == 0 && tid == 0) {
-        check_len_vs_plan(row_len(p.seq_lens, p.q_tokens, seq), p.n_parts, p.part_tokens,
-                          p.status);
-    }
-    // a direct CTA: the whole row, output written here (every CTA of a direct
-    // plan, and the leading rows of a wave-filling plan)
-    const bool dir = p.direct || seq < p.n_direct;
-    const int32_t Lrow = row_len(p.seq_lens, p.q_tokens, seq);
+    const uint32_t s0 = s, u0 = phase * NSW + s;  // this warp's ring use at the range start
     const int32_t L = Lrow > 0 ? Lrow : 0;
-    const uint32_t t0 = dir ? 0u : part * p.part_tokens;
-    const uint32_t t1 = dir ? (uint32_t)L : min((uint32_t)L, t0 + p.part_tokens);
+    const uint32_t t0 = t0in;
+    const uint32_t t1 = min((uint32_t)L, t1in);
     const uint32_t n_tiles = (t1 - t0 + kTile - 1) / kTile;
     const int gid = lane >> 2, tig = lane & 3;
     const uint32_t g = warp % hkv, sub = warp / hkv;
@@ -1455,8 +1441,10 @@ __global__ void __launch_bounds__(T::kMaxWarps * 32, 1)
     const uint32_t pro = n_my < NSW ? n_my : NSW;
     for (uint32_t k = 0; k < pro; ++k) {
         const int32_t b = __shfl_sync(0xffffffffu, ids, k);
+        uint32_t sk = s0 + k;
+        sk = sk >= NSW ? sk - NSW : sk;
         if (lane == 0)
-            issue(k, k, b);
+            issue(k, sk, b);
     }
     __syncwarp();
 
@@ -1480,7 +1468,6 @@ __global__ void __launch_bounds__(T::kMaxWarps * 32, 1)
     bool aborted = false;
     uint32_t issued = pro;
 
-    uint32_t s = 0, phase = 0;  // slot of tile k and the parity of its current use
     for (uint32_t k = 0; k < n_my; ++k) {
         // every lane waits (bounded) and so acquires the slot's TMA writes itself
         bool done = mbar_try_wait(&full[s], phase);
@@ -1577,8 +1564,9 @@ __global__ void __launch_bounds__(T::kMaxWarps * 32, 1)
     if (aborted && lane == 0) {
         // let my copies still in flight land (bounded) before the CTA moves on
         for (uint32_t k = issued > NSW ? issued - NSW : 0; k < issued; ++k) {
+            const uint32_t u = u0 + k;
             const uint64_t tw = global_ns();
-            while (!mbar_try_wait(&full[k % NSW], (k / NSW) & 1) && global_ns() - tw < kWaitNs) {
+            while (!mbar_try_wait(&full[u % NSW], (u / NSW) & 1) && global_ns() - tw < kWaitNs) {
             }
         }
     }
@@ -1590,8 +1578,7 @@ __global__ void __launch_bounds__(T::kMaxWarps * 32, 1)
 
     // park (m, l, O) of every warp in the now idle rings, head-major, then
     // all warps of the CTA combine them
-    bool any_abort = false;
-    if constexpr (kStaged)
+    if constexpr (kReportAbort)
         any_abort = __syncthreads_or(aborted);
     else
         __syncthreads();
@@ -1626,6 +1613,55 @@ __global__ void __launch_bounds__(T::kMaxWarps * 32, 1)
     }
     __syncthreads();
     combine_and_write<T>(p, park, park + nwarps * Park<T>::kWarp, hkv, wph, G, seq, part, dir);
+    n_my_out = n_my;
+}
+
+// kStaged: the instance for plans of more than 32 partitions, whose merges
+// run in two passes (merge_tail_staged); the other plans take the instance
+// without it, whose code stays as it was tuned.
+template <class T, bool kStaged = false>
+__global__ void __launch_bounds__(T::kMaxWarps * 32, 1)
+    fast_decode_kernel(const __grid_constant__ FastArgs a)
+{
+    const DecodeParams &p = a.p;
+    extern __shared__ __align__(16) uint8_t smem_raw[];
+    uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    const uint32_t NSW = a.n_slots, nwarps = blockDim.x >> 5;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + a.region_bytes) + warp * NSW;
+
+    if (lane == 0) {
+        for (uint32_t s = 0; s < NSW; ++s)
+            mbar_init(&full[s], 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    // everything below reads inputs that an earlier grid may have written
+    grid_dependency_wait();
+
+    uint32_t seq, part;
+    if (!p.direct && blockIdx.x == gridDim.x - 1 && warp == 0)
+        check_grid_vs_plan(p.seq_lens, p.q_tokens, p.n_seqs, p.part_tokens, p.n_parts,
+                           p.n_direct, p.status);
+    if (p.direct) {
+        seq = blockIdx.x;
+        part = 0;
+    } else if (!cta_work(p.seq_lens, p.q_tokens, p.n_seqs, p.part_tokens, p.n_parts,
+                         p.n_direct, blockIdx.x, &seq, &part)) {
+        return;  // past the last live partition: nothing was issued
+    } else if (seq >= p.n_direct && part == 0 && tid == 0) {
+        check_len_vs_plan(row_len(p.seq_lens, p.q_tokens, seq), p.n_parts, p.part_tokens,
+                          p.status);
+    }
+    // a direct CTA: the whole row, output written here (every CTA of a direct
+    // plan, and the leading rows of a wave-filling plan)
+    const bool dir = p.direct || seq < p.n_direct;
+    const int32_t Lrow = row_len(p.seq_lens, p.q_tokens, seq);
+    const uint32_t t0 = dir ? 0u : part * p.part_tokens;
+    const uint32_t t1 = dir ? (uint32_t)max(Lrow, 0) : t0 + p.part_tokens;
+    uint32_t s = 0, phase = 0, n_my = 0;  // fresh rings
+    bool any_abort = false;
+    range_body<T, kStaged>(a, smem, seq, part, Lrow, t0, dir, t1, s, phase, n_my, any_abort);
     if (p.counters && !dir) {
         if (a.coop) {
             merge_coop<T>(p, seq, part, Lrow, warp, nwarps, a.coop_wait_ns, smem_u32(smem),
@@ -1642,6 +1678,223 @@ __global__ void __launch_bounds__(T::kMaxWarps * 32, 1)
         } else {
             merge_tail<T::kMergeBatch>(p, seq, part, warp, nwarps);
         }
+    }
+}
+
+// range_body out of line, for the stream kernel: the segment walk's own
+// values are saved around the call, not held through the tile loop.
+// Returns the rings' next slot, with their parity in bit 8 and an abort in
+// bit 9.
+template <class T>
+__device__ __noinline__ uint32_t stream_range(const FastArgs &a, uint8_t *smem, uint32_t seq,
+                                              uint32_t part, int32_t L, uint32_t t0, bool dir,
+                                              uint32_t t1, uint32_t ring)
+{
+    uint32_t s = ring & 0xffu, phase = (ring >> 8) & 1u, n_my = 0;
+    bool any_abort = false;
+    range_body<T, true>(a, smem, seq, part, L, t0, dir, t1, s, phase, n_my, any_abort);
+    return s | phase << 8 | (any_abort ? 1u : 0u) << 9;
+}
+
+// Exclusive prefix of the query rows' tile counts (ceil(L / 16), 0 for an
+// empty row) into pre[0 .. rows], pre[rows] = all tiles; every thread of the
+// CTA takes part.  Each thread sums a run of consecutive rows, the run sums
+// are scanned across the CTA, then each thread writes its run's prefixes.
+__device__ __forceinline__ void block_tile_prefix(const DecodeParams &p, uint32_t *pre,
+                                                  uint32_t rows)
+{
+    __shared__ uint32_t wsum[32];
+    const uint32_t nt = blockDim.x, t = threadIdx.x, lane = t & 31, w = t >> 5;
+    const uint32_t per = (rows + nt - 1) / nt;
+    const uint32_t r0 = min(t * per, rows), r1 = min(r0 + per, rows);
+    auto tiles = [&](uint32_t r) -> uint32_t {
+        const int32_t L = row_len(p.seq_lens, p.q_tokens, r);
+        return L > 0 ? ((uint32_t)L + kTile - 1) / kTile : 0u;
+    };
+    uint32_t sum = 0;
+    for (uint32_t r = r0; r < r1; ++r)
+        sum += tiles(r);
+    uint32_t x = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+        if ((int)lane >= o)
+            x += y;
+    }
+    if (lane == 31)
+        wsum[w] = x;
+    __syncthreads();
+    if (w == 0) {
+        uint32_t v = lane < (nt >> 5) ? wsum[lane] : 0u;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t y = __shfl_up_sync(0xffffffffu, v, o);
+            if ((int)lane >= o)
+                v += y;
+        }
+        __syncwarp();
+        wsum[lane] = v;
+    }
+    __syncthreads();
+    uint32_t base = (w > 0 ? wsum[w - 1] : 0u) + x - sum;
+    for (uint32_t r = r0; r < r1; ++r) {
+        pre[r] = base;
+        base += tiles(r);
+    }
+    if (t == nt - 1)
+        pre[rows] = base;
+}
+
+// Stream-K decode for batches wider than the machine (a stream plan): the
+// tiles of all query rows, in row order, are cut into equal ranges of
+// chunk = part_tokens / 16 tiles, one per CTA ("feat: add paged-attention
+// monolithic decode-only AR foundation", lucebox pull 555, Roadmap: the
+// stream-K decode kernel for ragged batches).  A CTA walks the segments of
+// its range (a row's tiles inside it) in order on the same per-warp rings:
+// a segment that is a whole row writes the row's output; a row cut by range
+// boundaries gets one partial per CTA that covers it (index: the CTA minus
+// the row's first CTA), counted on the row's completion counter, and the CTA
+// that completes the count merges the row after its own segments, with the
+// arithmetic of pa_merge.  Nothing waits.  Rows without tokens are written as
+// zeros by CTA (row mod grid).
+template <class T>
+__global__ void __launch_bounds__(T::kMaxWarps * 32, 1)
+    stream_decode_kernel(const __grid_constant__ FastArgs a)
+{
+    const DecodeParams &p = a.p;
+    extern __shared__ __align__(16) uint8_t smem_raw[];
+    uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    const uint32_t NSW = a.n_slots, nwarps = blockDim.x >> 5;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + a.region_bytes) + warp * NSW;
+    __shared__ uint32_t s_row0, s_pre0, s_total;
+
+    if (lane == 0) {
+        for (uint32_t s = 0; s < NSW; ++s)
+            mbar_init(&full[s], 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    // everything below reads inputs that an earlier grid may have written
+    grid_dependency_wait();
+
+    // the rows' tile prefix, in the ring region before any copy lands there
+    const uint32_t rows = p.n_seqs, chunk = p.part_tokens / kTile;
+    uint32_t *pre = reinterpret_cast<uint32_t *>(smem);
+    block_tile_prefix(p, pre, rows);
+    __syncthreads();
+    const uint32_t c0 = blockIdx.x * chunk;
+    if (tid == 0) {
+        // the first row whose tiles reach past c0
+        uint32_t lo = 0, hi = rows;
+        while (lo < hi) {
+            const uint32_t mid = (lo + hi) / 2;
+            if (pre[mid + 1] > c0)
+                hi = mid;
+            else
+                lo = mid + 1;
+        }
+        s_row0 = lo;
+        s_pre0 = lo < rows ? pre[lo] : pre[rows];
+        s_total = pre[rows];
+        if (blockIdx.x == gridDim.x - 1 && (uint64_t)pre[rows] > (uint64_t)gridDim.x * chunk)
+            atomicOr(p.status, PA_STATUS_LEN_OVER_PLAN);  // tiles past the last range
+    }
+    __syncthreads();  // the rings take the region back below
+    // The segment walk keeps its CTA-wide state in shared memory (st_row:
+    // the next row, st_pre: its first tile; st_m*: the rows this CTA merges),
+    // so that only the rings' slot and parity stay in registers through the
+    // tile loops.
+    __shared__ uint32_t st_row, st_pre, st_nm, st_mrow[2], st_mn[2];
+    if (tid == 0) {
+        st_row = s_row0;
+        st_pre = s_pre0;
+        st_nm = 0;
+    }
+    __syncthreads();
+    uint32_t s = 0, phase = 0;  // the rings' next use
+    bool any_abort = false;
+    // one segment of row r starting at tile pr of the concatenation: its
+    // tile range [at, bt) in the row, whether it is the whole row, the CTA of
+    // the row's first tile and the number of CTAs the row spans (nothing of
+    // it stays live through a segment's tile loop: it is formed again after)
+    struct Seg {
+        int32_t L;
+        uint32_t tiles, at, bt, cf, nr;
+        bool dir;
+    };
+    auto segment = [&](uint32_t r, uint32_t pr) -> Seg {
+        Seg g;
+        g.L = row_len(p.seq_lens, p.q_tokens, r);
+        g.tiles = g.L > 0 ? ((uint32_t)g.L + kTile - 1) / kTile : 0u;
+        const uint32_t c1 = min(c0 + chunk, s_total);
+        g.at = c0 > pr ? c0 - pr : 0u;
+        g.bt = min(c1 - pr, g.tiles);
+        g.dir = g.at == 0 && g.bt == g.tiles;
+        g.cf = pr / chunk;
+        g.nr = g.tiles ? (pr + g.tiles - 1) / chunk - g.cf + 1 : 0u;
+        return g;
+    };
+    while (!any_abort) {
+        if (st_row >= rows || st_pre >= min(c0 + chunk, s_total))
+            break;
+        {
+            const Seg g = segment(st_row, st_pre);
+            if (g.tiles > 0 && !g.dir && g.nr > p.n_parts) {
+                // lengths past what the plan covers: the row is left out
+                if (tid == 0)
+                    atomicOr(p.status, PA_STATUS_LEN_OVER_PLAN);
+            } else if (g.tiles > 0) {
+                const uint32_t rs =
+                    stream_range<T>(a, smem, st_row, blockIdx.x - g.cf, g.L, g.at * kTile, g.dir,
+                                    g.bt * kTile, s | phase << 8);
+                s = rs & 0xffu;
+                phase = (rs >> 8) & 1u;
+                any_abort = (rs >> 9) & 1u;
+                const Seg h = segment(st_row, st_pre);
+                const bool last =
+                    !h.dir && merge_arrive(p.counters + (uint64_t)st_row *
+                                                            merge_counters_per_seq(p.n_parts),
+                                           h.nr);
+                if (last && tid == 0 && st_nm < 2) {
+                    st_mrow[st_nm] = st_row;
+                    st_mn[st_nm] = h.nr;
+                    ++st_nm;
+                }
+            }
+        }
+        __syncthreads();  // every thread is done with st_row / st_pre
+        if (tid == 0) {
+            const Seg g = segment(st_row, st_pre);
+            st_pre += g.tiles;
+            ++st_row;
+        }
+        __syncthreads();  // the combine's reads of the rings before the next copies
+    }
+    // the rows whose count this CTA completed: all partials written and visible
+    const __half *po = static_cast<const __half *>(p.part_o);
+    const float2 *pml = reinterpret_cast<const float2 *>(p.part_ml);
+    for (uint32_t i = 0; i < st_nm; ++i) {
+        for (uint32_t h = warp; h < p.hq; h += nwarps) {
+            const uint64_t row = (uint64_t)st_mrow[i] * p.hq + h;
+            const __half *rpo = po + row * p.n_parts * p.d;
+            const float2 *rml = pml + row * p.n_parts;
+            float *rout = p.out + row * p.d;
+            if (p.d == 256)
+                merge_rows_warp_v<8, 1, false, 8>(&rpo, &rml, st_mn[i], 1, p.d, 1, &rout, nullptr,
+                                                  nullptr);
+            else
+                merge_rows_warp_v<4, 1, false, 8>(&rpo, &rml, st_mn[i], 1, p.d, 1, &rout,
+                                                  nullptr, nullptr);
+        }
+    }
+    // rows without tokens: zero output
+    for (uint32_t rz = blockIdx.x; rz < rows; rz += gridDim.x) {
+        if (row_len(p.seq_lens, p.q_tokens, rz) > 0)
+            continue;
+        float4 *o4 = reinterpret_cast<float4 *>(p.out + (uint64_t)rz * p.hq * p.d);
+        for (uint32_t i = tid; i < p.hq * p.d / 4; i += blockDim.x)
+            o4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
 }
 
@@ -1832,6 +2085,11 @@ cudaError_t allow_smem()
             e = cudaFuncSetAttribute(fast_decode_kernel<T, T::kStagedMerge>,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      (int)(kSmemBudget + 4096));
+        if constexpr (T::kStream)
+            if (e == cudaSuccess)
+                e = cudaFuncSetAttribute(stream_decode_kernel<T>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)(kSmemBudget + 4096));
         if (e != cudaSuccess)
             return e;
         done[dev] = true;
@@ -1972,8 +2230,22 @@ int launch_t(const DecodeParams &p, cudaStream_t st, const char *entry)
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl_on ? 1 : 0;
-    cudaError_t e = staged ? cudaLaunchKernelEx(&cfg, fast_decode_kernel<T, T::kStagedMerge>, a)
-                           : cudaLaunchKernelEx(&cfg, fast_decode_kernel<T, false>, a);
+    cudaError_t e;
+    if (p.stream) {
+        // stream plans: the rows' tile prefix is formed in the ring region
+        if (!T::kStream || (uint64_t)(p.n_seqs + 1) * 4 > gm.region)
+            return fail(PA_ERR_INVALID, entry, "stream plan: %u query rows unsupported here",
+                        p.n_seqs);
+        a.coop = 0;
+        if constexpr (T::kStream)
+            e = cudaLaunchKernelEx(&cfg, stream_decode_kernel<T>, a);
+        else
+            e = cudaErrorInvalidValue;
+    } else if (staged) {
+        e = cudaLaunchKernelEx(&cfg, fast_decode_kernel<T, T::kStagedMerge>, a);
+    } else {
+        e = cudaLaunchKernelEx(&cfg, fast_decode_kernel<T, false>, a);
+    }
     if (e != cudaSuccess)
         return cuda_check(e, entry, "fast_decode_kernel launch");
     return cuda_check(cudaGetLastError(), entry, "fast_decode_kernel launch");

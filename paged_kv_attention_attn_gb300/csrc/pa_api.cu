@@ -41,6 +41,12 @@ int check_shapes(uint32_t n_seqs, uint32_t hq, uint32_t hkv, uint32_t d, uint32_
     return PA_OK;
 }
 
+bool use_fast(const pa_decode_args *a)
+{
+    return !(a->flags & PA_FLAG_PLAIN) &&
+           pa::fast_decode_supported(a->k_type, a->v_type, a->d, a->hq, a->hkv, a->block_size);
+}
+
 // Validates a decode call and resolves it into kernel parameters.
 int resolve(const pa_decode_args *a, const pa_plan_t *plan, const char *E, pa::DecodeParams *p)
 {
@@ -106,13 +112,14 @@ int resolve(const pa_decode_args *a, const pa_plan_t *plan, const char *E, pa::D
     p->q_f32 = 0;
     p->n_direct = plan->direct ? 0 : plan->n_direct;
     p->merge_no_wait = (a->flags & PA_FLAG_MERGE_NO_WAIT) ? 1u : 0u;
+    p->stream = plan->stream ? 1u : 0u;
+    if (plan->stream) {
+        if (plan->direct || plan->n_direct || plan->n_parts > 32)
+            return fail(PA_ERR_INVALID, E, "inconsistent stream plan");
+        if (a->k_type != a->v_type || !use_fast(a))
+            return fail(PA_ERR_INVALID, E, "stream plans need the fast kernel and one K/V type");
+    }
     return PA_OK;
-}
-
-bool use_fast(const pa_decode_args *a)
-{
-    return !(a->flags & PA_FLAG_PLAIN) &&
-           pa::fast_decode_supported(a->k_type, a->v_type, a->d, a->hq, a->hkv, a->block_size);
 }
 
 int launch_decode(const pa_decode_args *a, const pa::DecodeParams &p, cudaStream_t st,
@@ -183,6 +190,8 @@ extern "C" int pa_decode_partial(const pa_decode_args *args, const pa_plan_t *pl
     int rc = resolve(args, plan, E, &p);
     if (rc)
         return rc;
+    if (plan->stream)
+        return fail(PA_ERR_INVALID, E, "stream plans run only through the fused calls");
     return launch_decode(args, p, pa::stream_of(stream), E);
 }
 
@@ -233,7 +242,7 @@ extern "C" int pa_decode_step_fused(const pa_decode_args *args, const pa_plan_t 
     if (args->k_type != PA_F16) {
         if (!q8_1_scratch || (reinterpret_cast<uintptr_t>(q8_1_scratch) & 15))
             return fail(PA_ERR_INVALID, E, "quantised K needs a 16-byte aligned q8_1_scratch");
-        if (use_fast(args)) {
+        if (use_fast(args) && !plan->stream) {
             // the fast kernel quantises the query rows itself: one launch per step
             p.q_f32 = 1;
             return launch_decode(args, p, st, E);
@@ -255,6 +264,8 @@ extern "C" int pa_merge(const void *part_o, const float *part_ml, const int32_t 
     int rc = check_plan(plan, E);
     if (rc)
         return rc;
+    if (plan->stream)
+        return fail(PA_ERR_INVALID, E, "stream plans merge inside the fused calls");
     if (plan->direct)
         return fail(PA_ERR_INVALID, E, "a direct plan has no partials to merge");
     if (!part_o || !part_ml || !seq_lens || !out)
@@ -285,6 +296,8 @@ extern "C" int pa_decode_step(const pa_decode_args *args, const pa_plan_t *plan,
     int rc = resolve(args, plan, E, &p);
     if (rc)
         return rc;
+    if (plan->stream)
+        return fail(PA_ERR_INVALID, E, "stream plans run only through the fused calls");
     cudaStream_t st = pa::stream_of(stream);
     if (args->k_type != PA_F16) {
         if (!q8_1_scratch || (reinterpret_cast<uintptr_t>(q8_1_scratch) & 15))

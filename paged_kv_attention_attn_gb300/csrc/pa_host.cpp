@@ -262,6 +262,37 @@ extern "C" int pa_plan(const pa_plan_in *in, pa_plan_t *out)
             }
         }
     }
+    // a stream plan for a batch wider than the machine (see pa.h): equal
+    // ranges of the rows' tiles per CTA instead of whole rows in waves
+    {
+        const uint64_t slots = (uint64_t)in->sm_count * (uint64_t)in->ctas_per_sm;
+        const bool shapes = in->k_type == in->v_type &&
+                            (in->hkv == 1 || in->hkv == 2 || in->hkv == 4 || in->hkv == 8) &&
+                            (in->d == 256 || in->k_type == PA_F16);
+        if ((in->flags & PA_PLAN_STREAM_OK) && in->force_parts == 0 && in->max_len > 0 &&
+            rows > slots && rows <= 16384 && shapes) {
+            const uint64_t bound = cdiv(work + 15 * rows, 16);
+            const uint64_t chunk = roundup(cdiv(bound, slots), 2);
+            const uint64_t np = cdiv(cdiv(in->max_len, 16), chunk) + 1;
+            if (np <= 32) {
+                pa_plan_t p;
+                memset(&p, 0, sizeof p);
+                p.part_tokens = (uint32_t)(16 * chunk);
+                p.n_parts = (uint32_t)np;
+                p.n_ctas = (uint32_t)(cdiv(bound, chunk) < slots ? cdiv(bound, chunk) : slots);
+                p.q_tokens = (uint32_t)T;
+                p.stream = 1;
+                p.part_o_bytes = rows * in->hq * np * in->d * 2ull;
+                p.part_ml_bytes = rows * in->hq * np * 8ull;
+                p.counter_bytes = rows * pa::merge_counters_per_seq((uint32_t)np) * 4ull;
+                part = p.part_tokens;
+                n_parts = np;
+                *out = p;
+                goto logged;
+            }
+        }
+    }
+    {
     pa_plan_t p;
     memset(&p, 0, sizeof p);
     p.part_tokens = (uint32_t)part;
@@ -284,14 +315,18 @@ extern "C" int pa_plan(const pa_plan_in *in, pa_plan_t *out)
         p.counter_bytes = m * pa::merge_counters_per_seq((uint32_t)n_parts) * 4ull;
     }
     *out = p;
+    }
+logged:
     // PA_LOG_PLAN (set, not "0"): one line per plan on stderr
     const char *log = getenv("PA_LOG_PLAN");
     if (log && *log && strcmp(log, "0") != 0)
         fprintf(stderr,
                 "pa_plan: n_seqs=%u q_tokens=%u max_len=%u total_len=%llu slots=%lld "
-                "force_parts=%d -> part_tokens=%u n_parts=%u direct=%u n_direct=%u n_ctas=%u\n",
-                in->n_seqs, p.q_tokens, in->max_len, (unsigned long long)in->total_len,
-                (long long)in->sm_count * in->ctas_per_sm, in->force_parts, p.part_tokens,
-                p.n_parts, p.direct, p.n_direct, p.n_ctas);
+                "force_parts=%d flags=%u -> part_tokens=%u n_parts=%u direct=%u n_direct=%u "
+                "n_ctas=%u stream=%u\n",
+                in->n_seqs, out->q_tokens, in->max_len, (unsigned long long)in->total_len,
+                (long long)in->sm_count * in->ctas_per_sm, in->force_parts, in->flags,
+                out->part_tokens, out->n_parts, out->direct, out->n_direct, out->n_ctas,
+                out->stream);
     return PA_OK;
 }

@@ -73,6 +73,7 @@ struct DecodeParams {
     uint32_t n_direct;      // leading rows decoded directly in a partitioned plan; the
                             // partials, counters and merges index row r at r - n_direct
     uint32_t merge_no_wait; // PA_FLAG_MERGE_NO_WAIT: cooperative merges give up waiting
+    uint32_t stream;        // a stream plan: CTA c takes tiles [c, c + 1) * part_tokens / 16
 };
 
 // The argument checks of pa_decode_partial alone: PA_OK, or the error

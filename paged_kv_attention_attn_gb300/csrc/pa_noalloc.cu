@@ -116,6 +116,8 @@ extern "C" int pa_decode_step_noalloc(const pa_decode_args *args, const pa_plan_
         return pa::fail(PA_ERR_INVALID, E, "NULL args or plan");
     if (plan->n_parts == 0 || plan->direct != (plan->n_parts == 1u))
         return pa::fail(PA_ERR_INVALID, E, "inconsistent plan");
+    if (plan->stream)
+        return pa::fail(PA_ERR_INVALID, E, "stream plans run only through the fused calls");
     const bool quantised = args->k_type != PA_F16;
     const uint64_t rows = (uint64_t)args->n_seqs * (plan->q_tokens > 1 ? plan->q_tokens : 1) *
                           args->hq;

@@ -103,14 +103,15 @@ def test_pool_refusals():
 def test_plan_matches_model():
     rng = random.Random(2)
     for _ in range(4000):
-        S = rng.randint(1, 64)
+        S = rng.choice([rng.randint(1, 64), rng.randint(100, 2000)])
         lens = [rng.choice([0, 1, 16, 33, rng.randint(0, 400000)]) for _ in range(S)]
         kw = dict(n_seqs=S, max_len=max(lens), total_len=sum(lens),
                   block_size=rng.choice([16, 32, 8]), hq=rng.choice([24, 32, 12, 7]),
                   hkv=rng.choice([4, 8, 1]), d=rng.choice([128, 256, 64]),
                   k_type=rng.choice([0, 1, 2]), v_type=rng.choice([0, 1, 2]),
                   sm_count=rng.choice([152, 148, 1]), ctas_per_sm=rng.choice([1, 2]),
-                  force_parts=rng.choice([0, 0, 3, 64]), q_tokens=rng.choice([1, 1, 2, 5]))
+                  force_parts=rng.choice([0, 0, 3, 64]), q_tokens=rng.choice([1, 1, 2, 5]),
+                  flags=rng.choice([0, 1]))
         mrc, mp = plan_model.plan(**kw)
         pin = pa.PlanIn(**kw)
         out = pa.Plan()
@@ -207,7 +208,7 @@ def test_plan_log_line_when_asked():
         lines = [l for l in r.stderr.splitlines() if l.startswith("pa_plan:")]
         if expect:
             assert lines == ["pa_plan: n_seqs=8 q_tokens=1 max_len=131072 total_len=1048576 "
-                             "slots=152 force_parts=0 -> part_tokens=6912 n_parts=19 direct=0 "
-                             "n_direct=0 n_ctas=152"]
+                             "slots=152 force_parts=0 flags=0 -> part_tokens=6912 n_parts=19 "
+                             "direct=0 n_direct=0 n_ctas=152 stream=0"]
         else:
             assert lines == []
