@@ -916,23 +916,25 @@ struct F16T {
         }
     }
 
+    // Two accumulator chains (even and odd k-steps), added at the end: with
+    // one warp per scheduler a single chain of KS dependent MMAs is latency.
     __device__ static void scores(const Consts &, const Frag &f, uint32_t kh, uint32_t,
                                   int gid, int tig, float (&s)[4])
     {
         const int lane = gid * 4 + tig;
         const int mi = lane >> 3, r = lane & 7;
         const int token = (mi & 1) * 8 + r;
-        float c[4] = {0.f, 0.f, 0.f, 0.f};
+        float c[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
         for (int j = 0; j < KS; ++j) {
             uint32_t a[4];
             ldsm_x4(a, chunk_addr(kh + (j >> 2) * kTile * 128, token, 2 * (j & 3) + (mi >> 1)));
-            mma16816(c, a[0], a[1], a[2], a[3], f.qb[j][0], f.qb[j][1]);
+            mma16816(c[j & 1], a[0], a[1], a[2], a[3], f.qb[j][0], f.qb[j][1]);
         }
-        s[0] = c[0];
-        s[1] = c[1];
-        s[2] = c[2];
-        s[3] = c[3];
+        s[0] = c[0][0] + c[1][0];
+        s[1] = c[0][1] + c[1][1];
+        s[2] = c[0][2] + c[1][2];
+        s[3] = c[0][3] + c[1][3];
     }
 
     __device__ static void pv(const Consts &, float (&o)[MT][4], uint32_t vh, uint32_t,
