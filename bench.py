@@ -389,7 +389,8 @@ def run_ours(a, world, rank, local):
     pl = pa.plan(q_tokens=int(spec.extra.get("q_tokens", 1)),
                  seq_lens=spec.seq_lens, block_size=spec.block_size, hq=spec.hq, hkv=spec.hkv,
                  d=spec.d, k_type=spec.k_type, v_type=spec.v_type,
-                 stream_ok=not a.unfused and not a.plain and a.stream == "on")
+                 stream_ok=not a.unfused and not a.plain and a.stream == "on",
+                 multi=not a.plain and a.multi == "on")
     ws = pa.workspace(pl, n_seqs=spec.n_seqs, hq=spec.hq, d=spec.d, device=dev)
     quantised = spec.k_type != synth.F16
     kv_bytes = (case.k_pool.numel() + case.v_pool.numel())
@@ -616,6 +617,8 @@ def run_ours(a, world, rank, local):
                             if in_kernel_q else
                             "stream plan: q8_1 pre-pass + stream-K decode with in-launch merges"
                             if pl.stream else
+                            "multi-token plan: q8_1 pre-pass + decode of each sequence's tokens "
+                            "together + merge kernel" if pl.multi else
                             "q8_1 pre-pass + decode with in-launch merge" if fused else
                             "q8_1 pre-pass + decode + merge kernel"),
                    "bytes_per_step": nb},
@@ -628,8 +631,9 @@ def run_ours(a, world, rank, local):
         "append": append,
         "e2e": e2e,
         "gpu_launches": K * (1 if in_kernel_q else
-                             (2 if quantised else 1) + (0 if (pl.direct or fused or pl.stream)
-                                                        else 1)),
+                             (2 if quantised else 1) +
+                             (0 if (pl.direct or ((fused or pl.stream) and not pl.multi))
+                              else 1)),
         "clocks": clk,
     }
     if rank == 0:
@@ -651,6 +655,8 @@ def main():
     ap.add_argument("--flush", choices=["auto", "on", "off"], default="auto",
                     help="auto: K/V under 2 x L2 cycles through pool copies (one per step); "
                          "on: flush the L2 before every step instead; off: neither")
+    ap.add_argument("--multi", choices=["on", "off"], default="on",
+                    help="several query tokens per sequence: decode a sequence's tokens together")
     ap.add_argument("--stream", choices=["on", "off"], default="off",
                     help="let the planner return stream plans (batches wider than the grid)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,

@@ -181,6 +181,14 @@ int pa_quantize_q(const float *q, void *q8_1, uint32_t n_rows, uint32_t d, pa_st
  * max_len / 16) / chunk) + 1 (the most CTAs one row can span), stream = 1,
  * direct = 0, n_direct = 0, partial buffers and counters for every row
  * (m = rows below), if n_parts <= 32 and rows <= 16384; else the rules above.
+ * Multi-token plans ([P2] What: a verify window or prompt chunk as several
+ * query rows over one paged cache): with PA_PLAN_MULTI_TOKEN in flags,
+ * q_tokens = T >= 2, Q4_0 K and V, d = 256, hkv in {1, 2, 4} and T * hq /
+ * hkv <= 24, the plan is the one-token plan of the n_seqs sequences (the
+ * rules above with q_tokens = 1; a plan that would keep direct rows becomes
+ * direct), with multi = 1, q_tokens = T, and the partial buffers and
+ * counters of the n_seqs * T query rows: one CTA takes one partition of a
+ * sequence for all its T tokens, whose partials pa_merge merges per row.
  * Limits: block_size 16 or 32, d 128 or 256, hq a multiple of hkv with
  * hq / hkv <= 8, total_len <= n_seqs * max_len.  PA_ERR_INVALID otherwise. */
 typedef struct {
@@ -197,6 +205,9 @@ typedef struct {
 /* pa_plan_in.flags: the plan may be a stream plan (see below); only
  * pa_decode_fused and pa_decode_step_fused on the fast kernel run those. */
 #define PA_PLAN_STREAM_OK 1u
+/* pa_plan_in.flags: with q_tokens = T >= 2, decode the T query tokens of a
+ * sequence together (see below); the fast kernel runs those plans. */
+#define PA_PLAN_MULTI_TOKEN 2u
 
 typedef struct {
     uint32_t part_tokens, n_parts, direct, n_ctas;
@@ -205,6 +216,7 @@ typedef struct {
     uint32_t q_tokens;           /* query tokens per sequence (>= 1) */
     uint32_t n_direct;           /* leading query rows decoded directly in a partitioned plan */
     uint32_t stream;             /* 1: a stream plan (equal tile ranges per CTA) */
+    uint32_t multi;              /* 1: a multi-token plan (the T tokens of a sequence together) */
 } pa_plan_t;
 
 /* With the environment variable PA_LOG_PLAN set (to anything but "" or

@@ -55,6 +55,11 @@ frozen here so that the C++ planner can be compared with it exactly:
   chunk, n_parts = ceil(ceil(max_len / 16) / chunk) + 1 when that is <= 32
   (else the rules above), n_ctas = min(slots, ceil(B / chunk)), direct = 0,
   n_direct = 0, stream = 1, partials and counters for every row;
+- a multi-token plan (flags & MULTI_TOKEN, T >= 2, Q4_0 K and V, d = 256,
+  hkv in {1, 2, 4}, T * hq / hkv <= 24): the one-token plan of the
+  sequences (a plan with direct rows becomes direct: part_tokens =
+  roundup(max_len, 32), n_parts = 1, n_ctas = n_seqs) with multi = 1,
+  q_tokens = T and partial buffers and counters for the n_seqs * T rows;
 - with q_tokens = T > 1 (several query tokens per sequence, each a query
   row of its own that attends causally) the rule runs over the S * T query
   rows with T * total_len tokens of work: every S above reads S * T and
@@ -66,6 +71,7 @@ TILE = 32
 MIN_PART = 128
 CTA_COST = 512  # a CTA's fixed work in tokens of streaming (wave-filling plans)
 STREAM_OK = 1   # flags: the plan may be a stream plan
+MULTI_TOKEN = 2  # flags: decode the T query tokens of a sequence together
 
 OK, INVALID = 0, -1
 
@@ -81,7 +87,8 @@ def _roundup(a: int, b: int) -> int:
 def plan(*, n_seqs, max_len, total_len, block_size, hq, hkv, d, k_type, v_type,
          sm_count, ctas_per_sm, force_parts=0, q_tokens=1, flags=0):
     """Returns (rc, dict).  dict keys: part_tokens, n_parts, direct, n_ctas,
-    part_o_bytes, part_ml_bytes, counter_bytes, q_tokens, n_direct, stream."""
+    part_o_bytes, part_ml_bytes, counter_bytes, q_tokens, n_direct, stream,
+    multi."""
     if (n_seqs < 1 or block_size not in (16, 32) or hkv < 1 or hq < hkv or hq % hkv
             or hq // hkv > 8 or d not in (128, 256) or k_type not in (0, 1, 2)
             or v_type not in (0, 1, 2) or sm_count < 1 or ctas_per_sm < 1
@@ -91,6 +98,23 @@ def plan(*, n_seqs, max_len, total_len, block_size, hq, hkv, d, k_type, v_type,
     T = max(1, q_tokens)
     if T > 4096:
         return INVALID, None
+    if ((flags & MULTI_TOKEN) and T >= 2 and k_type == 2 and v_type == 2 and d == 256
+            and hkv in (1, 2, 4) and T * (hq // hkv) <= 24):
+        rc, b = plan(n_seqs=n_seqs, max_len=max_len, total_len=total_len,
+                     block_size=block_size, hq=hq, hkv=hkv, d=d, k_type=k_type, v_type=v_type,
+                     sm_count=sm_count, ctas_per_sm=ctas_per_sm, force_parts=force_parts)
+        if rc != OK:
+            return rc, None
+        if b["n_direct"]:
+            b.update(part_tokens=_roundup(max_len, TILE), n_parts=1, direct=1, n_direct=0,
+                     n_ctas=n_seqs)
+        rows, P = n_seqs * T, b["n_parts"]
+        direct = b["direct"]
+        b.update(q_tokens=T, multi=1,
+                 part_o_bytes=0 if direct else rows * hq * P * d * 2,
+                 part_ml_bytes=0 if direct else rows * hq * P * 8,
+                 counter_bytes=0 if direct else 4 * rows * (1 + math.isqrt(P - 1) + 1))
+        return OK, b
     rows, work = n_seqs * T, T * total_len   # query rows and their work at most
     n_direct = 0
     if max_len == 0:
@@ -138,7 +162,7 @@ def plan(*, n_seqs, max_len, total_len, block_size, hq, hkv, d, k_type, v_type,
                             part_o_bytes=rows * hq * np_ * d * 2,
                             part_ml_bytes=rows * hq * np_ * 8,
                             counter_bytes=4 * rows * (1 + math.isqrt(np_ - 1) + 1),
-                            q_tokens=T, n_direct=0, stream=1)
+                            q_tokens=T, n_direct=0, stream=1, multi=0)
     direct = 1 if n_parts == 1 else 0
     if direct:
         n_ctas = rows
@@ -152,4 +176,4 @@ def plan(*, n_seqs, max_len, total_len, block_size, hq, hkv, d, k_type, v_type,
         cb = 4 * m * (1 + math.isqrt(n_parts - 1) + 1)
     return OK, dict(part_tokens=part, n_parts=n_parts, direct=direct, n_ctas=n_ctas,
                     part_o_bytes=po, part_ml_bytes=pm, counter_bytes=cb, q_tokens=T,
-                    n_direct=n_direct, stream=0)
+                    n_direct=n_direct, stream=0, multi=0)

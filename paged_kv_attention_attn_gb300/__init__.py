@@ -25,6 +25,7 @@ PA_STATUS_APPEND_RANGE = 8
 PA_FLAG_PLAIN = 1
 PA_FLAG_MERGE_NO_WAIT = 2
 PA_PLAN_STREAM_OK = 1
+PA_PLAN_MULTI_TOKEN = 2
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_build", "libpa.so")
 
@@ -50,7 +51,8 @@ class Plan(ctypes.Structure):
                 ("direct", ctypes.c_uint32), ("n_ctas", ctypes.c_uint32),
                 ("part_o_bytes", ctypes.c_uint64), ("part_ml_bytes", ctypes.c_uint64),
                 ("counter_bytes", ctypes.c_uint64), ("q_tokens", ctypes.c_uint32),
-                ("n_direct", ctypes.c_uint32), ("stream", ctypes.c_uint32)]
+                ("n_direct", ctypes.c_uint32), ("stream", ctypes.c_uint32),
+                ("multi", ctypes.c_uint32)]
 
     def as_dict(self):
         return {k: int(getattr(self, k)) for k, _ in self._fields_}
@@ -227,9 +229,10 @@ def query_occupancy(*, hq, hkv, d, block_size, k_type, v_type) -> tuple[int, int
 
 
 def plan(*, seq_lens, block_size, hq, hkv, d, k_type, v_type, sm_count=None,
-         ctas_per_sm=None, force_parts=0, q_tokens=1, stream_ok=False) -> Plan:
+         ctas_per_sm=None, force_parts=0, q_tokens=1, stream_ok=False, multi=False) -> Plan:
     """pa_plan for these lengths; q_tokens query tokens per sequence;
-    stream_ok lets the planner return a stream plan (fused calls only)."""
+    stream_ok lets the planner return a stream plan (fused calls only);
+    multi asks for a multi-token plan (the tokens of a sequence together)."""
     lens = [int(x) for x in seq_lens]
     if sm_count is None or ctas_per_sm is None:
         sm, cps = query_occupancy(hq=hq, hkv=hkv, d=d, block_size=block_size, k_type=k_type,
@@ -239,7 +242,7 @@ def plan(*, seq_lens, block_size, hq, hkv, d, k_type, v_type, sm_count=None,
     pin = _plan_in(len(lens), max(lens) if lens else 0, sum(lens), block_size, hq, hkv, d,
                    k_type, v_type, sm_count, ctas_per_sm, force_parts)
     pin.q_tokens = int(q_tokens)
-    pin.flags = PA_PLAN_STREAM_OK if stream_ok else 0
+    pin.flags = (PA_PLAN_STREAM_OK if stream_ok else 0) | (PA_PLAN_MULTI_TOKEN if multi else 0)
     out = Plan()
     _check(lib().pa_plan(ctypes.byref(pin), ctypes.byref(out)))
     return out

@@ -2,6 +2,7 @@
 // with D = 128 or 256, Q8_0 and Q4_0 with D = 256), and the dispatch between
 // these, the mixed-type instances (k_fast_mix.cu) and the plain kernel.
 #include "fast_kernel.cuh"
+#include "mt_kernel.cuh"
 
 namespace pa {
 
@@ -35,9 +36,17 @@ int fast_decode_occupancy(pa_type kt, pa_type vt, uint32_t d, uint32_t, uint32_t
                     : occupancy_t<F16T<128>>(hkv, ctas_per_sm);
 }
 
+bool mt_decode_supported(pa_type kt, pa_type vt, uint32_t d, uint32_t hq, uint32_t hkv,
+                         uint32_t T)
+{
+    return mt_supported(kt, vt, d, hq, hkv, T);
+}
+
 int launch_fast_decode(const DecodeParams &p, pa_type kt, pa_type vt, cudaStream_t st,
                        const char *entry)
 {
+    if (p.multi)
+        return launch_mt(p, st, entry);
     // TMA slot coordinates are int32: larger pools take the plain kernel
     if (p.n_pool_blocks * p.block_size >= (1ull << 31))
         return launch_plain_decode(p, kt, vt, st, entry);

@@ -72,8 +72,11 @@ int resolve(const pa_decode_args *a, const pa_plan_t *plan, const char *E, pa::D
     const uint32_t T = plan->q_tokens > 1 ? plan->q_tokens : 1;
     if ((uint64_t)a->n_seqs * T > 0x7fffffffull)
         return fail(PA_ERR_RANGE, E, "n_seqs * q_tokens exceeds 2^31 - 1");
-    if (plan->direct && plan->n_ctas != a->n_seqs * T)
-        return fail(PA_ERR_INVALID, E, "direct plan must have n_ctas == n_seqs * q_tokens");
+    // a direct plan has one CTA per query row, or per sequence when the
+    // sequence's T rows are decoded together (a multi-token plan)
+    if (plan->direct && plan->n_ctas != (plan->multi ? a->n_seqs : a->n_seqs * T))
+        return fail(PA_ERR_INVALID, E, "direct plan must have n_ctas == n_seqs%s",
+                    plan->multi ? "" : " * q_tokens");
     if (plan->direct ? plan->n_direct != 0
                      : (plan->n_direct >= a->n_seqs * T || plan->n_ctas <= plan->n_direct))
         return fail(PA_ERR_INVALID, E, "inconsistent n_direct %u for %u query rows",
@@ -113,6 +116,13 @@ int resolve(const pa_decode_args *a, const pa_plan_t *plan, const char *E, pa::D
     p->n_direct = plan->direct ? 0 : plan->n_direct;
     p->merge_no_wait = (a->flags & PA_FLAG_MERGE_NO_WAIT) ? 1u : 0u;
     p->stream = plan->stream ? 1u : 0u;
+    p->multi = plan->multi ? 1u : 0u;
+    if (plan->multi) {
+        if (plan->stream || plan->n_direct ||
+            !pa::mt_decode_supported(a->k_type, a->v_type, a->d, a->hq, a->hkv, T) ||
+            !use_fast(a))
+            return fail(PA_ERR_INVALID, E, "multi-token plans need the fast kernel and its shapes");
+    }
     if (plan->stream) {
         if (plan->direct || plan->n_direct || plan->n_parts > 32)
             return fail(PA_ERR_INVALID, E, "inconsistent stream plan");
@@ -205,6 +215,19 @@ extern "C" const char *pa_decode_kernel_name(pa_type kt, pa_type vt, uint32_t d,
     return "plain_decode_kernel";
 }
 
+// The decode launch of a fused call, and for a partitioned multi-token plan
+// (whose kernel writes partials only) the merge kernel after it.
+static int decode_then_merge(const pa_decode_args *args, const pa_plan_t *plan,
+                             const pa::DecodeParams &p, cudaStream_t st, const char *E)
+{
+    int rc = launch_decode(args, p, st, E);
+    if (rc || !plan->multi || plan->direct)
+        return rc;
+    return pa::launch_merge(args->part_o, args->part_ml, args->seq_lens, p.out, args->n_seqs,
+                            plan->q_tokens, args->hq, args->d, plan->n_parts, plan->part_tokens,
+                            0, st, E);
+}
+
 extern "C" int pa_decode_fused(const pa_decode_args *args, const pa_plan_t *plan,
                                int32_t *counters, pa_stream_t stream)
 {
@@ -218,9 +241,10 @@ extern "C" int pa_decode_fused(const pa_decode_args *args, const pa_plan_t *plan
             return fail(PA_ERR_INVALID, E, "a partitioned plan needs 4-byte aligned counters");
         if (!args->out)
             return fail(PA_ERR_INVALID, E, "out is NULL");
-        p.counters = counters;
+        if (!plan->multi)
+            p.counters = counters;
     }
-    return launch_decode(args, p, pa::stream_of(stream), E);
+    return decode_then_merge(args, plan, p, pa::stream_of(stream), E);
 }
 
 extern "C" int pa_decode_step_fused(const pa_decode_args *args, const pa_plan_t *plan,
@@ -236,13 +260,14 @@ extern "C" int pa_decode_step_fused(const pa_decode_args *args, const pa_plan_t 
             return fail(PA_ERR_INVALID, E, "a partitioned plan needs 4-byte aligned counters");
         if (!args->out)
             return fail(PA_ERR_INVALID, E, "out is NULL");
-        p.counters = counters;
+        if (!plan->multi)
+            p.counters = counters;
     }
     cudaStream_t st = pa::stream_of(stream);
     if (args->k_type != PA_F16) {
         if (!q8_1_scratch || (reinterpret_cast<uintptr_t>(q8_1_scratch) & 15))
             return fail(PA_ERR_INVALID, E, "quantised K needs a 16-byte aligned q8_1_scratch");
-        if (use_fast(args) && !plan->stream) {
+        if (use_fast(args) && !plan->stream && !plan->multi) {
             // the fast kernel quantises the query rows itself: one launch per step
             p.q_f32 = 1;
             return launch_decode(args, p, st, E);
@@ -253,7 +278,7 @@ extern "C" int pa_decode_step_fused(const pa_decode_args *args, const pa_plan_t 
             return rc;
         p.q = q8_1_scratch;
     }
-    return launch_decode(args, p, st, E);
+    return decode_then_merge(args, plan, p, st, E);
 }
 
 extern "C" int pa_merge(const void *part_o, const float *part_ml, const int32_t *seq_lens,

@@ -171,7 +171,28 @@ extern "C" uint32_t pa_pool_capacity(const pa_pool *pool) { return pool ? pool->
 static uint64_t cdiv(uint64_t a, uint64_t b) { return (a + b - 1) / b; }
 static uint64_t roundup(uint64_t a, uint64_t b) { return cdiv(a, b) * b; }
 
+static int pa_plan_quiet(const pa_plan_in *in, pa_plan_t *out);
+
 extern "C" int pa_plan(const pa_plan_in *in, pa_plan_t *out)
+{
+    const int rc = pa_plan_quiet(in, out);
+    if (rc)
+        return rc;
+    // PA_LOG_PLAN (set, not "0"): one line per plan on stderr
+    const char *log = getenv("PA_LOG_PLAN");
+    if (log && *log && strcmp(log, "0") != 0)
+        fprintf(stderr,
+                "pa_plan: n_seqs=%u q_tokens=%u max_len=%u total_len=%llu slots=%lld "
+                "force_parts=%d flags=%u -> part_tokens=%u n_parts=%u direct=%u n_direct=%u "
+                "n_ctas=%u stream=%u multi=%u\n",
+                in->n_seqs, out->q_tokens, in->max_len, (unsigned long long)in->total_len,
+                (long long)in->sm_count * in->ctas_per_sm, in->force_parts, in->flags,
+                out->part_tokens, out->n_parts, out->direct, out->n_direct, out->n_ctas,
+                out->stream, out->multi);
+    return PA_OK;
+}
+
+static int pa_plan_quiet(const pa_plan_in *in, pa_plan_t *out)
 {
     static const char *E = "pa_plan";
     const uint64_t TILE = 32, MIN_PART = 128;
@@ -197,6 +218,34 @@ extern "C" int pa_plan(const pa_plan_in *in, pa_plan_t *out)
     const uint64_t T = in->q_tokens > 1 ? in->q_tokens : 1;
     if (T > 4096)
         return fail(PA_ERR_INVALID, E, "q_tokens %u exceeds 4096", in->q_tokens);
+    // a multi-token plan: the one-token plan of the sequences, for T rows each
+    if ((in->flags & PA_PLAN_MULTI_TOKEN) && T >= 2 && in->k_type == PA_Q4_0 &&
+        in->v_type == PA_Q4_0 && in->d == 256 &&
+        (in->hkv == 1 || in->hkv == 2 || in->hkv == 4) && T * (in->hq / in->hkv) <= 24) {
+        pa_plan_in one = *in;
+        one.q_tokens = 1;
+        one.flags = 0;
+        pa_plan_t b;
+        int rc = pa_plan_quiet(&one, &b);
+        if (rc)
+            return rc;
+        if (b.n_direct) {  // no direct rows in a partitioned multi-token plan
+            b.part_tokens = (uint32_t)roundup(in->max_len, TILE);
+            b.n_parts = 1;
+            b.direct = 1;
+            b.n_direct = 0;
+            b.n_ctas = in->n_seqs;
+        }
+        const uint64_t rows = (uint64_t)in->n_seqs * T;
+        b.q_tokens = (uint32_t)T;
+        b.multi = 1;
+        b.part_o_bytes = b.direct ? 0 : rows * in->hq * b.n_parts * in->d * 2ull;
+        b.part_ml_bytes = b.direct ? 0 : rows * in->hq * b.n_parts * 8ull;
+        b.counter_bytes =
+            b.direct ? 0 : rows * pa::merge_counters_per_seq(b.n_parts) * 4ull;
+        *out = b;
+        return PA_OK;
+    }
     const uint64_t rows = (uint64_t)in->n_seqs * T, work = T * in->total_len;
     if (rows > 0x7fffffffull)
         return fail(PA_ERR_RANGE, E, "n_seqs * q_tokens exceeds 2^31 - 1");
@@ -285,10 +334,8 @@ extern "C" int pa_plan(const pa_plan_in *in, pa_plan_t *out)
                 p.part_o_bytes = rows * in->hq * np * in->d * 2ull;
                 p.part_ml_bytes = rows * in->hq * np * 8ull;
                 p.counter_bytes = rows * pa::merge_counters_per_seq((uint32_t)np) * 4ull;
-                part = p.part_tokens;
-                n_parts = np;
                 *out = p;
-                goto logged;
+                return PA_OK;
             }
         }
     }
@@ -316,17 +363,5 @@ extern "C" int pa_plan(const pa_plan_in *in, pa_plan_t *out)
     }
     *out = p;
     }
-logged:
-    // PA_LOG_PLAN (set, not "0"): one line per plan on stderr
-    const char *log = getenv("PA_LOG_PLAN");
-    if (log && *log && strcmp(log, "0") != 0)
-        fprintf(stderr,
-                "pa_plan: n_seqs=%u q_tokens=%u max_len=%u total_len=%llu slots=%lld "
-                "force_parts=%d flags=%u -> part_tokens=%u n_parts=%u direct=%u n_direct=%u "
-                "n_ctas=%u stream=%u\n",
-                in->n_seqs, out->q_tokens, in->max_len, (unsigned long long)in->total_len,
-                (long long)in->sm_count * in->ctas_per_sm, in->force_parts, in->flags,
-                out->part_tokens, out->n_parts, out->direct, out->n_direct, out->n_ctas,
-                out->stream);
     return PA_OK;
 }

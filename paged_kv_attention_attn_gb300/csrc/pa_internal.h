@@ -74,6 +74,7 @@ struct DecodeParams {
                             // partials, counters and merges index row r at r - n_direct
     uint32_t merge_no_wait; // PA_FLAG_MERGE_NO_WAIT: cooperative merges give up waiting
     uint32_t stream;        // a stream plan: CTA c takes tiles [c, c + 1) * part_tokens / 16
+    uint32_t multi;         // a multi-token plan: a CTA takes a sequence's T query rows
 };
 
 // The argument checks of pa_decode_partial alone: PA_OK, or the error
@@ -104,6 +105,9 @@ int fast_decode_occupancy(pa_type kt, pa_type vt, uint32_t d, uint32_t hq, uint3
                           uint32_t block_size, int *ctas_per_sm);
 int launch_fast_decode(const DecodeParams &p, pa_type kt, pa_type vt, cudaStream_t st,
                        const char *entry);
+// Whether the multi-token kernel serves these shapes with T query tokens.
+bool mt_decode_supported(pa_type kt, pa_type vt, uint32_t d, uint32_t hq, uint32_t hkv,
+                         uint32_t T);
 // The mixed K x V type instances of the fast kernel (D = 256).
 bool fast_mixed_supported(pa_type kt, pa_type vt, uint32_t hkv);
 int fast_mixed_occupancy(pa_type kt, pa_type vt, uint32_t hkv, int *ctas_per_sm);

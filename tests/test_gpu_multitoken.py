@@ -79,3 +79,73 @@ def test_several_query_tokens_paged_equals_contiguous(kernel):
     a, _, _, _ = H.run(case, plan=pl, q=q4, flags=KERNELS[kernel], fused=True)
     b, _, _, _ = H.run(twin, plan=pl, q=q4, flags=KERNELS[kernel], fused=True)
     assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+
+
+# ---------------------------------------------------- multi-token plans
+#
+# The T tokens of a sequence decoded together (T * G query columns of each
+# K/V head per tile, a warp pair per head splitting the head dimension).
+
+def _mt_plan(spec, T, force=0, sm_count=None):
+    kw = dict(seq_lens=spec.seq_lens, block_size=spec.block_size, hq=spec.hq, hkv=spec.hkv,
+              d=spec.d, k_type=spec.k_type, v_type=spec.v_type, force_parts=force, q_tokens=T,
+              multi=True)
+    if sm_count is not None:
+        kw.update(sm_count=sm_count, ctas_per_sm=1)
+    pl = pa.plan(**kw)
+    assert pl.multi == 1 and pl.q_tokens == T
+    return pl
+
+
+@pytest.mark.parametrize("T,hq,hkv,B", [(2, 24, 4, 16), (4, 24, 4, 16), (3, 24, 4, 32),
+                                        (6, 8, 2, 16), (3, 8, 1, 16)])
+@pytest.mark.parametrize("force", [0, 1, 5])
+def test_multi_token_plan_matches_the_oracle(T, hq, hkv, B, force):
+    """Every mode (auto, direct, partitioned), every entry point (three
+    launches, fused), lengths shorter than the window and empty sequences:
+    against the oracle's causal form, and the fused step equal to the
+    three-launch step bit for bit."""
+    lens = [700, 3, 0, 130, 16, 2, 1999]
+    spec = synth.CaseSpec(seq_lens=lens, k_type=synth.Q4_0, v_type=synth.Q4_0, hq=hq, hkv=hkv,
+                          block_size=B, junk=4, outliers=True)
+    case = synth.build_case(spec, seed=3600 + T + hkv, device=DEV)
+    q4 = _q4(spec, T, 3700 + T)
+    ref, vmax = _oracle(case, q4), H.oracle_vmax(case)
+    pl = _mt_plan(spec, T, force)
+    assert pl.direct == (force == 1)
+    a, ws_a, _, tails = H.run(case, plan=pl, q=q4, canary=True, out_fill=float("nan"))
+    b, ws_b, _, _ = H.run(case, plan=pl, q=q4, fused=True, out_fill=float("nan"))
+    H.check_canaries(tails)
+    assert pa.status_read(ws_a.status) == 0 and pa.status_read(ws_b.status) == 0
+    H.assert_close(case, a, ref, vmax, label=f"multi-token T{T} G{hq // hkv}")
+    assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+
+
+def test_multi_token_plan_against_the_row_plan_and_contiguous():
+    """The multi-token plan and the per-row plan of the same window agree
+    within the gate; the paged layout equals its contiguous twin bit for
+    bit; a small machine gives many partitions per sequence."""
+    spec = synth.CaseSpec(seq_lens=[3000, 1025, 64, 4100], k_type=synth.Q4_0, v_type=synth.Q4_0,
+                          junk=6)
+    case = synth.build_case(spec, seed=3800, device=DEV)
+    q4 = _q4(spec, 4, 3801)
+    pl = _mt_plan(spec, 4, sm_count=20)
+    assert not pl.direct and pl.n_parts >= 4
+    a, _, _, _ = H.run(case, plan=pl, q=q4, fused=True)
+    twin = synth.contiguous_twin(case)
+    b, _, _, _ = H.run(twin, plan=pl, q=q4, fused=True)
+    assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+    row, _, _, _ = H.run(case, plan=_plan(spec, 4, 0), q=q4, fused=True)
+    vmax = H.oracle_vmax(case)
+    assert float((a - row).abs().max()) <= H.tol_for(spec) * vmax
+    H.assert_close(case, a, _oracle(case, q4), vmax, label="multi-token 4 x ragged")
+
+
+def test_multi_token_plans_need_the_fast_kernel():
+    spec = synth.CaseSpec(seq_lens=[200, 300], k_type=synth.Q4_0, v_type=synth.Q4_0)
+    case = synth.build_case(spec, seed=3900, device=DEV)
+    q4 = _q4(spec, 2, 3901)
+    pl = _mt_plan(spec, 2)
+    with pytest.raises(pa.PAError) as e:
+        H.run(case, plan=pl, q=q4, flags=pa.PA_FLAG_PLAIN)
+    assert e.value.code == pa.PA_ERR_INVALID

@@ -111,7 +111,7 @@ def test_plan_matches_model():
                   k_type=rng.choice([0, 1, 2]), v_type=rng.choice([0, 1, 2]),
                   sm_count=rng.choice([152, 148, 1]), ctas_per_sm=rng.choice([1, 2]),
                   force_parts=rng.choice([0, 0, 3, 64]), q_tokens=rng.choice([1, 1, 2, 5]),
-                  flags=rng.choice([0, 1]))
+                  flags=rng.choice([0, 1, 2, 3]))
         mrc, mp = plan_model.plan(**kw)
         pin = pa.PlanIn(**kw)
         out = pa.Plan()
@@ -209,6 +209,6 @@ def test_plan_log_line_when_asked():
         if expect:
             assert lines == ["pa_plan: n_seqs=8 q_tokens=1 max_len=131072 total_len=1048576 "
                              "slots=152 force_parts=0 flags=0 -> part_tokens=6912 n_parts=19 "
-                             "direct=0 n_direct=0 n_ctas=152 stream=0"]
+                             "direct=0 n_direct=0 n_ctas=152 stream=0 multi=0"]
         else:
             assert lines == []
