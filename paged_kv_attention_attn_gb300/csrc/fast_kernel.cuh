@@ -167,6 +167,39 @@ __device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// D = A B + C with C separate from D (C may be a constant quad).
+__device__ __forceinline__ void mma16816_c(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                           uint32_t a3, uint32_t b0, uint32_t b1, const float (&c)[4])
+{
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%10,%11,%12,%13};"
+        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(c[0]), "f"(c[1]), "f"(c[2]),
+          "f"(c[3]));
+}
+
+// D = A B + C, m16n8k8 in tf32 with f32 accumulation.
+__device__ __forceinline__ void mma1688_tf32(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                             uint32_t a3, uint32_t b0, uint32_t b1,
+                                             const float (&c)[4])
+{
+    asm volatile(
+        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%10,%11,%12,%13};"
+        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(c[0]), "f"(c[1]), "f"(c[2]),
+          "f"(c[3]));
+}
+
+// f32 to tf32, rounded to nearest (ties away), as the f32 bit pattern.
+__device__ __forceinline__ uint32_t to_tf32(float x)
+{
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return r;
+}
+
 __device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], uint32_t addr)
 {
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
@@ -201,6 +234,13 @@ __device__ __forceinline__ uint32_t lds_u32(uint32_t a)
 {
     uint32_t v;
     asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(a) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ float lds_f32(uint32_t a)
+{
+    float v;
+    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(a) : "memory");
     return v;
 }
 
@@ -405,14 +445,16 @@ struct Q40T {
     static constexpr bool kExtract = !kZeroInvalidV;
     static constexpr uint32_t kTypeKey = PA_Q4_0 * 3 + PA_Q4_0;
 
-    // Query fragments live in shared memory, one 32-byte record per (block,
-    // lane) of each K/V head: the four B registers, then the C quad that
-    // starts the accumulator at minus the bias contribution (heads 2tig, 2tig+1).
-    static constexpr int QREC = 16;                     // one uint4 per (block, lane)
-    static constexpr int QCORR = NB * 32 * QREC;         // offset of the C quads
-    static constexpr int QBYTES = 2 * NB * 32 * QREC;    // per K/V head
+    // Query fragments live in shared memory, one 16-byte record per (block,
+    // lane) of each K/V head (the four B registers), then the bias term of
+    // each (query head, block): minus the sum of the block's qhat times 1032
+    // (low nibbles, read as 1024 + n) or 72 (high nibbles, read as 64 + n).
+    static constexpr int QREC = 16;                      // one uint4 per (block, lane)
+    static constexpr int QCORR = NB * 32 * QREC;         // offset of the bias terms
+    static constexpr int QBYTES = QCORR + 8 * NB * 4;    // per K/V head
     struct Frag {
-        uint32_t q;  // shared address of this lane's records (block 0)
+        uint32_t q;                 // shared address of this lane's records (block 0)
+        uint32_t ch0, ch1, cl0, cl1;  // bias of head gid, blocks tig, tig+4: tf32 high, low parts
     };
 
     using Consts = NibbleConsts;
@@ -449,20 +491,30 @@ struct Q40T {
             }
             corr += __shfl_xor_sync(0xffffffffu, corr, 1);
             corr += __shfl_xor_sync(0xffffffffu, corr, 2);
-            const float n0 = -__shfl_sync(0xffffffffu, corr, 8 * tig);
-            const float n1 = -__shfl_sync(0xffffffffu, corr, 8 * tig + 4);
             const uint32_t rr = qsm + (b * 32 + lane) * QREC;
             asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(rr),
                          "r"(h2_bits(__halves2half2(qh[0], qh[2]))),
                          "r"(h2_bits(__halves2half2(qh[1], qh[3]))),
                          "r"(h2_bits(__halves2half2(qh[4], qh[6]))),
                          "r"(h2_bits(__halves2half2(qh[5], qh[7]))));
-            asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(rr + QCORR), "f"(n0),
-                         "f"(n1), "f"(n0), "f"(n1));
+            if (tig == 0)
+                sts_f32(qsm + QCORR + 4 * (gid * NB + b), -corr);
         }
     }
 
-    __device__ static void load_q(uint32_t qsm, int lane, Frag &f) { f.q = qsm + lane * QREC; }
+    // The B fragments of the bias product (see scores()): blocks tig and
+    // tig+4 of head gid, as a tf32 high part and the tf32 remainder, so the
+    // pair holds the f32 term to about 21 bits.
+    __device__ static void load_q(uint32_t qsm, int lane, Frag &f)
+    {
+        f.q = qsm + lane * QREC;
+        const uint32_t c = qsm + QCORR + 4 * ((lane >> 2) * NB + (lane & 3));
+        const float c0 = lds_f32(c), c1 = lds_f32(c + 16);
+        f.ch0 = to_tf32(c0);
+        f.ch1 = to_tf32(c1);
+        f.cl0 = to_tf32(c0 - __uint_as_float(f.ch0));
+        f.cl1 = to_tf32(c1 - __uint_as_float(f.ch1));
+    }
 
     // Block scales of the tile into the warp's scratch: dk as float with the
     // pair (t, t+8) adjacent, dv as half in token order; zero for invalid tokens.
@@ -508,22 +560,20 @@ struct Q40T {
 
     // One 32-value block: x0 / x1 are the nibble words of tokens gid / gid+8
     // holding dims 4tig..4tig+3 (low nibbles) and 16+4tig..19+4tig (high).
+    // The block's dot of the biased nibbles, times d_k, adds to s.
     __device__ static __forceinline__ void block(const NibbleConsts &K, uint32_t qrec, uint32_t x0,
                                                  uint32_t x1, float2 dk, float (&s)[4])
     {
         uint32_t qb0, qb1, qb2, qb3;
         float c[4];
+        const float zero[4] = {0.0f, 0.0f, 0.0f, 0.0f};
         asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
             : "=r"(qb0), "=r"(qb1), "=r"(qb2), "=r"(qb3)
             : "r"(qrec)
             : "memory");
-        asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
-            : "=f"(c[0]), "=f"(c[1]), "=f"(c[2]), "=f"(c[3])
-            : "r"(qrec + QCORR)
-            : "memory");
         const uint32_t y0 = x0 >> 8, y1 = x1 >> 8;
-        mma16816(c, and_or(x0, K.mlo, K.blo), and_or(x1, K.mlo, K.blo), and_or(y0, K.mlo, K.blo),
-                 and_or(y1, K.mlo, K.blo), qb0, qb1);
+        mma16816_c(c, and_or(x0, K.mlo, K.blo), and_or(x1, K.mlo, K.blo), and_or(y0, K.mlo, K.blo),
+                   and_or(y1, K.mlo, K.blo), qb0, qb1, zero);
         mma16816(c, and_or(x0, K.mhi, K.bhi), and_or(x1, K.mhi, K.bhi), and_or(y0, K.mhi, K.bhi),
                  and_or(y1, K.mhi, K.bhi), qb2, qb3);
         s[0] = fmaf(c[0], dk.x, s[0]);
@@ -532,13 +582,25 @@ struct Q40T {
         s[3] = fmaf(c[3], dk.y, s[3]);
     }
 
+    // Scores of the tile: s starts at the bias term sum_b d_k[t][b] *
+    // bias[head][b], two tf32 MMAs over the 8 blocks (A: the d_k of tokens
+    // gid, gid+8, blocks tig, tig+4, exact in tf32 as f16 values; B: the
+    // bias's high part, then its remainder); then each block adds d_k times
+    // the dot of its biased nibbles.
     __device__ static void scores(const NibbleConsts &K, const Frag &f, uint32_t kh, uint32_t scr,
                                   int gid, int tig, float (&s)[4])
     {
         uint32_t r0 = kh + gid * RB + 4 * tig;
         uint32_t dk = scr + DK + 8 * gid;
         uint32_t qr = f.q;
-        s[0] = s[1] = s[2] = s[3] = 0.0f;
+        {
+            const float2 d0 = lds_f2(dk + 4 * kTile * tig), d1 = lds_f2(dk + 4 * kTile * (tig + 4));
+            const uint32_t a0 = __float_as_uint(d0.x), a1 = __float_as_uint(d0.y);
+            const uint32_t a2 = __float_as_uint(d1.x), a3 = __float_as_uint(d1.y);
+            const float zero[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+            mma1688_tf32(s, a0, a1, a2, a3, f.ch0, f.ch1, zero);
+            mma1688_tf32(s, a0, a1, a2, a3, f.cl0, f.cl1, s);
+        }
 #pragma unroll
         for (int pb = 0; pb < NB / 2; ++pb) {
             // blocks 2pb and 2pb+1 share 36 bytes = 9 aligned words
