@@ -390,7 +390,7 @@ def run_ours(a, world, rank, local):
                  seq_lens=spec.seq_lens, block_size=spec.block_size, hq=spec.hq, hkv=spec.hkv,
                  d=spec.d, k_type=spec.k_type, v_type=spec.v_type,
                  stream_ok=not a.unfused and not a.plain and a.stream == "on",
-                 multi=not a.plain and a.multi == "on")
+                 multi=not a.plain and a.multi == "on", force_parts=a.force_parts)
     ws = pa.workspace(pl, n_seqs=spec.n_seqs, hq=spec.hq, d=spec.d, device=dev)
     quantised = spec.k_type != synth.F16
     kv_bytes = (case.k_pool.numel() + case.v_pool.numel())
@@ -659,6 +659,9 @@ def main():
                     help="several query tokens per sequence: decode a sequence's tokens together")
     ap.add_argument("--stream", choices=["on", "off"], default="off",
                     help="let the planner return stream plans (batches wider than the grid)")
+    ap.add_argument("--force-parts", type=int, default=0,
+                    help="partitions per sequence instead of the planner's choice (profiling "
+                         "cases: the benchmark's partition length on a smaller batch)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="oracle work timed for cpu_baseline (whole sequences in turn)")
     a = ap.parse_args()
