@@ -192,6 +192,16 @@ __device__ __forceinline__ void mma1688_tf32(float (&d)[4], uint32_t a0, uint32_
           "f"(c[3]));
 }
 
+// 2^x by the hardware's approximation (relative error about 2^-22), results
+// below 2^-126 flushed to zero: the probabilities of the online softmax,
+// whose arguments are at most -4 there.
+__device__ __forceinline__ float ex2_ftz(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 // f32 to tf32, rounded to nearest (ties away), as the f32 bit pattern.
 __device__ __forceinline__ uint32_t to_tf32(float x)
 {
@@ -1595,8 +1605,8 @@ __device__ __forceinline__ void range_body(const FastArgs &a, uint8_t *smem, uin
         }
         const float ms0 = mref0 == -INFINITY ? 0.0f : mref0;
         const float ms1 = mref1 == -INFINITY ? 0.0f : mref1;
-        const float q00 = exp2f(sc[0] - ms0), q01 = exp2f(sc[1] - ms1);
-        const float q10 = exp2f(sc[2] - ms0), q11 = exp2f(sc[3] - ms1);
+        const float q00 = ex2_ftz(sc[0] - ms0), q01 = ex2_ftz(sc[1] - ms1);
+        const float q10 = ex2_ftz(sc[2] - ms0), q11 = ex2_ftz(sc[3] - ms1);
         l0 += q00 + q10;
         l1 += q01 + q11;
         // P[token][head] as two 8x8 blocks (tokens 0-7, 8-15) -> PV B operand
