@@ -359,9 +359,15 @@ int pa_decode_step(const pa_decode_args *args, const pa_plan_t *plan, void *q8_1
  * When out_host is page-locked memory mapped into the device's address space
  * (cudaHostAlloc / cudaMallocHost under unified addressing, 16-byte aligned),
  * the kernels store the output into it directly and args->out is left
- * untouched; otherwise args->out is copied back into out_host.  Page-locked
- * q_host makes the query copy asynchronous.  The caller synchronises before
- * reading out_host. */
+ * untouched; otherwise args->out is copied back into out_host.  Page-locked,
+ * mapped q_host (16-byte aligned) is staged into args->q by a small kernel
+ * launched with programmatic stream serialisation: it may run while the
+ * previous kernel on the stream finishes, once that kernel has let its
+ * dependents be scheduled, and it completes only after that kernel, so the
+ * decode after it sees both.  A previous kernel that lets its dependents be
+ * scheduled must then be done reading args->q (this library's kernels are).
+ * Other q_host is copied with cudaMemcpyAsync.  The caller synchronises
+ * before reading out_host. */
 int pa_decode_step_host(const float *q_host, float *out_host, const pa_decode_args *args,
                         const pa_plan_t *plan, void *q8_1_scratch, pa_stream_t stream);
 

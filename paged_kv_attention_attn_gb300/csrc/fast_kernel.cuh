@@ -1431,8 +1431,11 @@ __device__ __noinline__ void merge_coop(const DecodeParams &p, uint32_t seq, uin
 // parity (u / NSW) % 2) and are left drained, at the slot and parity after
 // the range's last tile.  any_abort: a bounded wait of some warp ran out
 // (status flagged; the rings may then hold copies of this range), reported
-// only by the kReportAbort instances.
-template <class T, bool kReportAbort>
+// only by the kReportAbort instances.  kTrigger: the CTA allows the next
+// grid on the stream to be scheduled once its tile loop ends (a caller that
+// reads inputs after the range, as the stream kernel's next segment does,
+// passes false and triggers after its last read).
+template <class T, bool kReportAbort, bool kTrigger = true>
 __device__ __forceinline__ void range_body(const FastArgs &a, uint8_t *smem, uint32_t seq,
                                            uint32_t part, int32_t Lrow, uint32_t t0in,
                                            bool dir, uint32_t t1in, uint32_t &s,
@@ -1633,8 +1636,9 @@ __device__ __forceinline__ void range_body(const FastArgs &a, uint8_t *smem, uin
     }
     // the next grid on this stream may be scheduled once every CTA is here
     // (its CTAs take the SMs that this grid's CTAs leave, and wait for this
-    // grid's completion before they read anything)
-    launch_dependents();
+    // grid's completion before they read anything); no input is read after
+    if constexpr (kTrigger)
+        launch_dependents();
     if (aborted && lane == 0) {
         // let my copies still in flight land (bounded) before the CTA moves on
         for (uint32_t k = issued > NSW ? issued - NSW : 0; k < issued; ++k) {
@@ -1766,7 +1770,7 @@ __device__ __noinline__ uint32_t stream_range(const FastArgs &a, uint8_t *smem, 
 {
     uint32_t s = ring & 0xffu, phase = (ring >> 8) & 1u, n_my = 0;
     bool any_abort = false;
-    range_body<T, true>(a, smem, seq, part, L, t0, dir, t1, s, phase, n_my, any_abort);
+    range_body<T, true, false>(a, smem, seq, part, L, t0, dir, t1, s, phase, n_my, any_abort);
     return s | phase << 8 | (any_abort ? 1u : 0u) << 9;
 }
 
@@ -1945,6 +1949,9 @@ __global__ void __launch_bounds__(T::kMaxWarps * 32, 1)
         }
         __syncthreads();  // the combine's reads of the rings before the next copies
     }
+    // every input read (the last segment's query included): the next grid on
+    // the stream may be scheduled
+    launch_dependents();
     // the rows whose count this CTA completed: all partials written and visible
     const __half *po = static_cast<const __half *>(p.part_o);
     const float2 *pml = reinterpret_cast<const float2 *>(p.part_ml);

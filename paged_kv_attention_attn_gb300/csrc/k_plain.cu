@@ -56,6 +56,61 @@ int launch_quantize_q(const float *q, void *q8_1, uint32_t n_rows, uint32_t d, c
     return cuda_check(cudaGetLastError(), entry, "quantize_q8_1_kernel launch");
 }
 
+// -------------------------------------------------------- query staging
+//
+// The query of a host-buffer step, read from page-locked host memory that the
+// device maps and written to the device query buffer.  The grid lets the next
+// grid on the stream (the decode) be scheduled at once, copies, and then waits
+// for the previous grid on the stream before it completes, so the decode,
+// which waits for this grid before it reads anything, comes after both.  It
+// may run while the previous grid finishes, once that grid allows its
+// dependents to be scheduled; this library's kernels do so only after their
+// last read of the query.  One warp per CTA and few registers, so that its
+// CTAs fit beside a decode CTA on an SM.
+__global__ void __maxnreg__(32) stage_query_kernel(const uint4 *__restrict__ src,
+                                                   uint4 *__restrict__ dst, uint32_t n16)
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    const uint32_t stride = gridDim.x * 32u;
+    uint32_t i = blockIdx.x * 32u + threadIdx.x;
+    for (; i + 3 * stride < n16; i += 4 * stride) {
+        const uint4 a = src[i], b = src[i + stride], c = src[i + 2 * stride],
+                    e = src[i + 3 * stride];
+        dst[i] = a;
+        dst[i + stride] = b;
+        dst[i + 2 * stride] = c;
+        dst[i + 3 * stride] = e;
+    }
+    for (; i < n16; i += stride)
+        dst[i] = src[i];
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+int launch_stage_q(const void *src_dev, void *dst, size_t bytes, cudaStream_t st,
+                   const char *entry)
+{
+    if (bytes == 0)
+        return PA_OK;
+    if ((bytes & 15u) || bytes / 16 > 0xffffffffull ||
+        (reinterpret_cast<uintptr_t>(src_dev) & 15u) || (reinterpret_cast<uintptr_t>(dst) & 15u))
+        return fail(PA_ERR_INVALID, entry, "query staging needs 16-byte sizes and addresses");
+    const uint32_t n16 = (uint32_t)(bytes / 16);
+    const uint32_t want = (n16 + 127) / 128;  // four 16-byte loads per thread in flight
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(want < 1024 ? want : 1024);
+    cfg.blockDim = dim3(32);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cuda_check(cudaLaunchKernelEx(&cfg, stage_query_kernel,
+                                         static_cast<const uint4 *>(src_dev),
+                                         static_cast<uint4 *>(dst), n16),
+                      entry, "stage_query_kernel launch");
+}
+
 // ------------------------------------------------------------ plain decode
 
 template <int T>

@@ -341,10 +341,10 @@ extern "C" int pa_decode_step(const pa_decode_args *args, const pa_plan_t *plan,
                             plan->part_tokens, plan->n_direct, st, E);
 }
 
-// The device address of page-locked host memory that the kernels may store
-// to directly (16-byte aligned for their vector stores), or nullptr for any
-// other pointer: pageable memory is never handed to a kernel.
-static float *mapped_host_out(float *h)
+// The device address of page-locked host memory that the kernels may load
+// from or store to directly (16-byte aligned for their vector accesses), or
+// nullptr for any other pointer: pageable memory is never handed to a kernel.
+static float *mapped_host(float *h)
 {
     cudaPointerAttributes at;
     if (cudaPointerGetAttributes(&at, h) != cudaSuccess) {
@@ -355,6 +355,20 @@ static float *mapped_host_out(float *h)
         (reinterpret_cast<uintptr_t>(at.devicePointer) & 15u) != 0)
         return nullptr;
     return static_cast<float *>(at.devicePointer);
+}
+
+// The query of a host-buffer step into args->q: page-locked host memory that
+// the device maps is staged by a kernel that overlaps the previous kernel's
+// end (launch_stage_q); anything else takes an asynchronous copy.
+static int copy_q_in(const float *q_host, const void *q_dev, size_t bytes, cudaStream_t st,
+                     const char *E)
+{
+    const float *mapped = mapped_host(const_cast<float *>(q_host));
+    if (mapped && (bytes & 15u) == 0 && (reinterpret_cast<uintptr_t>(q_dev) & 15u) == 0)
+        return pa::launch_stage_q(mapped, const_cast<void *>(q_dev), bytes, st, E);
+    return cuda_check(cudaMemcpyAsync(const_cast<void *>(q_dev), q_host, bytes,
+                                      cudaMemcpyHostToDevice, st),
+                      E, "copy of q to the device");
 }
 
 extern "C" int pa_decode_step_host(const float *q_host, float *out_host,
@@ -370,14 +384,12 @@ extern "C" int pa_decode_step_host(const float *q_host, float *out_host,
         return rc;
     const size_t bytes = (size_t)p.n_seqs * args->hq * args->d * sizeof(float);
     cudaStream_t st = pa::stream_of(stream);
-    rc = cuda_check(cudaMemcpyAsync(const_cast<void *>(args->q), q_host, bytes,
-                                    cudaMemcpyHostToDevice, st),
-                    E, "copy of q to the device");
+    rc = copy_q_in(q_host, args->q, bytes, st, E);
     if (rc)
         return rc;
     // page-locked out_host: the kernels write it directly, no copy back
     pa_decode_args a = *args;
-    float *out_mapped = mapped_host_out(out_host);
+    float *out_mapped = mapped_host(out_host);
     if (out_mapped)
         a.out = out_mapped;
     rc = pa_decode_step(&a, plan, q8_1_scratch, stream);
@@ -403,14 +415,12 @@ extern "C" int pa_decode_step_fused_host(const float *q_host, float *out_host,
         return fail(PA_ERR_INVALID, E, "a partitioned plan needs counters");
     const size_t bytes = (size_t)p.n_seqs * args->hq * args->d * sizeof(float);
     cudaStream_t st = pa::stream_of(stream);
-    rc = cuda_check(cudaMemcpyAsync(const_cast<void *>(args->q), q_host, bytes,
-                                    cudaMemcpyHostToDevice, st),
-                    E, "copy of q to the device");
+    rc = copy_q_in(q_host, args->q, bytes, st, E);
     if (rc)
         return rc;
     // page-locked out_host: the kernels write it directly, no copy back
     pa_decode_args a = *args;
-    float *out_mapped = mapped_host_out(out_host);
+    float *out_mapped = mapped_host(out_host);
     if (out_mapped)
         a.out = out_mapped;
     rc = pa_decode_step_fused(&a, plan, q8_1_scratch, counters, stream);

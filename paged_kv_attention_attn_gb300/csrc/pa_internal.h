@@ -82,6 +82,11 @@ struct DecodeParams {
 int check_decode(const pa_decode_args *a, const pa_plan_t *plan, const char *entry);
 
 // Launchers (each returns PA_OK or an error already recorded for `entry`).
+// Copies `bytes` (a multiple of 16) from src_dev, a device-mapped host
+// buffer, to dst on the stream, as a grid that lets the next grid be
+// scheduled at once and completes after the previous grid (k_plain.cu).
+int launch_stage_q(const void *src_dev, void *dst, size_t bytes, cudaStream_t st,
+                   const char *entry);
 int launch_quantize_q(const float *q, void *q8_1, uint32_t n_rows, uint32_t d,
                       cudaStream_t st, const char *entry);
 int launch_plain_decode(const DecodeParams &p, pa_type kt, pa_type vt, cudaStream_t st,

@@ -206,14 +206,16 @@ def test_merge_kernel_against_oracle_merge():
 
 
 @pytest.mark.parametrize("kernel", KERNELS)
-def test_host_buffer_step_equals_device_step(kernel):
+@pytest.mark.parametrize("q_pinned", [True, False])
+def test_host_buffer_step_equals_device_step(kernel, q_pinned):
     """The host-buffer steps give the device step's bits, for a partitioned
-    and a direct plan.  Page-locked out_host: the kernels store into it and
-    the device out buffer is left as it was; pageable out_host: the device
-    out buffer is copied back."""
+    and a direct plan.  Page-locked q_host is staged by a kernel, pageable
+    q_host copied.  Page-locked out_host: the kernels store into it and the
+    device out buffer is left as it was; pageable out_host: the device out
+    buffer is copied back."""
     spec = synth.CaseSpec(seq_lens=[700, 90], k_type=synth.Q4_0, v_type=synth.Q4_0, junk=3)
     case = synth.build_case(spec, seed=1900, device=DEV)
-    q_host = case.q.cpu().pin_memory()
+    q_host = case.q.cpu().pin_memory() if q_pinned else case.q.cpu().clone()
     for force in (0, 1):
         dev_out, _, _, _ = H.run(case, force_parts=force, flags=KERNELS[kernel])
         pl = pa.plan(seq_lens=spec.seq_lens, block_size=16, hq=24, hkv=4, d=256,
@@ -233,6 +235,37 @@ def test_host_buffer_step_equals_device_step(kernel):
                 torch.cuda.synchronize()
                 assert torch.equal(out_host.view(torch.int32), dev_out.cpu().view(torch.int32))
                 assert bool(ws.out.isnan().all()) == direct_store
+                assert torch.equal(qdev.view(torch.int32), case.q.view(torch.int32))
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("t", [synth.Q4_0, synth.F16])
+def test_host_buffer_steps_back_to_back(kernel, t):
+    """Host-buffer steps queued back to back, each with its own query in
+    page-locked memory and the same device query buffer: a step's query is
+    staged while the previous step's kernels finish, so each step must still
+    see its own query.  Each output equals the device step of its query bit
+    for bit."""
+    spec = synth.CaseSpec(seq_lens=[3000, 700, 90, 5000], k_type=t, v_type=t, junk=3)
+    case = synth.build_case(spec, seed=1950 + t, device=DEV)
+    g = torch.Generator().manual_seed(1951)
+    qs = [torch.randn(tuple(case.q.shape), generator=g) for _ in range(6)]
+    refs = [H.run(case, q=q.to(DEV), flags=KERNELS[kernel], fused=True)[0].cpu() for q in qs]
+    pl = pa.plan(seq_lens=spec.seq_lens, block_size=16, hq=24, hkv=4, d=256, k_type=t, v_type=t)
+    ws = pa.workspace(pl, n_seqs=spec.n_seqs, hq=24, d=256, device=DEV)
+    qdev = torch.empty_like(case.q)
+    args = pa.make_args(k_pool=case.k_pool, v_pool=case.v_pool, block_table=case.block_table,
+                        seq_lens=case.seq_lens, q=qdev, ws=ws, hkv=4, block_size=16, k_type=t,
+                        v_type=t, flags=KERNELS[kernel])
+    q_hosts = [q.pin_memory() for q in qs]
+    outs = [torch.full(tuple(case.q.shape), float("nan")).pin_memory() for _ in qs]
+    for rep in range(3):
+        for q_host, out_host in zip(q_hosts, outs):
+            pa.decode_step_fused_host(q_host, out_host, args, ws)
+        torch.cuda.synchronize()
+        assert pa.status_read(ws.status) == 0
+        for out_host, ref in zip(outs, refs):
+            assert torch.equal(out_host.view(torch.int32), ref.view(torch.int32))
 
 
 # ------------------------------------------------------------- fused merge
