@@ -62,6 +62,7 @@ struct FastArgs {
     uint32_t region_bytes;       // all rings; reused at the end to park (m, l, O)
     uint32_t coop;               // in-launch merge shared by the CTAs of a sequence
     uint32_t coop_wait_ns;       // bound of a CTA's wait for the others of its sequence
+    uint32_t n_slots32;          // 32-token slots per K/V head (types with kTile32)
 };
 
 // Bound of the wait of the cooperative merge: far above the spread of the
@@ -440,6 +441,10 @@ struct Q40T {
     static constexpr uint32_t kMaxWarps = KMAXW;
     static constexpr int kMergeBatch = 8;
     static constexpr bool kStagedMerge = true;
+    // the one-launch instance takes 32-token tiles from rings shared by the
+    // warps of a K/V head (range_body32); its scratch holds two 16-token halves
+    static constexpr bool kTile32 = true;
+    static constexpr int SCRATCH2 = 2 * SCRATCH;
     static constexpr bool kStream = true;
 
     static __host__ __device__ constexpr uint32_t side_bytes(uint32_t hkv)
@@ -597,6 +602,87 @@ struct Q40T {
     // gid, gid+8, blocks tig, tig+4, exact in tf32 as f16 values; B: the
     // bias's high part, then its remainder); then each block adds d_k times
     // the dot of its biased nibbles.
+    // block() for the two 16-token halves of a 32-token tile: one load of
+    // the query record serves both (x: rows gid, gid+8; z: rows 16+gid, 24+gid).
+    __device__ static __forceinline__ void block2(const NibbleConsts &K, uint32_t qrec, uint32_t x0,
+                                                  uint32_t x1, uint32_t z0, uint32_t z1, float2 dkx,
+                                                  float2 dkz, float (&sx)[4], float (&sz)[4])
+    {
+        uint32_t qb0, qb1, qb2, qb3;
+        const float zero[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+            : "=r"(qb0), "=r"(qb1), "=r"(qb2), "=r"(qb3)
+            : "r"(qrec)
+            : "memory");
+        {
+            float c[4];
+            const uint32_t y0 = x0 >> 8, y1 = x1 >> 8;
+            mma16816_c(c, and_or(x0, K.mlo, K.blo), and_or(x1, K.mlo, K.blo),
+                       and_or(y0, K.mlo, K.blo), and_or(y1, K.mlo, K.blo), qb0, qb1, zero);
+            mma16816(c, and_or(x0, K.mhi, K.bhi), and_or(x1, K.mhi, K.bhi),
+                     and_or(y0, K.mhi, K.bhi), and_or(y1, K.mhi, K.bhi), qb2, qb3);
+            sx[0] = fmaf(c[0], dkx.x, sx[0]);
+            sx[1] = fmaf(c[1], dkx.x, sx[1]);
+            sx[2] = fmaf(c[2], dkx.y, sx[2]);
+            sx[3] = fmaf(c[3], dkx.y, sx[3]);
+        }
+        {
+            float c[4];
+            const uint32_t y0 = z0 >> 8, y1 = z1 >> 8;
+            mma16816_c(c, and_or(z0, K.mlo, K.blo), and_or(z1, K.mlo, K.blo),
+                       and_or(y0, K.mlo, K.blo), and_or(y1, K.mlo, K.blo), qb0, qb1, zero);
+            mma16816(c, and_or(z0, K.mhi, K.bhi), and_or(z1, K.mhi, K.bhi),
+                     and_or(y0, K.mhi, K.bhi), and_or(y1, K.mhi, K.bhi), qb2, qb3);
+            sz[0] = fmaf(c[0], dkz.x, sz[0]);
+            sz[1] = fmaf(c[1], dkz.x, sz[1]);
+            sz[2] = fmaf(c[2], dkz.y, sz[2]);
+            sz[3] = fmaf(c[3], dkz.y, sz[3]);
+        }
+    }
+
+    // The bias product of scores() for one 16-token half (scratch scr).
+    __device__ static __forceinline__ void bias16(const Frag &f, uint32_t scr, int gid, int tig,
+                                                  float (&s)[4])
+    {
+        const uint32_t dk = scr + DK + 8 * gid;
+        const float2 d0 = lds_f2(dk + 4 * kTile * tig), d1 = lds_f2(dk + 4 * kTile * (tig + 4));
+        const uint32_t a0 = __float_as_uint(d0.x), a1 = __float_as_uint(d0.y);
+        const uint32_t a2 = __float_as_uint(d1.x), a3 = __float_as_uint(d1.y);
+        const float zero[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        mma1688_tf32(s, a0, a1, a2, a3, f.ch0, f.ch1, zero);
+        mma1688_tf32(s, a0, a1, a2, a3, f.cl0, f.cl1, s);
+    }
+
+    // scores() of a 32-token tile: K rows 0..31 at kh (pitch RB), the two
+    // halves' scales at scr and scr + SCRATCH; sx: tokens 0..15, sz: 16..31.
+    __device__ static void scores2(const NibbleConsts &K, const Frag &f, uint32_t kh, uint32_t scr,
+                                   int gid, int tig, float (&sx)[4], float (&sz)[4])
+    {
+        uint32_t r0 = kh + gid * RB + 4 * tig;
+        uint32_t dk = scr + DK + 8 * gid;
+        uint32_t qr = f.q;
+        bias16(f, scr, gid, tig, sx);
+        bias16(f, scr + SCRATCH, gid, tig, sz);
+#pragma unroll
+        for (int pb = 0; pb < NB / 2; ++pb) {
+            const uint32_t a0 = lds_u32(r0), a1 = lds_u32(r0 + 4), a2 = lds_u32(r0 + 20);
+            const uint32_t b0 = lds_u32(r0 + 8 * RB), b1 = lds_u32(r0 + 8 * RB + 4);
+            const uint32_t b2 = lds_u32(r0 + 8 * RB + 20);
+            const uint32_t c0 = lds_u32(r0 + 16 * RB), c1 = lds_u32(r0 + 16 * RB + 4);
+            const uint32_t c2 = lds_u32(r0 + 16 * RB + 20);
+            const uint32_t d0 = lds_u32(r0 + 24 * RB), d1 = lds_u32(r0 + 24 * RB + 4);
+            const uint32_t d2 = lds_u32(r0 + 24 * RB + 20);
+            const float2 kx0 = lds_f2(dk), kx1 = lds_f2(dk + 4 * kTile);
+            const float2 kz0 = lds_f2(dk + SCRATCH), kz1 = lds_f2(dk + SCRATCH + 4 * kTile);
+            block2(K, qr, __funnelshift_r(a0, a1, 16), __funnelshift_r(b0, b1, 16),
+                   __funnelshift_r(c0, c1, 16), __funnelshift_r(d0, d1, 16), kx0, kz0, sx, sz);
+            block2(K, qr + 32 * QREC, a2, b2, c2, d2, kx1, kz1, sx, sz);
+            r0 += 36;
+            dk += 2 * 4 * kTile;
+            qr += 2 * 32 * QREC;
+        }
+    }
+
     __device__ static void scores(const NibbleConsts &K, const Frag &f, uint32_t kh, uint32_t scr,
                                   int gid, int tig, float (&s)[4])
     {
@@ -691,6 +777,7 @@ struct Q80T {
     static constexpr int kMergeBatch = 12;
     static constexpr bool kStagedMerge = true;
     static constexpr bool kStream = true;
+    static constexpr bool kTile32 = false;
 
     static __host__ __device__ constexpr uint32_t side_bytes(uint32_t hkv)
     {
@@ -922,6 +1009,7 @@ struct F16T {
     static constexpr int kMergeBatch = 12;
     static constexpr bool kStagedMerge = true;
     static constexpr bool kStream = true;
+    static constexpr bool kTile32 = false;
 
     static __host__ __device__ constexpr uint32_t side_bytes(uint32_t hkv)
     {
@@ -1048,6 +1136,7 @@ struct Mix {
         KT::kMergeBatch < VT::kMergeBatch ? KT::kMergeBatch : VT::kMergeBatch;
     static constexpr bool kStagedMerge = false;  // one instance per mixed pair
     static constexpr bool kStream = false;       // stream plans take one K/V type
+    static constexpr bool kTile32 = false;
     static constexpr uint32_t kSideK = KT::kSideK, kSideV = VT::kSideV;
     static constexpr uint32_t kTmaXK = KT::kTmaXK, kTmaXV = VT::kTmaXV;
     static constexpr uint32_t kRowK = KT::kRowK, kRowV = VT::kRowV;
@@ -1423,6 +1512,58 @@ __device__ __noinline__ void merge_coop(const DecodeParams &p, uint32_t seq, uin
     }
 }
 
+// The end of a range: each warp parks (m, l, O) of its query heads in the
+// idle rings, head-major (the lanes' sums l first added across the warp),
+// then all warps of the CTA combine them into the partial or the output.
+// Called by every thread after a barrier that follows the last ring read.
+template <class T>
+__device__ __forceinline__ void park_and_combine(const DecodeParams &p, uint8_t *smem,
+                                                 const float (&o)[T::MT][4], float mref0,
+                                                 float mref1, float l0, float l1, uint32_t nwarps,
+                                                 uint32_t hkv, uint32_t G, uint32_t seq,
+                                                 uint32_t part, bool dir)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int gid = lane >> 2, tig = lane & 3;
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+        l0 += __shfl_xor_sync(0xffffffffu, l0, off);
+        l1 += __shfl_xor_sync(0xffffffffu, l1, off);
+    }
+    float *park = reinterpret_cast<float *>(smem);
+    float *mine = park + warp * Park<T>::kWarp;
+    if (gid == 0) {
+        mine[2 * tig] = mref0;
+        mine[2 * tig + 1] = mref1;
+        mine[8 + 2 * tig] = l0;
+        mine[8 + 2 * tig + 1] = l1;
+    }
+    // the columns of query heads past the group (2 tig + e % 2 >= G) are not read
+    if (2u * tig < G) {
+#pragma unroll
+        for (int mt = 0; mt < T::MT; ++mt) {
+            if constexpr (T::kDimPairs) {
+                // the two rows of a column are adjacent dimensions: one 8-byte store
+#pragma unroll
+                for (int c = 0; c < 2; ++c)
+                    if (c == 0 || 2u * tig + 1 < G)
+                        *reinterpret_cast<float2 *>(
+                            mine + 16 + (2 * tig + c) * Park<T>::kRow + T::dim_of(mt, gid, 0)) =
+                            make_float2(o[mt][c], o[mt][c + 2]);
+            } else {
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    if ((e & 1) == 0 || 2u * tig + 1 < G)
+                        mine[16 + (2 * tig + (e & 1)) * Park<T>::kRow +
+                             T::dim_of(mt, gid, e >> 1)] = o[mt][e];
+            }
+        }
+    }
+    __syncthreads();
+    combine_and_write<T>(p, park, park + nwarps * Park<T>::kWarp, hkv, nwarps / hkv, G, seq, part,
+                         dir);
+}
+
 // The decode of one token range [t0, t1) of one query row (`seq`), by the whole
 // CTA: the table walk, the per-warp TMA rings, the tile loop, and the combine
 // of the warps' results into the range's partial (index `part`), or into the
@@ -1648,50 +1789,247 @@ __device__ __forceinline__ void range_body(const FastArgs &a, uint8_t *smem, uin
             }
         }
     }
-#pragma unroll
-    for (int off = 4; off < 32; off <<= 1) {
-        l0 += __shfl_xor_sync(0xffffffffu, l0, off);
-        l1 += __shfl_xor_sync(0xffffffffu, l1, off);
-    }
-
-    // park (m, l, O) of every warp in the now idle rings, head-major, then
-    // all warps of the CTA combine them
+    // every ring is drained: the rings are free
     if constexpr (kReportAbort)
         any_abort = __syncthreads_or(aborted);
     else
         __syncthreads();
-    float *park = reinterpret_cast<float *>(smem);
-    float *mine = park + warp * Park<T>::kWarp;
-    if (gid == 0) {
-        mine[2 * tig] = mref0;
-        mine[2 * tig + 1] = mref1;
-        mine[8 + 2 * tig] = l0;
-        mine[8 + 2 * tig + 1] = l1;
+    park_and_combine<T>(p, smem, o, mref0, mref1, l0, l1, nwarps, hkv, G, seq, part, dir);
+    n_my_out = n_my;
+}
+
+// range_body for one-token rows of a type with kTile32 (Q4_0) in 32-token
+// tiles, which halves the per-tile work that does not grow with the tokens:
+// the wait, the copy issue, the softmax vote and the loop, and each query
+// record load serves 32 tokens.  The warps of K/V head g share a ring of
+// S = n_slots32 slots, each the K rows then the V rows of 32 tokens (one
+// 16-row box per side and 16-token half); warp sub of the head takes tiles
+// sub, sub + wph, ... of [t0, t1); tile t sits in slot t % S with parity
+// (t / S) % 2, and the warp that has read tile t refills the slot with tile
+// t + S.  A slot's flag word holds which halves were copied (bits 0, 1: a
+// half with tokens whose block is in the pool) and, above them, the number
+// of copies issued into the slot (the drain after a timeout uses it).  The
+// arithmetic per 16-token half is that of range_body; the online softmax
+// moves its reference once per 32 tokens.
+template <class T, bool kReportAbort>
+__device__ __forceinline__ void range_body32(const FastArgs &a, uint8_t *smem, uint32_t seq,
+                                             uint32_t part, int32_t Lrow, uint32_t t0in,
+                                             bool dir, uint32_t t1in, bool &any_abort)
+{
+    const DecodeParams &p = a.p;
+    const uint32_t NSW = a.n_slots, S = a.n_slots32, nwarps = blockDim.x >> 5;
+    constexpr uint32_t HALF = T::kSideK;  // 16 rows of one side
+    constexpr uint32_t SLOT = 4 * HALF;   // K rows 0..31, then V rows 0..31
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const uint32_t hkv = p.hkv, G = p.hq / p.hkv, wph = nwarps / hkv;
+    const int gid = lane >> 2, tig = lane & 3;
+    const uint32_t g = warp % hkv, sub = warp / hkv;
+    uint8_t *ring = smem + (size_t)g * S * SLOT;
+    const uint32_t ring_u = smem_u32(ring);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + a.region_bytes);
+    uint64_t *full = bars + g * S;
+    int *ok_all = reinterpret_cast<int *>(bars + nwarps * NSW);
+    int *slot_ok = ok_all + g * S;
+    const uint32_t scr_base = (smem_u32(ok_all + nwarps * NSW) + 15u) & ~15u;
+    const uint32_t scr_u = scr_base + warp * T::SCRATCH2;
+    const uint32_t qsm_base = scr_base + nwarps * T::SCRATCH2;  // per K/V head: T::QBYTES
+    const int32_t L = Lrow > 0 ? Lrow : 0;
+    const uint32_t t0 = t0in, t1 = min((uint32_t)L, t1in);
+    const uint32_t n_tiles = t1 > t0 ? (t1 - t0 + 31) / 32 : 0u;
+    const uint32_t n_my = n_tiles > sub ? (n_tiles - sub + wph - 1) / wph : 0u;
+    const int32_t *bt = p.block_table + (uint64_t)table_row(p.q_tokens, seq) * p.table_stride;
+    const CUtensorMap *tmk = &a.tm[0][g], *tmv = &a.tm[1][g];
+    const uint32_t bshift = p.block_size == 32 ? 5 : 4, bmask = p.block_size - 1;
+
+    // the block ids of tile t's halves (0 past the range)
+    auto ids_of = [&](uint32_t t, int32_t &b0, int32_t &b1) {
+        const uint32_t tok = t0 + 32 * t;
+        b0 = t < n_tiles && tok < t1 ? bt[tok >> bshift] : 0;
+        b1 = t < n_tiles && tok + 16 < t1 ? bt[(tok + 16) >> bshift] : 0;
+    };
+    // lane 0: the copies of tile t (block ids b0, b1 of its halves) into slot s = t % S
+    auto issue = [&](uint32_t t, uint32_t s, int32_t b0, int32_t b1) {
+        const uint32_t tok = t0 + 32 * t;
+        uint8_t *dst = ring + (size_t)s * SLOT;
+        uint32_t bits = 0;
+        if (tok < t1) {
+            if (block_in_pool(b0, p.n_pool_blocks))
+                bits |= 1u;
+            else
+                atomicOr(p.status, PA_STATUS_CORRUPT_TABLE);
+        }
+        if (tok + 16 < t1) {
+            if (block_in_pool(b1, p.n_pool_blocks))
+                bits |= 2u;
+            else
+                atomicOr(p.status, PA_STATUS_CORRUPT_TABLE);
+        }
+        slot_ok[s] = (int)(((((uint32_t)slot_ok[s]) >> 2) + 1u) << 2 | bits);
+        fence_proxy_async();  // earlier generic reads of this slot come first
+        // K/V rows are read once: evict-first in the L2
+        const uint64_t pol = l2_evict_first_policy();
+        mbar_arrive_expect_tx(&full[s], (bits & 1u ? 2 * HALF : 0u) + (bits & 2u ? 2 * HALF : 0u));
+        if (bits & 1u) {
+            const int y = (b0 << bshift) + (int)(tok & bmask);
+            tma_load_2d_hint(dst, tmk, 0, y, &full[s], pol);
+            tma_load_2d_hint(dst + 2 * HALF, tmv, 0, y, &full[s], pol);
+        }
+        if (bits & 2u) {
+            const int y = (b1 << bshift) + (int)((tok + 16) & bmask);
+            tma_load_2d_hint(dst + HALF, tmk, 0, y, &full[s], pol);
+            tma_load_2d_hint(dst + 3 * HALF, tmv, 0, y, &full[s], pol);
+        }
+    };
+    // the block ids of my refills r0 .. r0+31, one refill per lane: refill r
+    // follows my tile r and brings tile sub + S + r * wph
+    auto fetch_refills = [&](uint32_t r0, int32_t &b0, int32_t &b1) {
+        const uint32_t r = r0 + (uint32_t)lane;
+        ids_of(r < n_my ? sub + S + r * wph : n_tiles, b0, b1);
+    };
+
+    int32_t rb0 = 0, rb1 = 0, nb0 = 0, nb1 = 0;
+    fetch_refills(0, rb0, rb1);
+    fetch_refills(32, nb0, nb1);
+    // quantised K: the wph warps of a head split its query blocks
+    typename T::QRaw qraw;
+    T::fetch_q(p, seq, g * G, G, gid, tig, sub, wph, qraw);
+    // my tiles among the ring's first S
+    for (uint32_t t = sub; t < S && t < n_tiles; t += wph) {
+        int32_t b0, b1;
+        ids_of(t, b0, b1);
+        if (lane == 0)
+            issue(t, t, b0, b1);
     }
-    // the columns of query heads past the group (2 tig + e % 2 >= G) are not read
-    if (2u * tig < G) {
+    __syncwarp();
+
+    typename T::Consts K;
+    K.init();
+    typename T::Frag f;
+    T::store_q(p, qraw, G, gid, tig, sub, wph, qsm_base + g * T::QBYTES);
+    __syncthreads();
+    T::load_q(qsm_base + g * T::QBYTES, lane, f);
+    float o[T::MT][4];
 #pragma unroll
-        for (int mt = 0; mt < T::MT; ++mt) {
-            if constexpr (T::kDimPairs) {
-                // the two rows of a column are adjacent dimensions: one 8-byte store
-#pragma unroll
-                for (int c = 0; c < 2; ++c)
-                    if (c == 0 || 2u * tig + 1 < G)
-                        *reinterpret_cast<float2 *>(
-                            mine + 16 + (2 * tig + c) * Park<T>::kRow + T::dim_of(mt, gid, 0)) =
-                            make_float2(o[mt][c], o[mt][c + 2]);
-            } else {
-#pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    if ((e & 1) == 0 || 2u * tig + 1 < G)
-                        mine[16 + (2 * tig + (e & 1)) * Park<T>::kRow +
-                             T::dim_of(mt, gid, e >> 1)] = o[mt][e];
+    for (int mt = 0; mt < T::MT; ++mt)
+        o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.0f;
+    float mref0 = -INFINITY, mref1 = -INFINITY, l0 = 0.0f, l1 = 0.0f;
+    bool aborted = false;
+
+    // my tile t = sub + i * wph in slot s with parity par (wph < S: one wrap at most per step)
+    uint32_t s = sub, par = 0;
+    for (uint32_t i = 0; i < n_my; ++i) {
+        const uint32_t t = sub + i * wph;
+        // every lane waits (bounded) and so acquires the slot's TMA writes itself
+        bool done = mbar_try_wait(&full[s], par);
+        if (!done) {
+            const uint64_t tw = global_ns();
+            while (!(done = mbar_try_wait(&full[s], par)) && global_ns() - tw < kWaitNs) {
             }
         }
+        if (!__all_sync(0xffffffffu, done)) {
+            if (lane == 0)
+                atomicOr(p.status, PA_STATUS_TIMEOUT);
+            aborted = true;
+            break;
+        }
+        const uint32_t okb = (uint32_t)slot_ok[s] & 3u;
+        const uint32_t nv = t1 - (t0 + 32 * t);  // >= 1 tokens from the tile's start
+        const int nva = okb & 1u ? (int)min(16u, nv) : 0;
+        const int nvb = okb & 2u && nv > 16 ? (int)min(16u, nv - 16) : 0;
+        const uint32_t kh = ring_u + s * SLOT, vh = kh + 2 * HALF;
+        T::extract(kh, vh, scr_u, nva, lane);
+        T::extract(kh + HALF, vh + HALF, scr_u + T::SCRATCH, nvb, lane);
+        __syncwarp();
+        float sx[4], sz[4];
+        T::scores2(K, f, kh, scr_u, gid, tig, sx, sz);
+        if (gid >= nva)
+            sx[0] = sx[1] = -INFINITY;
+        if (gid + 8 >= nva)
+            sx[2] = sx[3] = -INFINITY;
+        if (gid >= nvb)
+            sz[0] = sz[1] = -INFINITY;
+        if (gid + 8 >= nvb)
+            sz[2] = sz[3] = -INFINITY;
+        const float m0 = fmaxf(fmaxf(sx[0], sx[2]), fmaxf(sz[0], sz[2]));
+        const float m1 = fmaxf(fmaxf(sx[1], sx[3]), fmaxf(sz[1], sz[3]));
+        if (__builtin_expect(__any_sync(0xffffffffu, m0 > mref0 || m1 > mref1), 0)) {
+            float t0m = m0, t1m = m1;
+#pragma unroll
+            for (int off = 4; off < 32; off <<= 1) {
+                t0m = fmaxf(t0m, __shfl_xor_sync(0xffffffffu, t0m, off));
+                t1m = fmaxf(t1m, __shfl_xor_sync(0xffffffffu, t1m, off));
+            }
+            const float n0 = t0m > mref0 ? t0m + kHeadroom : mref0;
+            const float n1 = t1m > mref1 ? t1m + kHeadroom : mref1;
+            const float a0 = mref0 == -INFINITY ? 0.0f : exp2f(mref0 - n0);
+            const float a1 = mref1 == -INFINITY ? 0.0f : exp2f(mref1 - n1);
+#pragma unroll
+            for (int mt = 0; mt < T::MT; ++mt) {
+                o[mt][0] *= a0;
+                o[mt][1] *= a1;
+                o[mt][2] *= a0;
+                o[mt][3] *= a1;
+            }
+            l0 *= a0;
+            l1 *= a1;
+            mref0 = n0;
+            mref1 = n1;
+        }
+        const float ms0 = mref0 == -INFINITY ? 0.0f : mref0;
+        const float ms1 = mref1 == -INFINITY ? 0.0f : mref1;
+        const float x00 = ex2_ftz(sx[0] - ms0), x01 = ex2_ftz(sx[1] - ms1);
+        const float x10 = ex2_ftz(sx[2] - ms0), x11 = ex2_ftz(sx[3] - ms1);
+        const float z00 = ex2_ftz(sz[0] - ms0), z01 = ex2_ftz(sz[1] - ms1);
+        const float z10 = ex2_ftz(sz[2] - ms0), z11 = ex2_ftz(sz[3] - ms1);
+        l0 += (x00 + x10) + (z00 + z10);
+        l1 += (x01 + x11) + (z01 + z11);
+        // P[token][head] as 8x8 blocks (tokens 0-7, 8-15 of each half) -> PV B operands
+        T::pv(K, o, vh, scr_u, movmatrix_t(h2_bits(__floats2half2_rn(x00, x01))),
+              movmatrix_t(h2_bits(__floats2half2_rn(x10, x11))), gid, tig);
+        T::pv(K, o, vh + HALF, scr_u + T::SCRATCH,
+              movmatrix_t(h2_bits(__floats2half2_rn(z00, z01))),
+              movmatrix_t(h2_bits(__floats2half2_rn(z10, z11))), gid, tig);
+        __syncwarp();  // all reads of this slot are done
+        // refill the slot with tile t + S (my refill i)
+        if (t + S < n_tiles) {
+            if ((i & 31u) == 0 && i > 0) {
+                rb0 = nb0;
+                rb1 = nb1;
+                fetch_refills(i + 32, nb0, nb1);
+            }
+            const int32_t b0 = __shfl_sync(0xffffffffu, rb0, i & 31u);
+            const int32_t b1 = __shfl_sync(0xffffffffu, rb1, i & 31u);
+            if (lane == 0)
+                issue(t + S, s, b0, b1);
+        }
+        s += wph;
+        if (s >= S) {
+            s -= S;
+            par ^= 1u;
+        }
     }
-    __syncthreads();
-    combine_and_write<T>(p, park, park + nwarps * Park<T>::kWarp, hkv, wph, G, seq, part, dir);
-    n_my_out = n_my;
+    // the next grid on this stream may be scheduled once every CTA is here
+    // (no input is read after)
+    launch_dependents();
+    const bool cta_abort = __syncthreads_or(aborted);
+    if constexpr (kReportAbort)
+        any_abort = cta_abort;
+    if (cta_abort) {
+        // copies still in flight land (bounded) before the rings are reused:
+        // the last copy issued into each slot of each ring
+        if (sub == 0 && lane == 0) {
+            for (uint32_t k = 0; k < S; ++k) {
+                const uint32_t n = (uint32_t)slot_ok[k] >> 2;
+                if (n == 0)
+                    continue;
+                const uint64_t tw = global_ns();
+                while (!mbar_try_wait(&full[k], (n - 1) & 1u) && global_ns() - tw < kWaitNs) {
+                }
+            }
+        }
+        __syncthreads();
+    }
+    park_and_combine<T>(p, smem, o, mref0, mref1, l0, l1, nwarps, hkv, G, seq, part, dir);
 }
 
 // kStaged: the instance for plans of more than 32 partitions, whose merges
@@ -1708,9 +2046,16 @@ __global__ void __launch_bounds__(T::kMaxWarps * 32, 1)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + a.region_bytes) + warp * NSW;
 
+    // a kTile32 type takes 32-token tiles (range_body32) in both instances,
+    // so that a step gives the same bits through either
+    constexpr bool k32 = T::kTile32;
     if (lane == 0) {
-        for (uint32_t s = 0; s < NSW; ++s)
+        for (uint32_t s = 0; s < NSW; ++s) {
             mbar_init(&full[s], 1);
+            if constexpr (k32)  // the 32-token rings' flag words (copy counts)
+                reinterpret_cast<int *>(reinterpret_cast<uint64_t *>(smem + a.region_bytes) +
+                                        nwarps * NSW)[warp * NSW + s] = 0;
+        }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
@@ -1739,7 +2084,10 @@ __global__ void __launch_bounds__(T::kMaxWarps * 32, 1)
     const uint32_t t1 = dir ? (uint32_t)max(Lrow, 0) : t0 + p.part_tokens;
     uint32_t s = 0, phase = 0, n_my = 0;  // fresh rings
     bool any_abort = false;
-    range_body<T, kStaged>(a, smem, seq, part, Lrow, t0, dir, t1, s, phase, n_my, any_abort);
+    if constexpr (k32)
+        range_body32<T, kStaged>(a, smem, seq, part, Lrow, t0, dir, t1, any_abort);
+    else
+        range_body<T, kStaged>(a, smem, seq, part, Lrow, t0, dir, t1, s, phase, n_my, any_abort);
     if (p.counters && !dir) {
         if (a.coop) {
             merge_coop<T>(p, seq, part, Lrow, warp, nwarps, a.coop_wait_ns, smem_u32(smem),
@@ -1749,7 +2097,20 @@ __global__ void __launch_bounds__(T::kMaxWarps * 32, 1)
             // and waits on its slot-0 mbarrier, whose next parity follows the
             // loop's uses of slot 0 (all landed unless the loop aborted)
             const uint32_t share = (a.region_bytes / nwarps) & ~15u;
-            const uint32_t phase0 = ((n_my + NSW - 1) / NSW) & 1u;
+            uint32_t phase0 = ((n_my + NSW - 1) / NSW) & 1u;
+            if constexpr (k32) {
+                // the 32-token rings used these barriers head by head: the
+                // warp's slot-0 barrier starts afresh for the merge (no copy
+                // is pending on it: the rings were drained before the combine)
+                if (lane == 0 && !any_abort) {
+                    asm volatile("mbarrier.inval.shared::cta.b64 [%0];" ::"r"(smem_u32(full))
+                                 : "memory");
+                    mbar_init(full, 1);
+                    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+                }
+                __syncwarp();
+                phase0 = 0;
+            }
             merge_tail_staged<T::kMergeBatch>(p, seq, part, warp, nwarps,
                                               smem_u32(smem) + warp * share, share / (p.d * 2),
                                               any_abort ? nullptr : full, phase0);
@@ -2083,6 +2444,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
 // Launch geometry of one kernel instance: warps per head and ring slots.
 struct Geometry {
     uint32_t wph = 0, warps = 0, n_slots = 0, slot_bytes = 0, region = 0;
+    uint32_t slots32 = 0;  // 32-token slots per K/V head (kTile32 types)
     size_t smem = 0;
 };
 
@@ -2110,6 +2472,24 @@ Geometry geometry(uint32_t hkv)
             gm.region = (uint32_t)(ring > park ? ring : park);
             gm.smem = 1024 + gm.region + warps * ns * (8 + 4) + 16 + warps * (size_t)T::SCRATCH +
                       hkv * (size_t)T::QBYTES;
+            if constexpr (T::kTile32) {
+                // the 32-token rings of range_body32: S slots of 4 * kSideK per
+                // head, at least one per warp of the head and one more, their
+                // barriers and flag words within the warps * ns of the layout,
+                // and twice the scratch per warp
+                const size_t slot32 = 4 * (size_t)T::kSideK;
+                const size_t fixed32 = 1024 + warps * ns * (8 + 4) + 16 +
+                                       warps * (size_t)T::SCRATCH2 + hkv * (size_t)T::QBYTES;
+                size_t s32 = fixed32 < kSmemBudget ? (kSmemBudget - fixed32) / (hkv * slot32) : 0;
+                if (s32 > warps * ns / hkv)
+                    s32 = warps * ns / hkv;
+                if (s32 < wph + 1)
+                    return Geometry{};
+                gm.slots32 = (uint32_t)s32;
+                if (hkv * s32 * slot32 > gm.region)
+                    gm.region = (uint32_t)(hkv * s32 * slot32);
+                gm.smem = fixed32 + gm.region;
+            }
             return gm;
         }
         if (wph == 1)
@@ -2284,6 +2664,7 @@ int launch_t(const DecodeParams &p, cudaStream_t st, const char *entry)
     a.n_slots = gm.n_slots;
     a.slot_bytes = gm.slot_bytes;
     a.region_bytes = gm.region;
+    a.n_slots32 = gm.slots32;
     rc = cuda_check(allow_smem<T>(), entry, "cudaFuncSetAttribute");
     if (rc)
         return rc;
