@@ -295,6 +295,22 @@ __device__ __forceinline__ uint32_t ld_acquire_u32(const int32_t *p)
     return v;
 }
 
+// A shared-memory word published by one warp to the others of the CTA.
+__device__ __forceinline__ uint32_t ld_acquire_shared(const int *p)
+{
+    uint32_t v;
+    asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];"
+                 : "=r"(v)
+                 : "r"(smem_u32(p))
+                 : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_release_shared(int *p, uint32_t v)
+{
+    asm volatile("st.release.cta.shared::cta.u32 [%0], %1;" ::"r"(smem_u32(p)), "r"(v) : "memory");
+}
+
 // Programmatic dependent launch: the wait for the grids this one depends on
 // (their writes visible), and the signal that the grids depending on this
 // one may be scheduled.
@@ -1807,10 +1823,15 @@ __device__ __forceinline__ void range_body(const FastArgs &a, uint8_t *smem, uin
 // sub, sub + wph, ... of [t0, t1); tile t sits in slot t % S with parity
 // (t / S) % 2, and the warp that has read tile t refills the slot with tile
 // t + S.  A slot's flag word holds which halves were copied (bits 0, 1: a
-// half with tokens whose block is in the pool) and, above them, the number
-// of copies issued into the slot (the drain after a timeout uses it).  The
-// arithmetic per 16-token half is that of range_body; the online softmax
-// moves its reference once per 32 tokens.
+// half with tokens whose block is in the pool) and, above them, t + 1 for
+// the tile last issued into the slot, published (release) before the copy's
+// mbarrier arrival.  The warp that takes tile t waits until the word names
+// t and only then on the barrier's parity: a slot's consumers change from
+// warp to warp, so a warp may reach the slot while an earlier tile of it is
+// still in flight, and a parity alone would then match the earlier phase.
+// The issuer of tile t has read tile t - S, so once the word names t the
+// barrier is in tile t's phase.  The arithmetic per 16-token half is that of
+// range_body; the online softmax moves its reference once per 32 tokens.
 template <class T, bool kReportAbort>
 __device__ __forceinline__ void range_body32(const FastArgs &a, uint8_t *smem, uint32_t seq,
                                              uint32_t part, int32_t Lrow, uint32_t t0in,
@@ -1848,9 +1869,9 @@ __device__ __forceinline__ void range_body32(const FastArgs &a, uint8_t *smem, u
         b1 = t < n_tiles && tok + 16 < t1 ? bt[(tok + 16) >> bshift] : 0;
     };
     // lane 0: the copies of tile t (block ids b0, b1 of its halves) into slot s = t % S
-    auto issue = [&](uint32_t t, uint32_t s, int32_t b0, int32_t b1) {
+    // at shared address dst
+    auto issue = [&](uint32_t t, uint32_t s, uint8_t *dst, int32_t b0, int32_t b1) {
         const uint32_t tok = t0 + 32 * t;
-        uint8_t *dst = ring + (size_t)s * SLOT;
         uint32_t bits = 0;
         if (tok < t1) {
             if (block_in_pool(b0, p.n_pool_blocks))
@@ -1864,7 +1885,7 @@ __device__ __forceinline__ void range_body32(const FastArgs &a, uint8_t *smem, u
             else
                 atomicOr(p.status, PA_STATUS_CORRUPT_TABLE);
         }
-        slot_ok[s] = (int)(((((uint32_t)slot_ok[s]) >> 2) + 1u) << 2 | bits);
+        st_release_shared(&slot_ok[s], (t + 1u) << 2 | bits);
         fence_proxy_async();  // earlier generic reads of this slot come first
         // K/V rows are read once: evict-first in the L2
         const uint64_t pol = l2_evict_first_policy();
@@ -1898,7 +1919,7 @@ __device__ __forceinline__ void range_body32(const FastArgs &a, uint8_t *smem, u
         int32_t b0, b1;
         ids_of(t, b0, b1);
         if (lane == 0)
-            issue(t, t, b0, b1);
+            issue(t, t, ring + (size_t)t * SLOT, b0, b1);
     }
     __syncwarp();
 
@@ -1915,15 +1936,19 @@ __device__ __forceinline__ void range_body32(const FastArgs &a, uint8_t *smem, u
     float mref0 = -INFINITY, mref1 = -INFINITY, l0 = 0.0f, l1 = 0.0f;
     bool aborted = false;
 
-    // my tile t = sub + i * wph in slot s with parity par (wph < S: one wrap at most per step)
-    uint32_t s = sub, par = 0;
-    for (uint32_t i = 0; i < n_my; ++i) {
-        const uint32_t t = sub + i * wph;
-        // every lane waits (bounded) and so acquires the slot's TMA writes itself
-        bool done = mbar_try_wait(&full[s], par);
+    // my tile t = sub + i * wph in slot s (shared address kh) with parity par
+    // (wph < S: one wrap at most per step), its first token t0 + 32 t
+    uint32_t s = sub, par = 0, t = sub, kh = ring_u + sub * SLOT, tok = t0 + 32 * sub;
+    for (uint32_t i = 0; i < n_my; ++i, t += wph, tok += 32 * wph) {
+        // every lane waits (bounded) for the slot's word to name tile t, then
+        // on the barrier, and so acquires the slot's TMA writes itself
+        uint32_t word = ld_acquire_shared(&slot_ok[s]);
+        bool done = (word >> 2) == t + 1u && mbar_try_wait(&full[s], par);
         if (!done) {
             const uint64_t tw = global_ns();
-            while (!(done = mbar_try_wait(&full[s], par)) && global_ns() - tw < kWaitNs) {
+            while (!done && global_ns() - tw < kWaitNs) {
+                word = ld_acquire_shared(&slot_ok[s]);
+                done = (word >> 2) == t + 1u && mbar_try_wait(&full[s], par);
             }
         }
         if (!__all_sync(0xffffffffu, done)) {
@@ -1932,11 +1957,11 @@ __device__ __forceinline__ void range_body32(const FastArgs &a, uint8_t *smem, u
             aborted = true;
             break;
         }
-        const uint32_t okb = (uint32_t)slot_ok[s] & 3u;
-        const uint32_t nv = t1 - (t0 + 32 * t);  // >= 1 tokens from the tile's start
+        const uint32_t okb = word & 3u;
+        const uint32_t nv = t1 - tok;  // >= 1 tokens from the tile's start
         const int nva = okb & 1u ? (int)min(16u, nv) : 0;
         const int nvb = okb & 2u && nv > 16 ? (int)min(16u, nv - 16) : 0;
-        const uint32_t kh = ring_u + s * SLOT, vh = kh + 2 * HALF;
+        const uint32_t vh = kh + 2 * HALF;
         T::extract(kh, vh, scr_u, nva, lane);
         T::extract(kh + HALF, vh + HALF, scr_u + T::SCRATCH, nvb, lane);
         __syncwarp();
@@ -2000,11 +2025,13 @@ __device__ __forceinline__ void range_body32(const FastArgs &a, uint8_t *smem, u
             const int32_t b0 = __shfl_sync(0xffffffffu, rb0, i & 31u);
             const int32_t b1 = __shfl_sync(0xffffffffu, rb1, i & 31u);
             if (lane == 0)
-                issue(t + S, s, b0, b1);
+                issue(t + S, s, ring + (kh - ring_u), b0, b1);
         }
         s += wph;
+        kh += wph * SLOT;
         if (s >= S) {
             s -= S;
+            kh -= S * SLOT;
             par ^= 1u;
         }
     }
@@ -2016,14 +2043,16 @@ __device__ __forceinline__ void range_body32(const FastArgs &a, uint8_t *smem, u
         any_abort = cta_abort;
     if (cta_abort) {
         // copies still in flight land (bounded) before the rings are reused:
-        // the last copy issued into each slot of each ring
+        // the tile last issued into each slot of each ring (t = word / 4 - 1,
+        // parity (t / S) % 2)
         if (sub == 0 && lane == 0) {
             for (uint32_t k = 0; k < S; ++k) {
-                const uint32_t n = (uint32_t)slot_ok[k] >> 2;
+                const uint32_t n = ld_acquire_shared(&slot_ok[k]) >> 2;
                 if (n == 0)
                     continue;
                 const uint64_t tw = global_ns();
-                while (!mbar_try_wait(&full[k], (n - 1) & 1u) && global_ns() - tw < kWaitNs) {
+                while (!mbar_try_wait(&full[k], ((n - 1) / S) & 1u) &&
+                       global_ns() - tw < kWaitNs) {
                 }
             }
         }
@@ -2052,7 +2081,7 @@ __global__ void __launch_bounds__(T::kMaxWarps * 32, 1)
     if (lane == 0) {
         for (uint32_t s = 0; s < NSW; ++s) {
             mbar_init(&full[s], 1);
-            if constexpr (k32)  // the 32-token rings' flag words (copy counts)
+            if constexpr (k32)  // the 32-token rings' flag words (no tile issued)
                 reinterpret_cast<int *>(reinterpret_cast<uint64_t *>(smem + a.region_bytes) +
                                         nwarps * NSW)[warp * NSW + s] = 0;
         }
