@@ -63,6 +63,7 @@ struct FastArgs {
     uint32_t coop;               // in-launch merge shared by the CTAs of a sequence
     uint32_t coop_wait_ns;       // bound of a CTA's wait for the others of its sequence
     uint32_t n_slots32;          // 32-token slots per K/V head (types with kTile32)
+    uint32_t bar_slots;          // mbarriers and flag words per warp (>= n_slots)
 };
 
 // Bound of the wait of the cooperative merge: far above the spread of the
@@ -293,22 +294,6 @@ __device__ __forceinline__ uint32_t ld_acquire_u32(const int32_t *p)
     uint32_t v;
     asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
     return v;
-}
-
-// A shared-memory word published by one warp to the others of the CTA.
-__device__ __forceinline__ uint32_t ld_acquire_shared(const int *p)
-{
-    uint32_t v;
-    asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];"
-                 : "=r"(v)
-                 : "r"(smem_u32(p))
-                 : "memory");
-    return v;
-}
-
-__device__ __forceinline__ void st_release_shared(int *p, uint32_t v)
-{
-    asm volatile("st.release.cta.shared::cta.u32 [%0], %1;" ::"r"(smem_u32(p)), "r"(v) : "memory");
 }
 
 // Programmatic dependent launch: the wait for the grids this one depends on
@@ -1605,10 +1590,13 @@ __device__ __forceinline__ void range_body(const FastArgs &a, uint8_t *smem, uin
     const uint32_t hkv = p.hkv, G = p.hq / p.hkv, wph = nwarps / hkv;
     uint8_t *ring = smem + (size_t)warp * NSW * SLOT;
     const uint32_t ring_u = smem_u32(ring);
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + a.region_bytes) + warp * NSW;
-    int *slot_ok = reinterpret_cast<int *>(reinterpret_cast<uint64_t *>(smem + a.region_bytes) +
-                                           nwarps * NSW) + warp * NSW;
-    const uint32_t scr_base = (smem_u32(slot_ok + (nwarps - warp) * NSW) + 15u) & ~15u;
+    // after the rings: mbarriers [nwarps][bar_slots], flag words likewise,
+    // then the scratch; this body uses the first nwarps * NSW of each
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + a.region_bytes);
+    uint64_t *full = bars + warp * NSW;
+    int *ok_all = reinterpret_cast<int *>(bars + nwarps * a.bar_slots);
+    int *slot_ok = ok_all + warp * NSW;
+    const uint32_t scr_base = (smem_u32(ok_all + nwarps * a.bar_slots) + 15u) & ~15u;
     const uint32_t scr_u = scr_base + warp * T::SCRATCH;
     const uint32_t qsm_base = scr_base + nwarps * T::SCRATCH;  // per K/V head: T::QBYTES
     const uint32_t s0 = s, u0 = phase * NSW + s;  // this warp's ring use at the range start
@@ -1822,15 +1810,18 @@ __device__ __forceinline__ void range_body(const FastArgs &a, uint8_t *smem, uin
 // 16-row box per side and 16-token half); warp sub of the head takes tiles
 // sub, sub + wph, ... of [t0, t1); tile t sits in slot t % S with parity
 // (t / S) % 2, and the warp that has read tile t refills the slot with tile
-// t + S.  A slot's flag word holds which halves were copied (bits 0, 1: a
-// half with tokens whose block is in the pool) and, above them, t + 1 for
-// the tile last issued into the slot, published (release) before the copy's
-// mbarrier arrival.  The warp that takes tile t waits until the word names
-// t and only then on the barrier's parity: a slot's consumers change from
-// warp to warp, so a warp may reach the slot while an earlier tile of it is
-// still in flight, and a parity alone would then match the earlier phase.
-// The issuer of tile t has read tile t - S, so once the word names t the
-// barrier is in tile t's phase.  The arithmetic per 16-token half is that of
+// t + S.  Each slot has wph mbarriers used in turn: tile t completes barrier
+// (t % S, (t / S) % wph), the (t / (S wph))-th time, so a barrier's tiles
+// are t, t + wph S, ..., all of one warp.  Its waits therefore always come
+// after its previous phase completed (a tile the same warp read), and the
+// issuer of tile t, who read tile t - S, arrives on it after that phase too
+// (t - wph S came through the ring before t - S did), so a parity names
+// one phase.  (With one barrier per slot, the warp waiting for tile t could
+// meet the barrier still in the phase of tile t - S, another warp's, and a
+// parity would match that.)  A slot's flag word holds which halves were
+// copied (bits 0, 1: a half with tokens whose block is in the pool) and,
+// above them, t + 1 for the tile last issued into the slot (the drain after
+// a timeout uses it).  The arithmetic per 16-token half is that of
 // range_body; the online softmax moves its reference once per 32 tokens.
 template <class T, bool kReportAbort>
 __device__ __forceinline__ void range_body32(const FastArgs &a, uint8_t *smem, uint32_t seq,
@@ -1838,7 +1829,7 @@ __device__ __forceinline__ void range_body32(const FastArgs &a, uint8_t *smem, u
                                              bool dir, uint32_t t1in, bool &any_abort)
 {
     const DecodeParams &p = a.p;
-    const uint32_t NSW = a.n_slots, S = a.n_slots32, nwarps = blockDim.x >> 5;
+    const uint32_t BS = a.bar_slots, S = a.n_slots32, nwarps = blockDim.x >> 5;
     constexpr uint32_t HALF = T::kSideK;  // 16 rows of one side
     constexpr uint32_t SLOT = 4 * HALF;   // K rows 0..31, then V rows 0..31
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -1848,10 +1839,10 @@ __device__ __forceinline__ void range_body32(const FastArgs &a, uint8_t *smem, u
     uint8_t *ring = smem + (size_t)g * S * SLOT;
     const uint32_t ring_u = smem_u32(ring);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + a.region_bytes);
-    uint64_t *full = bars + g * S;
-    int *ok_all = reinterpret_cast<int *>(bars + nwarps * NSW);
+    uint64_t *hbar = bars + g * wph * S;  // head g's barriers: slot s, turn e at s + S e
+    int *ok_all = reinterpret_cast<int *>(bars + nwarps * BS);
     int *slot_ok = ok_all + g * S;
-    const uint32_t scr_base = (smem_u32(ok_all + nwarps * NSW) + 15u) & ~15u;
+    const uint32_t scr_base = (smem_u32(ok_all + nwarps * BS) + 15u) & ~15u;
     const uint32_t scr_u = scr_base + warp * T::SCRATCH2;
     const uint32_t qsm_base = scr_base + nwarps * T::SCRATCH2;  // per K/V head: T::QBYTES
     const int32_t L = Lrow > 0 ? Lrow : 0;
@@ -1868,9 +1859,9 @@ __device__ __forceinline__ void range_body32(const FastArgs &a, uint8_t *smem, u
         b0 = t < n_tiles && tok < t1 ? bt[tok >> bshift] : 0;
         b1 = t < n_tiles && tok + 16 < t1 ? bt[(tok + 16) >> bshift] : 0;
     };
-    // lane 0: the copies of tile t (block ids b0, b1 of its halves) into slot s = t % S
-    // at shared address dst
-    auto issue = [&](uint32_t t, uint32_t s, uint8_t *dst, int32_t b0, int32_t b1) {
+    // lane 0: the copies of tile t (block ids b0, b1 of its halves) into slot
+    // s = t % S at shared address dst, completing barrier fb
+    auto issue = [&](uint32_t t, uint32_t s, uint8_t *dst, uint64_t *fb, int32_t b0, int32_t b1) {
         const uint32_t tok = t0 + 32 * t;
         uint32_t bits = 0;
         if (tok < t1) {
@@ -1885,20 +1876,20 @@ __device__ __forceinline__ void range_body32(const FastArgs &a, uint8_t *smem, u
             else
                 atomicOr(p.status, PA_STATUS_CORRUPT_TABLE);
         }
-        st_release_shared(&slot_ok[s], (t + 1u) << 2 | bits);
+        slot_ok[s] = (int)((t + 1u) << 2 | bits);
         fence_proxy_async();  // earlier generic reads of this slot come first
         // K/V rows are read once: evict-first in the L2
         const uint64_t pol = l2_evict_first_policy();
-        mbar_arrive_expect_tx(&full[s], (bits & 1u ? 2 * HALF : 0u) + (bits & 2u ? 2 * HALF : 0u));
+        mbar_arrive_expect_tx(fb, (bits & 1u ? 2 * HALF : 0u) + (bits & 2u ? 2 * HALF : 0u));
         if (bits & 1u) {
             const int y = (b0 << bshift) + (int)(tok & bmask);
-            tma_load_2d_hint(dst, tmk, 0, y, &full[s], pol);
-            tma_load_2d_hint(dst + 2 * HALF, tmv, 0, y, &full[s], pol);
+            tma_load_2d_hint(dst, tmk, 0, y, fb, pol);
+            tma_load_2d_hint(dst + 2 * HALF, tmv, 0, y, fb, pol);
         }
         if (bits & 2u) {
             const int y = (b1 << bshift) + (int)((tok + 16) & bmask);
-            tma_load_2d_hint(dst + HALF, tmk, 0, y, &full[s], pol);
-            tma_load_2d_hint(dst + 3 * HALF, tmv, 0, y, &full[s], pol);
+            tma_load_2d_hint(dst + HALF, tmk, 0, y, fb, pol);
+            tma_load_2d_hint(dst + 3 * HALF, tmv, 0, y, fb, pol);
         }
     };
     // the block ids of my refills r0 .. r0+31, one refill per lane: refill r
@@ -1919,7 +1910,7 @@ __device__ __forceinline__ void range_body32(const FastArgs &a, uint8_t *smem, u
         int32_t b0, b1;
         ids_of(t, b0, b1);
         if (lane == 0)
-            issue(t, t, ring + (size_t)t * SLOT, b0, b1);
+            issue(t, t, ring + (size_t)t * SLOT, hbar + t, b0, b1);
     }
     __syncwarp();
 
@@ -1936,19 +1927,16 @@ __device__ __forceinline__ void range_body32(const FastArgs &a, uint8_t *smem, u
     float mref0 = -INFINITY, mref1 = -INFINITY, l0 = 0.0f, l1 = 0.0f;
     bool aborted = false;
 
-    // my tile t = sub + i * wph in slot s (shared address kh) with parity par
-    // (wph < S: one wrap at most per step), its first token t0 + 32 t
-    uint32_t s = sub, par = 0, t = sub, kh = ring_u + sub * SLOT, tok = t0 + 32 * sub;
+    // my tile t = sub + i * wph: slot s (shared address kh), barrier turn e,
+    // parity par (wph < S: one wrap at most per step), first token t0 + 32 t
+    uint32_t s = sub, e = 0, par = 0, t = sub, kh = ring_u + sub * SLOT, tok = t0 + 32 * sub;
     for (uint32_t i = 0; i < n_my; ++i, t += wph, tok += 32 * wph) {
-        // every lane waits (bounded) for the slot's word to name tile t, then
-        // on the barrier, and so acquires the slot's TMA writes itself
-        uint32_t word = ld_acquire_shared(&slot_ok[s]);
-        bool done = (word >> 2) == t + 1u && mbar_try_wait(&full[s], par);
+        uint64_t *fb = hbar + s + S * e;
+        // every lane waits (bounded) and so acquires the slot's TMA writes itself
+        bool done = mbar_try_wait(fb, par);
         if (!done) {
             const uint64_t tw = global_ns();
-            while (!done && global_ns() - tw < kWaitNs) {
-                word = ld_acquire_shared(&slot_ok[s]);
-                done = (word >> 2) == t + 1u && mbar_try_wait(&full[s], par);
+            while (!(done = mbar_try_wait(fb, par)) && global_ns() - tw < kWaitNs) {
             }
         }
         if (!__all_sync(0xffffffffu, done)) {
@@ -1957,7 +1945,7 @@ __device__ __forceinline__ void range_body32(const FastArgs &a, uint8_t *smem, u
             aborted = true;
             break;
         }
-        const uint32_t okb = word & 3u;
+        const uint32_t okb = (uint32_t)slot_ok[s] & 3u;
         const uint32_t nv = t1 - tok;  // >= 1 tokens from the tile's start
         const int nva = okb & 1u ? (int)min(16u, nv) : 0;
         const int nvb = okb & 2u && nv > 16 ? (int)min(16u, nv - 16) : 0;
@@ -2024,15 +2012,20 @@ __device__ __forceinline__ void range_body32(const FastArgs &a, uint8_t *smem, u
             }
             const int32_t b0 = __shfl_sync(0xffffffffu, rb0, i & 31u);
             const int32_t b1 = __shfl_sync(0xffffffffu, rb1, i & 31u);
+            // tile t + S: the same slot, the next barrier turn
+            uint64_t *nb = hbar + s + S * (e + 1 == wph ? 0u : e + 1);
             if (lane == 0)
-                issue(t + S, s, ring + (kh - ring_u), b0, b1);
+                issue(t + S, s, ring + (kh - ring_u), nb, b0, b1);
         }
         s += wph;
         kh += wph * SLOT;
         if (s >= S) {
             s -= S;
             kh -= S * SLOT;
-            par ^= 1u;
+            if (++e == wph) {
+                e = 0;
+                par ^= 1u;
+            }
         }
     }
     // the next grid on this stream may be scheduled once every CTA is here
@@ -2043,16 +2036,16 @@ __device__ __forceinline__ void range_body32(const FastArgs &a, uint8_t *smem, u
         any_abort = cta_abort;
     if (cta_abort) {
         // copies still in flight land (bounded) before the rings are reused:
-        // the tile last issued into each slot of each ring (t = word / 4 - 1,
-        // parity (t / S) % 2)
+        // the tile last issued into each slot of each ring (tl = word / 4 - 1)
         if (sub == 0 && lane == 0) {
             for (uint32_t k = 0; k < S; ++k) {
-                const uint32_t n = ld_acquire_shared(&slot_ok[k]) >> 2;
+                const uint32_t n = (uint32_t)slot_ok[k] >> 2;
                 if (n == 0)
                     continue;
+                const uint32_t tl = n - 1;
+                uint64_t *lb = hbar + k + S * ((tl / S) % wph);
                 const uint64_t tw = global_ns();
-                while (!mbar_try_wait(&full[k], ((n - 1) / S) & 1u) &&
-                       global_ns() - tw < kWaitNs) {
+                while (!mbar_try_wait(lb, (tl / (S * wph)) & 1u) && global_ns() - tw < kWaitNs) {
                 }
             }
         }
@@ -2079,11 +2072,12 @@ __global__ void __launch_bounds__(T::kMaxWarps * 32, 1)
     // so that a step gives the same bits through either
     constexpr bool k32 = T::kTile32;
     if (lane == 0) {
-        for (uint32_t s = 0; s < NSW; ++s) {
-            mbar_init(&full[s], 1);
-            if constexpr (k32)  // the 32-token rings' flag words (no tile issued)
-                reinterpret_cast<int *>(reinterpret_cast<uint64_t *>(smem + a.region_bytes) +
-                                        nwarps * NSW)[warp * NSW + s] = 0;
+        // every mbarrier and flag word after the rings (bar_slots per warp)
+        uint64_t *bars = reinterpret_cast<uint64_t *>(smem + a.region_bytes);
+        int *flags = reinterpret_cast<int *>(bars + nwarps * a.bar_slots);
+        for (uint32_t s = 0; s < a.bar_slots; ++s) {
+            mbar_init(&bars[warp * a.bar_slots + s], 1);
+            flags[warp * a.bar_slots + s] = 0;  // no tile issued
         }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -2239,7 +2233,7 @@ __global__ void __launch_bounds__(T::kMaxWarps * 32, 1)
 
     if (lane == 0) {
         for (uint32_t s = 0; s < NSW; ++s)
-            mbar_init(&full[s], 1);
+            mbar_init(&full[s], 1);  // range_body's: the first NSW of the warp's
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
@@ -2473,7 +2467,8 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
 // Launch geometry of one kernel instance: warps per head and ring slots.
 struct Geometry {
     uint32_t wph = 0, warps = 0, n_slots = 0, slot_bytes = 0, region = 0;
-    uint32_t slots32 = 0;  // 32-token slots per K/V head (kTile32 types)
+    uint32_t slots32 = 0;    // 32-token slots per K/V head (kTile32 types)
+    uint32_t bar_slots = 0;  // mbarriers and flag words per warp
     size_t smem = 0;
 };
 
@@ -2499,25 +2494,33 @@ Geometry geometry(uint32_t hkv)
             gm.slot_bytes = (uint32_t)slot;
             size_t ring = warps * ns * slot, park = warps * park_per_warp + fac_bytes;
             gm.region = (uint32_t)(ring > park ? ring : park);
+            gm.bar_slots = (uint32_t)ns;
             gm.smem = 1024 + gm.region + warps * ns * (8 + 4) + 16 + warps * (size_t)T::SCRATCH +
                       hkv * (size_t)T::QBYTES;
             if constexpr (T::kTile32) {
                 // the 32-token rings of range_body32: S slots of 4 * kSideK per
-                // head, at least one per warp of the head and one more, their
-                // barriers and flag words within the warps * ns of the layout,
-                // and twice the scratch per warp
+                // head, at least one per warp of the head and one more; wph
+                // barriers per slot (S per warp), flag words likewise; twice
+                // the scratch per warp
                 const size_t slot32 = 4 * (size_t)T::kSideK;
-                const size_t fixed32 = 1024 + warps * ns * (8 + 4) + 16 +
-                                       warps * (size_t)T::SCRATCH2 + hkv * (size_t)T::QBYTES;
-                size_t s32 = fixed32 < kSmemBudget ? (kSmemBudget - fixed32) / (hkv * slot32) : 0;
-                if (s32 > warps * ns / hkv)
-                    s32 = warps * ns / hkv;
+                size_t s32 = 32;
+                for (; s32 > wph; --s32) {
+                    const size_t bs = s32 > ns ? s32 : ns;
+                    const size_t need = 1024 + warps * bs * (8 + 4) + 16 +
+                                        warps * (size_t)T::SCRATCH2 + hkv * (size_t)T::QBYTES +
+                                        (hkv * s32 * slot32 > gm.region ? hkv * s32 * slot32
+                                                                        : gm.region);
+                    if (need <= kSmemBudget)
+                        break;
+                }
                 if (s32 < wph + 1)
                     return Geometry{};
                 gm.slots32 = (uint32_t)s32;
+                gm.bar_slots = (uint32_t)(s32 > ns ? s32 : ns);
                 if (hkv * s32 * slot32 > gm.region)
                     gm.region = (uint32_t)(hkv * s32 * slot32);
-                gm.smem = fixed32 + gm.region;
+                gm.smem = 1024 + warps * (size_t)gm.bar_slots * (8 + 4) + 16 +
+                          warps * (size_t)T::SCRATCH2 + hkv * (size_t)T::QBYTES + gm.region;
             }
             return gm;
         }
@@ -2694,6 +2697,7 @@ int launch_t(const DecodeParams &p, cudaStream_t st, const char *entry)
     a.slot_bytes = gm.slot_bytes;
     a.region_bytes = gm.region;
     a.n_slots32 = gm.slots32;
+    a.bar_slots = gm.bar_slots;
     rc = cuda_check(allow_smem<T>(), entry, "cudaFuncSetAttribute");
     if (rc)
         return rc;
