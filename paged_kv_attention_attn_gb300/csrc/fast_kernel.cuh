@@ -415,9 +415,22 @@ struct Q81Query {
             amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
             amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
             const float d = amax / 127.0f, inv_d = 1.0f / d;
+            // q8_1_code without its division: the product by 1 / d rounds
+            // to the quotient's code unless it lies within 3e-5 of a
+            // half-integer (or is not finite) in some lane; then the warp
+            // takes q8_1_code itself for the block
+            bool near = false;
 #pragma unroll
-            for (int j = 0; j < 8; ++j)
-                code[j] = q8_1_code(v[j], amax, d, inv_d);
+            for (int j = 0; j < 8; ++j) {
+                const float rj = v[j] * inv_d, a = fabsf(rj);
+                near |= !(fabsf(a - truncf(a) - 0.5f) > 3.0e-5f);
+                code[j] = (int)fminf(fmaxf(roundf(rj), -127.0f), 127.0f);
+            }
+            if (__any_sync(0xffffffffu, near)) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    code[j] = q8_1_code(v[j], amax, d, inv_d);
+            }
             d16 = __half2float(__float2half_rn(amax == 0.0f ? 0.0f : d));
         } else {
 #pragma unroll
@@ -516,6 +529,132 @@ struct Q40T {
             if (tig == 0)
                 sts_f32(qsm + QCORR + 4 * (gid * NB + b), -corr);
         }
+    }
+
+    // The query records of every K/V head of query row s (what store_q
+    // writes, bit for bit), by all threads of the CTA at once: thread item
+    // i = (head h, block b, half c) holds the 16 values of lanes tig = 2c,
+    // 2c+1 of the block's quad -- dims 8c..8c+7 and 16+8c..16+8c+7.  One
+    // item per thread instead of NB / wph blocks per warp in turn; the
+    // codes, scales and bias sums are formed in the same order as there.
+    struct QItems {
+        float4 x[4];      // f32 query: dims 8c..8c+3, 8c+4.., 16+8c.., 20+8c..
+        uint32_t w[4];    // q8_1 query: the codes of the same dims
+        uint32_t d;       // q8_1 query: the block's f16 scale
+    };
+    __device__ static void fetch_q_cta(const DecodeParams &p, uint32_t s, uint32_t i, QItems &r)
+    {
+        if (i >= p.hq * 16)
+            return;
+        const uint32_t h = i >> 4, b = (i >> 1) & 7, c = i & 1;
+        const uint64_t row = (uint64_t)s * p.hq + h;
+        if (p.q_f32) {
+            const float *x = static_cast<const float *>(p.q) + row * D + 32 * b + 8 * c;
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                r.x[k] = *reinterpret_cast<const float4 *>(x + 16 * (k >> 1) + 4 * (k & 1));
+        } else {
+            const uint8_t *blk = static_cast<const uint8_t *>(p.q) + row * NB * 36 + 36 * b;
+            r.d = load_u16(blk);
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                r.w[k] = *reinterpret_cast<const uint32_t *>(blk + 4 + 8 * c + 16 * (k >> 1) +
+                                                             4 * (k & 1));
+        }
+    }
+    // Every thread of the CTA, after fetch_q_cta of item threadIdx.x: the
+    // records of the live heads (items past the CTA's threads in further
+    // rounds), zero records and bias terms for the columns past each group.
+    __device__ static void store_q_cta(const DecodeParams &p, uint32_t s, QItems &r,
+                                       uint32_t qsm_base)
+    {
+        const uint32_t hq = p.hq, G = hq / p.hkv, n = hq * 16, nt = blockDim.x;
+        for (uint32_t k = threadIdx.x; k < p.hkv * (8 - G) * NB * 4; k += nt) {
+            const uint32_t tig = k & 3, b = (k >> 2) % NB, rr = (k >> 2) / NB;
+            const uint32_t g = rr / (8 - G), gid = G + rr % (8 - G);
+            const uint32_t base = qsm_base + g * QBYTES;
+            asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(
+                             base + (b * 32 + gid * 4 + tig) * QREC),
+                         "r"(0u));
+            if (tig == 0)
+                sts_f32(base + QCORR + 4 * (gid * NB + b), 0.0f);
+        }
+        // a warp's items: all of it or none live but at the end (n is a
+        // multiple of 16, nt of 32)
+        for (uint32_t i = threadIdx.x; i - (i & 31) < n; i += nt) {
+            if (i >= nt)
+                fetch_q_cta(p, s, i, r);
+            item_q_cta(p, r, i, qsm_base);
+        }
+    }
+    __device__ static __forceinline__ void item_q_cta(const DecodeParams &p, const QItems &r,
+                                                      uint32_t i, uint32_t qsm_base)
+    {
+        const uint32_t hq = p.hq, G = hq / p.hkv, n = hq * 16;
+        const bool live = i < n;
+        const uint32_t h = i >> 4, b = (i >> 1) & 7, c = i & 1;
+        int code[16];  // dims 8c+k (k < 8), 16+8c+k-8 (k >= 8)
+        float d16;
+        if (p.q_f32) {
+            float v[16];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                v[4 * k] = live ? r.x[k].x : 0.0f;
+                v[4 * k + 1] = live ? r.x[k].y : 0.0f;
+                v[4 * k + 2] = live ? r.x[k].z : 0.0f;
+                v[4 * k + 3] = live ? r.x[k].w : 0.0f;
+            }
+            float amax = 0.0f;
+#pragma unroll
+            for (int k = 0; k < 16; ++k)
+                amax = fmaxf(amax, fabsf(v[k]));
+            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+            const float d = amax / 127.0f, inv_d = 1.0f / d;
+            bool near = false;
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+                const float rk = v[k] * inv_d, a = fabsf(rk);
+                near |= !(fabsf(a - truncf(a) - 0.5f) > 3.0e-5f);
+                code[k] = (int)fminf(fmaxf(roundf(rk), -127.0f), 127.0f);
+            }
+            if (__any_sync(0xffffffffu, near)) {
+#pragma unroll
+                for (int k = 0; k < 16; ++k)
+                    code[k] = q8_1_code(v[k], amax, d, inv_d);
+            }
+            d16 = __half2float(__float2half_rn(amax == 0.0f ? 0.0f : d));
+        } else {
+#pragma unroll
+            for (int k = 0; k < 16; ++k)
+                code[k] = (int)(int8_t)(uint8_t)(r.w[k >> 2] >> (8 * (k & 3)));
+            d16 = half_bits_to_float((uint16_t)r.d);
+        }
+        const float d = d16 * p.scale_log2;
+        const uint32_t g = h / G, gid = h % G;
+        const uint32_t base = qsm_base + g * QBYTES;
+        float cc = 0.0f;
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            // lane tig = 2c + e: j = 0..3 dims 4tig.., j = 4..7 dims 16+4tig..
+            __half qh[8];
+            float corr = 0.0f;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                qh[j] = __float2half_rn((float)code[(j < 4 ? 0 : 8) + 4 * e + (j & 3)] * d);
+                corr += __half2float(qh[j]) * (j < 4 ? 1032.0f : 72.0f);
+            }
+            cc = e == 0 ? corr : cc + corr;
+            if (live)
+                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
+                                 base + (b * 32 + gid * 4 + 2 * c + e) * QREC),
+                             "r"(h2_bits(__halves2half2(qh[0], qh[2]))),
+                             "r"(h2_bits(__halves2half2(qh[1], qh[3]))),
+                             "r"(h2_bits(__halves2half2(qh[4], qh[6]))),
+                             "r"(h2_bits(__halves2half2(qh[5], qh[7]))));
+        }
+        cc += __shfl_xor_sync(0xffffffffu, cc, 1);
+        if (live && c == 0)
+            sts_f32(base + QCORR + 4 * (gid * NB + b), -cc);
     }
 
     // The B fragments of the bias product (see scores()): blocks tig and
@@ -1902,9 +2041,9 @@ __device__ __forceinline__ void range_body32(const FastArgs &a, uint8_t *smem, u
     int32_t rb0 = 0, rb1 = 0, nb0 = 0, nb1 = 0;
     fetch_refills(0, rb0, rb1);
     fetch_refills(32, nb0, nb1);
-    // quantised K: the wph warps of a head split its query blocks
-    typename T::QRaw qraw;
-    T::fetch_q(p, seq, g * G, G, gid, tig, sub, wph, qraw);
+    // the query of the row: one (head, block, half) item per thread
+    typename T::QItems qitems;
+    T::fetch_q_cta(p, seq, threadIdx.x, qitems);
     // my tiles among the ring's first S
     for (uint32_t t = sub; t < S && t < n_tiles; t += wph) {
         int32_t b0, b1;
@@ -1917,7 +2056,7 @@ __device__ __forceinline__ void range_body32(const FastArgs &a, uint8_t *smem, u
     typename T::Consts K;
     K.init();
     typename T::Frag f;
-    T::store_q(p, qraw, G, gid, tig, sub, wph, qsm_base + g * T::QBYTES);
+    T::store_q_cta(p, seq, qitems, qsm_base);
     __syncthreads();
     T::load_q(qsm_base + g * T::QBYTES, lane, f);
     float o[T::MT][4];
