@@ -296,6 +296,18 @@ __device__ __forceinline__ uint32_t ld_acquire_u32(const int32_t *p)
     return v;
 }
 
+// Atomic add at GPU scope with acquire and release semantics; returns the
+// old value.
+__device__ __forceinline__ uint32_t atom_add_acq_rel(int32_t *p, uint32_t v)
+{
+    uint32_t old;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;"
+                 : "=r"(old)
+                 : "l"(p), "r"(v)
+                 : "memory");
+    return old;
+}
+
 // Programmatic dependent launch: the wait for the grids this one depends on
 // (their writes visible), and the signal that the grids depending on this
 // one may be scheduled.
@@ -1547,8 +1559,9 @@ __device__ __noinline__ void merge_tail_staged(const DecodeParams &p, uint32_t s
 // the count merges the rows of every partition whose bit it sees.  The two
 // sides order their write and read of words 0 and 1 with sequentially
 // consistent fences, so at least one of them merges each such row (both may:
-// they write the same bits).  Word 2 counts the CTAs that are done; the last
-// one resets the three words to 0.
+// they write the same bits).  Word 2 counts the CTAs that have read words 0
+// and 1 (counted while the rows are merged); the last one resets the three
+// words to 0.
 // A row's partials are contiguous, so a merging warp copies them into its
 // share of the idle rings with one bulk copy and sums them from shared
 // memory (merge_row_staged): one round trip, and a short loop -- this code
@@ -1595,6 +1608,18 @@ __device__ __noinline__ void merge_coop(const DecodeParams &p, uint32_t seq, uin
     }
     __syncthreads();
     const uint32_t set = s_set;
+    // this CTA's reads of words 0 and 1 are done (thread 0, before the
+    // barrier): the first thread of the last warp counts it on word 2 while
+    // the rows are merged, and the CTA that completes that count resets the
+    // three words for the next launch (the partials need no such order: a
+    // later launch writes them only after this grid has completed)
+    if (threadIdx.x == blockDim.x - 32) {
+        if (atom_add_acq_rel(cnt + 2, 1u) + 1 == na) {
+            cnt[0] = 0;
+            cnt[1] = 0;
+            cnt[2] = 0;
+        }
+    }
     if (set) {
         const __half *po = static_cast<const __half *>(p.part_o);
         const float2 *pml = reinterpret_cast<const float2 *>(p.part_ml);
@@ -1639,15 +1664,6 @@ __device__ __noinline__ void merge_coop(const DecodeParams &p, uint32_t seq, uin
                                                       nullptr);
             }
             ++u;
-        }
-    }
-    __syncthreads();  // this CTA's reads of the words and the partials are done
-    if (threadIdx.x == 0) {
-        __threadfence();
-        if (atomicAdd(reinterpret_cast<unsigned *>(cnt + 2), 1u) + 1 == na) {
-            cnt[0] = 0;
-            cnt[1] = 0;
-            cnt[2] = 0;
         }
     }
 }
