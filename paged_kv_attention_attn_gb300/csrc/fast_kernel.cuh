@@ -1644,11 +1644,13 @@ __device__ __noinline__ void merge_coop(const DecodeParams &p, uint32_t seq, uin
             }
             __syncwarp();
         }
-        uint32_t u = 0;  // rows of this CTA, in order; row u goes to worker u % workers
-        for (uint32_t r = 0; r < p.hq; ++r) {
-            if (!((set >> (r % na)) & 1u))
-                continue;
-            if (worker && wid < workers && u % workers == wid) {
+        // rows r = j, j + na, ... of each partition j in the set; the u-th
+        // goes to worker u % workers
+        uint32_t u = 0;
+        for (uint32_t bits = set; bits; bits &= bits - 1) {
+            for (uint32_t r = __ffs(bits) - 1; r < p.hq; r += na, ++u) {
+                if (!(worker && wid < workers && u % workers == wid))
+                    continue;
                 const uint64_t row = pseq * p.hq + r;
                 const __half *rpo = po + row * p.n_parts * p.d;
                 const float2 *rml = pml + row * p.n_parts;
@@ -1663,7 +1665,6 @@ __device__ __noinline__ void merge_coop(const DecodeParams &p, uint32_t seq, uin
                     merge_rows_warp_v<4, 1, false, 8>(&rpo, &rml, n, 1, p.d, 1, &rout, nullptr,
                                                       nullptr);
             }
-            ++u;
         }
     }
 }
@@ -2015,8 +2016,10 @@ __device__ __forceinline__ void range_body32(const FastArgs &a, uint8_t *smem, u
         b1 = t < n_tiles && tok + 16 < t1 ? bt[(tok + 16) >> bshift] : 0;
     };
     // lane 0: the copies of tile t (block ids b0, b1 of its halves) into slot
-    // s = t % S at shared address dst, completing barrier fb
-    auto issue = [&](uint32_t t, uint32_t s, uint8_t *dst, uint64_t *fb, int32_t b0, int32_t b1) {
+    // s = t % S at shared address dst, completing barrier fb; a refill
+    // (after this warp's reads of the slot) first orders those reads
+    auto issue = [&](uint32_t t, uint32_t s, uint8_t *dst, uint64_t *fb, int32_t b0, int32_t b1,
+                     bool refill) {
         const uint32_t tok = t0 + 32 * t;
         uint32_t bits = 0;
         if (tok < t1) {
@@ -2032,7 +2035,8 @@ __device__ __forceinline__ void range_body32(const FastArgs &a, uint8_t *smem, u
                 atomicOr(p.status, PA_STATUS_CORRUPT_TABLE);
         }
         slot_ok[s] = (int)((t + 1u) << 2 | bits);
-        fence_proxy_async();  // earlier generic reads of this slot come first
+        if (refill)
+            fence_proxy_async();  // earlier generic reads of this slot come first
         // K/V rows are read once: evict-first in the L2
         const uint64_t pol = l2_evict_first_policy();
         mbar_arrive_expect_tx(fb, (bits & 1u ? 2 * HALF : 0u) + (bits & 2u ? 2 * HALF : 0u));
@@ -2060,12 +2064,20 @@ __device__ __forceinline__ void range_body32(const FastArgs &a, uint8_t *smem, u
     // the query of the row: one (head, block, half) item per thread
     typename T::QItems qitems;
     T::fetch_q_cta(p, seq, threadIdx.x, qitems);
-    // my tiles among the ring's first S
-    for (uint32_t t = sub; t < S && t < n_tiles; t += wph) {
-        int32_t b0, b1;
-        ids_of(t, b0, b1);
-        if (lane == 0)
-            issue(t, t, ring + (size_t)t * SLOT, hbar + t, b0, b1);
+    // my tiles among the ring's first S (fresh slots): lane k loads the
+    // block ids of the k-th, so that one round trip serves them all
+    {
+        const uint32_t tk = sub + (uint32_t)lane * wph;
+        int32_t kb0 = 0, kb1 = 0;
+        if (tk < S)
+            ids_of(tk, kb0, kb1);
+        uint32_t k = 0;
+        for (uint32_t t = sub; t < S && t < n_tiles; t += wph, ++k) {
+            const int32_t b0 = __shfl_sync(0xffffffffu, kb0, k);
+            const int32_t b1 = __shfl_sync(0xffffffffu, kb1, k);
+            if (lane == 0)
+                issue(t, t, ring + (size_t)t * SLOT, hbar + t, b0, b1, false);
+        }
     }
     __syncwarp();
 
@@ -2170,7 +2182,7 @@ __device__ __forceinline__ void range_body32(const FastArgs &a, uint8_t *smem, u
             // tile t + S: the same slot, the next barrier turn
             uint64_t *nb = hbar + s + S * (e + 1 == wph ? 0u : e + 1);
             if (lane == 0)
-                issue(t + S, s, ring + (kh - ring_u), nb, b0, b1);
+                issue(t + S, s, ring + (kh - ring_u), nb, b0, b1, true);
         }
         s += wph;
         kh += wph * SLOT;
