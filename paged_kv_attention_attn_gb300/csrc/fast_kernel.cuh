@@ -2016,10 +2016,14 @@ __device__ __forceinline__ void range_body32(const FastArgs &a, uint8_t *smem, u
         b1 = t < n_tiles && tok + 16 < t1 ? bt[(tok + 16) >> bshift] : 0;
     };
     // lane 0: the copies of tile t (block ids b0, b1 of its halves) into slot
-    // s = t % S at shared address dst, completing barrier fb; a refill
-    // (after this warp's reads of the slot) first orders those reads
-    auto issue = [&](uint32_t t, uint32_t s, uint8_t *dst, uint64_t *fb, int32_t b0, int32_t b1,
-                     bool refill) {
+    // s = t % S at shared address dst, completing barrier fb.  A refill
+    // follows this warp's reads of the slot without a proxy fence: each of
+    // those loads has returned its value (consumed by the tensor-core
+    // operations before the warp barrier that precedes the issue), so a copy
+    // issued after them cannot change what they read -- the ordering the TMA
+    // pipelines of CUTLASS rely on when a consumer releases a stage with a
+    // bare mbarrier arrive.
+    auto issue = [&](uint32_t t, uint32_t s, uint8_t *dst, uint64_t *fb, int32_t b0, int32_t b1) {
         const uint32_t tok = t0 + 32 * t;
         uint32_t bits = 0;
         if (tok < t1) {
@@ -2035,8 +2039,6 @@ __device__ __forceinline__ void range_body32(const FastArgs &a, uint8_t *smem, u
                 atomicOr(p.status, PA_STATUS_CORRUPT_TABLE);
         }
         slot_ok[s] = (int)((t + 1u) << 2 | bits);
-        if (refill)
-            fence_proxy_async();  // earlier generic reads of this slot come first
         // K/V rows are read once: evict-first in the L2
         const uint64_t pol = l2_evict_first_policy();
         mbar_arrive_expect_tx(fb, (bits & 1u ? 2 * HALF : 0u) + (bits & 2u ? 2 * HALF : 0u));
@@ -2064,8 +2066,8 @@ __device__ __forceinline__ void range_body32(const FastArgs &a, uint8_t *smem, u
     // the query of the row: one (head, block, half) item per thread
     typename T::QItems qitems;
     T::fetch_q_cta(p, seq, threadIdx.x, qitems);
-    // my tiles among the ring's first S (fresh slots): lane k loads the
-    // block ids of the k-th, so that one round trip serves them all
+    // my tiles among the ring's first S: lane k loads the block ids of the
+    // k-th, so that one round trip serves them all
     {
         const uint32_t tk = sub + (uint32_t)lane * wph;
         int32_t kb0 = 0, kb1 = 0;
@@ -2076,7 +2078,7 @@ __device__ __forceinline__ void range_body32(const FastArgs &a, uint8_t *smem, u
             const int32_t b0 = __shfl_sync(0xffffffffu, kb0, k);
             const int32_t b1 = __shfl_sync(0xffffffffu, kb1, k);
             if (lane == 0)
-                issue(t, t, ring + (size_t)t * SLOT, hbar + t, b0, b1, false);
+                issue(t, t, ring + (size_t)t * SLOT, hbar + t, b0, b1);
         }
     }
     __syncwarp();
@@ -2182,7 +2184,7 @@ __device__ __forceinline__ void range_body32(const FastArgs &a, uint8_t *smem, u
             // tile t + S: the same slot, the next barrier turn
             uint64_t *nb = hbar + s + S * (e + 1 == wph ? 0u : e + 1);
             if (lane == 0)
-                issue(t + S, s, ring + (kh - ring_u), nb, b0, b1, true);
+                issue(t + S, s, ring + (kh - ring_u), nb, b0, b1);
         }
         s += wph;
         kh += wph * SLOT;
