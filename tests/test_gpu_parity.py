@@ -79,6 +79,30 @@ def test_other_head_shapes(kernel, shape):
 
 
 @pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("hq,hkv", [(8, 8), (8, 2), (32, 4), (64, 8)])
+def test_q4_0_other_head_shapes(kernel, hq, hkv):
+    """Q4_0 (D = 256) beyond the 24 / 4 heads of the benchmark: one query head
+    per K/V head, groups narrower than the tensor-core tile (dead query
+    columns), and rows whose query items outnumber the CTA's threads (hq * 16
+    > warps * 32: the CTA-wide query quantisation of the 32-token path takes
+    several rounds).  Against the oracle, and the one-launch step (query
+    quantised in the kernel) equal to the three-launch step (q8_1 pre-pass)
+    bit for bit."""
+    spec = synth.CaseSpec(seq_lens=[700, 33, 0, 2000], k_type=synth.Q4_0, v_type=synth.Q4_0,
+                          hq=hq, hkv=hkv, junk=5, outliers=True)
+    case = synth.build_case(spec, seed=1250 + hq + hkv, device=DEV)
+    ref, vmax = H.oracle_out(case), H.oracle_vmax(case)
+    for force in (0, 3):
+        a, ws, _, tails = H.run(case, force_parts=force, flags=KERNELS[kernel], canary=True)
+        H.check_canaries(tails)
+        assert pa.status_read(ws.status) == 0
+        H.assert_close(case, a, ref, vmax, label=f"Q4_0 hq{hq} hkv{hkv} force{force}")
+        b, ws_b, _, _ = H.run(case, force_parts=force, flags=KERNELS[kernel], fused=True)
+        assert pa.status_read(ws_b.status) == 0
+        assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
 def test_block_boundary_lengths(kernel):
     lens = [0, 1, 15, 16, 17, 31, 32, 33, 200, 127, 128, 129, 255, 256, 257]
     spec = synth.CaseSpec(seq_lens=lens, k_type=synth.Q4_0, v_type=synth.Q4_0, junk=13)
