@@ -51,3 +51,21 @@ def test_wave_filling_plan_bytes():
     parts = 8 * 18 * 24 * (2 * 256 + 8)           # only the 8 split rows have partials
     out = 160 * 24 * 256 * 4                      # 152 rows by the decode, 8 by the merge
     assert nb["decode"] == kv + table + q + 2 * parts + out + 2 * 160 * 4
+
+
+def test_dram_record_is_consistent_with_its_workload():
+    """The committed ncu DRAM record that bench.py reports as roofline.traffic:
+    its plan is the planner's plan for the workload it names (152 SMs), and
+    its bytes are the algorithmic bytes of that launch to ncu's three
+    significant figures (every K/V byte read once).  bench.py reports it only
+    while its source hash matches the kernel sources."""
+    import json
+    rec = json.load(open(os.path.join(bench.ROOT, "profiles", "decode_traffic.json")))
+    assert rec["workload_name"] == "uniform-q4_0-b8x131072"
+    spec = synth.uniform_spec(8, 131072)
+    pl = _plan(spec)
+    assert rec["plan"] == pl.as_dict()
+    nb = bench.algorithmic_bytes(spec, pl, fused=True, in_kernel_q=True)["step"]
+    assert abs(rec["dram_bytes_per_launch"] - nb) <= 0.005 * nb
+    assert rec["dram_bytes_per_launch"] == rec["dram_bytes_read"] + rec["dram_bytes_write"]
+    assert len(rec["source_sha"]) == 16
