@@ -103,6 +103,25 @@ def test_q4_0_other_head_shapes(kernel, hq, hkv):
 
 
 @pytest.mark.parametrize("kernel", KERNELS)
+def test_q4_0_32_token_blocks(kernel):
+    """Q4_0 with 32-token blocks: the two 16-token halves of a 32-token tile
+    come from one block (partitions start on block boundaries).  Against the
+    oracle in every mode, and the one-launch step equal to the three-launch
+    step bit for bit."""
+    spec = synth.CaseSpec(seq_lens=[1000, 17, 0, 64, 333], k_type=synth.Q4_0,
+                          v_type=synth.Q4_0, block_size=32, junk=7, outliers=True)
+    case = synth.build_case(spec, seed=1280, device=DEV)
+    ref, vmax = H.oracle_out(case), H.oracle_vmax(case)
+    for force in (0, 1, 5):
+        a, ws, _, tails = H.run(case, force_parts=force, flags=KERNELS[kernel], canary=True)
+        H.check_canaries(tails)
+        assert pa.status_read(ws.status) == 0
+        H.assert_close(case, a, ref, vmax, label=f"Q4_0 B32 force{force}")
+        b, _, _, _ = H.run(case, force_parts=force, flags=KERNELS[kernel], fused=True)
+        assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
 def test_block_boundary_lengths(kernel):
     lens = [0, 1, 15, 16, 17, 31, 32, 33, 200, 127, 128, 129, 255, 256, 257]
     spec = synth.CaseSpec(seq_lens=lens, k_type=synth.Q4_0, v_type=synth.Q4_0, junk=13)
